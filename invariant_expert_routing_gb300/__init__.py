@@ -1,0 +1,192 @@
+"""Python binding of the batch-invariant MoE layer C ABI (libmoe_gb300.so).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  Functions carry the C names (moe_route, moe_dispatch_align,
+moe_expert_ffn, moe_combine, moe_forward, ...) and take torch tensors, whose
+device pointers are passed through; PyTorch only provides device memory and
+streams.  There is no fallback: if the library is missing, importing this
+package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                      "(nvcc, sm_103a); there is no CPU fallback")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE = 5
+MOE_DEV_ERR_EXPERT_RANGE = 0x1
+MOE_DEV_ERR_TIMEOUT = 0x2
+MOE_DEV_ERR_BAD_BLOCKS = 0x4
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("shared_intermediate", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = _lib.moe_status_string(status).decode()
+        super().__init__(f"{fn} failed: {msg} ({status})")
+
+
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_cfgp = ctypes.POINTER(moe_config)
+_SIGS = {
+    "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "moe_check_config": ([_cfgp], ctypes.c_int),
+    "moe_capacity": ([_cfgp, _i32], _i32),
+    "moe_max_padded_rows": ([_cfgp, _i32], ctypes.c_int64),
+    "moe_max_blocks": ([_cfgp, _i32], ctypes.c_int64),
+    "moe_workspace_bytes": ([_cfgp, _i32], _sz),
+    "moe_route": ([_cfgp, _i32] + [_vp] * 6 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_dispatch_align": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_expert_ffn": ([_cfgp, _i32] + [_vp] * 10 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_combine": ([_cfgp, _i32] + [_vp] * 7 + [_vp], ctypes.c_int),
+    "moe_forward": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_forward_hostio": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_get_device_status": ([_vp, ctypes.POINTER(_i32), _vp], ctypes.c_int),
+    "moe_clear_device_status": ([_vp, _vp], ctypes.c_int),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+def make_config(hidden, num_experts, top_k, intermediate, block_size, capacity_factor=0.0,
+                shared_intermediate=0) -> moe_config:
+    return moe_config(hidden, num_experts, top_k, intermediate, block_size, capacity_factor,
+                      shared_intermediate)
+
+
+def _cfg(cfg) -> moe_config:
+    if isinstance(cfg, moe_config):
+        return cfg
+    return make_config(**cfg)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(fn, st):
+    if st != MOE_OK:
+        raise MoEError(fn, st)
+
+
+def moe_capacity(cfg, T: int) -> int:
+    return int(_lib.moe_capacity(ctypes.byref(_cfg(cfg)), T))
+
+
+def moe_max_padded_rows(cfg, T: int) -> int:
+    return int(_lib.moe_max_padded_rows(ctypes.byref(_cfg(cfg)), T))
+
+
+def moe_max_blocks(cfg, T: int) -> int:
+    return int(_lib.moe_max_blocks(ctypes.byref(_cfg(cfg)), T))
+
+
+def moe_workspace_bytes(cfg, max_tokens: int) -> int:
+    return int(_lib.moe_workspace_bytes(ctypes.byref(_cfg(cfg)), max_tokens))
+
+
+def moe_check_config(cfg) -> int:
+    return int(_lib.moe_check_config(ctypes.byref(_cfg(cfg))))
+
+
+def workspace(cfg, max_tokens: int, device="cuda"):
+    """A torch uint8 tensor sized for moe_* calls with up to max_tokens tokens."""
+    import torch
+    n = moe_workspace_bytes(cfg, max_tokens)
+    if n == 0:
+        raise MoEError("moe_workspace_bytes", MOE_ERR_UNSUPPORTED)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_route(cfg, h, w_gate, router_bias, topk_idx, topk_gate, logits_out, ws, stream=None):
+    T = h.shape[0]
+    _check("moe_route", _lib.moe_route(ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate),
+                                       _ptr(router_bias), _ptr(topk_idx), _ptr(topk_gate),
+                                       _ptr(logits_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_align(cfg, topk_idx, route_kept, route_pos, sorted_route_ids, block_expert,
+                       num_padded, expert_counts, num_dropped, ws, stream=None):
+    T = topk_idx.shape[0]
+    _check("moe_dispatch_align", _lib.moe_dispatch_align(
+        ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), _ptr(route_kept), _ptr(route_pos),
+        _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded), _ptr(expert_counts),
+        _ptr(num_dropped), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn(cfg, h, w13, w2, w13_shared, w2_shared, sorted_route_ids, block_expert,
+                   num_padded, y_perm, y_shared, ws, stream=None):
+    T = h.shape[0]
+    _check("moe_expert_ffn", _lib.moe_expert_ffn(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w13), _ptr(w2), _ptr(w13_shared),
+        _ptr(w2_shared), _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded),
+        _ptr(y_perm), _ptr(y_shared), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_combine(cfg, h, topk_gate, route_kept, route_pos, y_perm, y_shared, out, stream=None):
+    T = h.shape[0]
+    _check("moe_combine", _lib.moe_combine(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(topk_gate), _ptr(route_kept), _ptr(route_pos),
+        _ptr(y_perm), _ptr(y_shared), _ptr(out), _stream(stream)))
+
+
+def moe_forward(cfg, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws,
+                stream=None):
+    T = h.shape[0]
+    _check("moe_forward", _lib.moe_forward(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(router_bias), _ptr(w13),
+        _ptr(w2), _ptr(w13_shared), _ptr(w2_shared), _ptr(out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_forward_hostio(cfg, h_host, w_gate, router_bias, w13, w2, w13_shared, w2_shared,
+                       out_host, ws, stream=None):
+    """h_host / out_host: CPU tensors (pinned for asynchronous copies)."""
+    T = h_host.shape[0]
+    _check("moe_forward_hostio", _lib.moe_forward_hostio(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h_host), _ptr(w_gate), _ptr(router_bias), _ptr(w13),
+        _ptr(w2), _ptr(w13_shared), _ptr(w2_shared), _ptr(out_host), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    st = _lib.moe_get_device_status(_ptr(ws), ctypes.byref(v), _stream(stream))
+    if st not in (MOE_OK, MOE_ERR_DEVICE):
+        raise MoEError("moe_get_device_status", st)
+    return int(v.value)
+
+
+def moe_clear_device_status(ws, stream=None) -> None:
+    _check("moe_clear_device_status", _lib.moe_clear_device_status(_ptr(ws), _stream(stream)))

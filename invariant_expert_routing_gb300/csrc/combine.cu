@@ -1,0 +1,76 @@
+// Gate-weighted combine into the residual stream ("Mixture-of-Experts Routing
+// at Inference Time": the output is the gate-weighted sum of the selected
+// experts added to h; a dropped route adds nothing, Figure 2).
+//
+// out[t,:] = bf16( h[t,:] + acc ),  acc = fma over kept slots j = 0..k-1 in
+// ascending order of gate[t,j] * y_perm[route_pos[t*k+j], :], then + y_shared.
+// One CTA per token row, 4 consecutive features per thread, 128-bit loads of
+// y_perm; the order of the sum is fixed and independent of T.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ h,
+                                                      const float* __restrict__ gates,
+                                                      const uint8_t* __restrict__ route_kept,
+                                                      const int32_t* __restrict__ route_pos,
+                                                      const float* __restrict__ y_perm,
+                                                      const float* __restrict__ y_shared,
+                                                      uint16_t* __restrict__ out, int H, int k,
+                                                      long long max_rows) {
+  const int t = blockIdx.x;
+  __shared__ int s_pos[16];
+  __shared__ float s_gate[16];
+  if (threadIdx.x < k) {
+    const size_t r = (size_t)t * k + threadIdx.x;
+    const int pos = route_pos[r];
+    const bool use = route_kept[r] && pos >= 0 && (long long)pos < max_rows;
+    s_pos[threadIdx.x] = use ? pos : -1;
+    s_gate[threadIdx.x] = gates[r];
+  }
+  __syncthreads();
+  for (int d = threadIdx.x * 4; d < H; d += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int pos = s_pos[j];
+      if (pos < 0) continue;
+      const float g = s_gate[j];
+      const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)pos * H + d));
+      acc.x = fmaf(g, y.x, acc.x);
+      acc.y = fmaf(g, y.y, acc.y);
+      acc.z = fmaf(g, y.z, acc.z);
+      acc.w = fmaf(g, y.w, acc.w);
+    }
+    if (y_shared) {
+      const float4 ys = __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * H + d));
+      acc.x = acc.x + ys.x;
+      acc.y = acc.y + ys.y;
+      acc.z = acc.z + ys.z;
+      acc.w = acc.w + ys.w;
+    }
+    const uint2 hv = __ldg(reinterpret_cast<const uint2*>(h + (size_t)t * H + d));
+    const float h0 = __uint_as_float(hv.x << 16), h1 = __uint_as_float(hv.x & 0xFFFF0000u);
+    const float h2 = __uint_as_float(hv.y << 16), h3 = __uint_as_float(hv.y & 0xFFFF0000u);
+    const __nv_bfloat16 o0 = __float2bfloat16_rn(h0 + acc.x), o1 = __float2bfloat16_rn(h1 + acc.y);
+    const __nv_bfloat16 o2 = __float2bfloat16_rn(h2 + acc.z), o3 = __float2bfloat16_rn(h3 + acc.w);
+    uint2 ov;
+    ov.x = (uint32_t)__bfloat16_as_ushort(o0) | ((uint32_t)__bfloat16_as_ushort(o1) << 16);
+    ov.y = (uint32_t)__bfloat16_as_ushort(o2) | ((uint32_t)__bfloat16_as_ushort(o3) << 16);
+    *reinterpret_cast<uint2*>(out + (size_t)t * H + d) = ov;
+  }
+}
+
+}  // namespace
+
+void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,
+                    const int32_t* route_pos, const float* y_perm, const float* y_shared,
+                    uint16_t* out, int T, int H, int k, int64_t max_rows, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
+                                   (long long)max_rows);
+}
+
+}  // namespace moe

@@ -1,0 +1,233 @@
+// Capacity-limited dispatch and stable alignment into padded expert blocks.
+//
+// Capacity is filled in batch order ("Mixture-of-experts routing and LLM
+// repeatability": the dispatcher fills capacity in order; overflow skips the
+// expert): expert e keeps its first C routes by ascending route id.  Stable
+// construction ("Route-Block Membership Selects Packed-AWQ Arithmetic",
+// section "Stable construction selected a third trajectory"): segments in
+// ascending expert id, routes inside a segment in ascending route id, each
+// segment padded with the sentinel R = T*k to a multiple of B.
+//
+// The rank of a route among the earlier routes of its expert is computed
+// without atomics: warp peers by __match_any_sync, per-warp counts scanned
+// across the warps of a 1024-route tile, per-tile counts scanned across tiles
+// in a single CTA.  All results are integers and unique, so every run and
+// every launch shape gives the same bits.
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxN = 256;
+
+__global__ void __launch_bounds__(1024) dispatch_count_kernel(const int32_t* __restrict__ topk_idx,
+                                                              int R, int N,
+                                                              int32_t* __restrict__ rank_in_tile,
+                                                              int32_t* __restrict__ tile_count,
+                                                              int* status) {
+  __shared__ int32_t wc[32][kMaxN + 1];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 32 * (kMaxN + 1); i += blockDim.x) (&wc[0][0])[i] = 0;
+  __syncthreads();
+  const int r = blockIdx.x * kDispatchTile + tid;
+  const int e = (r < R) ? topk_idx[r] : -1;
+  const bool valid = (r < R) && e >= 0 && e < N;
+  if (r < R && !valid) atomicOr(status, kDevErrExpertRange);
+  const int key = valid ? e : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank == 0) wc[w][e] = __popc(peers);
+  __syncthreads();
+  for (int ee = tid; ee < N; ee += blockDim.x) {
+    int run = 0;
+    for (int ww = 0; ww < 32; ++ww) {
+      const int c = wc[ww][ee];
+      wc[ww][ee] = run;
+      run += c;
+    }
+    tile_count[(size_t)blockIdx.x * N + ee] = run;
+  }
+  __syncthreads();
+  if (r < R) rank_in_tile[r] = valid ? wc[w][e] + rank : -1;
+}
+
+// Block-wide exclusive scan of one int per thread (256 threads).
+__device__ int block_exclusive_scan(int v, int* buf, int* total) {
+  const int tid = threadIdx.x;
+  buf[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    const int x = (tid >= off) ? buf[tid - off] : 0;
+    __syncthreads();
+    buf[tid] += x;
+    __syncthreads();
+  }
+  const int incl = buf[tid];
+  *total = buf[255];
+  __syncthreads();
+  return incl - v;
+}
+
+// One CTA of 256 threads; thread e owns expert e.  Turns per-tile counts into
+// per-tile bases (in place), applies the capacity, lays out the segments.
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(
+    int32_t* __restrict__ tile_count, int ntiles, int N, int B, int capacity, int R,
+    int32_t* __restrict__ seg_off, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_padded,
+    int32_t* __restrict__ num_dropped, int32_t* __restrict__ block_expert,
+    int32_t* __restrict__ sorted_route_ids) {
+  __shared__ int buf[256];
+  __shared__ int blk_off[kMaxN + 1];
+  const int e = threadIdx.x;
+  int load = 0;
+  if (e < N) {
+    for (int tl = 0; tl < ntiles; ++tl) {
+      const int c = tile_count[(size_t)tl * N + e];
+      tile_count[(size_t)tl * N + e] = load;
+      load += c;
+    }
+  }
+  const int kept = (e < N) ? (capacity < 0 ? load : min(load, capacity)) : 0;
+  const int padded = (kept + B - 1) / B * B;
+  int total_rows = 0, total_drop = 0;
+  const int seg = block_exclusive_scan(padded, buf, &total_rows);
+  block_exclusive_scan(load - kept, buf, &total_drop);
+  if (e < N) {
+    seg_off[e] = seg;
+    expert_counts[e] = kept;
+    for (int j = kept; j < padded; ++j) sorted_route_ids[seg + j] = R;
+    blk_off[e] = seg / B;
+  }
+  if (e == 0) {
+    blk_off[N] = total_rows / B;
+    *num_padded = total_rows;
+    *num_dropped = total_drop;
+  }
+  __syncthreads();
+  // block b belongs to the last expert whose first block is <= b
+  const int nb = total_rows / B;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    // largest e in [0, N) with blk_off[e] <= b; it has blk_off[e+1] > b, so
+    // empty segments (equal offsets) are skipped
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (blk_off[mid] <= b) lo = mid; else hi = mid;
+    }
+    block_expert[b] = lo;
+  }
+}
+
+__global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
+    const int32_t* __restrict__ topk_idx, int R, int N, int capacity,
+    const int32_t* __restrict__ rank_in_tile, const int32_t* __restrict__ tile_base,
+    const int32_t* __restrict__ seg_off, uint8_t* __restrict__ route_kept,
+    int32_t* __restrict__ route_pos, int32_t* __restrict__ sorted_route_ids) {
+  const int r = blockIdx.x * kDispatchTile + threadIdx.x;
+  if (r >= R) return;
+  const int e = topk_idx[r];
+  if (e < 0 || e >= N) {
+    route_kept[r] = 0;
+    route_pos[r] = -1;
+    return;
+  }
+  const int rank = tile_base[(size_t)blockIdx.x * N + e] + rank_in_tile[r];
+  const bool kept = capacity < 0 || rank < capacity;
+  route_kept[r] = kept ? 1 : 0;
+  if (kept) {
+    const int pos = seg_off[e] + rank;
+    route_pos[r] = pos;
+    sorted_route_ids[pos] = r;
+  } else {
+    route_pos[r] = -1;
+  }
+}
+
+// Grouped-GEMM tile list from the padded blocks: each expert segment is cut
+// into tiles of kTileRows rows from its start.  Rejects (no tiles, status
+// bit) a block list that is not sorted by expert or out of range.
+__global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
+                                                          const int32_t* __restrict__ num_padded, int N,
+                                                          int B, long long max_rows,
+                                                          GemmTile* __restrict__ tiles,
+                                                          int32_t* __restrict__ num_tiles, int max_tiles,
+                                                          int* status) {
+  __shared__ int buf[256];
+  __shared__ int s_bad;
+  const int P = *num_padded;
+  const bool bad_count = P < 0 || (long long)P > max_rows || (P % B) != 0;
+  const int nb = bad_count ? 0 : P / B;
+  if (threadIdx.x == 0) s_bad = bad_count ? 1 : 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    const int e = block_expert[b];
+    if (e < 0 || e >= N || (b > 0 && block_expert[b - 1] > e)) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) {
+      *num_tiles = 0;
+      atomicOr(status, kDevErrBadBlocks);
+    }
+    return;
+  }
+  const int e = threadIdx.x;
+  int first = 0, last = 0;
+  if (e < N) {
+    int lo = 0, hi = nb;  // first block with expert >= e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (block_expert[mid] < e) lo = mid + 1; else hi = mid;
+    }
+    first = lo;
+    hi = nb;  // first block with expert >= e + 1
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (block_expert[mid] <= e) lo = mid + 1; else hi = mid;
+    }
+    last = lo;
+  }
+  const int rows = (last - first) * B;
+  const int nt = (rows + kTileRows - 1) / kTileRows;
+  int total = 0;
+  const int off = block_exclusive_scan(nt, buf, &total);
+  for (int j = 0; j < nt; ++j) {
+    const int idx = off + j;
+    if (idx < max_tiles) {
+      GemmTile tl;
+      tl.expert = e;
+      tl.row0 = first * B + j * kTileRows;
+      tl.rows = min(kTileRows, rows - j * kTileRows);
+      tl.pad = 0;
+      tiles[idx] = tl;
+    }
+  }
+  if (threadIdx.x == 0) *num_tiles = min(total, max_tiles);
+}
+
+}  // namespace
+
+void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,
+                     uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                     int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                     int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
+                     int32_t* seg_off, int* status, cudaStream_t s) {
+  const int R = T * k;
+  const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
+  dispatch_count_kernel<<<ntiles, kDispatchTile, 0, s>>>(topk_idx, R, N, rank_in_tile, tile_count, status);
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
+                                         num_padded, num_dropped, block_expert, sorted_route_ids);
+  dispatch_scatter_kernel<<<ntiles, kDispatchTile, 0, s>>>(topk_idx, R, N, capacity, rank_in_tile,
+                                                           tile_count, seg_off, route_kept, route_pos,
+                                                           sorted_route_ids);
+}
+
+void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
+                        int64_t max_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles,
+                        int* status, cudaStream_t s) {
+  build_tiles_kernel<<<1, 256, 0, s>>>(block_expert, num_padded, N, B, (long long)max_rows, tiles,
+                                       num_tiles, max_tiles, status);
+}
+
+}  // namespace moe

@@ -1,0 +1,372 @@
+// Grouped SwiGLU expert GEMMs on the 5th-generation tensor cores (tcgen05).
+//
+// For each padded expert segment produced by the stable alignment
+// ("Route-Block Membership Selects Packed-AWQ Arithmetic", "The bookkeeping
+// before the matrix multiplication"), token tiles of kTileRows rows run
+//   W13: [g | u] = X . W13_e  ->  a = bf16(silu(g) * u)      (X gathered rows of h)
+//   W2 : y = a . W2_e         ->  y_perm (fp32)
+// The weights are operand A (M = 128 output features, MN-major straight from
+// the [K, features] layout), the tokens operand B (N = 128 rows, K-major).
+// Every tile of every batch runs the same instruction sequence: one tile
+// shape, K from 0 to the end in steps of 64 (four K=16 MMAs each), fp32
+// accumulation in TMEM, no split-K and no atomics, so the bits of a token's
+// row depend only on that row and the expert's weights ("Why temperature=0
+// Still Gives Different Answers: Batch Invariance": one tile configuration,
+// no split-K).  Which padded block a route lands in changes nothing, unlike
+// the split/non-split schedule classes of the packed kernel that page studies.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0      TMA producer (weight boxes; W13: tile::gather4 of the token
+//               rows of h; W2: the a tile)
+//   warp 1      TMEM allocation, one elected thread issues tcgen05.mma
+//   warps 2..5  epilogue: tcgen05.ld from TMEM, SiLU*up or fp32 store
+// Smem stages are guarded by full/empty mbarriers, the two TMEM accumulator
+// buffers by tmem_full/tmem_empty, so the epilogue of one tile overlaps the
+// MMAs of the next.  Every wait is bounded (see mbar_wait).
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;                             // K per stage: one 128-byte swizzle row
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // 64 K rows x 64 features of bf16
+constexpr uint32_t kBTileBytes = kTileRows * kBK * 2;  // 128 token rows x 64 K
+constexpr int kThreads = 192;
+
+template <bool kW13>
+struct GemmCfg {
+  static constexpr int kStages = kW13 ? 4 : 6;
+  static constexpr uint32_t kABytes = kW13 ? 4 * kBoxBytes : 2 * kBoxBytes;
+  static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
+  static constexpr uint32_t kAccCols = kW13 ? 2 * kTileRows : kTileRows;  // one accumulator buffer
+  static constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double buffered
+  static constexpr uint32_t kBarBytes = 256;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
+};
+
+// M = 128 features, N = 128 token rows; A (weights) MN-major, B (tokens) K-major.
+constexpr uint32_t kIdesc = idesc_bf16(kTileFeat, kTileRows, true, false);
+
+struct TileInfo {
+  int expert, row0, rows;
+};
+
+__device__ __forceinline__ TileInfo tile_of(const GemmArgs& a, int ti) {
+  TileInfo t;
+  if (a.identity_T) {
+    t.expert = 0;
+    t.row0 = ti * kTileRows;
+    t.rows = min(kTileRows, a.identity_T - t.row0);
+  } else {
+    const GemmTile g = a.tiles[ti];
+    t.expert = g.expert;
+    t.row0 = g.row0;
+    t.rows = g.rows;
+  }
+  return t;
+}
+
+template <bool kW13>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
+                       const __grid_constant__ CUtensorMap x_map, const GemmArgs args) {
+  using C = GemmCfg<kW13>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+
+  const int num_tiles = args.identity_T ? (args.identity_T + kTileRows - 1) / kTileRows : *args.num_tiles;
+  const int total = num_tiles * args.n_feat_tiles;
+  if ((int)blockIdx.x >= total) return;  // uniform for the whole CTA
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t tfull0 = empty0 + 8 * C::kStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = args.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4 * 32);
+    }
+    mbar_init(drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&w_map);
+    prefetch_tmap(&x_map);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_w = policy_evict_normal();
+    const uint64_t pol_x = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed = 0;  // stages armed and not yet known consumed (for the abort path)
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const int f = item / num_tiles, ti = item % num_tiles;
+      const TileInfo t = tile_of(args, ti);
+      int rows4[4] = {0, 0, 0, 0};
+      if (kW13) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = 4 * lane + q;
+          int tok = 0;
+          if (j < t.rows) {
+            if (args.identity_T) {
+              tok = t.row0 + j;
+            } else {
+              const int r = args.sorted_route_ids[t.row0 + j];
+              tok = (r >= 0 && r < args.num_routes) ? r / args.top_k : 0;
+            }
+          }
+          rows4[q] = tok;
+        }
+      }
+      const int wrow0 = t.expert * args.w_rows_per_e;
+      const int fcol = f * kTileFeat;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        // one lane waits, the warp follows its verdict (keeps the warp converged)
+        int got = 1;
+        if (lane == 0) got = mbar_wait(empty0 + 8 * stage, phase ^ 1u, &s_abort) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = smem + stage * C::kStageBytes;
+        uint8_t* sB = sA + C::kABytes;
+        const uint32_t fb = full0 + 8 * stage;
+        const int k0 = ks * kBK;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          tma_load_2d(smem_u32(sA), &w_map, fcol, wrow0 + k0, fb, pol_w);
+          tma_load_2d(smem_u32(sA + kBoxBytes), &w_map, fcol + 64, wrow0 + k0, fb, pol_w);
+          if (kW13) {
+            tma_load_2d(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
+            tma_load_2d(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb, pol_w);
+          } else {
+            tma_load_2d(smem_u32(sB), &x_map, k0, t.row0, fb, pol_x);
+          }
+        }
+        __syncwarp();
+        if (kW13)
+          tma_gather4(smem_u32(sB + lane * 4 * 128), &x_map, k0, rows4[0], rows4[1], rows4[2], rows4[3],
+                      fb, pol_x);
+        armed = min(armed + 1, C::kStages);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      s_abort = 1;
+      if (lane == 0) atomicOr(args.status, kDevErrTimeout);
+    }
+    if (s_abort && lane == 0) {
+      // Let the copies already issued into shared memory land before exit:
+      // wait (bounded) for the last `armed` stages' full barriers.
+      volatile int no_abort = 0;
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < armed; ++i) {
+        if (--s < 0) {
+          s = C::kStages - 1;
+          ph ^= 1u;
+        }
+        mbar_wait(full0 + 8 * s, ph, &no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem + acc * C::kAccCols;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!mbar_wait(full0 + 8 * stage, phase, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t b_base = a_base + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // B: K-major rows of 128 B; a K=16 step is 32 B inside the swizzle row.
+            const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            // A: MN-major; 64-feature atoms 8 KB apart (LBO), 8-row K groups
+            // 1 KB apart (SBO); a K=16 step is 16 rows = 2 KB.
+            const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
+            const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
+            mma_bf16(d0, adesc, bdesc, kIdesc, accum);
+            if (kW13) {
+              const uint64_t adesc_up = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+              mma_bf16(d0 + kTileRows, adesc_up, bdesc, kIdesc, accum);
+            }
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(args.status, kDevErrTimeout);
+      }
+      // all issued MMAs must be complete before TMEM is released
+      mma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int feat_local = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      const int f = item / num_tiles, ti = item % num_tiles;
+      const TileInfo t = tile_of(args, ti);
+      int got = 1;
+      if (lane == 0) got = mbar_wait(tfull0 + 8 * acc, acc_phase, &s_abort) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) {
+          s_abort = 1;
+          atomicOr(args.status, kDevErrTimeout);
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
+      const int feat = f * kTileFeat + feat_local;
+      for (int c = 0; c < kTileRows && c < t.rows; c += 16) {
+        float g[16];
+        tmem_ld16(tbase + c, g);
+        if (kW13) {
+          float u[16];
+          tmem_ld16(tbase + kTileRows + c, u);
+          tmem_wait_ld();
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.rows) {
+              const int row = t.row0 + j;
+              bool real = true;
+              if (!args.identity_T) {
+                const int r = args.sorted_route_ids[row];
+                real = r >= 0 && r < args.num_routes;
+              }
+              const float x = g[jj];
+              const float v = real ? (x / (1.0f + expf(-x))) * u[jj] : 0.0f;
+              out[(size_t)row * args.out_ld + feat] = __float2bfloat16_rn(v);
+            }
+          }
+        } else {
+          tmem_wait_ld();
+          float* out = reinterpret_cast<float*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.rows) out[(size_t)(t.row0 + j) * args.out_ld + feat] = g[jj];
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <bool kW13>
+void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a, int max_tiles,
+            int num_sms, cudaStream_t s) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaFuncSetAttribute(expert_gemm_kernel<kW13>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)GemmCfg<kW13>::kSmemBytes);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const long long items = (long long)max_tiles * a.n_feat_tiles;
+  if (items <= 0) return;
+  const int grid = (int)(items < num_sms ? items : num_sms);
+  expert_gemm_kernel<kW13><<<grid, kThreads, GemmCfg<kW13>::kSmemBytes, s>>>(w_map, x_map, a);
+}
+
+}  // namespace
+
+bool gemm_smem_ok() {
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return optin >= (int)GemmCfg<true>::kSmemBytes && optin >= (int)GemmCfg<false>::kSmemBytes;
+}
+
+void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
+                     int max_tiles, int num_sms, cudaStream_t s) {
+  launch<true>(w_map, x_map, a, max_tiles, num_sms, s);
+}
+
+void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
+                    int max_tiles, int num_sms, cudaStream_t s) {
+  launch<false>(w_map, x_map, a, max_tiles, num_sms, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,74 @@
+// Internal launchers of the MoE layer kernels (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// Status word bits (mirrors include/moe_api.h).
+constexpr int kDevErrExpertRange = 0x1;
+constexpr int kDevErrTimeout = 0x2;
+constexpr int kDevErrBadBlocks = 0x4;
+
+// Rows of one grouped-GEMM token tile (the N of every tcgen05 MMA).  Fixed
+// for every layer and every T: one tile shape, one K order.
+constexpr int kTileRows = 128;
+// Output features of one grouped-GEMM tile (the M of every MMA).
+constexpr int kTileFeat = 128;
+// Router reduction chunk (elements of H summed in order before combining).
+constexpr int kRouterChunk = 256;
+// Routes handled by one CTA of the dispatch count/scatter kernels.
+constexpr int kDispatchTile = 1024;
+
+struct GemmTile {
+  int32_t expert;
+  int32_t row0;
+  int32_t rows;
+  int32_t pad;
+};
+
+// ---- router
+void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
+                          int T, int H, int N, cudaStream_t s);
+void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,
+                       cudaStream_t s);
+
+// ---- dispatch / alignment
+void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,
+                     uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                     int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                     int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
+                     int32_t* seg_off, int* status, cudaStream_t s);
+void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
+                        int64_t max_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles,
+                        int* status, cudaStream_t s);
+
+// ---- grouped expert GEMMs (tcgen05)
+struct GemmArgs {
+  int K;               // reduction length (H for W13, I for W2)
+  int n_feat_tiles;    // output features / kTileFeat (I for W13, H for W2)
+  int w_rows_per_e;    // rows of one expert in the 2-D weight map (= K)
+  int up_col;          // column offset of the "up" half in W13 (= I)
+  const GemmTile* tiles;     // routed mode: tile list on the device
+  const int32_t* num_tiles;  // routed mode: device count
+  int identity_T;            // identity mode (shared expert): rows 0..T-1, else 0
+  const int32_t* sorted_route_ids;  // routed W13: row -> route id
+  int top_k;
+  int num_routes;      // R = T*k (the sentinel)
+  void* out;           // W13: bf16 a [rows, I]; W2: fp32 y [rows, H]
+  int out_ld;          // elements per output row
+  int* status;
+};
+bool gemm_smem_ok();
+void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
+                     int max_tiles, int num_sms, cudaStream_t s);
+void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
+                    int max_tiles, int num_sms, cudaStream_t s);
+
+// ---- combine
+void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,
+                    const int32_t* route_pos, const float* y_perm, const float* y_shared,
+                    uint16_t* out, int T, int H, int k, int64_t max_rows, cudaStream_t s);
+
+}  // namespace moe

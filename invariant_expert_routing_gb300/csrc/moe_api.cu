@@ -1,0 +1,486 @@
+// C ABI of the batch-invariant MoE layer (include/moe_api.h): argument
+// validation, workspace carving, TMA tensor maps and the launch sequence.
+#include "moe_api.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace {
+
+using moe::GemmTile;
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------- config
+moe_status check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->hidden <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->intermediate <= 0 ||
+      c->block_size <= 0 || c->shared_intermediate < 0 || std::isnan(c->capacity_factor))
+    return MOE_ERR_INVALID_ARG;
+  if (c->hidden % 128 || c->hidden > 32768) return MOE_ERR_UNSUPPORTED;
+  if (c->intermediate % 128 || c->intermediate > 65536) return MOE_ERR_UNSUPPORTED;
+  if (c->shared_intermediate % 128 || c->shared_intermediate > 65536) return MOE_ERR_UNSUPPORTED;
+  if (c->num_experts > 256) return MOE_ERR_UNSUPPORTED;
+  if (c->top_k > c->num_experts || c->top_k > 16) return MOE_ERR_UNSUPPORTED;
+  if (c->block_size % 8 || c->block_size > 128 || 128 % c->block_size) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_T(const moe_config* c, int32_t T) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > (1 << 20) || (int64_t)T * c->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int32_t capacity_of(const moe_config* c, int32_t T) {
+  if (!(c->capacity_factor > 0.0f)) return -1;
+  return (int32_t)std::ceil((double)c->capacity_factor * (double)T * (double)c->top_k /
+                            (double)c->num_experts);
+}
+
+int64_t max_rows_of(const moe_config* c, int32_t T) {
+  return (int64_t)T * c->top_k + (int64_t)c->num_experts * (c->block_size - 1);
+}
+int64_t max_blocks_of(const moe_config* c, int32_t T) {
+  return (int64_t)T * c->top_k / c->block_size + c->num_experts;
+}
+int64_t max_gemm_tiles_of(const moe_config* c, int32_t T) {
+  return (max_rows_of(c, T) + moe::kTileRows - 1) / moe::kTileRows + c->num_experts;
+}
+
+// ----------------------------------------------------------------- workspace
+// Regions, each 256-byte aligned; the status word is always at offset 0.
+struct Layout {
+  size_t status, logits, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
+      num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, a, y, a_sh, y_sh, h_stage, out_stage,
+      total;
+};
+
+Layout layout_of(const moe_config* c, int32_t T) {
+  const size_t R = (size_t)T * c->top_k, N = c->num_experts, H = c->hidden;
+  const size_t rows = (size_t)max_rows_of(c, T);
+  const size_t dtiles = (R + moe::kDispatchTile - 1) / moe::kDispatchTile;
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  L.status = take(sizeof(int32_t));
+  L.logits = take(sizeof(float) * T * N);
+  L.topk = take(sizeof(int32_t) * R);
+  L.gates = take(sizeof(float) * R);
+  L.kept = take(R);
+  L.pos = take(sizeof(int32_t) * R);
+  L.rank = take(sizeof(int32_t) * R);
+  L.tile_count = take(sizeof(int32_t) * dtiles * N);
+  L.seg_off = take(sizeof(int32_t) * N);
+  L.sorted = take(sizeof(int32_t) * rows);
+  L.blocks = take(sizeof(int32_t) * (size_t)max_blocks_of(c, T));
+  L.num_padded = take(sizeof(int32_t));
+  L.counts = take(sizeof(int32_t) * N);
+  L.dropped = take(sizeof(int32_t));
+  L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T));
+  L.num_gemm_tiles = take(sizeof(int32_t));
+  // a keeps kTileRows rows of slack so every W2 tile load stays inside it
+  L.a = take(sizeof(uint16_t) * (rows + moe::kTileRows) * c->intermediate);
+  L.y = take(sizeof(float) * rows * H);
+  const size_t Is = c->shared_intermediate;
+  L.a_sh = take(Is ? sizeof(uint16_t) * ((size_t)T + moe::kTileRows) * Is : 0);
+  L.y_sh = take(Is ? sizeof(float) * (size_t)T * H : 0);
+  L.h_stage = take(sizeof(uint16_t) * (size_t)T * H);
+  L.out_stage = take(sizeof(uint16_t) * (size_t)T * H);
+  L.total = off;
+  return L;
+}
+
+template <class P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+moe_status check_ws(const moe_config* c, int32_t T, const void* ws, size_t ws_bytes) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < layout_of(c, T).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// ----------------------------------------------------------------- device info / TMA maps
+int num_sms() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 2-D map with 128-byte swizzle: `inner` contiguous elements per row,
+// `outer` rows, box box_inner x box_outer.
+bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+            uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn || inner == 0 || outer == 0) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status last_cuda() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ----------------------------------------------------------------- stages
+moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* wg,
+                      const float* bias, int32_t* idx, float* gates, float* logits, cudaStream_t s) {
+  moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
+  moe::launch_topk_gates(logits, idx, gates, T, c->num_experts, c->top_k, s);
+  return last_cuda();
+}
+
+moe_status dispatch_impl(const moe_config* c, int32_t T, const int32_t* idx, uint8_t* kept,
+                         int32_t* pos, int32_t* sorted, int32_t* blocks, int32_t* num_padded,
+                         int32_t* counts, int32_t* dropped, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  moe::launch_dispatch(idx, T, c->num_experts, c->top_k, c->block_size, capacity_of(c, T), kept, pos,
+                       sorted, blocks, num_padded, counts, dropped, at<int32_t>(ws, L.rank),
+                       at<int32_t>(ws, L.tile_count), at<int32_t>(ws, L.seg_off), at<int>(ws, L.status), s);
+  return last_cuda();
+}
+
+moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
+                    const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
+                    const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
+                    void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = c->top_k;
+  const int64_t rows = max_rows_of(c, T);
+  const int max_tiles = (int)max_gemm_tiles_of(c, T);
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  int* status = at<int>(ws, L.status);
+  GemmTile* tiles = at<GemmTile>(ws, L.gemm_tiles);
+  int32_t* ntiles = at<int32_t>(ws, L.num_gemm_tiles);
+  uint16_t* a = at<uint16_t>(ws, L.a);
+
+  moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, tiles, ntiles, max_tiles, status, s);
+
+  CUtensorMap m_w13, m_h, m_w2, m_a;
+  if (!map_2d(&m_w13, w13, 2ull * I, (uint64_t)N * H, 64, 64) ||
+      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, 1) ||
+      !map_2d(&m_w2, w2, (uint64_t)H, (uint64_t)N * I, 64, 64) ||
+      !map_2d(&m_a, a, (uint64_t)I, (uint64_t)(rows + moe::kTileRows), 64, moe::kTileRows))
+    return MOE_ERR_CUDA;
+
+  moe::GemmArgs g13{};
+  g13.K = H;
+  g13.n_feat_tiles = I / moe::kTileFeat;
+  g13.w_rows_per_e = H;
+  g13.up_col = I;
+  g13.tiles = tiles;
+  g13.num_tiles = ntiles;
+  g13.identity_T = 0;
+  g13.sorted_route_ids = sorted;
+  g13.top_k = k;
+  g13.num_routes = T * k;
+  g13.out = a;
+  g13.out_ld = I;
+  g13.status = status;
+  moe::launch_w13_gemm(m_w13, m_h, g13, max_tiles, sms, s);
+
+  moe::GemmArgs g2 = g13;
+  g2.K = I;
+  g2.n_feat_tiles = H / moe::kTileFeat;
+  g2.w_rows_per_e = I;
+  g2.up_col = 0;
+  g2.out = y_perm;
+  g2.out_ld = H;
+  moe::launch_w2_gemm(m_w2, m_a, g2, max_tiles, sms, s);
+
+  const int Is = c->shared_intermediate;
+  if (Is > 0) {
+    uint16_t* ash = at<uint16_t>(ws, L.a_sh);
+    CUtensorMap m_w13s, m_w2s, m_ash;
+    if (!map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
+        !map_2d(&m_w2s, w2s, (uint64_t)H, (uint64_t)Is, 64, 64) ||
+        !map_2d(&m_ash, ash, (uint64_t)Is, (uint64_t)T + moe::kTileRows, 64, moe::kTileRows))
+      return MOE_ERR_CUDA;
+    const int sh_tiles = (T + moe::kTileRows - 1) / moe::kTileRows;
+    moe::GemmArgs s13{};
+    s13.K = H;
+    s13.n_feat_tiles = Is / moe::kTileFeat;
+    s13.w_rows_per_e = H;
+    s13.up_col = Is;
+    s13.identity_T = T;
+    s13.top_k = k;
+    s13.num_routes = T * k;
+    s13.out = ash;
+    s13.out_ld = Is;
+    s13.status = status;
+    moe::launch_w13_gemm(m_w13s, m_h, s13, sh_tiles, sms, s);
+    moe::GemmArgs s2 = s13;
+    s2.K = Is;
+    s2.n_feat_tiles = H / moe::kTileFeat;
+    s2.w_rows_per_e = Is;
+    s2.up_col = 0;
+    s2.out = y_shared;
+    s2.out_ld = H;
+    moe::launch_w2_gemm(m_w2s, m_ash, s2, sh_tiles, sms, s);
+  }
+  return last_cuda();
+}
+
+moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* wg,
+                        const float* bias, const uint16_t* w13, const uint16_t* w2, const uint16_t* w13s,
+                        const uint16_t* w2s, uint16_t* out, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  int32_t* idx = at<int32_t>(ws, L.topk);
+  float* gates = at<float>(ws, L.gates);
+  uint8_t* kept = at<uint8_t>(ws, L.kept);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  int32_t* sorted = at<int32_t>(ws, L.sorted);
+  int32_t* blocks = at<int32_t>(ws, L.blocks);
+  int32_t* num_padded = at<int32_t>(ws, L.num_padded);
+  float* y = at<float>(ws, L.y);
+  float* ysh = c->shared_intermediate ? at<float>(ws, L.y_sh) : nullptr;
+  moe_status st = route_impl(c, T, h, wg, bias, idx, gates, at<float>(ws, L.logits), s);
+  if (st != MOE_OK) return st;
+  st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, at<int32_t>(ws, L.counts),
+                     at<int32_t>(ws, L.dropped), ws, s);
+  if (st != MOE_OK) return st;
+  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s);
+  if (st != MOE_OK) return st;
+  moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, c->top_k, max_rows_of(c, T), s);
+  return last_cuda();
+}
+
+#define MOE_TRY(x)                   \
+  do {                               \
+    const moe_status _st = (x);      \
+    if (_st != MOE_OK) return _st;   \
+  } while (0)
+
+moe_status need(const void* p) { return (p && aligned16(p)) ? MOE_OK : MOE_ERR_INVALID_ARG; }
+moe_status opt(const void* p) { return (!p || aligned16(p)) ? MOE_OK : MOE_ERR_INVALID_ARG; }
+
+moe_status check_shared(const moe_config* c, const void* w13s, const void* w2s) {
+  if (c->shared_intermediate > 0) {
+    MOE_TRY(need(w13s));
+    MOE_TRY(need(w2s));
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device status word set";
+  }
+  return "unknown status";
+}
+
+moe_status moe_check_config(const moe_config* cfg) { return check_cfg(cfg); }
+
+int32_t moe_capacity(const moe_config* cfg, int32_t T) {
+  if (check_cfg(cfg) != MOE_OK || T < 0) return -1;
+  return capacity_of(cfg, T);
+}
+
+int64_t moe_max_padded_rows(const moe_config* cfg, int32_t T) {
+  if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
+  return max_rows_of(cfg, T);
+}
+
+int64_t moe_max_blocks(const moe_config* cfg, int32_t T) {
+  if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
+  return max_blocks_of(cfg, T);
+}
+
+size_t moe_workspace_bytes(const moe_config* cfg, int32_t max_tokens) {
+  if (check_cfg(cfg) != MOE_OK || check_T(cfg, max_tokens) != MOE_OK) return 0;
+  return layout_of(cfg, max_tokens).total;
+}
+
+moe_status moe_route(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w_gate,
+                     const float* router_bias, int32_t* topk_idx, float* topk_gate, float* logits_out,
+                     void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(opt(router_bias));
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(topk_gate));
+  MOE_TRY(opt(logits_out));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  float* logits = logits_out ? logits_out : at<float>(ws, layout_of(cfg, T).logits);
+  return route_impl(cfg, T, h, w_gate, router_bias, topk_idx, topk_gate, logits,
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dispatch_align(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                              uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                              int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                              int32_t* num_dropped, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(route_kept));
+  MOE_TRY(need(route_pos));
+  MOE_TRY(need(sorted_route_ids));
+  MOE_TRY(need(block_expert));
+  MOE_TRY(need(num_padded));
+  MOE_TRY(need(expert_counts));
+  MOE_TRY(need(num_dropped));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  return dispatch_impl(cfg, T, topk_idx, route_kept, route_pos, sorted_route_ids, block_expert,
+                       num_padded, expert_counts, num_dropped, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w13,
+                          const uint16_t* w2, const uint16_t* w13_shared, const uint16_t* w2_shared,
+                          const int32_t* sorted_route_ids, const int32_t* block_expert,
+                          const int32_t* num_padded, float* y_perm, float* y_shared, void* ws,
+                          size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w13));
+  MOE_TRY(need(w2));
+  MOE_TRY(check_shared(cfg, w13_shared, w2_shared));
+  if (cfg->shared_intermediate > 0) MOE_TRY(need(y_shared));
+  MOE_TRY(need(sorted_route_ids));
+  MOE_TRY(need(block_expert));
+  MOE_TRY(need(num_padded));
+  MOE_TRY(need(y_perm));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  if (!moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
+  return ffn_impl(cfg, T, h, w13, w2, w13_shared, w2_shared, sorted_route_ids, block_expert, num_padded,
+                  y_perm, cfg->shared_intermediate > 0 ? y_shared : nullptr, ws,
+                  static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_config* cfg, int32_t T, const uint16_t* h, const float* topk_gate,
+                       const uint8_t* route_kept, const int32_t* route_pos, const float* y_perm,
+                       const float* y_shared, uint16_t* out, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(h));
+  MOE_TRY(need(topk_gate));
+  MOE_TRY(need(route_kept));
+  MOE_TRY(need(route_pos));
+  MOE_TRY(need(y_perm));
+  MOE_TRY(opt(y_shared));
+  MOE_TRY(need(out));
+  moe::launch_combine(h, topk_gate, route_kept, route_pos, y_perm, y_shared, out, T, cfg->hidden,
+                      cfg->top_k, max_rows_of(cfg, T), static_cast<cudaStream_t>(stream));
+  return last_cuda();
+}
+
+moe_status moe_forward(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w_gate,
+                       const float* router_bias, const uint16_t* w13, const uint16_t* w2,
+                       const uint16_t* w13_shared, const uint16_t* w2_shared, uint16_t* out, void* ws,
+                       size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(opt(router_bias));
+  MOE_TRY(need(w13));
+  MOE_TRY(need(w2));
+  MOE_TRY(check_shared(cfg, w13_shared, w2_shared));
+  MOE_TRY(need(out));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  if (!moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
+  return forward_impl(cfg, T, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_hostio(const moe_config* cfg, int32_t T, const uint16_t* h_host,
+                              const uint16_t* w_gate, const float* router_bias, const uint16_t* w13,
+                              const uint16_t* w2, const uint16_t* w13_shared, const uint16_t* w2_shared,
+                              uint16_t* out_host, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  if (!h_host || !out_host) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need(w_gate));
+  MOE_TRY(opt(router_bias));
+  MOE_TRY(need(w13));
+  MOE_TRY(need(w2));
+  MOE_TRY(check_shared(cfg, w13_shared, w2_shared));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  if (!moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
+  const Layout L = layout_of(cfg, T);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t* h = at<uint16_t>(ws, L.h_stage);
+  uint16_t* out = at<uint16_t>(ws, L.out_stage);
+  const size_t bytes = sizeof(uint16_t) * (size_t)T * cfg->hidden;
+  if (cudaMemcpyAsync(h, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_TRY(forward_impl(cfg, T, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws, s));
+  if (cudaMemcpyAsync(out_host, out, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(const void* ws, int32_t* status_out, void* stream) {
+  if (!ws || !aligned16(ws) || !status_out) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status_out = v;
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status moe_clear_device_status(void* ws, void* stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+}  // extern "C"
