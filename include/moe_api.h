@@ -184,6 +184,23 @@ moe_status moe_forward_hostio(const moe_config* cfg, int32_t T, const uint16_t* 
                               const uint16_t* w13_shared, const uint16_t* w2_shared,
                               uint16_t* out_host, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_forward that also records caller-created CUDA events (cudaEvent_t
+ * handles, at least n_events = 8) on `stream` at the stage boundaries:
+ *   events[0] before the router          events[4] after the W13 GEMM
+ *   events[1] after the router           events[5] after the W2 GEMM
+ *   events[2] after dispatch/alignment   events[6] after the shared expert
+ *   events[3] after the GEMM tile list   events[7] after the combine
+ * so the caller can read per-kernel device times (cudaEventElapsedTime)
+ * without extra synchronisation.  Same computation and bits as moe_forward. */
+moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h,
+                             const uint16_t* w_gate, const float* router_bias, const uint16_t* w13,
+                             const uint16_t* w2, const uint16_t* w13_shared,
+                             const uint16_t* w2_shared, uint16_t* out, void* ws, size_t ws_bytes,
+                             void* const* events, int32_t n_events, void* stream);
+
+/* Number of kernel launches one moe_forward makes for this configuration. */
+int32_t moe_forward_launch_count(const moe_config* cfg);
+
 /* Reads the device status word of `ws` (synchronises `stream`). */
 moe_status moe_get_device_status(const void* ws, int32_t* status_out, void* stream);
 

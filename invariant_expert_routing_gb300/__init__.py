@@ -61,6 +61,8 @@ _SIGS = {
     "moe_combine": ([_cfgp, _i32] + [_vp] * 7 + [_vp], ctypes.c_int),
     "moe_forward": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_forward_hostio": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_forward_timed": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp, _i32, _vp], ctypes.c_int),
+    "moe_forward_launch_count": ([_cfgp], _i32),
     "moe_get_device_status": ([_vp, ctypes.POINTER(_i32), _vp], ctypes.c_int),
     "moe_clear_device_status": ([_vp, _vp], ctypes.c_int),
 }
@@ -178,6 +180,21 @@ def moe_forward_hostio(cfg, h_host, w_gate, router_bias, w13, w2, w13_shared, w2
         ctypes.byref(_cfg(cfg)), T, _ptr(h_host), _ptr(w_gate), _ptr(router_bias), _ptr(w13),
         _ptr(w2), _ptr(w13_shared), _ptr(w2_shared), _ptr(out_host), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def moe_forward_timed(cfg, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws,
+                      events, stream=None):
+    """moe_forward recording 8 torch.cuda.Event objects at the stage boundaries."""
+    T = h.shape[0]
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check("moe_forward_timed", _lib.moe_forward_timed(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(router_bias), _ptr(w13),
+        _ptr(w2), _ptr(w13_shared), _ptr(w2_shared), _ptr(out), _ptr(ws), ws.numel(), arr,
+        len(events), _stream(stream)))
+
+
+def moe_forward_launch_count(cfg) -> int:
+    return int(_lib.moe_forward_launch_count(ctypes.byref(_cfg(cfg))))
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -179,10 +179,17 @@ moe_status dispatch_impl(const moe_config* c, int32_t T, const int32_t* idx, uin
   return last_cuda();
 }
 
+struct Marks;
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
-                    void* ws, cudaStream_t s) {
+                    void* ws, cudaStream_t s, const Marks* mk = nullptr);
+void mark(const Marks* mk, int i);
+
+moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
+                    const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
+                    const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
+                    void* ws, cudaStream_t s, const Marks* mk) {
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = c->top_k;
   const int64_t rows = max_rows_of(c, T);
@@ -195,6 +202,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* a = at<uint16_t>(ws, L.a);
 
   moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, tiles, ntiles, max_tiles, status, s);
+  mark(mk, 3);
 
   CUtensorMap m_w13, m_h, m_w2, m_a;
   if (!map_2d(&m_w13, w13, 2ull * I, (uint64_t)N * H, 64, 64) ||
@@ -218,6 +226,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.out_ld = I;
   g13.status = status;
   moe::launch_w13_gemm(m_w13, m_h, g13, max_tiles, sms, s);
+  mark(mk, 4);
 
   moe::GemmArgs g2 = g13;
   g2.K = I;
@@ -227,6 +236,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.out = y_perm;
   g2.out_ld = H;
   moe::launch_w2_gemm(m_w2, m_a, g2, max_tiles, sms, s);
+  mark(mk, 5);
 
   const int Is = c->shared_intermediate;
   if (Is > 0) {
@@ -261,9 +271,24 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   return last_cuda();
 }
 
+// Records events[i] on s if events are given (stage boundary i).
+struct Marks {
+  void* const* ev;
+  cudaStream_t s;
+  void at(int i) const {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+  }
+};
+
+void mark(const Marks* mk, int i) {
+  if (mk) mk->at(i);
+}
+
 moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* wg,
                         const float* bias, const uint16_t* w13, const uint16_t* w2, const uint16_t* w13s,
-                        const uint16_t* w2s, uint16_t* out, void* ws, cudaStream_t s) {
+                        const uint16_t* w2s, uint16_t* out, void* ws, cudaStream_t s,
+                        void* const* events = nullptr) {
+  const Marks mk{events, s};
   const Layout L = layout_of(c, T);
   int32_t* idx = at<int32_t>(ws, L.topk);
   float* gates = at<float>(ws, L.gates);
@@ -274,14 +299,19 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   int32_t* num_padded = at<int32_t>(ws, L.num_padded);
   float* y = at<float>(ws, L.y);
   float* ysh = c->shared_intermediate ? at<float>(ws, L.y_sh) : nullptr;
+  mk.at(0);
   moe_status st = route_impl(c, T, h, wg, bias, idx, gates, at<float>(ws, L.logits), s);
   if (st != MOE_OK) return st;
+  mk.at(1);
   st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, at<int32_t>(ws, L.counts),
                      at<int32_t>(ws, L.dropped), ws, s);
   if (st != MOE_OK) return st;
-  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s);
+  mk.at(2);
+  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk);
   if (st != MOE_OK) return st;
+  mk.at(6);
   moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, c->top_k, max_rows_of(c, T), s);
+  mk.at(7);
   return last_cuda();
 }
 
@@ -438,6 +468,36 @@ moe_status moe_forward(const moe_config* cfg, int32_t T, const uint16_t* h, cons
   if (!moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
   return forward_impl(cfg, T, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws,
                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h,
+                             const uint16_t* w_gate, const float* router_bias, const uint16_t* w13,
+                             const uint16_t* w2, const uint16_t* w13_shared, const uint16_t* w2_shared,
+                             uint16_t* out, void* ws, size_t ws_bytes, void* const* events,
+                             int32_t n_events, void* stream) {
+  if (!events || n_events < 8) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 8; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(opt(router_bias));
+  MOE_TRY(need(w13));
+  MOE_TRY(need(w2));
+  MOE_TRY(check_shared(cfg, w13_shared, w2_shared));
+  MOE_TRY(need(out));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  if (!moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
+  return forward_impl(cfg, T, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws,
+                      static_cast<cudaStream_t>(stream), events);
+}
+
+int32_t moe_forward_launch_count(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  // router 2 + dispatch 3 + tile list 1 + W13 + W2 + combine 1 (+ shared W13, W2)
+  return 9 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }
 
 moe_status moe_forward_hostio(const moe_config* cfg, int32_t T, const uint16_t* h_host,

@@ -17,8 +17,8 @@ HEADER = os.path.join(ROOT, "include", "moe_api.h")
 def moe():
     lib = os.path.join(ROOT, "invariant_expert_routing_gb300", "libmoe_gb300.so")
     if not os.path.exists(lib):
-        from invariant_expert_routing_gb300 import _build
-        _build.build()
+        import __graft_entry__
+        __graft_entry__._build_module().build()
     import invariant_expert_routing_gb300 as m
     return m
 
