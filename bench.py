@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Benchmark of the batch-invariant MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+One step = one moe_forward (router, top-k, capacity dispatch, stable padded
+alignment, grouped SwiGLU expert GEMMs, combine) over one batch of synthetic
+tokens of the Mixtral-like layer (H 4096, 8 experts, top-2, I 14336, block
+64, T 4096), inputs resident in HBM.  Prints one JSON line: routed tokens/s
+for the whole job, the roofline of the dominant kernel, the end-to-end rate
+through the host-buffer entry point, the CPU oracle timed on the host cores,
+and the SM clocks seen during the timed region.
+
+Under torchrun (N > 1) every rank runs its own shard of tokens (a different
+token seed) against replicated weights: no collective on the data path
+(weak scaling); only the barrier and the max-over-ranks time use
+torch.distributed.
+
+--impl reference times the CPU oracle (the reference arm of this build) on
+the host cores, rank 0 only, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "mix"
+TOKENS = 4096
+METRIC = "routed tokens/sec per MoE layer"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_seed(rank: int) -> int:
+    """Token seed of a rank's shard (rank 0 holds the reference batch, seed 0)."""
+    return 0 if rank == 0 else 1000003 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- roofline inputs
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("expert_gemm.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "invariant_expert_routing_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload_tag: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    from the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_tag}.md")
+    if not os.path.exists(path):
+        return None, "no ncu summary"
+    text = open(path).read()
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_b:
+        return None, "summary lacks dram bytes"
+    if not m_sha or m_sha.group(1) != kernel_source_sha():
+        return None, "kernel changed since the ncu capture"
+    return float(m_b.group(1)), os.path.relpath(path, ROOT)
+
+
+# --------------------------------------------------------------------------- clocks
+def visible_gpu_index(local: int):
+    """nvidia-smi index of this process's GPU when CUDA_VISIBLE_DEVICES lists
+    plain indices, else None (query every visible GPU)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis is None:
+        return local
+    parts = [p.strip() for p in vis.split(",") if p.strip()]
+    if local < len(parts) and parts[local].isdigit():
+        return int(parts[local])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms; keeps the ones inside [t0, t1]."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            sel = [] if self.gpu is None else [f"--id={self.gpu}"]
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        in_region = len(rows)
+        if not rows and self.samples:  # region shorter than one sample period
+            mid = 0.5 * (t0 + t1)
+            rows = [min(self.samples, key=lambda x: abs(x[0] - mid))[1]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": in_region}
+
+
+# --------------------------------------------------------------------------- work accounting
+def algorithmic_work(wl, T, kept_routes: int, touched_experts: int):
+    """flops and bytes the method must do (not padded or intermediate work)."""
+    H, I, N, Is = wl.hidden, wl.intermediate, wl.num_experts, wl.shared_intermediate
+    flops = 2.0 * T * H * N + 6.0 * H * I * kept_routes + 6.0 * H * Is * T
+    bytes_ = 6.0 * H * I * touched_experts + 6.0 * H * Is + 2.0 * H * N + 4.0 * T * H
+    return flops, bytes_
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    import numpy as np
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synth import workloads as W
+    import oracle
+    wl = W.WORKLOADS[WORKLOAD]
+    T = TOKENS
+    h_all = W.make_h(wl, T, seed=0)
+    wg, bias = W.make_router(wl)
+    cores = os.cpu_count() or 1
+    w13, w2 = W.make_experts(wl)
+    steps, warm = args.steps, args.warmup
+    # size the per-step sample so that the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    _oracle_tokens(wl, h_all, wg, bias, w13, w2, np.arange(1))
+    per_tok = max(time.perf_counter() - t0, 1e-3)
+    S = int(max(1, min(64, 120.0 / ((steps + warm) * per_tok))))
+    rng = np.random.default_rng(7)
+    for _ in range(warm):
+        _oracle_tokens(wl, h_all, wg, bias, w13, w2, np.sort(rng.choice(T, S, replace=False)))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _oracle_tokens(wl, h_all, wg, bias, w13, w2, np.sort(rng.choice(T, S, replace=False)))
+    el = time.perf_counter() - t0
+    value = S * steps / el
+    sample = (f"{S} tokens per step drawn from the T={T} batch; router, top-k, FFN of their "
+              f"{S * wl.top_k} routes and combine, fp64 oracle with {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * el / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl, T, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def _oracle_tokens(wl, h_all, wg, bias, w13, w2, tokens, nthreads=0):
+    import numpy as np
+    import oracle
+    h = h_all[tokens]
+    l = oracle.router_logits(h, wg, bias, nthreads=nthreads)
+    idx, gates = oracle.select_topk(l, wl.top_k)
+    n = len(tokens)
+    toks = np.repeat(np.arange(n), wl.top_k).astype(np.int32)
+    y = oracle.expert_rows(toks, idx.reshape(-1), h, w13, w2, nthreads)
+    kept = np.ones(idx.size, np.uint8)
+    return oracle.combine_rows(np.arange(n), h, gates, kept, y.reshape(n, wl.top_k, wl.hidden))
+
+
+def workload_config(wl, T, world):
+    return {"workload": (f"mixtral-like MoE layer forward: hidden {wl.hidden}, {wl.num_experts} "
+                         f"experts, top-{wl.top_k}, SwiGLU intermediate {wl.intermediate}, "
+                         f"block {wl.block_size}, T={T} tokens per GPU"),
+            "tokens_per_gpu": T, "global_batch": T * world, "seed": 0,
+            "l2": "inputs larger than L2: 2.8 GB of expert weights are read every step",
+            "parallelism": "single GPU" if world == 1 else f"{world} token-shard replicas, no collective"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+
+    import invariant_expert_routing_gb300 as moe
+    from synth import workloads as W
+    from tests.gpu_util import dev, dev_bf16, host_bf16
+
+    wl = W.WORKLOADS[WORKLOAD]
+    T = TOKENS
+    cfg = wl.cfg
+    wg, bias = W.make_router(wl)
+    wg_d = dev_bf16(wg, device)
+    bias_d = None if bias is None else dev(bias, device)
+    w13_d, w2_d, w13s_d, w2s_d = W.make_experts_device(wl, 0, device)
+    h = W.make_h(wl, T, seed=shard_seed(rank))
+    h_d = dev_bf16(h, device)
+    out_d = torch.empty((T, wl.hidden), dtype=torch.bfloat16, device=device)
+    ws = moe.workspace(cfg, T, device)
+    moe.moe_clear_device_status(ws)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        moe.moe_forward(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_d, ws)
+
+    if args.profile_run:
+        # a short fixed run for profilers: warm-up forwards, then `steps` forwards
+        for _ in range(args.warmup + args.steps):
+            fwd()
+        torch.cuda.synchronize()
+        st = moe.moe_get_device_status(ws)
+        print(json.dumps({"profile_run": True, "forwards": args.warmup + args.steps, "status": st}))
+        return 0 if st == 0 else 1
+
+    for _ in range(max(args.warmup, 3)):
+        fwd()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    # ---- timed region: K forwards, stage events recorded inside each one
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(visible_gpu_index(local))
+    clocks.start()
+    time.sleep(0.6)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        moe.moe_forward_timed(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_d, ws, ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    time.sleep(0.3)
+    clocks.stop()
+    ms_total = start.elapsed_time(end)
+    ms_total = reduce_max(ms_total, device)
+    ms_step = ms_total / K
+    stage = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(7)] for i in range(K)])
+    stage_ms = stage.mean(axis=0)
+    names = ["router", "dispatch_align", "gemm_tile_list", "w13_gemm", "w2_gemm", "shared_expert",
+             "combine"]
+    if moe.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    # ---- what the batch did (for the algorithmic work)
+    idx = torch.empty((T, wl.top_k), dtype=torch.int32, device=device)
+    gates = torch.empty((T, wl.top_k), dtype=torch.float32, device=device)
+    moe.moe_route(cfg, h_d, wg_d, bias_d, idx, gates, None, ws)
+    idx_h = idx.cpu().numpy()
+    kept_routes = T * wl.top_k  # no capacity limit in this workload
+    touched = len(np.unique(idx_h))
+    flops, bytes_ = algorithmic_work(wl, T, kept_routes, touched)
+
+    peaks, peak_src = load_peaks()
+    i_w13 = names.index("w13_gemm")
+    w13_flops = 4.0 * wl.hidden * wl.intermediate * kept_routes
+    w13_s = stage_ms[i_w13] * 1e-3
+    achieved = w13_flops / w13_s / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic, traffic_src = profiled_traffic("expert_w13_gemm", "mix_T4096")
+    dominant = names[int(np.argmax(stage_ms))]
+
+    value = world * T / (ms_step * 1e-3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded counter-based generator; no checkpoints)",
+            "config": workload_config(wl, T, world),
+            "roofline": {"kernel": "expert_w13_gemm (tcgen05 grouped GEMM + SiLU*up)",
+                         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                         "traffic": traffic, "traffic_source": traffic_src,
+                         "algorithmic_flops_per_launch": w13_flops,
+                         "avg_launch_ms": stage_ms[i_w13], "dominant_stage": dominant},
+            "layer_roofline": {"algorithmic_gflop": flops / 1e9, "algorithmic_gb": bytes_ / 1e9,
+                               "tflops_achieved": flops / (ms_step * 1e-3) / 1e12,
+                               "frac_of_bf16_peak": flops / (ms_step * 1e-3) / 1e12 / peak},
+            "stage_ms": {n: float(v) for n, v in zip(names, stage_ms)},
+            "gpu_launches": moe.moe_forward_launch_count(cfg) * K,
+            "clocks": clocks.summary(t_wall0, t_wall1)}
+
+    # ---- decode-shaped batches of the same layer (secondary lines)
+    sweep = []
+    for Ts in ([] if args.no_sweep else [1, 16, 128]):
+        hs = dev_bf16(W.make_h(wl, Ts, seed=shard_seed(rank) + 17), device)
+        outs = torch.empty((Ts, wl.hidden), dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            moe.moe_forward(cfg, hs, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, outs, ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 50
+        e0.record(stream)
+        for _ in range(n):
+            moe.moe_forward(cfg, hs, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, outs, ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        moe.moe_route(cfg, hs, wg_d, bias_d, idx[:Ts], gates[:Ts], None, ws)
+        tch = len(np.unique(idx[:Ts].cpu().numpy()))
+        f_s, b_s = algorithmic_work(wl, Ts, Ts * wl.top_k, tch)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        sweep.append({"T": Ts, "ms": ms, "tokens_per_s": Ts / (ms * 1e-3), "bound": "hbm",
+                      "achieved_gbs": b_s / (ms * 1e-3) / 1e9, "peak_gbs": hbm,
+                      "frac": b_s / (ms * 1e-3) / 1e9 / hbm, "touched_experts": tch})
+    if sweep:
+        line["decode_sweep"] = sweep
+
+    # ---- end to end through the host-buffer entry point
+    h_host = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((T, wl.hidden), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        moe.moe_forward_hostio(cfg, h_host, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_host, ws)
+    torch.cuda.synchronize()
+    Ke = max(5, min(K, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(Ke):
+        moe.moe_forward_hostio(cfg, h_host, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_host, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = reduce_max(e0.elapsed_time(e1) / Ke, device)
+    line["e2e"] = {"value": world * T / (ms_e2e * 1e-3), "unit": UNIT,
+                   "h2d_bytes_per_step": T * wl.hidden * 2, "d2h_bytes_per_step": T * wl.hidden * 2,
+                   "ms_per_step": ms_e2e, "entry_point": "moe_forward_hostio (pinned host buffers)"}
+    e2e_out = host_bf16(out_host)
+    fwd()
+    torch.cuda.synchronize()
+    if not (host_bf16(out_d) == e2e_out).all():
+        raise RuntimeError("host-buffer path and device path disagree")
+
+    # ---- CPU oracle on the host cores (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, h, wg, bias, host_bf16(out_d))
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def cpu_baseline(wl, h, wg, bias, gpu_out):
+    """The oracle (as it stands) on a bounded sample of the batch; also checks
+    the sampled GPU rows against it."""
+    import numpy as np
+    from synth import workloads as W
+    from tests.checks import check_outputs
+    cores = os.cpu_count() or 1
+    w13, w2 = W.make_experts(wl)
+    rng = np.random.default_rng(123)
+    T = h.shape[0]
+    S = 8
+    toks = np.sort(rng.choice(T, S, replace=False))
+    _oracle_tokens(wl, h, wg, bias, w13, w2, toks[:1])           # warm (page-in)
+    t0 = time.perf_counter()
+    done = 0
+    outs = []
+    while done < 32 and time.perf_counter() - t0 < 20.0:
+        sel = toks if done == 0 else np.sort(rng.choice(T, S, replace=False))
+        o = _oracle_tokens(wl, h, wg, bias, w13, w2, sel)
+        if done == 0:
+            outs = o
+        done += S
+    el = time.perf_counter() - t0
+    err = check_outputs(gpu_out[toks], outs)
+    return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{done} tokens of the T={T} batch in groups of {S} (router, top-k, their "
+                       f"{done * wl.top_k} expert FFN routes in fp64, combine), {el:.1f} s"),
+            "parity_on_sample": {"tokens": S, "max_abs_err": err, "tolerance": "2e-2 + 1e-2*|ref|"}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="only warm-up + steps forwards of the main workload (for ncu)")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.profile_run:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
