@@ -309,6 +309,10 @@ def run_gpu(args):
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for row in ev:        # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(visible_gpu_index(local))
     clocks.start()
     time.sleep(0.6)

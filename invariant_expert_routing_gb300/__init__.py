@@ -184,8 +184,11 @@ def moe_forward_hostio(cfg, h_host, w_gate, router_bias, w13, w2, w13_shared, w2
 
 def moe_forward_timed(cfg, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, out, ws,
                       events, stream=None):
-    """moe_forward recording 8 torch.cuda.Event objects at the stage boundaries."""
+    """moe_forward recording 8 torch.cuda.Event objects at the stage boundaries
+    (each event must have been recorded once, so that torch has created it)."""
     T = h.shape[0]
+    if any(e.cuda_event == 0 for e in events):
+        raise ValueError("record each torch.cuda.Event once before passing it")
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check("moe_forward_timed", _lib.moe_forward_timed(
         ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(router_bias), _ptr(w13),
