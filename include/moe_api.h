@@ -189,7 +189,7 @@ moe_status moe_forward_hostio(const moe_config* cfg, int32_t T, const uint16_t* 
  *   events[0] before the router          events[4] after the W13 GEMM
  *   events[1] after the router           events[5] after the W2 GEMM
  *   events[2] after dispatch/alignment   events[6] after the shared expert
- *   events[3] after the GEMM tile list   events[7] after the combine
+ *   events[3] after tile list + row gather   events[7] after the combine
  * so the caller can read per-kernel device times (cudaEventElapsedTime)
  * without extra synchronisation.  Same computation and bits as moe_forward. */
 moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h,

@@ -199,14 +199,53 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
       tl.expert = e;
       tl.row0 = first * B + j * kTileRows;
       tl.rows = min(kTileRows, rows - j * kTileRows);
-      tl.pad = 0;
+      tl.first = off;
+      tl.count = nt;
+      tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
       tiles[idx] = tl;
     }
   }
   if (threadIdx.x == 0) *num_tiles = min(total, max_tiles);
 }
 
+// x_perm[p] = h[r / k] for padded row p holding route r, zeros for the
+// sentinel: the routed token rows in expert-segment order, so that the W13
+// GEMM loads whole 128-row tiles.  One warp per row, 16-byte accesses.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ h,
+                                                          const int32_t* __restrict__ sorted_route_ids,
+                                                          const int32_t* __restrict__ num_padded, int k,
+                                                          int R, int H, long long max_rows,
+                                                          uint16_t* __restrict__ x_perm) {
+  const long long P = min((long long)*num_padded, max_rows);
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int chunks = H / 8;
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P;
+       row += warps) {
+    const int r = sorted_route_ids[row];
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + row * H);
+    if (r >= 0 && r < R) {
+      const uint4* src = reinterpret_cast<const uint4*>(h + (size_t)(r / k) * H);
+      for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    } else {
+      for (int c = lane; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
 }  // namespace
+
+void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
+                        int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = (max_rows + 7) / 8;
+  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
+  const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+  gather_rows_kernel<<<grid, 256, 0, s>>>(h, sorted_route_ids, num_padded, k, R, H, (long long)max_rows,
+                                          x_perm);
+}
 
 void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,
                      uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,

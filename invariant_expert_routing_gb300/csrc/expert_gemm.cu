@@ -3,7 +3,7 @@
 // For each padded expert segment produced by the stable alignment
 // ("Route-Block Membership Selects Packed-AWQ Arithmetic", "The bookkeeping
 // before the matrix multiplication"), token tiles of kTileRows rows run
-//   W13: [g | u] = X . W13_e  ->  a = bf16(silu(g) * u)      (X gathered rows of h)
+//   W13: [g | u] = X . W13_e  ->  a = bf16(silu(g) * u)      (X = x_perm rows)
 //   W2 : y = a . W2_e         ->  y_perm (fp32)
 // The weights are operand A (M = 128 output features, MN-major straight from
 // the [K, features] layout), the tokens operand B (N = 128 rows, K-major).
@@ -16,8 +16,7 @@
 // the split/non-split schedule classes of the packed kernel that page studies.
 //
 // Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0      TMA producer (weight boxes; W13: tile::gather4 of the token
-//               rows of h; W2: the a tile)
+//   warp 0      TMA producer (weight boxes and the 128-row token tile)
 //   warp 1      TMEM allocation, one elected thread issues tcgen05.mma
 //   warps 2..5  epilogue: tcgen05.ld from TMEM, SiLU*up or fp32 store
 // Smem stages are guarded by full/empty mbarriers, the two TMEM accumulator
@@ -68,6 +67,35 @@ __device__ __forceinline__ TileInfo tile_of(const GemmArgs& a, int ti) {
     t.rows = g.rows;
   }
   return t;
+}
+
+// Work item -> (feature tile, token tile).  Items of one expert are
+// contiguous; inside an expert they run in groups of G feature tiles x all of
+// the expert's token tiles, G sized so that one wave of CTAs shares its weight
+// and token tiles through L2.  Only the order of tiles changes with the batch,
+// never the arithmetic of a tile.
+struct Work {
+  int f;
+  TileInfo t;
+};
+
+__device__ __forceinline__ Work work_of(const GemmArgs& a, int item, int num_tiles) {
+  const int nf = a.n_feat_tiles;
+  int first = 0, count = num_tiles;
+  if (!a.identity_T) {
+    const GemmTile g = a.tiles[item / nf];
+    first = g.first;
+    count = g.count;
+  }
+  const int l = item - first * nf;
+  const int G = max(1, min(nf, ((int)gridDim.x + count - 1) / count));
+  const int grp = l / (count * G);
+  const int gsz = min(G, nf - grp * G);
+  const int lin = l - grp * count * G;
+  Work w;
+  w.f = grp * G + lin % gsz;
+  w.t = tile_of(a, first + lin / gsz);
+  return w;
 }
 
 template <bool kW13>
@@ -129,25 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int armed = 0;  // stages armed and not yet known consumed (for the abort path)
     bool ok = true;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      const int f = item / num_tiles, ti = item % num_tiles;
-      const TileInfo t = tile_of(args, ti);
-      int rows4[4] = {0, 0, 0, 0};
-      if (kW13) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j = 4 * lane + q;
-          int tok = 0;
-          if (j < t.rows) {
-            if (args.identity_T) {
-              tok = t.row0 + j;
-            } else {
-              const int r = args.sorted_route_ids[t.row0 + j];
-              tok = (r >= 0 && r < args.num_routes) ? r / args.top_k : 0;
-            }
-          }
-          rows4[q] = tok;
-        }
-      }
+      const Work wk = work_of(args, item, num_tiles);
+      const TileInfo t = wk.t;
+      const int f = wk.f;
       const int wrow0 = t.expert * args.w_rows_per_e;
       const int fcol = f * kTileFeat;
       for (int ks = 0; ks < ksteps; ++ks) {
@@ -170,14 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kW13) {
             tma_load_2d(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
             tma_load_2d(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb, pol_w);
-          } else {
-            tma_load_2d(smem_u32(sB), &x_map, k0, t.row0, fb, pol_x);
           }
+          tma_load_2d(smem_u32(sB), &x_map, k0, t.row0, fb, pol_x);
         }
         __syncwarp();
-        if (kW13)
-          tma_gather4(smem_u32(sB + lane * 4 * 128), &x_map, k0, rows4[0], rows4[1], rows4[2], rows4[3],
-                      fb, pol_x);
         armed = min(armed + 1, C::kStages);
         if (++stage == C::kStages) {
           stage = 0;
@@ -270,8 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      const int f = item / num_tiles, ti = item % num_tiles;
-      const TileInfo t = tile_of(args, ti);
+      const Work wk = work_of(args, item, num_tiles);
+      const TileInfo t = wk.t;
+      const int f = wk.f;
       int got = 1;
       if (lane == 0) got = mbar_wait(tfull0 + 8 * acc, acc_phase, &s_abort) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -297,15 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c + jj;
             if (j < t.rows) {
-              const int row = t.row0 + j;
-              bool real = true;
-              if (!args.identity_T) {
-                const int r = args.sorted_route_ids[row];
-                real = r >= 0 && r < args.num_routes;
-              }
+              // sentinel rows have x = 0, hence g = u = 0 and a = 0
               const float x = g[jj];
-              const float v = real ? (x / (1.0f + expf(-x))) * u[jj] : 0.0f;
-              out[(size_t)row * args.out_ld + feat] = __float2bfloat16_rn(v);
+              const float v = (x / (1.0f + expf(-x))) * u[jj];
+              out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v);
             }
           }
         } else {

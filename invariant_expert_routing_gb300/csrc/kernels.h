@@ -23,9 +23,11 @@ constexpr int kDispatchTile = 1024;
 
 struct GemmTile {
   int32_t expert;
-  int32_t row0;
-  int32_t rows;
-  int32_t pad;
+  int32_t row0;   // first padded row of the tile
+  int32_t rows;   // valid rows (<= kTileRows)
+  int32_t first;  // index of the first tile of this expert in the list
+  int32_t count;  // tiles of this expert
+  int32_t pad[3];
 };
 
 // ---- router
@@ -40,6 +42,8 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
                      int32_t* seg_off, int* status, cudaStream_t s);
+void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
+                        int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
                         int64_t max_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles,
                         int* status, cudaStream_t s);
@@ -53,9 +57,6 @@ struct GemmArgs {
   const GemmTile* tiles;     // routed mode: tile list on the device
   const int32_t* num_tiles;  // routed mode: device count
   int identity_T;            // identity mode (shared expert): rows 0..T-1, else 0
-  const int32_t* sorted_route_ids;  // routed W13: row -> route id
-  int top_k;
-  int num_routes;      // R = T*k (the sentinel)
   void* out;           // W13: bf16 a [rows, I]; W2: fp32 y [rows, H]
   int out_ld;          // elements per output row
   int* status;

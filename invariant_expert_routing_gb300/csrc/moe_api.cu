@@ -62,8 +62,8 @@ int64_t max_gemm_tiles_of(const moe_config* c, int32_t T) {
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
   size_t status, logits, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
-      num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, a, y, a_sh, y_sh, h_stage, out_stage,
-      total;
+      num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, x_perm, a, y, a_sh, y_sh, h_stage,
+      out_stage, total;
 };
 
 Layout layout_of(const moe_config* c, int32_t T) {
@@ -93,7 +93,8 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.dropped = take(sizeof(int32_t));
   L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T));
   L.num_gemm_tiles = take(sizeof(int32_t));
-  // a keeps kTileRows rows of slack so every W2 tile load stays inside it
+  // x_perm and a keep kTileRows rows of slack so every 128-row tile load stays inside them
+  L.x_perm = take(sizeof(uint16_t) * (rows + moe::kTileRows) * H);
   L.a = take(sizeof(uint16_t) * (rows + moe::kTileRows) * c->intermediate);
   L.y = take(sizeof(float) * rows * H);
   const size_t Is = c->shared_intermediate;
@@ -201,12 +202,14 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   int32_t* ntiles = at<int32_t>(ws, L.num_gemm_tiles);
   uint16_t* a = at<uint16_t>(ws, L.a);
 
+  uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, tiles, ntiles, max_tiles, status, s);
+  moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
   mark(mk, 3);
 
-  CUtensorMap m_w13, m_h, m_w2, m_a;
+  CUtensorMap m_w13, m_x, m_w2, m_a;
   if (!map_2d(&m_w13, w13, 2ull * I, (uint64_t)N * H, 64, 64) ||
-      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, 1) ||
+      !map_2d(&m_x, x_perm, (uint64_t)H, (uint64_t)(rows + moe::kTileRows), 64, moe::kTileRows) ||
       !map_2d(&m_w2, w2, (uint64_t)H, (uint64_t)N * I, 64, 64) ||
       !map_2d(&m_a, a, (uint64_t)I, (uint64_t)(rows + moe::kTileRows), 64, moe::kTileRows))
     return MOE_ERR_CUDA;
@@ -219,13 +222,10 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.tiles = tiles;
   g13.num_tiles = ntiles;
   g13.identity_T = 0;
-  g13.sorted_route_ids = sorted;
-  g13.top_k = k;
-  g13.num_routes = T * k;
   g13.out = a;
   g13.out_ld = I;
   g13.status = status;
-  moe::launch_w13_gemm(m_w13, m_h, g13, max_tiles, sms, s);
+  moe::launch_w13_gemm(m_w13, m_x, g13, max_tiles, sms, s);
   mark(mk, 4);
 
   moe::GemmArgs g2 = g13;
@@ -241,8 +241,10 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   const int Is = c->shared_intermediate;
   if (Is > 0) {
     uint16_t* ash = at<uint16_t>(ws, L.a_sh);
-    CUtensorMap m_w13s, m_w2s, m_ash;
-    if (!map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
+    CUtensorMap m_w13s, m_w2s, m_ash, m_h;
+    // the last 128-row tile of h may run past row T-1: TMA fills those rows with zeros
+    if (!map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, moe::kTileRows) ||
+        !map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
         !map_2d(&m_w2s, w2s, (uint64_t)H, (uint64_t)Is, 64, 64) ||
         !map_2d(&m_ash, ash, (uint64_t)Is, (uint64_t)T + moe::kTileRows, 64, moe::kTileRows))
       return MOE_ERR_CUDA;
@@ -253,8 +255,6 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
     s13.w_rows_per_e = H;
     s13.up_col = Is;
     s13.identity_T = T;
-    s13.top_k = k;
-    s13.num_routes = T * k;
     s13.out = ash;
     s13.out_ld = Is;
     s13.status = status;
