@@ -201,6 +201,29 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
 /* Number of kernel launches one moe_forward makes for this configuration. */
 int32_t moe_forward_launch_count(const moe_config* cfg);
 
+/* moe_dispatch_align for callers that cannot allocate device memory (for
+ * example a serving loop whose memory is fixed at start-up, or code running
+ * while another framework owns the allocator), so cannot pass a workspace.
+ * The pages have no counterpart to this entry point; it is a deployment aid.
+ * Same inputs, outputs and bits as moe_dispatch_align, but it allocates
+ * nothing: its scratch is one fixed device array inside this library
+ * (~321 KB on every GPU that loads it, held until the process exits).
+ *   - Limit: T*k <= 65536 routes (and N <= 256); larger batches return
+ *     MOE_ERR_UNSUPPORTED without doing anything.
+ *   - status_out: device int32 or NULL; receives this call's device status
+ *     word (MOE_DEV_ERR_EXPERT_RANGE for expert ids outside [0, N)).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (the call clears what must start at zero).  Calls that
+ *     overlap on the GPU (e.g. on two streams at once) race on it: order them. */
+moe_status moe_dispatch_align_noalloc(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                                      uint8_t* route_kept, int32_t* route_pos,
+                                      int32_t* sorted_route_ids, int32_t* block_expert,
+                                      int32_t* num_padded, int32_t* expert_counts,
+                                      int32_t* num_dropped, int32_t* status_out, void* stream);
+
 /* Reads the device status word of `ws` (synchronises `stream`). */
 moe_status moe_get_device_status(const void* ws, int32_t* status_out, void* stream);
 

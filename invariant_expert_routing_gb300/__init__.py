@@ -63,6 +63,7 @@ _SIGS = {
     "moe_forward_hostio": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_forward_timed": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp, _i32, _vp], ctypes.c_int),
     "moe_forward_launch_count": ([_cfgp], _i32),
+    "moe_dispatch_align_noalloc": ([_cfgp, _i32] + [_vp] * 9 + [_vp], ctypes.c_int),
     "moe_get_device_status": ([_vp, ctypes.POINTER(_i32), _vp], ctypes.c_int),
     "moe_clear_device_status": ([_vp, _vp], ctypes.c_int),
 }
@@ -145,6 +146,17 @@ def moe_dispatch_align(cfg, topk_idx, route_kept, route_pos, sorted_route_ids, b
         ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), _ptr(route_kept), _ptr(route_pos),
         _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded), _ptr(expert_counts),
         _ptr(num_dropped), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_align_noalloc(cfg, topk_idx, route_kept, route_pos, sorted_route_ids,
+                               block_expert, num_padded, expert_counts, num_dropped,
+                               status_out=None, stream=None):
+    """moe_dispatch_align without a workspace (fixed in-library scratch, T*k <= 65536)."""
+    T = topk_idx.shape[0]
+    _check("moe_dispatch_align_noalloc", _lib.moe_dispatch_align_noalloc(
+        ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), _ptr(route_kept), _ptr(route_pos),
+        _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded), _ptr(expert_counts),
+        _ptr(num_dropped), _ptr(status_out), _stream(stream)))
 
 
 def moe_expert_ffn(cfg, h, w13, w2, w13_shared, w2_shared, sorted_route_ids, block_expert,
