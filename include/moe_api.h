@@ -18,8 +18,8 @@
  * Batch invariance ("Why temperature=0 Still Gives Different Answers: Batch
  * Invariance", section "What is batch invariance in LLM inference?"): every
  * reduction has one fixed split and order regardless of T, with no split-K
- * and no atomics, so a token's outputs are bitwise identical whatever else is
- * in the batch and whichever padded block its routes land in.  The only
+ * and no atomics, so a token's outputs are bitwise identical regardless of the
+ * other tokens of the batch and whichever padded block its routes land in.  The only
  * exception is the capacity rule itself, which couples tokens by design.
  *
  * Conventions for every entry point:

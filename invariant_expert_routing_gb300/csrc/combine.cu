@@ -1,6 +1,7 @@
 // Gate-weighted combine into the residual stream ("Mixture-of-Experts Routing
-// at Inference Time": the output is the gate-weighted sum of the selected
-// experts added to h; a dropped route adds nothing, Figure 2).
+// at Inference Time", "How sparse routing works" and Figure 2): each token
+// gets h plus its kept experts' outputs scaled by their gates; a route that
+// overflowed contributes nothing.
 //
 // out[t,:] = bf16( h[t,:] + acc ),  acc = fma over kept slots j = 0..k-1 in
 // ascending order of gate[t,j] * y_perm[route_pos[t*k+j], :], then + y_shared.

@@ -1,8 +1,8 @@
 // Capacity-limited dispatch and stable alignment into padded expert blocks.
 //
-// Capacity is filled in batch order ("Mixture-of-experts routing and LLM
-// repeatability": the dispatcher fills capacity in order; overflow skips the
-// expert): expert e keeps its first C routes by ascending route id.  Stable
+// Capacity is granted in batch order ("Mixture-of-experts routing and LLM
+// repeatability", the Switch capacity rule and in-order filling): expert e
+// keeps its first C routes by ascending route id; the others skip it.  Stable
 // construction ("Route-Block Membership Selects Packed-AWQ Arithmetic",
 // section "Stable construction selected a third trajectory"): segments in
 // ascending expert id, routes inside a segment in ascending route id, each

@@ -1,6 +1,6 @@
 // Router: fp32 logits in the fixed chunked order, then top-k and renormalised
 // gates ("Mixture-of-Experts Routing at Inference Time", section "How sparse
-// routing works": h x W_g -> N logits -> softmax + top-k -> renormalise).
+// routing works": one projection to N logits, softmax, top-k, renormalise).
 //
 // The logit of (token t, expert e) is, for every batch size,
 //   total = +0;  for each 256-element chunk c of H (ascending):
@@ -8,9 +8,9 @@
 //     total = total + part
 //   total = total + bias[e]
 // ("Why temperature=0 Still Gives Different Answers: Batch Invariance",
-// Tier 2: fixed 256-element chunks combined in a fixed order).  bf16 x bf16
-// products are exact in fp32, so the fma rounds exactly like the separate
-// add.  Chunks are spread over the warps of a CTA and their partial sums are
+// Tier 2: a reduction cut into constant 256-element pieces added in one
+// order).  bf16 x bf16 products are exact in fp32, so the fma rounds exactly
+// like the separate add.  Chunks are spread over the warps of a CTA and their partial sums are
 // combined in ascending chunk order through shared memory; no split crosses a
 // CTA and nothing depends on T.
 #include <cuda_bf16.h>

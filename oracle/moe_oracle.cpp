@@ -6,25 +6,26 @@
 // follows one passage of the pages that define the method:
 //
 //  * "Mixture-of-Experts Routing at Inference Time" (ACE Journal), section
-//    "How sparse routing works": the router is one matrix W_g [hidden, N]; the
-//    token's N logits go through a softmax, the top k experts are kept, their
-//    gates renormalised, and the output is the gate-weighted sum of those
-//    experts applied to h (also the TopKRouter of the worked example).
+//    "How sparse routing works" and its TopKRouter: one router matrix W_g
+//    [hidden, N] maps a token to N logits; softmax, keep the k best, rescale
+//    their gates to sum to one; the token's result adds each kept expert's
+//    output weighted by its gate.
 //  * Same page, "The hard part: token dropping is a silent correctness bug"
 //    and Figure 2: a route that overflows its expert's capacity contributes
-//    nothing; the token keeps its residual plus the surviving experts.
+//    nothing; the token keeps its residual plus its other kept routes.
 //  * "Mixture-of-experts routing and LLM repeatability"
 //    (vincentschmalbach.com): the per-token pseudo-code (scores, top_k,
 //    gate-weighted sum into the residual stream), the Switch capacity rule
 //    (tokens/experts x capacity factor) and in-order filling of capacity.
 //  * "Why temperature=0 Still Gives Different Answers: Batch Invariance",
-//    "Tier 2 - batch-invariant kernels": reduce in fixed 256-element chunks
-//    combined in a fixed order (the router's fp32 summation order below).
+//    Tier 2 of "How do I make LLM inference reproducible?": a reduction cut
+//    into constant 256-element pieces added in one order (the router's fp32
+//    summation order below).
 //  * "Route-Block Membership Selects Packed-AWQ Arithmetic", sections "The
 //    bookkeeping before the matrix multiplication" and "Stable construction
-//    selected a third trajectory": routed rows are grouped by expert and padded
-//    into fixed-size blocks; valid routes are ordered by (expert id, flattened
-//    route id).
+//    selected a third trajectory": routed rows are grouped per expert and
+//    padded to whole blocks; the kept routes are sorted by expert id, then by
+//    flattened route id.
 #include "moe_oracle.h"
 
 #include <algorithm>

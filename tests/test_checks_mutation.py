@@ -1,8 +1,8 @@
 """Negative controls for the parity checker.
 
 Following the evidence design of "Route-Block Membership Selects Packed-AWQ
-Arithmetic" (section "The evidence package": required mutations to routes,
-markers, hashes and raw tensors must be rejected), each test plants one
+Arithmetic" (section "The evidence package": a checker must refuse planted
+changes to routes, hashes and tensors), each test plants one
 mistake in a copy of the oracle's own results, on the CPU, and requires the
 checker to reject it.
 """

@@ -4,7 +4,7 @@ Layer output = h + sum of gate * expert(h) over the kept routes ("Mixture-of-
 Experts Routing at Inference Time", "How sparse routing works"; the per-token
 pseudo-code of "Mixture-of-experts routing and LLM repeatability").  A dropped
 route adds nothing and the gates are not renormalised ("The hard part" and
-Figure 2 of the first page: h plus the single surviving expert).  The expert
+Figure 2 of the first page: the residual plus the routes still kept).  The expert
 is SwiGLU: W13 = [gate | up], a = silu(gate) * up, y = a . W2.
 
 Pins: reductions to a dense SwiGLU computed independently in numpy fp64,

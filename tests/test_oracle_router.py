@@ -16,6 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 from synth import bf16_to_f32, f32_to_bf16
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -88,19 +89,25 @@ def test_error_bound_against_exact_dot(H, N):
     assert np.any(l != exact) or H <= 256
 
 
-def test_non_associativity_is_visible():
-    # The float demonstration of the batch-invariance page: the same values
-    # summed sequentially and in 4- and 8-way partitions give different fp32
-    # bits.  The order of a reduction is therefore observable, which is what
-    # lets the bit-exact tests see a change of order.
-    rng = np.random.default_rng(0)
-    x = (rng.standard_normal(4096) * 0.02).astype(np.float32)
-    seq = np.float32(0)
-    for v in x:
-        seq = np.float32(seq + v)
-    t4 = x.reshape(4, -1).sum(axis=1, dtype=np.float32).sum(dtype=np.float32)
-    t8 = x.reshape(8, -1).sum(axis=1, dtype=np.float32).sum(dtype=np.float32)
-    assert len({float(seq), float(t4), float(t8)}) >= 2
+def test_summation_order_is_visible_in_fp32():
+    # Float addition is not associative (the point of the batch-invariance
+    # page): the same fp32 values accumulated left to right and in 3 or 5
+    # slices give different bits, so the bit-exact tests can see a change of
+    # order in the kernels.
+    def left_to_right(v):
+        return np.cumsum(v, dtype=np.float32)[-1]
+
+    def sliced(v, n):
+        parts = [left_to_right(p) for p in np.array_split(v, n)]
+        return left_to_right(np.array(parts, dtype=np.float32))
+
+    differ = 0
+    for tid in range(10):
+        # full 24-bit mantissas: bf16 draws times an fp32 constant
+        vals = bf16_to_f32(synth.normal_bf16((5000,), 9, 100 + tid, 0.05)) * np.float32(1.1)
+        results = {float(left_to_right(vals)), float(sliced(vals, 3)), float(sliced(vals, 5))}
+        differ += len(results) >= 2
+    assert differ >= 5
 
 
 def test_thread_count_does_not_change_bits():
