@@ -247,13 +247,80 @@ def _oracle_tokens(wl, h_all, wg, bias, w13, w2, tokens, nthreads=0):
     return oracle.combine_rows(np.arange(n), h, gates, kept, y.reshape(n, wl.top_k, wl.hidden))
 
 
+WORKLOAD_NAMES = {"tiny": "tiny MoE layer", "mix": "mixtral-like MoE layer",
+                  "qw": "qwen3-moe-like MoE layer (near-tied router)",
+                  "cap": "capacity-limited top-2 MoE layer (cf 1.0, Zipf skew)",
+                  "ds": "deepseek-v3-like MoE layer (+1 shared expert)"}
+
+
 def workload_config(wl, T, world):
-    return {"workload": (f"mixtral-like MoE layer forward: hidden {wl.hidden}, {wl.num_experts} "
-                         f"experts, top-{wl.top_k}, SwiGLU intermediate {wl.intermediate}, "
-                         f"block {wl.block_size}, T={T} tokens per GPU"),
+    shared = f", shared expert {wl.shared_intermediate}" if wl.shared_intermediate else ""
+    cap = f", capacity factor {wl.capacity_factor}" if wl.capacity_factor > 0 else ""
+    return {"workload": (f"{WORKLOAD_NAMES.get(wl.name, wl.name)} forward: hidden {wl.hidden}, "
+                         f"{wl.num_experts} experts, top-{wl.top_k}, SwiGLU intermediate "
+                         f"{wl.intermediate}{shared}, block {wl.block_size}{cap}, T={T} tokens per GPU"),
             "tokens_per_gpu": T, "global_batch": T * world, "seed": 0,
-            "l2": "inputs larger than L2: 2.8 GB of expert weights are read every step",
+            "l2": (f"inputs larger than L2: {wl.weight_bytes() / 1e9:.1f} GB of expert weights, "
+                   "the touched experts' weights are read every step"),
             "parallelism": "single GPU" if world == 1 else f"{world} token-shard replicas, no collective"}
+
+
+def batch_counts(moe, cfg, wl, h_d, wg_d, bias_d, ws, device):
+    """Kept routes and touched experts of one batch (for the algorithmic work)."""
+    import numpy as np
+    import torch
+    T = h_d.shape[0]
+    R, N = T * wl.top_k, wl.num_experts
+    idx = torch.empty((T, wl.top_k), dtype=torch.int32, device=device)
+    gates = torch.empty((T, wl.top_k), dtype=torch.float32, device=device)
+    moe.moe_route(cfg, h_d, wg_d, bias_d, idx, gates, None, ws)
+    kept = torch.empty(R, dtype=torch.uint8, device=device)
+    pos = torch.empty(R, dtype=torch.int32, device=device)
+    srt = torch.empty(moe.moe_max_padded_rows(cfg, T), dtype=torch.int32, device=device)
+    blk = torch.empty(moe.moe_max_blocks(cfg, T), dtype=torch.int32, device=device)
+    npad = torch.empty(1, dtype=torch.int32, device=device)
+    counts = torch.empty(N, dtype=torch.int32, device=device)
+    dropped = torch.empty(1, dtype=torch.int32, device=device)
+    moe.moe_dispatch_align(cfg, idx, kept, pos, srt, blk, npad, counts, dropped, ws)
+    c = counts.cpu().numpy()
+    return int(c.sum()), int((c > 0).sum()), int(dropped.item())
+
+
+def time_graph(fwd, n):
+    """Per-forward device time of `fwd` captured once in a CUDA graph and
+    replayed n times (removes host launch overhead, which dominates small
+    batches)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fwd()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd()
+    for _ in range(3):
+        graph.replay()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def time_forwards(moe, fwd, n, stream):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -273,8 +340,8 @@ def run_gpu(args):
     from synth import workloads as W
     from tests.gpu_util import dev, dev_bf16, host_bf16
 
-    wl = W.WORKLOADS[WORKLOAD]
-    T = TOKENS
+    wl = W.WORKLOADS[args.workload]
+    T = args.tokens
     cfg = wl.cfg
     wg, bias = W.make_router(wl)
     wg_d = dev_bf16(wg, device)
@@ -283,7 +350,8 @@ def run_gpu(args):
     h = W.make_h(wl, T, seed=shard_seed(rank))
     h_d = dev_bf16(h, device)
     out_d = torch.empty((T, wl.hidden), dtype=torch.bfloat16, device=device)
-    ws = moe.workspace(cfg, T, device)
+    max_T = max([T] + ([] if args.no_sweep else list(wl.tokens)))
+    ws = moe.workspace(cfg, max_T, device)
     moe.moe_clear_device_status(ws)
     stream = torch.cuda.current_stream()
 
@@ -333,88 +401,91 @@ def run_gpu(args):
     ms_step = ms_total / K
     stage = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(7)] for i in range(K)])
     stage_ms = stage.mean(axis=0)
-    names = ["router", "dispatch_align", "gemm_tile_list", "w13_gemm", "w2_gemm", "shared_expert",
-             "combine"]
+    names = ["router", "dispatch_align", "tile_list_and_row_gather", "w13_gemm", "w2_gemm",
+             "shared_expert", "combine"]
     if moe.moe_get_device_status(ws) != 0:
         raise RuntimeError("device status word set during the timed region")
 
-    # ---- what the batch did (for the algorithmic work)
-    idx = torch.empty((T, wl.top_k), dtype=torch.int32, device=device)
-    gates = torch.empty((T, wl.top_k), dtype=torch.float32, device=device)
-    moe.moe_route(cfg, h_d, wg_d, bias_d, idx, gates, None, ws)
-    idx_h = idx.cpu().numpy()
-    kept_routes = T * wl.top_k  # no capacity limit in this workload
-    touched = len(np.unique(idx_h))
+    # ---- algorithmic work of this batch and the roofline of the dominant kernel
+    kept_routes, touched, dropped = batch_counts(moe, cfg, wl, h_d, wg_d, bias_d, ws, device)
     flops, bytes_ = algorithmic_work(wl, T, kept_routes, touched)
-
     peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_gb = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     i_w13 = names.index("w13_gemm")
-    w13_flops = 4.0 * wl.hidden * wl.intermediate * kept_routes
     w13_s = stage_ms[i_w13] * 1e-3
-    achieved = w13_flops / w13_s / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic, traffic_src = profiled_traffic("expert_w13_gemm", "mix_T4096")
-    dominant = names[int(np.argmax(stage_ms))]
+    w13_flops = 4.0 * wl.hidden * wl.intermediate * kept_routes
+    w13_bytes = 4.0 * wl.hidden * wl.intermediate * touched + 4.0 * kept_routes * wl.hidden
+    ridge = peak_tf * 1e12 / (peak_gb * 1e9)
+    traffic, traffic_src = profiled_traffic("expert_w13_gemm", f"{wl.name}_T{T}")
+    if w13_flops / w13_bytes >= ridge:
+        roof = {"bound": "tensor", "achieved": w13_flops / w13_s / 1e12, "peak": peak_tf,
+                "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16 burst",
+                "algorithmic_flops_per_launch": w13_flops}
+    else:
+        roof = {"bound": "hbm", "achieved": w13_bytes / w13_s / 1e9, "peak": peak_gb,
+                "unit": "GB/s", "peak_source": f"{peak_src} HBM copy",
+                "algorithmic_bytes_per_launch": w13_bytes}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"kernel": "expert_w13_gemm (tcgen05 grouped GEMM + SiLU*up)", "traffic": traffic,
+                 "traffic_source": traffic_src, "avg_launch_ms": float(stage_ms[i_w13]),
+                 "dominant_stage": names[int(np.argmax(stage_ms))]})
 
     value = world * T / (ms_step * 1e-3)
+    layer_tf = flops / (ms_step * 1e-3) / 1e12
+    layer_gb = bytes_ / (ms_step * 1e-3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded counter-based generator; no checkpoints)",
-            "config": workload_config(wl, T, world),
-            "roofline": {"kernel": "expert_w13_gemm (tcgen05 grouped GEMM + SiLU*up)",
-                         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
-                         "traffic": traffic, "traffic_source": traffic_src,
-                         "algorithmic_flops_per_launch": w13_flops,
-                         "avg_launch_ms": stage_ms[i_w13], "dominant_stage": dominant},
+            "config": workload_config(wl, T, world), "roofline": roof,
             "layer_roofline": {"algorithmic_gflop": flops / 1e9, "algorithmic_gb": bytes_ / 1e9,
-                               "tflops_achieved": flops / (ms_step * 1e-3) / 1e12,
-                               "frac_of_bf16_peak": flops / (ms_step * 1e-3) / 1e12 / peak},
+                               "kept_routes": kept_routes, "dropped_routes": dropped,
+                               "touched_experts": touched, "tflops": layer_tf,
+                               "frac_of_bf16_peak": layer_tf / peak_tf, "gbs": layer_gb,
+                               "frac_of_hbm": layer_gb / peak_gb},
             "stage_ms": {n: float(v) for n, v in zip(names, stage_ms)},
             "gpu_launches": moe.moe_forward_launch_count(cfg) * K,
             "clocks": clocks.summary(t_wall0, t_wall1)}
 
-    # ---- decode-shaped batches of the same layer (secondary lines)
+    # ---- the workload's other batch sizes (secondary lines, same layer)
     sweep = []
-    for Ts in ([] if args.no_sweep else [1, 16, 128]):
+    for Ts in ([] if args.no_sweep else [t for t in wl.tokens if t != T]):
         hs = dev_bf16(W.make_h(wl, Ts, seed=shard_seed(rank) + 17), device)
         outs = torch.empty((Ts, wl.hidden), dtype=torch.bfloat16, device=device)
+
+        def fwd_s():
+            moe.moe_forward(cfg, hs, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, outs, ws)
+
         for _ in range(3):
-            moe.moe_forward(cfg, hs, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, outs, ws)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n = 50
-        e0.record(stream)
-        for _ in range(n):
-            moe.moe_forward(cfg, hs, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, outs, ws)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / n
-        moe.moe_route(cfg, hs, wg_d, bias_d, idx[:Ts], gates[:Ts], None, ws)
-        tch = len(np.unique(idx[:Ts].cpu().numpy()))
-        f_s, b_s = algorithmic_work(wl, Ts, Ts * wl.top_k, tch)
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        sweep.append({"T": Ts, "ms": ms, "tokens_per_s": Ts / (ms * 1e-3), "bound": "hbm",
-                      "achieved_gbs": b_s / (ms * 1e-3) / 1e9, "peak_gbs": hbm,
-                      "frac": b_s / (ms * 1e-3) / 1e9 / hbm, "touched_experts": tch})
+            fwd_s()
+        n_it = 50 if Ts <= 1024 else 10
+        ms_eager = time_forwards(moe, fwd_s, n_it, stream)
+        ms = time_graph(fwd_s, n_it)
+        kr, tch, _ = batch_counts(moe, cfg, wl, hs, wg_d, bias_d, ws, device)
+        f_s, b_s = algorithmic_work(wl, Ts, kr, tch)
+        entry = {"T": Ts, "ms": ms, "ms_eager": ms_eager, "timing": "CUDA graph replay",
+                 "tokens_per_s": Ts / (ms * 1e-3), "touched_experts": tch,
+                 "tflops": f_s / (ms * 1e-3) / 1e12, "gbs": b_s / (ms * 1e-3) / 1e9}
+        entry["bound"] = "tensor" if f_s / b_s >= ridge else "hbm"
+        entry["frac"] = (entry["tflops"] / peak_tf if entry["bound"] == "tensor"
+                         else entry["gbs"] / peak_gb)
+        sweep.append(entry)
     if sweep:
-        line["decode_sweep"] = sweep
+        line["sweep"] = sweep
 
     # ---- end to end through the host-buffer entry point
     h_host = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory()
     out_host = torch.empty((T, wl.hidden), dtype=torch.bfloat16).pin_memory()
+
+    def fwd_host():
+        moe.moe_forward_hostio(cfg, h_host, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_host, ws)
+
     for _ in range(2):
-        moe.moe_forward_hostio(cfg, h_host, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_host, ws)
+        fwd_host()
     torch.cuda.synchronize()
-    Ke = max(5, min(K, 50))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    e0.record(stream)
-    for _ in range(Ke):
-        moe.moe_forward_hostio(cfg, h_host, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_host, ws)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = reduce_max(e0.elapsed_time(e1) / Ke, device)
+    ms_e2e = reduce_max(time_forwards(moe, fwd_host, max(5, min(K, 50)), stream), device)
     line["e2e"] = {"value": world * T / (ms_e2e * 1e-3), "unit": UNIT,
                    "h2d_bytes_per_step": T * wl.hidden * 2, "d2h_bytes_per_step": T * wl.hidden * 2,
                    "ms_per_step": ms_e2e, "entry_point": "moe_forward_hostio (pinned host buffers)"}
@@ -425,7 +496,8 @@ def run_gpu(args):
         raise RuntimeError("host-buffer path and device path disagree")
 
     # ---- CPU oracle on the host cores (rank 0, N = 1)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and wl.capacity_factor <= 0
+            and wl.weight_bytes() < (8 << 30)):
         line["cpu_baseline"] = cpu_baseline(wl, h, wg, bias, host_bf16(out_d))
 
     if world > 1:
@@ -438,7 +510,8 @@ def run_gpu(args):
 
 def cpu_baseline(wl, h, wg, bias, gpu_out):
     """The oracle (as it stands) on a bounded sample of the batch; also checks
-    the sampled GPU rows against it."""
+    the sampled GPU rows against it.  Without capacity a token's routing
+    depends on its own row, so a sample of tokens is a faithful sub-batch."""
     import numpy as np
     from synth import workloads as W
     from tests.checks import check_outputs
@@ -447,23 +520,24 @@ def cpu_baseline(wl, h, wg, bias, gpu_out):
     rng = np.random.default_rng(123)
     T = h.shape[0]
     S = 16
-    toks = np.sort(rng.choice(T, S, replace=False))
+    toks = np.sort(rng.choice(T, min(S, T), replace=False))
     _oracle_tokens(wl, h, wg, bias, w13, w2, toks[:1])           # warm (page-in)
     t0 = time.perf_counter()
     done = 0
-    outs = []
+    outs = None
     while done < 4096 and time.perf_counter() - t0 < 15.0:
-        sel = toks if done == 0 else np.sort(rng.choice(T, S, replace=False))
+        sel = toks if done == 0 else np.sort(rng.choice(T, len(toks), replace=False))
         o = _oracle_tokens(wl, h, wg, bias, w13, w2, sel)
-        if done == 0:
+        if outs is None:
             outs = o
-        done += S
+        done += len(sel)
     el = time.perf_counter() - t0
     err = check_outputs(gpu_out[toks], outs)
     return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"{done} tokens of the T={T} batch in groups of {S} (router, top-k, their "
-                       f"{done * wl.top_k} expert FFN routes in fp64, combine), {el:.1f} s"),
-            "parity_on_sample": {"tokens": S, "max_abs_err": err, "tolerance": "2e-2 + 1e-2*|ref|"}}
+            "sample": (f"{done} tokens of the T={T} batch in groups of {len(toks)} (router, top-k, "
+                       f"their {done * wl.top_k} expert FFN routes in fp64, combine), {el:.1f} s"),
+            "parity_on_sample": {"tokens": len(toks), "max_abs_err": err,
+                                 "tolerance": "2e-2 + 1e-2*|ref|"}}
 
 
 def main():
@@ -474,6 +548,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=["tiny", "mix", "qw", "cap", "ds"])
+    ap.add_argument("--tokens", type=int, default=TOKENS)
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up + steps forwards of the main workload (for ncu)")
     args = ap.parse_args()

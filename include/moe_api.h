@@ -118,6 +118,38 @@ moe_status moe_route(const moe_config* cfg, int32_t T, const uint16_t* h, const 
                      const float* router_bias, int32_t* topk_idx, float* topk_gate,
                      float* logits_out, void* ws, size_t ws_bytes, void* stream);
 
+/* Router paths.  With logits_out != NULL, when N is not a multiple of 128, or
+ * when H > 8192, moe_route computes every logit in the canonical order on CUDA cores.
+ * Otherwise (moe_forward, or moe_route without logits_out, N % 128 == 0) it
+ * first computes l_tc = h . W_g on the tensor cores, bounds |l_tc - l| by
+ * delta_t = beta(H) * ||h_t|| * max_e ||W_g[:,e]|| (+ bias rounding), keeps
+ * as candidates the experts with l_tc >= L_k - 2 delta_t (L_k = k-th largest
+ * l_tc; all experts if anything is non-finite) and computes canonical logits
+ * for those only.  Experts below the cut provably cannot be in the top-k,
+ * so topk_idx and topk_gate are bit-identical on both paths.
+ *   beta(H) = (H/16 + 1) 2^-20 + (256 + ceil(H/256) + 1) 2^-24 covers
+ *   H/16 tensor-core K=16 steps at a relative error of 2^-20 each (several
+ *   times the truncation error of a 16-term fp32 block sum) and the fp32
+ *   additions of the canonical order. */
+float moe_router_cert_beta(int32_t hidden);
+
+/* Diagnostic: the tensor-core logits l_tc = h . W_g [T, N] fp32 (no bias) that
+ * the filter uses (MOE_ERR_UNSUPPORTED unless N % 128 == 0).  Not the
+ * canonical logits; the router margin and the filter width can be studied
+ * with them. */
+moe_status moe_router_tc_logits(const moe_config* cfg, int32_t T, const uint16_t* h,
+                                const uint16_t* w_gate, float* logits_out, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/* Diagnostic: the tensor-core router path of moe_route (same topk_idx and
+ * topk_gate), also reporting per token how many experts passed the filter
+ * and had their canonical logits computed: n_candidates [T] int32 (k..N).
+ * MOE_ERR_UNSUPPORTED unless N % 128 == 0 and H <= 8192. */
+moe_status moe_route_filtered(const moe_config* cfg, int32_t T, const uint16_t* h,
+                              const uint16_t* w_gate, const float* router_bias, int32_t* topk_idx,
+                              float* topk_gate, int32_t* n_candidates, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* Capacity-limited dispatch and stable alignment into padded expert blocks.
  * Input topk_idx [T, k] (from moe_route, or recorded routes to replay).
  * Capacity is filled in batch order: an expert keeps its first C routes by

@@ -63,6 +63,9 @@ _SIGS = {
     "moe_forward_hostio": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_forward_timed": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp, _i32, _vp], ctypes.c_int),
     "moe_forward_launch_count": ([_cfgp], _i32),
+    "moe_router_cert_beta": ([_i32], ctypes.c_float),
+    "moe_route_filtered": ([_cfgp, _i32] + [_vp] * 6 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_router_tc_logits": ([_cfgp, _i32] + [_vp] * 3 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_dispatch_align_noalloc": ([_cfgp, _i32] + [_vp] * 9 + [_vp], ctypes.c_int),
     "moe_get_device_status": ([_vp, ctypes.POINTER(_i32), _vp], ctypes.c_int),
     "moe_clear_device_status": ([_vp, _vp], ctypes.c_int),
@@ -206,6 +209,27 @@ def moe_forward_timed(cfg, h, w_gate, router_bias, w13, w2, w13_shared, w2_share
         ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(router_bias), _ptr(w13),
         _ptr(w2), _ptr(w13_shared), _ptr(w2_shared), _ptr(out), _ptr(ws), ws.numel(), arr,
         len(events), _stream(stream)))
+
+
+def moe_router_cert_beta(hidden: int) -> float:
+    return float(_lib.moe_router_cert_beta(hidden))
+
+
+def moe_route_filtered(cfg, h, w_gate, router_bias, topk_idx, topk_gate, n_candidates, ws,
+                       stream=None):
+    """Tensor-core router path with per-token candidate counts (diagnostic)."""
+    T = h.shape[0]
+    _check("moe_route_filtered", _lib.moe_route_filtered(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(router_bias), _ptr(topk_idx),
+        _ptr(topk_gate), _ptr(n_candidates), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_router_tc_logits(cfg, h, w_gate, logits_out, ws, stream=None):
+    """Tensor-core logits h . W_g (no bias): the input of the certified filter."""
+    T = h.shape[0]
+    _check("moe_router_tc_logits", _lib.moe_router_tc_logits(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(logits_out), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def moe_forward_launch_count(cfg) -> int:

@@ -35,6 +35,14 @@ void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float
                           int T, int H, int N, cudaStream_t s);
 void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,
                        cudaStream_t s);
+// tensor-core router with a certified candidate filter (N % 128 == 0)
+void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
+                      cudaStream_t s);
+float router_cert_beta(int H);
+bool route_certified_ok(int H);
+void launch_route_certified(const float* logits_tc, const float* bias, const uint16_t* h,
+                            const uint16_t* wgT, const float* norm_w, int T, int H, int N, int k,
+                            int32_t* topk_idx, float* gates, int32_t* n_cand, cudaStream_t s);
 
 // ---- dispatch / alignment
 void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,

@@ -61,7 +61,7 @@ int64_t max_gemm_tiles_of(const moe_config* c, int32_t T) {
 // ----------------------------------------------------------------- workspace
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
-  size_t status, logits, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
+  size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
       num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, x_perm, a, y, a_sh, y_sh, h_stage,
       out_stage, total;
 };
@@ -79,6 +79,8 @@ Layout layout_of(const moe_config* c, int32_t T) {
   };
   L.status = take(sizeof(int32_t));
   L.logits = take(sizeof(float) * T * N);
+  L.wgT = take(sizeof(uint16_t) * N * H);
+  L.norm_w = take(sizeof(float) * N);
   L.topk = take(sizeof(int32_t) * R);
   L.gates = take(sizeof(float) * R);
   L.kept = take(R);
@@ -163,10 +165,50 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
 moe_status last_cuda() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // ----------------------------------------------------------------- stages
+bool use_tc_router(const moe_config* c) {
+  return c->num_experts % moe::kTileFeat == 0 && moe::route_certified_ok(c->hidden);
+}
+
+// Tensor-core logits l_tc = h . W_g (no bias) into `logits` [T, N]: the
+// grouped GEMM kernel in identity mode with W_g [H, N] as the weights operand.
+moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* wg,
+                     float* logits, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  const int H = c->hidden, N = c->num_experts;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  CUtensorMap m_wg, m_h;
+  if (!map_2d(&m_wg, wg, (uint64_t)N, (uint64_t)H, 64, 64) ||
+      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, moe::kTileRows))
+    return MOE_ERR_CUDA;
+  moe::GemmArgs g{};
+  g.K = H;
+  g.n_feat_tiles = N / moe::kTileFeat;
+  g.w_rows_per_e = H;
+  g.identity_T = T;
+  g.out = logits;
+  g.out_ld = N;
+  g.status = at<int>(ws, L.status);
+  moe::launch_w2_gemm(m_wg, m_h, g, (T + moe::kTileRows - 1) / moe::kTileRows, sms, s);
+  return last_cuda();
+}
+
 moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* wg,
-                      const float* bias, int32_t* idx, float* gates, float* logits, cudaStream_t s) {
-  moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
-  moe::launch_topk_gates(logits, idx, gates, T, c->num_experts, c->top_k, s);
+                      const float* bias, int32_t* idx, float* gates, float* logits, bool canonical_logits,
+                      void* ws, cudaStream_t s, int32_t* n_cand = nullptr) {
+  const int H = c->hidden, N = c->num_experts, k = c->top_k;
+  if (!canonical_logits && use_tc_router(c) && moe::gemm_smem_ok()) {
+    const Layout L = layout_of(c, T);
+    uint16_t* wgT = at<uint16_t>(ws, L.wgT);
+    float* norm_w = at<float>(ws, L.norm_w);
+    moe::launch_gate_prep(wg, wgT, norm_w, H, N, s);
+    const moe_status st = tc_logits(c, T, h, wg, logits, ws, s);
+    if (st != MOE_OK) return st;
+    moe::launch_route_certified(logits, bias, h, wgT, norm_w, T, H, N, k, idx, gates, n_cand, s);
+    return last_cuda();
+  }
+  moe::launch_router_logits(h, wg, bias, logits, T, H, N, s);
+  moe::launch_topk_gates(logits, idx, gates, T, N, k, s);
   return last_cuda();
 }
 
@@ -300,7 +342,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   float* y = at<float>(ws, L.y);
   float* ysh = c->shared_intermediate ? at<float>(ws, L.y_sh) : nullptr;
   mk.at(0);
-  moe_status st = route_impl(c, T, h, wg, bias, idx, gates, at<float>(ws, L.logits), s);
+  moe_status st = route_impl(c, T, h, wg, bias, idx, gates, at<float>(ws, L.logits), false, ws, s);
   if (st != MOE_OK) return st;
   mk.at(1);
   st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, at<int32_t>(ws, L.counts),
@@ -383,9 +425,12 @@ moe_status moe_route(const moe_config* cfg, int32_t T, const uint16_t* h, const 
   MOE_TRY(need(topk_gate));
   MOE_TRY(opt(logits_out));
   MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  // with logits_out the canonical fp32 logits of every expert are produced
+  // (CUDA-core router); without, large-N layers use the tensor-core router
+  // with the certified filter (same indices and gates, bit for bit)
   float* logits = logits_out ? logits_out : at<float>(ws, layout_of(cfg, T).logits);
-  return route_impl(cfg, T, h, w_gate, router_bias, topk_idx, topk_gate, logits,
-                    static_cast<cudaStream_t>(stream));
+  return route_impl(cfg, T, h, w_gate, router_bias, topk_idx, topk_gate, logits, logits_out != nullptr,
+                    ws, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_dispatch_align(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
@@ -496,9 +541,49 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
 
 int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
-  // router 2 + dispatch 3 + tile list 1 + W13 + W2 + combine 1 (+ shared W13, W2)
-  return 9 + (cfg->shared_intermediate > 0 ? 2 : 0);
+  // router (CUDA cores: logits + top-k = 2; tensor cores: transpose, norms,
+  // GEMM, certified select = 4) + dispatch 3 + tile list 1 + row gather 1
+  // + W13 + W2 + combine 1 (+ shared W13, W2)
+  const int router = use_tc_router(cfg) ? 4 : 2;
+  return router + 3 + 1 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }
+
+moe_status moe_router_tc_logits(const moe_config* cfg, int32_t T, const uint16_t* h,
+                                const uint16_t* w_gate, float* logits_out, void* ws, size_t ws_bytes,
+                                void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  if (!use_tc_router(cfg)) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(need(logits_out));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  if (!moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
+  return tc_logits(cfg, T, h, w_gate, logits_out, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route_filtered(const moe_config* cfg, int32_t T, const uint16_t* h,
+                              const uint16_t* w_gate, const float* router_bias, int32_t* topk_idx,
+                              float* topk_gate, int32_t* n_candidates, void* ws, size_t ws_bytes,
+                              void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  if (!use_tc_router(cfg) || !moe::gemm_smem_ok()) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(opt(router_bias));
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(topk_gate));
+  MOE_TRY(need(n_candidates));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  return route_impl(cfg, T, h, w_gate, router_bias, topk_idx, topk_gate,
+                    at<float>(ws, layout_of(cfg, T).logits), false, ws, static_cast<cudaStream_t>(stream),
+                    n_candidates);
+}
+
+float moe_router_cert_beta(int32_t hidden) { return hidden > 0 ? moe::router_cert_beta(hidden) : 0.0f; }
 
 moe_status moe_forward_hostio(const moe_config* cfg, int32_t T, const uint16_t* h_host,
                               const uint16_t* w_gate, const float* router_bias, const uint16_t* w13,

@@ -112,6 +112,38 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return ia < ib;
 }
 
+// Sorts the k selected (expert, logit) pairs by expert index and writes the
+// renormalised gates exp(l_j - m) / sum_s exp(l_s - m), m = max selected,
+// summed in slot order.  Shared by both router paths, so they agree bitwise.
+__device__ __forceinline__ void write_slots_and_gates(int (&sel)[16], float (&selv)[16], int k,
+                                                      int32_t* __restrict__ idx_out,
+                                                      float* __restrict__ gate_out, int lane) {
+  for (int a = 1; a < k; ++a) {
+    const int si = sel[a];
+    const float sv = selv[a];
+    int b = a - 1;
+    while (b >= 0 && sel[b] > si) {
+      sel[b + 1] = sel[b];
+      selv[b + 1] = selv[b];
+      --b;
+    }
+    sel[b + 1] = si;
+    selv[b + 1] = sv;
+  }
+  float m = -INFINITY;
+  for (int j = 0; j < k; ++j) m = fmaxf(m, selv[j]);
+  float ex[16];
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    ex[j] = expf(selv[j] - m);
+    S = S + ex[j];
+  }
+  for (int j = lane; j < k; j += 32) {
+    idx_out[j] = sel[j];
+    gate_out[j] = ex[j] / S;
+  }
+}
+
 // One warp per token: k rounds of a warp-shuffle tournament over the N
 // logits, slots sorted by expert index, gates = softmax over the selected.
 __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict__ logits,
@@ -158,31 +190,238 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
     selv[j] = bv;
     if ((bi & 31) == lane) used |= 1u << (bi >> 5);
   }
-  // slots in ascending expert index (insertion sort, same in every lane)
-  for (int a = 1; a < k; ++a) {
-    const int si = sel[a];
-    const float sv = selv[a];
-    int b = a - 1;
-    while (b >= 0 && sel[b] > si) {
-      sel[b + 1] = sel[b];
-      selv[b + 1] = selv[b];
-      --b;
+  write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
+}
+
+
+// ------------------------------------------------------------------------
+// Tensor-core router with a certified candidate filter.
+//
+// The logits are also computed on the tensor cores (the grouped GEMM kernel
+// in identity mode, W_g as the weights operand): l_tc.  tcgen05 does not
+// publish its accumulation order, so l_tc is used only to exclude experts
+// that provably cannot enter the top-k.  With S = sum_i |h_i w_ie| <=
+// ||h_t|| ||w_e|| (Cauchy-Schwarz), the tensor-core result and the canonical
+// fp32 result of the chunked order both lie within their error bounds of the
+// exact dot product, so |l_tc - l_canonical| <= delta_t = beta ||h_t||
+// max_e ||w_e|| (+ the bias roundings), beta covering (K/16 + 1) MMA steps at
+// a per-step relative error of 2^-18 and the (256 + chunks + 1) fp32
+// additions of the canonical order.  If L_k is the k-th largest l_tc, every
+// expert with l_tc < L_k - 2 delta_t has a canonical logit strictly below the
+// canonical k-th value, so only the remaining candidates get their canonical
+// logits computed (in the exact order of router_logits_kernel), and the
+// top-k and gates are chosen from those.  The indices and gates are
+// therefore bit-identical to the CUDA-core router's; only the work differs.
+// Every decision depends on the token's own values alone.
+
+__global__ void __launch_bounds__(256) gate_transpose_kernel(const uint16_t* __restrict__ wg,
+                                                             uint16_t* __restrict__ wgT, int H, int N) {
+  __shared__ uint16_t tile[32][33];
+  const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int i = i0 + r, e = e0 + threadIdx.x;
+    tile[r][threadIdx.x] = (i < H && e < N) ? wg[(size_t)i * N + e] : 0;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int e = e0 + r, i = i0 + threadIdx.x;
+    if (e < N && i < H) wgT[(size_t)e * H + i] = tile[threadIdx.x][r];
+  }
+}
+
+// norm_w[e] >= ||W_g[:, e]||_2 (fp32 sum of squares scaled up to cover its rounding).
+__global__ void __launch_bounds__(256) gate_norm_kernel(const uint16_t* __restrict__ wgT,
+                                                        float* __restrict__ norm_w, int H, int N) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= N) return;
+  float ss = 0.0f;
+  for (int i = lane * 8; i < H; i += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(wgT + (size_t)e * H + i));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
     }
-    sel[b + 1] = si;
-    selv[b + 1] = sv;
   }
-  float m = -INFINITY;
-  for (int j = 0; j < k; ++j) m = fmaxf(m, selv[j]);
-  float ex[16];
-  float S = 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if (lane == 0) norm_w[e] = sqrtf(ss * (1.0f + 0x1p-7f)) * (1.0f + 0x1p-7f);
+}
+
+constexpr int kCertWarps = 8;
+constexpr int kCertMaxH = 8192;   // rows up to 32 chunks: one chunk per lane at most
+constexpr int kCertPass = 16;     // candidates whose canonical logits one pass evaluates
+
+// One warp per token.  Shared memory per warp: candidate list and canonical
+// values, and the chunk partial sums of one pass of candidates.
+struct CertSmem {
+  int cidx[kCertWarps][256];
+  float cval[kCertWarps][256];
+  float part[kCertWarps][kCertPass * 32];
+};
+
+__global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
+    const float* __restrict__ logits_tc, const float* __restrict__ bias, const uint16_t* __restrict__ h,
+    const uint16_t* __restrict__ wgT, const float* __restrict__ norm_w, int T, int H, int N, int k,
+    float beta, int32_t* __restrict__ topk_idx, float* __restrict__ gates, int32_t* __restrict__ n_cand) {
+  __shared__ CertSmem sm;
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kCertWarps + wib;
+  if (t >= T) return;
+  const unsigned full = 0xffffffffu;
+  const uint16_t* hrow = h + (size_t)t * H;
+  // ||h_t||^2
+  float ss = 0.0f;
+  for (int i = lane * 8; i < H; i += 256) {
+    const uint4 hv = __ldg(reinterpret_cast<const uint4*>(hrow + i));
+    const uint32_t w[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+    }
+  }
+  // tensor-core logits (+ bias) of the experts this lane holds, and the
+  // lane's best one under the ranking
+  float v[8];
+  uint32_t present = 0;
+  float vmax_abs = 0.0f, lane_best = 0.0f;
+  int lane_best_e = -1;
+  bool finite = true;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int e = lane + 32 * s;
+    v[s] = 0.0f;
+    if (e < N) {
+      v[s] = logits_tc[(size_t)t * N + e] + (bias ? bias[e] : 0.0f);
+      present |= 1u << s;
+      finite = finite && isfinite(v[s]);
+      vmax_abs = fmaxf(vmax_abs, fabsf(v[s]));
+      if (lane_best_e < 0 || ranks_before(v[s], e, lane_best, lane_best_e)) {
+        lane_best = v[s];
+        lane_best_e = e;
+      }
+    }
+  }
+  float wmax = 0.0f;
+  for (int e = lane; e < N; e += 32) wmax = fmaxf(wmax, norm_w[e]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ss += __shfl_xor_sync(full, ss, off);
+    wmax = fmaxf(wmax, __shfl_xor_sync(full, wmax, off));
+    vmax_abs = fmaxf(vmax_abs, __shfl_xor_sync(full, vmax_abs, off));
+  }
+  finite = __all_sync(full, finite);
+  const float hn = sqrtf(ss * (1.0f + 0x1p-7f)) * (1.0f + 0x1p-7f);
+  const float delta = beta * hn * wmax * (1.0f + 0x1p-6f) + 0x1p-21f * vmax_abs;
+  finite = finite && isfinite(delta);
+  // V = k-th best of the 32 lane bests: at least k experts have l_tc >= V,
+  // so the canonical k-th logit is >= V - delta and every expert with
+  // l_tc < V - 2 delta is out.  (N >= 128 here: every lane holds experts.)
+  float V = 0.0f;
+  {
+    int rank = 0;  // lanes whose best ranks before mine
+    for (int o = 0; o < 32; ++o) {
+      const float ov = __shfl_sync(full, lane_best, o);
+      const int oe = __shfl_sync(full, lane_best_e, o);
+      rank += (oe >= 0 && ranks_before(ov, oe, lane_best, lane_best_e)) ? 1 : 0;
+    }
+    const unsigned who = __ballot_sync(full, rank == k - 1);
+    V = __shfl_sync(full, lane_best, __ffs(who) - 1);
+  }
+  const float cut = V - 2.0f * delta;
+  int nc = 0;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const bool cand = ((present >> s) & 1u) && (!finite || v[s] >= cut);
+    const unsigned m = __ballot_sync(full, cand);
+    if (cand) sm.cidx[wib][nc + __popc(m & ((1u << lane) - 1u))] = lane + 32 * s;
+    nc += __popc(m);
+  }
+  __syncwarp();
+  // canonical logits of the candidates.  Lane (chunk c, group g): c = lane %
+  // C, g = lane / C, G = 32 / C groups; it sums chunk c from +0 in ascending
+  // index with fma for the pass's candidates q = g, g+G, ... (four at a time,
+  // sharing the unpacked token values).  Then each candidate's chunk sums
+  // are added to +0 in ascending chunk order, then the bias.
+  const int C = (H + kRouterChunk - 1) / kRouterChunk;
+  const int G = 32 / C;
+  const int c = lane % C, g = lane / C;
+  const bool active = g < G;
+  const int i0 = c * kRouterChunk, len = min(H, i0 + kRouterChunk) - i0;
+  float* part = sm.part[wib];
+  for (int q0 = 0; q0 < nc; q0 += kCertPass) {
+    const int nq = min(kCertPass, nc - q0);
+    for (int qb = g; active && qb < nq; qb += 4 * G) {
+      int ce[4];
+      float acc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = qb + u * G;
+        ce[u] = (q < nq) ? sm.cidx[wib][q0 + q] : -1;
+        acc[u] = 0.0f;
+      }
+      // 16 elements (two full 32-byte sectors) per step; chunk lengths are
+      // multiples of 128
+      for (int i = 0; i < len; i += 16) {
+        const uint4 hv0 = __ldg(reinterpret_cast<const uint4*>(hrow + i0 + i));
+        const uint4 hv1 = __ldg(reinterpret_cast<const uint4*>(hrow + i0 + i + 8));
+        const uint32_t hw[8] = {hv0.x, hv0.y, hv0.z, hv0.w, hv1.x, hv1.y, hv1.z, hv1.w};
+        float hx[16];
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) hx[ii] = (ii & 1) ? bf16_hi(hw[ii >> 1]) : bf16_lo(hw[ii >> 1]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (ce[u] < 0) continue;
+          const uint4* wp = reinterpret_cast<const uint4*>(wgT + (size_t)ce[u] * H + i0 + i);
+          const uint4 wv0 = __ldg(wp), wv1 = __ldg(wp + 1);
+          const uint32_t ww[8] = {wv0.x, wv0.y, wv0.z, wv0.w, wv1.x, wv1.y, wv1.z, wv1.w};
+#pragma unroll
+          for (int ii = 0; ii < 16; ++ii) {
+            const float wx = (ii & 1) ? bf16_hi(ww[ii >> 1]) : bf16_lo(ww[ii >> 1]);
+            acc[u] = fmaf(hx[ii], wx, acc[u]);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (ce[u] >= 0) part[(qb + u * G) * C + c] = acc[u];
+    }
+    __syncwarp();
+    if (lane < nq) {
+      float total = 0.0f;
+      for (int cc = 0; cc < C; ++cc) total = total + part[lane * C + cc];
+      const int e = sm.cidx[wib][q0 + lane];
+      if (bias) total = total + bias[e];
+      sm.cval[wib][q0 + lane] = total;
+    }
+    __syncwarp();
+  }
+  // top-k among the candidates: each candidate's rank = number of candidates
+  // that beat it; ranks 0..k-1 are selected
+  int sel[16];
+  float selv[16];
+  for (int q = lane; q < nc; q += 32) {
+    const int e = sm.cidx[wib][q];
+    const float cv = sm.cval[wib][q];
+    int rank = 0;
+    for (int o = 0; o < nc; ++o) rank += ranks_before(sm.cval[wib][o], sm.cidx[wib][o], cv, e) ? 1 : 0;
+    if (rank < k) {
+      sm.part[wib][rank] = cv;                 // reuse the partials buffer for the winners
+      reinterpret_cast<int*>(sm.part[wib])[kCertPass * 32 - 16 + rank] = e;
+    }
+  }
+  __syncwarp();
   for (int j = 0; j < k; ++j) {
-    ex[j] = expf(selv[j] - m);
-    S = S + ex[j];
+    selv[j] = sm.part[wib][j];
+    sel[j] = reinterpret_cast<const int*>(sm.part[wib])[kCertPass * 32 - 16 + j];
   }
-  for (int j = lane; j < k; j += 32) {
-    topk_idx[(size_t)t * k + j] = sel[j];
-    gates[(size_t)t * k + j] = ex[j] / S;
-  }
+  write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
+  if (n_cand && lane == 0) n_cand[t] = nc;
 }
 
 }  // namespace
@@ -205,6 +444,27 @@ void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float
       cudaFuncSetAttribute(router_logits_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     router_logits_kernel<false><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
   }
+}
+
+void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
+                      cudaStream_t s) {
+  dim3 grid((N + 31) / 32, (H + 31) / 32), block(32, 8);
+  gate_transpose_kernel<<<grid, block, 0, s>>>(w_gate, wgT, H, N);
+  gate_norm_kernel<<<(N + 7) / 8, 256, 0, s>>>(wgT, norm_w, H, N);
+}
+
+float router_cert_beta(int H) {
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+  return (float)((H / 16 + 1) * 0x1p-20 + (kRouterChunk + chunks + 1) * 0x1p-24);
+}
+
+bool route_certified_ok(int H) { return H <= kCertMaxH; }
+
+void launch_route_certified(const float* logits_tc, const float* bias, const uint16_t* h,
+                            const uint16_t* wgT, const float* norm_w, int T, int H, int N, int k,
+                            int32_t* topk_idx, float* gates, int32_t* n_cand, cudaStream_t s) {
+  route_certified_kernel<<<(T + kCertWarps - 1) / kCertWarps, kCertWarps * 32, 0, s>>>(
+      logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
 }
 
 void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,

@@ -1,0 +1,85 @@
+"""The tensor-core router with the certified candidate filter.
+
+For N a multiple of 128 the fused forward (and moe_route without logits)
+filters experts with tensor-core logits and recomputes canonical logits only
+for the candidates.  Its top-k indices and gates must be bit-identical to the
+CUDA-core router's, including exact ties (tokens with h = 0), near-tied
+routers and adversarial experts whose columns differ in one element; and the
+tensor-core logits must stay well inside the error bound the filter assumes.
+"""
+import numpy as np
+import pytest
+
+from synth import bf16_to_f32, f32_to_bf16
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _route_both(moe, cfg, h_d, wg_d, bias_d, ws):
+    import torch
+    T, N, k = h_d.shape[0], cfg["num_experts"], cfg["top_k"]
+    dev = h_d.device
+    out = []
+    for with_logits in (True, False):
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        g = torch.empty((T, k), dtype=torch.float32, device=dev)
+        lg = torch.empty((T, N), dtype=torch.float32, device=dev) if with_logits else None
+        moe.moe_route(cfg, h_d, wg_d, bias_d, idx, g, lg, ws)
+        out.append((idx, g, lg))
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name,T", [("qw", 1), ("qw", 700), ("qw", 8192), ("ds", 5), ("ds", 3000)])
+def test_tensor_core_router_matches_canonical_router(name, T):
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev, dev_bf16
+    wl = W.WORKLOADS[name]
+    cfg = wl.cfg
+    h = W.make_h(wl, T, seed=31)
+    wg, bias = W.make_router(wl)
+    h_d, wg_d = dev_bf16(h), dev_bf16(wg)
+    bias_d = None if bias is None else dev(bias)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    (i_c, g_c, l_c), (i_t, g_t, _) = _route_both(moe, cfg, h_d, wg_d, bias_d, ws)
+    assert torch.equal(i_c, i_t)
+    assert torch.equal(g_c.view(torch.int32), g_t.view(torch.int32))
+    # the tensor-core logits stay far inside the assumed bound
+    ltc = torch.empty((T, wl.num_experts), dtype=torch.float32, device=h_d.device)
+    moe.moe_router_tc_logits(cfg, h_d, wg_d, ltc, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    lc = l_c.double().cpu().numpy() - (0 if bias is None else bias.astype(np.float64))
+    lt = ltc.double().cpu().numpy()
+    hn = np.linalg.norm(bf16_to_f32(h).astype(np.float64), axis=1)
+    wn = np.linalg.norm(bf16_to_f32(wg).astype(np.float64), axis=0).max()
+    bound = moe.moe_router_cert_beta(wl.hidden) * hn * wn + 1e-30
+    ratio = (np.abs(lt - lc).max(axis=1) / bound).max()
+    assert ratio < 1.0 / 16, f"tensor-core error uses {ratio:.3g} of the certified bound"
+
+
+def test_adversarial_near_identical_experts():
+    # 256 experts whose router columns differ from expert 0 in a single
+    # element: every logit is within a few ulps of the others, so almost all
+    # experts are candidates and the canonical order decides the top-k.
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16
+    H, N, k, T = 1024, 256, 8, 96
+    cfg = dict(hidden=H, num_experts=N, top_k=k, intermediate=128, block_size=16)
+    rng = np.random.default_rng(5)
+    base = (rng.standard_normal(H) / np.sqrt(H)).astype(np.float32)
+    wg = np.repeat(base[:, None], N, axis=1)
+    for e in range(N):
+        wg[rng.integers(H), e] *= np.float32(1.0 + 2.0 ** -7)
+    wg_b = f32_to_bf16(wg)
+    h = f32_to_bf16(rng.standard_normal((T, H)).astype(np.float32))
+    h[:4] = 0
+    ws = moe.workspace(cfg, T)
+    (i_c, g_c, _), (i_t, g_t, _) = _route_both(moe, cfg, dev_bf16(h), dev_bf16(wg_b), None, ws)
+    assert torch.equal(i_c, i_t)
+    assert torch.equal(g_c.view(torch.int32), g_t.view(torch.int32))
+    assert (i_t[:4].cpu().numpy() == np.arange(k)).all()   # exact ties: lowest indices
