@@ -145,11 +145,11 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
 }
 
 // Grouped-GEMM tile list from the padded blocks: each expert segment is cut
-// into tiles of kTileRows rows from its start.  Rejects (no tiles, status
+// into tiles of tile_rows rows from its start.  Rejects (no tiles, status
 // bit) a block list that is not sorted by expert or out of range.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
                                                           const int32_t* __restrict__ num_padded, int N,
-                                                          int B, long long max_rows,
+                                                          int B, long long max_rows, int tile_rows,
                                                           GemmTile* __restrict__ tiles,
                                                           int32_t* __restrict__ num_tiles, int max_tiles,
                                                           int* status) {
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     last = lo;
   }
   const int rows = (last - first) * B;
-  const int nt = (rows + kTileRows - 1) / kTileRows;
+  const int nt = (rows + tile_rows - 1) / tile_rows;
   int total = 0;
   const int off = block_exclusive_scan(nt, buf, &total);
   for (int j = 0; j < nt; ++j) {
@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     if (idx < max_tiles) {
       GemmTile tl;
       tl.expert = e;
-      tl.row0 = first * B + j * kTileRows;
-      tl.rows = min(kTileRows, rows - j * kTileRows);
+      tl.row0 = first * B + j * tile_rows;
+      tl.rows = min(tile_rows, rows - j * tile_rows);
       tl.first = off;
       tl.count = nt;
       tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
@@ -263,10 +263,10 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
 }
 
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
-                        int64_t max_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles,
-                        int* status, cudaStream_t s) {
-  build_tiles_kernel<<<1, 256, 0, s>>>(block_expert, num_padded, N, B, (long long)max_rows, tiles,
-                                       num_tiles, max_tiles, status);
+                        int64_t max_rows, int tile_rows, GemmTile* tiles, int32_t* num_tiles,
+                        int max_tiles, int* status, cudaStream_t s) {
+  build_tiles_kernel<<<1, 256, 0, s>>>(block_expert, num_padded, N, B, (long long)max_rows, tile_rows,
+                                       tiles, num_tiles, max_tiles, status);
 }
 
 }  // namespace moe

@@ -2,26 +2,28 @@
 //
 // For each padded expert segment produced by the stable alignment
 // ("Route-Block Membership Selects Packed-AWQ Arithmetic", "The bookkeeping
-// before the matrix multiplication"), token tiles of kTileRows rows run
+// before the matrix multiplication"), token tiles of BN rows run
 //   W13: [g | u] = X . W13_e  ->  a = bf16(silu(g) * u)      (X = x_perm rows)
 //   W2 : y = a . W2_e         ->  y_perm (fp32)
 // The weights are operand A (M = 128 output features, MN-major straight from
-// the [K, features] layout), the tokens operand B (N = 128 rows, K-major).
-// Every tile of every batch runs the same instruction sequence: one tile
-// shape, K from 0 to the end in steps of 64 (four K=16 MMAs each), fp32
+// the [K, features] layout), the tokens operand B (N = BN rows, K-major; BN =
+// 128 for W13, 256 for W2).  Every tile of every batch runs the same
+// instruction sequence: one tile shape per GEMM, K from 0 to the end in steps
+// of 64 (four K=16 MMAs each), fp32
 // accumulation in TMEM, no split-K and no atomics, so the bits of a token's
 // row depend only on that row and the expert's weights ("Why temperature=0
 // Still Gives Different Answers: Batch Invariance": one tile configuration,
 // no split-K).  Which padded block a route lands in changes nothing, unlike
 // the split/non-split schedule classes of the packed kernel that page studies.
 //
-// Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0      TMA producer (weight boxes and the 128-row token tile)
+// Persistent kernel, one CTA per SM, 10 warps:
+//   warp 0      TMA producer (weight boxes and the token tile)
 //   warp 1      TMEM allocation, one elected thread issues tcgen05.mma
-//   warps 2..5  epilogue: tcgen05.ld from TMEM, SiLU*up or fp32 store
-// Smem stages are guarded by full/empty mbarriers, the two TMEM accumulator
-// buffers by tmem_full/tmem_empty, so the epilogue of one tile overlaps the
-// MMAs of the next.  Every wait is bounded (see mbar_wait).
+//   warps 2..9  epilogue: tcgen05.ld from TMEM, SiLU*up or fp32 store (two
+//               warps per TMEM lane quarter, one half of the columns each)
+// Smem stages are guarded by full/empty mbarriers, the TMEM accumulators by
+// tmem_full/tmem_empty; where two buffers fit in the 512 TMEM columns (W2)
+// the epilogue of one tile overlaps the MMAs of the next.  Every wait is bounded (see mbar_wait).
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -33,33 +35,45 @@ namespace {
 
 constexpr int kBK = 64;                             // K per stage: one 128-byte swizzle row
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // 64 K rows x 64 features of bf16
-constexpr uint32_t kBTileBytes = kTileRows * kBK * 2;  // 128 token rows x 64 K
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter, one column half each
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kSmallRows = 32;                      // token box used when a tile has <= 32 rows
+constexpr uint32_t kStageBudget = 192 * 1024;       // shared memory for the operand stages
 
-template <bool kW13>
+constexpr uint32_t pow2_at_least(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// BN = token rows per tile (the N of every MMA): one fixed value per kernel
+// instance, the same for every batch.
+template <bool kW13, int BN>
 struct GemmCfg {
-  static constexpr int kStages = kW13 ? 4 : 6;
   static constexpr uint32_t kABytes = kW13 ? 4 * kBoxBytes : 2 * kBoxBytes;
+  static constexpr uint32_t kBTileBytes = BN * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
-  static constexpr uint32_t kAccCols = kW13 ? 2 * kTileRows : kTileRows;  // one accumulator buffer
-  static constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double buffered
+  static constexpr int kStages = (int)(kStageBudget / kStageBytes) < 6 ? (int)(kStageBudget / kStageBytes) : 6;
+  static constexpr uint32_t kAccCols = kW13 ? 2 * BN : BN;            // one accumulator buffer
+  static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;       // TMEM double buffering
+  static constexpr uint32_t kTmemCols = pow2_at_least(kNumAcc * kAccCols);
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
+  // M = 128 features, N = BN token rows; A (weights) MN-major, B (tokens) K-major.
+  static constexpr uint32_t kIdesc = idesc_bf16(kTileFeat, BN, true, false);
 };
-
-// M = 128 features, N = 128 token rows; A (weights) MN-major, B (tokens) K-major.
-constexpr uint32_t kIdesc = idesc_bf16(kTileFeat, kTileRows, true, false);
 
 struct TileInfo {
   int expert, row0, rows;
 };
 
+template <int BN>
 __device__ __forceinline__ TileInfo tile_of(const GemmArgs& a, int ti) {
   TileInfo t;
   if (a.identity_T) {
     t.expert = 0;
-    t.row0 = ti * kTileRows;
-    t.rows = min(kTileRows, a.identity_T - t.row0);
+    t.row0 = ti * BN;
+    t.rows = min(BN, a.identity_T - t.row0);
   } else {
     const GemmTile g = a.tiles[ti];
     t.expert = g.expert;
@@ -79,8 +93,8 @@ struct Work {
   TileInfo t;
 };
 
-__device__ __forceinline__ Work work_of(const GemmArgs& a, int item, int num_tiles) {
-  const int nf = a.n_feat_tiles;
+template <int BN>
+__device__ __forceinline__ Work work_of(const GemmArgs& a, int item, int num_tiles, int nf) {
   int first = 0, count = num_tiles;
   if (!a.identity_T) {
     const GemmTile g = a.tiles[item / nf];
@@ -88,28 +102,33 @@ __device__ __forceinline__ Work work_of(const GemmArgs& a, int item, int num_til
     count = g.count;
   }
   const int l = item - first * nf;
-  const int G = max(1, min(nf, ((int)gridDim.x + count - 1) / count));
+  const int waves = a.concurrent;  // work units that run at the same time
+  const int G = max(1, min(nf, (waves + count - 1) / count));
   const int grp = l / (count * G);
   const int gsz = min(G, nf - grp * G);
   const int lin = l - grp * count * G;
   Work w;
   w.f = grp * G + lin % gsz;
-  w.t = tile_of(a, first + lin / gsz);
+  w.t = tile_of<BN>(a, first + lin / gsz);
   return w;
 }
 
-template <bool kW13>
+template <bool kW13, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
-                       const __grid_constant__ CUtensorMap x_map, const GemmArgs args) {
-  using C = GemmCfg<kW13>;
+                       const __grid_constant__ CUtensorMap x_map,
+                       const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
+  using C = GemmCfg<kW13, BN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
 
-  const int num_tiles = args.identity_T ? (args.identity_T + kTileRows - 1) / kTileRows : *args.num_tiles;
-  const int total = num_tiles * args.n_feat_tiles;
-  if ((int)blockIdx.x >= total) return;  // uniform for the whole CTA
+  const int num_tiles = args.identity_T ? (args.identity_T + BN - 1) / BN : *args.num_tiles;
+  const int nfe = args.n_feat_tiles;
+  const int unit0 = (int)blockIdx.x;
+  const int units = (int)gridDim.x;
+  const int total = num_tiles * nfe;
+  if (unit0 >= total) return;  // uniform for the whole CTA
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -127,9 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kNumAcc; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4 * 32);
+      mbar_init(tempty0 + 8 * b, kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     s_abort = 0;
@@ -142,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&w_map);
     prefetch_tmap(&x_map);
+    prefetch_tmap(&x_map_small);
   }
   tc_fence_before();
   __syncthreads();
@@ -156,12 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int armed = 0;  // stages armed and not yet known consumed (for the abort path)
     bool ok = true;
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      const Work wk = work_of(args, item, num_tiles);
+    for (int item = unit0; item < total && ok; item += units) {
+      const Work wk = work_of<BN>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
       const int f = wk.f;
       const int wrow0 = t.expert * args.w_rows_per_e;
       const int fcol = f * kTileFeat;
+      // A tile with few rows (decode) loads a 32-row token box: the rows past
+      // it keep stale data, which only feeds MMA columns that are never
+      // stored (columns of an MMA are independent).
+      const bool small = t.rows <= kSmallRows;
+      const int b_rows = small ? kSmallRows : BN;
+      const uint32_t stage_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
         // one lane waits, the warp follows its verdict (keeps the warp converged)
         int got = 1;
@@ -176,14 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = full0 + 8 * stage;
         const int k0 = ks * kBK;
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          mbar_arrive_expect_tx(fb, stage_tx);
           tma_load_2d(smem_u32(sA), &w_map, fcol, wrow0 + k0, fb, pol_w);
           tma_load_2d(smem_u32(sA + kBoxBytes), &w_map, fcol + 64, wrow0 + k0, fb, pol_w);
           if (kW13) {
             tma_load_2d(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
             tma_load_2d(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb, pol_w);
           }
-          tma_load_2d(smem_u32(sB), &x_map, k0, t.row0, fb, pol_x);
+          tma_load_2d(smem_u32(sB), small ? &x_map_small : &x_map, k0, t.row0, fb, pol_x);
         }
         __syncwarp();
         armed = min(armed + 1, C::kStages);
@@ -219,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      for (int item = unit0; item < total && ok; item += units) {
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
           ok = false;
           break;
@@ -242,10 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 1 KB apart (SBO); a K=16 step is 16 rows = 2 KB.
             const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16(d0, adesc, bdesc, kIdesc, accum);
+            mma_bf16(d0, adesc, bdesc, C::kIdesc, accum);
             if (kW13) {
               const uint64_t adesc_up = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
-              mma_bf16(d0 + kTileRows, adesc_up, bdesc, kIdesc, accum);
+              mma_bf16(d0 + BN, adesc_up, bdesc, C::kIdesc, accum);
             }
           }
           mma_commit(empty0 + 8 * stage);
@@ -256,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(tfull0 + 8 * acc);
-        if (++acc == 2) {
+        if (++acc == C::kNumAcc) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -275,10 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int feat_local = quarter * 32 + lane;
+    const int col0 = ((warp - 2) / 4) * (BN / 2), col1 = col0 + BN / 2;  // this warp's column half
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      const Work wk = work_of(args, item, num_tiles);
+    for (int item = unit0; item < total; item += units) {
+      const Work wk = work_of<BN>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
       const int f = wk.f;
       int got = 1;
@@ -294,12 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
       const int feat = f * kTileFeat + feat_local;
-      for (int c = 0; c < kTileRows && c < t.rows; c += 16) {
+      for (int c = col0; c < col1 && c < t.rows; c += 16) {
         float g[16];
         tmem_ld16(tbase + c, g);
         if (kW13) {
           float u[16];
-          tmem_ld16(tbase + kTileRows + c, u);
+          tmem_ld16(tbase + BN + c, u);
           tmem_wait_ld();
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
 #pragma unroll
@@ -324,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
-      if (++acc == 2) {
+      if (++acc == C::kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -337,21 +364,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <bool kW13>
-void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a, int max_tiles,
-            int num_sms, cudaStream_t s) {
+template <bool kW13, int BN>
+void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+            GemmArgs a, int max_tiles, int num_sms, cudaStream_t s) {
+  auto kernel = expert_gemm_kernel<kW13, BN>;
+  const int smem = (int)GemmCfg<kW13, BN>::kSmemBytes;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaFuncSetAttribute(expert_gemm_kernel<kW13>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)GemmCfg<kW13>::kSmemBytes);
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const long long items = (long long)max_tiles * a.n_feat_tiles;
   if (items <= 0) return;
   const int grid = (int)(items < num_sms ? items : num_sms);
-  expert_gemm_kernel<kW13><<<grid, kThreads, GemmCfg<kW13>::kSmemBytes, s>>>(w_map, x_map, a);
+  a.concurrent = grid;
+  kernel<<<grid, kThreads, smem, s>>>(w_map, x_map, x_small, a);
 }
 
 }  // namespace
@@ -360,17 +389,24 @@ bool gemm_smem_ok() {
   int dev = 0, optin = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  return optin >= (int)GemmCfg<true>::kSmemBytes && optin >= (int)GemmCfg<false>::kSmemBytes;
+  return optin >= (int)GemmCfg<true, kW13TileRows>::kSmemBytes &&
+         optin >= (int)GemmCfg<false, kW2TileRows>::kSmemBytes &&
+         optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes;
 }
 
-void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
-                     int max_tiles, int num_sms, cudaStream_t s) {
-  launch<true>(w_map, x_map, a, max_tiles, num_sms, s);
+void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
+  launch<true, kW13TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
 }
 
-void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
-                    int max_tiles, int num_sms, cudaStream_t s) {
-  launch<false>(w_map, x_map, a, max_tiles, num_sms, s);
+void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                    const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
+  launch<false, kW2TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+}
+
+void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
+  launch<false, kRouterTileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
 }
 
 }  // namespace moe

@@ -11,9 +11,16 @@ constexpr int kDevErrExpertRange = 0x1;
 constexpr int kDevErrTimeout = 0x2;
 constexpr int kDevErrBadBlocks = 0x4;
 
-// Rows of one grouped-GEMM token tile (the N of every tcgen05 MMA).  Fixed
-// for every layer and every T: one tile shape, one K order.
-constexpr int kTileRows = 128;
+// Rows of one grouped-GEMM token tile (the N of every tcgen05 MMA), one
+// fixed value per GEMM for every layer and every T: one tile shape, one K
+// order.  W2 takes 256-row tiles (fewer shared-memory bytes per flop); W13
+// keeps 128 rows so that its gate and up accumulators stay double-buffered in
+// the 512 TMEM columns and the epilogue overlaps the next tile's MMAs; the
+// router's tensor-core logits use 128.
+constexpr int kW13TileRows = 128;
+constexpr int kW2TileRows = 256;
+constexpr int kRouterTileRows = 128;
+constexpr int kMaxTileRows = 256;
 // Output features of one grouped-GEMM tile (the M of every MMA).
 constexpr int kTileFeat = 128;
 // Router reduction chunk (elements of H summed in order before combining).
@@ -24,7 +31,7 @@ constexpr int kDispatchTile = 1024;
 struct GemmTile {
   int32_t expert;
   int32_t row0;   // first padded row of the tile
-  int32_t rows;   // valid rows (<= kTileRows)
+  int32_t rows;   // valid rows (<= the tile size)
   int32_t first;  // index of the first tile of this expert in the list
   int32_t count;  // tiles of this expert
   int32_t pad[3];
@@ -53,8 +60,8 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
-                        int64_t max_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles,
-                        int* status, cudaStream_t s);
+                        int64_t max_rows, int tile_rows, GemmTile* tiles, int32_t* num_tiles,
+                        int max_tiles, int* status, cudaStream_t s);
 
 // ---- grouped expert GEMMs (tcgen05)
 struct GemmArgs {
@@ -68,12 +75,17 @@ struct GemmArgs {
   void* out;           // W13: bf16 a [rows, I]; W2: fp32 y [rows, H]
   int out_ld;          // elements per output row
   int* status;
+  int concurrent;      // work units resident at once (set by the launcher)
 };
+
 bool gemm_smem_ok();
-void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
-                     int max_tiles, int num_sms, cudaStream_t s);
-void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const GemmArgs& a,
-                    int max_tiles, int num_sms, cudaStream_t s);
+// x_small: the same token tensor with a 32-row box (tiles with <= 32 rows)
+void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
+void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                    const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
+void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
 
 // ---- combine
 void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,

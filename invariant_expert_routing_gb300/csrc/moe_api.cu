@@ -54,15 +54,16 @@ int64_t max_rows_of(const moe_config* c, int32_t T) {
 int64_t max_blocks_of(const moe_config* c, int32_t T) {
   return (int64_t)T * c->top_k / c->block_size + c->num_experts;
 }
-int64_t max_gemm_tiles_of(const moe_config* c, int32_t T) {
-  return (max_rows_of(c, T) + moe::kTileRows - 1) / moe::kTileRows + c->num_experts;
+int64_t max_gemm_tiles_of(const moe_config* c, int32_t T, int tile_rows) {
+  return (max_rows_of(c, T) + tile_rows - 1) / tile_rows + c->num_experts;
 }
 
 // ----------------------------------------------------------------- workspace
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
   size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
-      num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, x_perm, a, y, a_sh, y_sh, h_stage,
+      num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, gemm_tiles2, num_gemm_tiles2, x_perm,
+      a, y, a_sh, y_sh, h_stage,
       out_stage, total;
 };
 
@@ -93,14 +94,17 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.num_padded = take(sizeof(int32_t));
   L.counts = take(sizeof(int32_t) * N);
   L.dropped = take(sizeof(int32_t));
-  L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T));
+  // tile lists of the W13 (128-row) and W2 (256-row) GEMMs
+  L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW13TileRows));
   L.num_gemm_tiles = take(sizeof(int32_t));
-  // x_perm and a keep kTileRows rows of slack so every 128-row tile load stays inside them
-  L.x_perm = take(sizeof(uint16_t) * (rows + moe::kTileRows) * H);
-  L.a = take(sizeof(uint16_t) * (rows + moe::kTileRows) * c->intermediate);
+  L.gemm_tiles2 = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW2TileRows));
+  L.num_gemm_tiles2 = take(sizeof(int32_t));
+  // x_perm and a keep one tile of rows of slack so every tile load stays inside them
+  L.x_perm = take(sizeof(uint16_t) * (rows + moe::kMaxTileRows) * H);
+  L.a = take(sizeof(uint16_t) * (rows + moe::kMaxTileRows) * c->intermediate);
   L.y = take(sizeof(float) * rows * H);
   const size_t Is = c->shared_intermediate;
-  L.a_sh = take(Is ? sizeof(uint16_t) * ((size_t)T + moe::kTileRows) * Is : 0);
+  L.a_sh = take(Is ? sizeof(uint16_t) * ((size_t)T + moe::kMaxTileRows) * Is : 0);
   L.y_sh = take(Is ? sizeof(float) * (size_t)T * H : 0);
   L.h_stage = take(sizeof(uint16_t) * (size_t)T * H);
   L.out_stage = take(sizeof(uint16_t) * (size_t)T * H);
@@ -162,6 +166,13 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token-tile maps of a GEMM whose tiles have `bn` rows: the full box and the
+// 32-row box used for tiles of at most 32 rows.
+bool token_maps(CUtensorMap* full, CUtensorMap* small, const void* base, uint64_t inner, uint64_t outer,
+                int bn) {
+  return map_2d(full, base, inner, outer, 64, (uint32_t)bn) && map_2d(small, base, inner, outer, 64, 32u);
+}
+
 moe_status last_cuda() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // ----------------------------------------------------------------- stages
@@ -177,9 +188,10 @@ moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const ui
   const int H = c->hidden, N = c->num_experts;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
-  CUtensorMap m_wg, m_h;
+  CUtensorMap m_wg, m_h, m_hs;
   if (!map_2d(&m_wg, wg, (uint64_t)N, (uint64_t)H, 64, 64) ||
-      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, moe::kTileRows))
+      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, moe::kRouterTileRows) ||
+      !map_2d(&m_hs, h, (uint64_t)H, (uint64_t)T, 64, 32))
     return MOE_ERR_CUDA;
   moe::GemmArgs g{};
   g.K = H;
@@ -189,7 +201,8 @@ moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const ui
   g.out = logits;
   g.out_ld = N;
   g.status = at<int>(ws, L.status);
-  moe::launch_w2_gemm(m_wg, m_h, g, (T + moe::kTileRows - 1) / moe::kTileRows, sms, s);
+  moe::launch_router_gemm(m_wg, m_h, m_hs, g, (T + moe::kRouterTileRows - 1) / moe::kRouterTileRows, sms,
+                          s);
   return last_cuda();
 }
 
@@ -236,24 +249,30 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = c->top_k;
   const int64_t rows = max_rows_of(c, T);
-  const int max_tiles = (int)max_gemm_tiles_of(c, T);
+  const int max_tiles13 = (int)max_gemm_tiles_of(c, T, moe::kW13TileRows);
+  const int max_tiles2 = (int)max_gemm_tiles_of(c, T, moe::kW2TileRows);
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   int* status = at<int>(ws, L.status);
-  GemmTile* tiles = at<GemmTile>(ws, L.gemm_tiles);
-  int32_t* ntiles = at<int32_t>(ws, L.num_gemm_tiles);
+  GemmTile* tiles13 = at<GemmTile>(ws, L.gemm_tiles);
+  int32_t* ntiles13 = at<int32_t>(ws, L.num_gemm_tiles);
+  GemmTile* tiles2 = at<GemmTile>(ws, L.gemm_tiles2);
+  int32_t* ntiles2 = at<int32_t>(ws, L.num_gemm_tiles2);
   uint16_t* a = at<uint16_t>(ws, L.a);
-
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
-  moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, tiles, ntiles, max_tiles, status, s);
+
+  moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW13TileRows, tiles13, ntiles13,
+                          max_tiles13, status, s);
+  moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW2TileRows, tiles2, ntiles2,
+                          max_tiles2, status, s);
   moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
   mark(mk, 3);
 
-  CUtensorMap m_w13, m_x, m_w2, m_a;
+  CUtensorMap m_w13, m_x, m_xs, m_w2, m_a, m_as;
   if (!map_2d(&m_w13, w13, 2ull * I, (uint64_t)N * H, 64, 64) ||
-      !map_2d(&m_x, x_perm, (uint64_t)H, (uint64_t)(rows + moe::kTileRows), 64, moe::kTileRows) ||
+      !token_maps(&m_x, &m_xs, x_perm, (uint64_t)H, (uint64_t)(rows + moe::kMaxTileRows), moe::kW13TileRows) ||
       !map_2d(&m_w2, w2, (uint64_t)H, (uint64_t)N * I, 64, 64) ||
-      !map_2d(&m_a, a, (uint64_t)I, (uint64_t)(rows + moe::kTileRows), 64, moe::kTileRows))
+      !token_maps(&m_a, &m_as, a, (uint64_t)I, (uint64_t)(rows + moe::kMaxTileRows), moe::kW2TileRows))
     return MOE_ERR_CUDA;
 
   moe::GemmArgs g13{};
@@ -261,13 +280,13 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.n_feat_tiles = I / moe::kTileFeat;
   g13.w_rows_per_e = H;
   g13.up_col = I;
-  g13.tiles = tiles;
-  g13.num_tiles = ntiles;
+  g13.tiles = tiles13;
+  g13.num_tiles = ntiles13;
   g13.identity_T = 0;
   g13.out = a;
   g13.out_ld = I;
   g13.status = status;
-  moe::launch_w13_gemm(m_w13, m_x, g13, max_tiles, sms, s);
+  moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, max_tiles13, sms, s);
   mark(mk, 4);
 
   moe::GemmArgs g2 = g13;
@@ -275,22 +294,23 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.n_feat_tiles = H / moe::kTileFeat;
   g2.w_rows_per_e = I;
   g2.up_col = 0;
+  g2.tiles = tiles2;
+  g2.num_tiles = ntiles2;
   g2.out = y_perm;
   g2.out_ld = H;
-  moe::launch_w2_gemm(m_w2, m_a, g2, max_tiles, sms, s);
+  moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
   const int Is = c->shared_intermediate;
   if (Is > 0) {
     uint16_t* ash = at<uint16_t>(ws, L.a_sh);
-    CUtensorMap m_w13s, m_w2s, m_ash, m_h;
-    // the last 128-row tile of h may run past row T-1: TMA fills those rows with zeros
-    if (!map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, moe::kTileRows) ||
+    CUtensorMap m_w13s, m_w2s, m_ash, m_ashs, m_h, m_hs;
+    // the last tile of h may run past row T-1: TMA fills those rows with zeros
+    if (!token_maps(&m_h, &m_hs, h, (uint64_t)H, (uint64_t)T, moe::kW13TileRows) ||
         !map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
         !map_2d(&m_w2s, w2s, (uint64_t)H, (uint64_t)Is, 64, 64) ||
-        !map_2d(&m_ash, ash, (uint64_t)Is, (uint64_t)T + moe::kTileRows, 64, moe::kTileRows))
+        !token_maps(&m_ash, &m_ashs, ash, (uint64_t)Is, (uint64_t)T + moe::kMaxTileRows, moe::kW2TileRows))
       return MOE_ERR_CUDA;
-    const int sh_tiles = (T + moe::kTileRows - 1) / moe::kTileRows;
     moe::GemmArgs s13{};
     s13.K = H;
     s13.n_feat_tiles = Is / moe::kTileFeat;
@@ -300,7 +320,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
     s13.out = ash;
     s13.out_ld = Is;
     s13.status = status;
-    moe::launch_w13_gemm(m_w13s, m_h, s13, sh_tiles, sms, s);
+    moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + moe::kW13TileRows - 1) / moe::kW13TileRows, sms, s);
     moe::GemmArgs s2 = s13;
     s2.K = Is;
     s2.n_feat_tiles = H / moe::kTileFeat;
@@ -308,7 +328,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
     s2.up_col = 0;
     s2.out = y_shared;
     s2.out_ld = H;
-    moe::launch_w2_gemm(m_w2s, m_ash, s2, sh_tiles, sms, s);
+    moe::launch_w2_gemm(m_w2s, m_ash, m_ashs, s2, (T + moe::kW2TileRows - 1) / moe::kW2TileRows, sms, s);
   }
   return last_cuda();
 }
@@ -542,10 +562,10 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
 int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   // router (CUDA cores: logits + top-k = 2; tensor cores: transpose, norms,
-  // GEMM, certified select = 4) + dispatch 3 + tile list 1 + row gather 1
+  // GEMM, certified select = 4) + dispatch 3 + tile lists 2 + row gather 1
   // + W13 + W2 + combine 1 (+ shared W13, W2)
   const int router = use_tc_router(cfg) ? 4 : 2;
-  return router + 3 + 1 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
+  return router + 3 + 2 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }
 
 moe_status moe_router_tc_logits(const moe_config* cfg, int32_t T, const uint16_t* h,

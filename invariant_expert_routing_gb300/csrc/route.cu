@@ -26,80 +26,109 @@ constexpr int kRouterWarps = 8;
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// CTA tile: TT = 4*G tokens x NE = 2*P experts.  Lane l of a warp owns the
-// expert pair p = l % P and the token quad g = l / P (P*G = 32).  Warp w sums
-// chunks w, w+8, ...; partial sums go to part[chunk][token][expert].
+// CTA tile: TT = 4*G tokens x NE = 2*P experts (NE <= 32).  Lane l of a warp
+// owns the expert pair p = l % P and the token quad g = l / P (P*G = 32).
+// Warp w sums chunks w, w+8, ...: it first copies the chunk's W_g slice
+// [256 x NE] and the TT token rows [TT x 256] into its shared-memory stage with
+// one burst of independent loads, then runs the in-order fma chains from
+// shared memory.  After each round of 8 chunks the partial sums are added, in
+// ascending chunk order, to running totals held by the threads that own each
+// (token, expert).
 template <bool kEvenN>
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ h,
                                                             const uint16_t* __restrict__ wg,
                                                             const float* __restrict__ bias,
                                                             float* __restrict__ logits, int T, int H,
                                                             int N, int P, int G) {
-  extern __shared__ float part[];
+  extern __shared__ __align__(16) uint8_t rsm[];
   const int NE = 2 * P, TT = 4 * G;
   const int t0 = blockIdx.x * TT, e0 = blockIdx.y * NE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = lane % P, g = lane / P;
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const int ea = e0 + 2 * p, eb = ea + 1;
-  const bool va = ea < N, vb = eb < N;
-  int tok[4];
-  bool vt[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    tok[q] = t0 + 4 * g + q;
-    vt[q] = tok[q] < T;
-  }
-  for (int c = warp; c < chunks; c += kRouterWarps) {
-    float acc[4][2];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.0f;
-    const int i0 = c * kRouterChunk, i1 = min(H, i0 + kRouterChunk);
-    for (int i = i0; i < i1; i += 8) {
-      uint4 hv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        hv[q] = vt[q] ? __ldg(reinterpret_cast<const uint4*>(h + (size_t)tok[q] * H + i))
-                      : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int ii = 0; ii < 8; ++ii) {
-        float wa = 0.0f, wb = 0.0f;
-        const size_t off = (size_t)(i + ii) * N + ea;
+  const size_t stage_bytes = (size_t)kRouterChunk * NE * 2 + (size_t)TT * kRouterChunk * 2;
+  uint32_t* sw = reinterpret_cast<uint32_t*>(rsm + warp * stage_bytes);  // [256][P] expert pairs
+  uint4* sh = reinterpret_cast<uint4*>(rsm + warp * stage_bytes + (size_t)kRouterChunk * NE * 2);  // [TT][32]
+  float* part = reinterpret_cast<float*>(rsm + kRouterWarps * stage_bytes);  // [8][TT][NE]
+  const int slot = TT * NE;
+  constexpr int kMaxOwn = 2;  // (token, expert) pairs per thread: TT*NE <= 512
+  float total[kMaxOwn] = {0.0f, 0.0f};
+  for (int round = 0; round < chunks; round += kRouterWarps) {
+    const int c = round + warp;
+    if (c < chunks) {
+      const int i0 = c * kRouterChunk, len = min(H, i0 + kRouterChunk) - i0;
+      // W_g[i0 .. i0+len, e0 .. e0+NE) as expert pairs; experts >= N read as 0
+      for (int idx = lane; idx < len * P; idx += 32) {
+        const int row = idx / P, pp = idx % P;
+        const int e = e0 + 2 * pp;
+        const size_t off = (size_t)(i0 + row) * N + e;
+        uint32_t v = 0;
         if (kEvenN) {
-          if (va) {
-            uint32_t w2 = __ldg(reinterpret_cast<const unsigned int*>(wg + off));
-            wa = bf16_lo(w2);
-            wb = bf16_hi(w2);
-          }
+          if (e < N) v = __ldg(reinterpret_cast<const unsigned int*>(wg + off));
         } else {
-          if (va) wa = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(wg + off)) << 16);
-          if (vb) wb = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(wg + off + 1)) << 16);
+          if (e < N) v = (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(wg + off));
+          if (e + 1 < N) v |= (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(wg + off + 1)) << 16;
         }
+        sw[row * P + pp] = v;
+      }
+      // token rows t0 .. t0+TT, columns i0 .. i0+len (missing tokens read as 0)
+      const int vec = len / 8;
+      for (int idx = lane; idx < TT * vec; idx += 32) {
+        const int q = idx / vec, v = idx % vec;
+        const int t = t0 + q;
+        sh[q * 32 + v] = (t < T) ? __ldg(reinterpret_cast<const uint4*>(h + (size_t)t * H + i0) + v)
+                                 : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      float acc[4][2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t word = (ii < 2) ? hv[q].x : (ii < 4) ? hv[q].y : (ii < 6) ? hv[q].z : hv[q].w;
-          const float hx = (ii & 1) ? bf16_hi(word) : bf16_lo(word);
-          acc[q][0] = fmaf(hx, wa, acc[q][0]);
-          acc[q][1] = fmaf(hx, wb, acc[q][1]);
+      for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.0f;
+      for (int i = 0; i < len; i += 8) {
+        uint4 hv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hv[q] = sh[(4 * g + q) * 32 + i / 8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          const uint32_t w2 = sw[(i + ii) * P + p];
+          const float wa = bf16_lo(w2), wb = bf16_hi(w2);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t word = (ii < 2) ? hv[q].x : (ii < 4) ? hv[q].y : (ii < 6) ? hv[q].z : hv[q].w;
+            const float hx = (ii & 1) ? bf16_hi(word) : bf16_lo(word);
+            acc[q][0] = fmaf(hx, wa, acc[q][0]);
+            acc[q][1] = fmaf(hx, wb, acc[q][1]);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float* dst = part + ((size_t)c * TT + 4 * g + q) * NE + 2 * p;
-      dst[0] = acc[q][0];
-      dst[1] = acc[q][1];
+      for (int q = 0; q < 4; ++q) {
+        float* dst = part + (size_t)warp * slot + (size_t)(4 * g + q) * NE + 2 * p;
+        dst[0] = acc[q][0];
+        dst[1] = acc[q][1];
+      }
+      __syncwarp();
     }
+    __syncthreads();
+    const int nc = min(kRouterWarps, chunks - round);
+#pragma unroll
+    for (int o = 0; o < kMaxOwn; ++o) {
+      const int idx = threadIdx.x + o * blockDim.x;
+      if (idx < slot)
+        for (int w = 0; w < nc; ++w) total[o] = total[o] + part[(size_t)w * slot + idx];
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < TT * NE; idx += blockDim.x) {
-    const int tl = idx / NE, el = idx % NE;
-    const int t = t0 + tl, e = e0 + el;
-    if (t < T && e < N) {
-      float total = 0.0f;
-      for (int c = 0; c < chunks; ++c) total = total + part[((size_t)c * TT + tl) * NE + el];
-      if (bias) total = total + bias[e];
-      logits[(size_t)t * N + e] = total;
+#pragma unroll
+  for (int o = 0; o < kMaxOwn; ++o) {
+    const int idx = threadIdx.x + o * blockDim.x;
+    if (idx < slot) {
+      const int tl = idx / NE, el = idx % NE;
+      const int t = t0 + tl, e = e0 + el;
+      if (t < T && e < N) {
+        float v = total[o];
+        if (bias) v = v + bias[e];
+        logits[(size_t)t * N + e] = v;
+      }
     }
   }
 }
@@ -428,20 +457,19 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
 
 void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
                           int T, int H, int N, cudaStream_t s) {
-  // NE experts per CTA (power of two, 8..64), P = NE/2 pairs, G = 32/P token quads.
+  // NE experts per CTA (power of two, 8..32), P = NE/2 pairs, G = 32/P token
+  // quads: the tile shape depends on N only, never on T.
   int NE = 8;
-  while (NE < N && NE < 64) NE *= 2;
+  while (NE < N && NE < 32) NE *= 2;
   const int P = NE / 2, G = 32 / P, TT = 4 * G;
-  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const size_t smem = (size_t)chunks * TT * NE * sizeof(float);
+  const size_t stage = (size_t)kRouterChunk * NE * 2 + (size_t)TT * kRouterChunk * 2;
+  const size_t smem = kRouterWarps * stage + (size_t)kRouterWarps * TT * NE * sizeof(float);
   dim3 grid((T + TT - 1) / TT, (N + NE - 1) / NE);
   if (N % 2 == 0) {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(router_logits_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(router_logits_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     router_logits_kernel<true><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
   } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(router_logits_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(router_logits_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     router_logits_kernel<false><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
   }
 }
