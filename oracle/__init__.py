@@ -50,8 +50,13 @@ def lib():
         L.oracle_expert_row.argtypes = [c.c_int32] * 2 + [vp] * 5
         L.oracle_expert_rows.argtypes = [c.c_int32, vp, vp, c.c_int32, c.c_int32] + [vp] * 4 + [c.c_int32]
         L.oracle_combine_rows.argtypes = [c.c_int32, vp, c.c_int32, c.c_int32] + [vp] * 6
-        L.oracle_moe_forward.argtypes = ([c.c_int32] * 6 + [c.c_double, c.c_int32] + [vp] * 8
-                                         + [c.c_int32])
+        L.oracle_moe_forward.argtypes = ([c.c_int32] * 6 + [c.c_double] + [c.c_int32] * 3
+                                         + [vp] * 8 + [c.c_int32])
+        L.oracle_reroute.argtypes = [c.c_int32] * 4 + [vp] * 5
+        L.oracle_routing_stats.argtypes = [c.c_int32] * 3 + [vp, c.c_double] + [vp] * 3
+        L.oracle_expert_choice.argtypes = [c.c_int32] * 3 + [vp] * 3
+        L.oracle_ec_capacity.argtypes = [c.c_int32] * 3 + [c.c_double]
+        L.oracle_ec_capacity.restype = c.c_int32
         L.oracle_bf16_round.argtypes = [c.c_double]
         L.oracle_bf16_round.restype = c.c_uint16
         _lib = L
@@ -117,6 +122,56 @@ def dispatch(topk_idx, N: int, B: int, capacity_: int):
                 num_dropped=int(dropped[0]))
 
 
+def reroute(logits, topk_idx, capacity_: int):
+    """Overflow reroute: returns (route_expert [R] int32, -1 = dropped;
+    num_rerouted; num_dropped)."""
+    logits = _c(logits, np.float32)
+    topk_idx = _c(topk_idx, np.int32)
+    T, k = topk_idx.shape
+    N = logits.shape[1]
+    out = np.empty(T * k, dtype=np.int32)
+    nr = np.zeros(1, dtype=np.int32)
+    nd = np.zeros(1, dtype=np.int32)
+    lib().oracle_reroute(T, N, k, capacity_, _p(logits), _p(topk_idx), _p(out), _p(nr), _p(nd))
+    return out, int(nr[0]), int(nd[0])
+
+
+def dispatch_routes(route_expert, N: int, B: int, slots: int):
+    """Stable alignment of routes that already have their expert (-1 = not
+    routed), `slots` routes per token: the layout after reroute or expert
+    choice."""
+    route_expert = _c(route_expert, np.int32).reshape(-1, slots)
+    return dispatch(route_expert, N, B, -1)
+
+
+def routing_stats(topk_idx, N: int, capacity_factor: float = 1.25):
+    """The routing_stats probe: (load [N], dict)."""
+    topk_idx = _c(topk_idx, np.int32)
+    T, k = topk_idx.shape
+    load = np.empty(N, dtype=np.int32)
+    ints = np.empty(5, dtype=np.int32)
+    reals = np.empty(2, dtype=np.float64)
+    lib().oracle_routing_stats(T, N, k, _p(topk_idx), float(capacity_factor), _p(load), _p(ints),
+                               _p(reals))
+    return load, dict(max_expert_load=int(ints[0]), min_expert_load=int(ints[1]),
+                      capacity=int(ints[2]), dropped_tokens=int(ints[3]), total_routes=int(ints[4]),
+                      imbalance_ratio=float(reals[0]), drop_fraction=float(reals[1]))
+
+
+def ec_capacity(T: int, N: int, k: int, capacity_factor: float) -> int:
+    return int(lib().oracle_ec_capacity(T, N, k, float(capacity_factor)))
+
+
+def expert_choice(logits, capacity_: int):
+    """Expert-choice selection: (selected [T, N] uint8, probs [T, N] fp64)."""
+    logits = _c(logits, np.float32)
+    T, N = logits.shape
+    sel = np.empty((T, N), dtype=np.uint8)
+    probs = np.empty((T, N), dtype=np.float64)
+    lib().oracle_expert_choice(T, N, capacity_, _p(logits), _p(sel), _p(probs))
+    return sel, probs
+
+
 def expert_row(x, w13_e, w2_e):
     """One SwiGLU expert on one row: returns (y fp64 [H], a bf16 bits [I])."""
     x = _c(x, np.uint16)
@@ -174,7 +229,8 @@ def moe_forward(cfg: dict, h, w_gate, bias, w13, w2, w13s=None, w2s=None,
     N, k, I, B = cfg["num_experts"], cfg["top_k"], cfg["intermediate"], cfg["block_size"]
     Is = cfg.get("shared_intermediate", 0) or 0
     out = np.empty((T, H), dtype=np.uint16)
-    lib().oracle_moe_forward(T, H, N, k, I, B, float(cfg.get("capacity_factor", 0.0)), Is,
+    lib().oracle_moe_forward(T, H, N, k, I, B, float(cfg.get("capacity_factor", 0.0)),
+                             int(cfg.get("overflow_policy", 0)), int(cfg.get("routing", 0)), Is,
                              _p(h), _p(w_gate), _p(bias), _p(w13), _p(w2), _p(w13s), _p(w2s),
                              _p(out), nthreads)
     return out

@@ -212,6 +212,130 @@ void oracle_dispatch(int32_t T, int32_t N, int32_t k, int32_t B, int32_t capacit
   *num_dropped = (int32_t)dropped;
 }
 
+void oracle_reroute(int32_t T, int32_t N, int32_t k, int32_t capacity, const float* logits,
+                    const int32_t* topk_idx, int32_t* route_expert, int32_t* num_rerouted,
+                    int32_t* num_dropped) {
+  const int64_t R = (int64_t)T * k;
+  std::vector<int64_t> used(N, 0);
+  // phase 1: the drop policy's rule, first `capacity` routes of each expert
+  for (int64_t r = 0; r < R; ++r) {
+    int32_t e = topk_idx[r];
+    route_expert[r] = -1;
+    if (e < 0 || e >= N) continue;
+    if (capacity < 0 || used[e] < capacity) {
+      route_expert[r] = e;
+      used[e] += 1;
+    }
+  }
+  int32_t rerouted = 0, dropped = 0;
+  // phase 2: overflowing routes in ascending route id, each to the token's
+  // best-ranked expert with room that the token does not use yet
+  std::vector<int32_t> order(N);
+  for (int64_t r = 0; r < R && capacity >= 0; ++r) {
+    int32_t e = topk_idx[r];
+    if (e < 0 || e >= N || route_expert[r] >= 0) continue;
+    const int64_t t = r / k;
+    const float* l = logits + (size_t)t * N;
+    for (int32_t x = 0; x < N; ++x) order[x] = x;
+    std::sort(order.begin(), order.end(),
+              [&](int32_t a, int32_t b) { return ranks_before(l[a], a, l[b], b); });
+    int32_t target = -1;
+    for (int32_t cand : order) {
+      if (used[cand] >= capacity) continue;
+      bool taken = false;
+      for (int64_t q = t * k; q < (t + 1) * k; ++q)
+        if (topk_idx[q] == cand || (q < r && route_expert[q] == cand)) taken = true;
+      if (taken) continue;
+      target = cand;
+      break;
+    }
+    if (target >= 0) {
+      route_expert[r] = target;
+      used[target] += 1;
+      ++rerouted;
+    } else {
+      ++dropped;
+    }
+  }
+  *num_rerouted = rerouted;
+  *num_dropped = dropped;
+}
+
+void oracle_routing_stats(int32_t T, int32_t N, int32_t k, const int32_t* topk_idx,
+                          double capacity_factor, int32_t* load, int32_t* ints, double* reals) {
+  for (int32_t e = 0; e < N; ++e) load[e] = 0;
+  int64_t total = 0;
+  for (int64_t r = 0; r < (int64_t)T * k; ++r) {
+    int32_t e = topk_idx[r];
+    if (e < 0 || e >= N) continue;
+    load[e] += 1;
+    total += 1;
+  }
+  for (int i = 0; i < 5; ++i) ints[i] = 0;
+  reals[0] = reals[1] = 0.0;
+  if (total == 0) return;
+  int32_t mx = load[0], mn = load[0];
+  for (int32_t e = 1; e < N; ++e) {
+    mx = std::max(mx, load[e]);
+    mn = std::min(mn, load[e]);
+  }
+  const double mean = (double)total / (double)N;
+  const int32_t cap = (int32_t)std::floor(mean * capacity_factor);
+  int64_t drops = 0;
+  for (int32_t e = 0; e < N; ++e) drops += std::max<int64_t>(0, (int64_t)load[e] - cap);
+  ints[0] = mx;
+  ints[1] = mn;
+  ints[2] = cap;
+  ints[3] = (int32_t)drops;
+  ints[4] = (int32_t)total;
+  reals[0] = (double)mx / mean;
+  reals[1] = (double)drops / (double)total;
+}
+
+int32_t oracle_ec_capacity(int32_t T, int32_t N, int32_t k, double capacity_factor) {
+  const double cf = capacity_factor > 0.0 ? capacity_factor : 1.0;
+  const int32_t c = (int32_t)std::ceil(cf * (double)T * (double)k / (double)N);
+  return std::min(c, T);
+}
+
+void oracle_expert_choice(int32_t T, int32_t N, int32_t capacity, const float* logits,
+                          uint8_t* selected, double* probs) {
+  std::vector<double> key((size_t)T * N);
+  for (int32_t t = 0; t < T; ++t) {
+    const float* l = logits + (size_t)t * N;
+    double m = -std::numeric_limits<double>::infinity();
+    for (int32_t e = 0; e < N; ++e)
+      if (!std::isnan(l[e])) m = std::max(m, (double)l[e]);
+    double s = 0.0;
+    for (int32_t e = 0; e < N; ++e)
+      if (!std::isnan(l[e])) s += std::exp((double)l[e] - m);
+    const double log_s = std::log(s);
+    for (int32_t e = 0; e < N; ++e) {
+      // log p = (l - m) - log(sum): shifting all of a token's logits by a
+      // constant leaves every term, and so the key, unchanged
+      const double kv = std::isnan(l[e]) ? std::numeric_limits<double>::quiet_NaN()
+                                         : ((double)l[e] - m) - log_s;
+      key[(size_t)t * N + e] = kv;
+      probs[(size_t)t * N + e] = std::exp(kv);
+      selected[(size_t)t * N + e] = 0;
+    }
+  }
+  const int32_t C = std::min(std::max(capacity, 0), T);
+  std::vector<int32_t> order(T);
+  for (int32_t e = 0; e < N; ++e) {
+    for (int32_t t = 0; t < T; ++t) order[t] = t;
+    // larger key first, NaN last, equal keys by lower token index
+    std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+      const double ka = key[(size_t)a * N + e], kb = key[(size_t)b * N + e];
+      const bool na = std::isnan(ka), nb = std::isnan(kb);
+      if (na != nb) return nb;
+      if (!na && ka != kb) return ka > kb;
+      return a < b;
+    });
+    for (int32_t i = 0; i < C; ++i) selected[(size_t)order[i] * N + e] = 1;
+  }
+}
+
 void oracle_expert_row(int32_t H, int32_t I, const uint16_t* x, const uint16_t* w13,
                        const uint16_t* w2, double* y, uint16_t* a_out) {
   std::vector<double> g(I, 0.0), u(I, 0.0);
@@ -266,37 +390,63 @@ void oracle_combine_rows(int32_t n, const int32_t* tokens, int32_t H, int32_t k,
 }
 
 void oracle_moe_forward(int32_t T, int32_t H, int32_t N, int32_t k, int32_t I, int32_t B,
-                        double capacity_factor, int32_t Is, const uint16_t* h,
+                        double capacity_factor, int32_t overflow_policy, int32_t routing,
+                        int32_t Is, const uint16_t* h,
                         const uint16_t* w_gate, const float* bias, const uint16_t* w13,
                         const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s,
                         uint16_t* out, int32_t nthreads) {
   if (T <= 0) return;
-  const int64_t R = (int64_t)T * k;
   std::vector<float> logits((size_t)T * N);
   oracle_router_logits(T, H, N, h, w_gate, bias, logits.data(), nthreads);
-  std::vector<int32_t> idx(R);
+  // routes: token choice has k slots per token (its top-k experts), expert
+  // choice has N (slot e = expert e, routed if the expert took the token)
+  const int32_t slots = routing == 1 ? N : k;
+  const int64_t R = (int64_t)T * slots;
+  std::vector<int32_t> route_expert(R);
   std::vector<double> gates(R);
-  oracle_select_topk(T, N, k, logits.data(), idx.data(), gates.data());
-  int32_t cap = oracle_capacity(T, N, k, capacity_factor);
+  if (routing == 1) {
+    std::vector<uint8_t> sel(R);
+    oracle_expert_choice(T, N, oracle_ec_capacity(T, N, k, capacity_factor), logits.data(),
+                         sel.data(), gates.data());
+    for (int64_t r = 0; r < R; ++r) route_expert[r] = sel[r] ? (int32_t)(r % N) : -1;
+  } else {
+    std::vector<int32_t> idx(R);
+    oracle_select_topk(T, N, k, logits.data(), idx.data(), gates.data());
+    int32_t cap = oracle_capacity(T, N, k, capacity_factor);
+    if (overflow_policy == 1) {
+      int32_t rerouted = 0, dropped = 0;
+      oracle_reroute(T, N, k, cap, logits.data(), idx.data(), route_expert.data(), &rerouted,
+                     &dropped);
+    } else {
+      // drop policy: the routes kept by the capacity rule keep their expert
+      std::vector<uint8_t> kept0(R);
+      std::vector<int32_t> pos0(R), sorted0(R + (int64_t)N * B), blocks0(R / B + N + 1), counts0(N);
+      int32_t np0 = 0, nd0 = 0;
+      oracle_dispatch(T, N, k, B, cap, idx.data(), kept0.data(), pos0.data(), sorted0.data(),
+                      blocks0.data(), &np0, counts0.data(), &nd0);
+      for (int64_t r = 0; r < R; ++r) route_expert[r] = kept0[r] ? idx[r] : -1;
+    }
+  }
+  // every route that has an expert is kept; the stable layout follows
   std::vector<uint8_t> kept(R);
   std::vector<int32_t> pos(R), sorted(R + (int64_t)N * B), blocks(R / B + N + 1), counts(N);
   int32_t num_padded = 0, num_dropped = 0;
-  oracle_dispatch(T, N, k, B, cap, idx.data(), kept.data(), pos.data(), sorted.data(),
+  oracle_dispatch(T, N, slots, B, -1, route_expert.data(), kept.data(), pos.data(), sorted.data(),
                   blocks.data(), &num_padded, counts.data(), &num_dropped);
-  // expert outputs for every kept route, stored at [t, j]
-  std::vector<int32_t> toks, exps, slots;
+  // expert outputs for every kept route, stored at [t, slot]
+  std::vector<int32_t> toks, exps, slot_of;
   for (int64_t r = 0; r < R; ++r)
     if (kept[r]) {
-      toks.push_back((int32_t)(r / k));
-      exps.push_back(idx[r]);
-      slots.push_back((int32_t)r);
+      toks.push_back((int32_t)(r / slots));
+      exps.push_back(route_expert[r]);
+      slot_of.push_back((int32_t)r);
     }
   std::vector<double> y_kept(toks.size() * (size_t)H);
   oracle_expert_rows((int32_t)toks.size(), toks.data(), exps.data(), H, I, h, w13, w2,
                      y_kept.data(), nthreads);
   std::vector<double> y_route((size_t)R * H, 0.0);
-  for (size_t i = 0; i < slots.size(); ++i)
-    std::memcpy(&y_route[(size_t)slots[i] * H], &y_kept[i * H], sizeof(double) * H);
+  for (size_t i = 0; i < slot_of.size(); ++i)
+    std::memcpy(&y_route[(size_t)slot_of[i] * H], &y_kept[i * H], sizeof(double) * H);
   std::vector<double> y_shared;
   if (Is > 0 && w13s && w2s) {
     y_shared.assign((size_t)T * H, 0.0);
@@ -306,7 +456,7 @@ void oracle_moe_forward(int32_t T, int32_t H, int32_t N, int32_t k, int32_t I, i
   }
   std::vector<int32_t> all(T);
   for (int32_t t = 0; t < T; ++t) all[t] = t;
-  oracle_combine_rows(T, all.data(), H, k, h, gates.data(), kept.data(), y_route.data(),
+  oracle_combine_rows(T, all.data(), H, slots, h, gates.data(), kept.data(), y_route.data(),
                       y_shared.empty() ? nullptr : y_shared.data(), out);
 }
 

@@ -56,6 +56,52 @@ void oracle_dispatch(int32_t T, int32_t N, int32_t k, int32_t B, int32_t capacit
                      int32_t* sorted_route_ids, int32_t* block_expert, int32_t* num_padded,
                      int32_t* expert_counts, int32_t* num_dropped);
 
+/* Overflow policy "reroute" ("Mixture-of-Experts Routing at Inference Time",
+ * Figure 2 and the mitigations after routing_stats: an overflowing token goes
+ * to its next-choice expert instead of skipping the expert tier).
+ * Phase 1 is the drop policy's capacity rule (each expert keeps its first
+ * `capacity` routes by ascending route id).  Phase 2 takes the routes that
+ * overflowed, in ascending route id; each goes to the best-ranked expert (the
+ * top-k total order on the token's logits) that still has room and that the
+ * token does not already use (its k chosen experts and the targets of its
+ * earlier slots).  A route with no such expert stays dropped.
+ *   route_expert [R]  expert the route is finally sent to, -1 if dropped
+ * capacity < 0 (no limit): nothing overflows.  Entries of topk_idx outside
+ * [0, N) are not routed (-1, not counted). */
+void oracle_reroute(int32_t T, int32_t N, int32_t k, int32_t capacity, const float* logits,
+                    const int32_t* topk_idx, int32_t* route_expert, int32_t* num_rerouted,
+                    int32_t* num_dropped);
+
+/* routing_stats of "Mixture-of-Experts Routing at Inference Time" (section
+ * "The hard part"): per-expert load = number of routes in topk_idx [T, k]
+ * naming the expert (ids outside [0, N) are ignored); mean = total / N;
+ * probe capacity = floor(mean * capacity_factor); dropped = sum over experts
+ * of max(0, load - capacity).  All in fp64:
+ *   load [N];  ints = {max_load, min_load, capacity, dropped, total}
+ *   reals = {imbalance_ratio = max_load / mean, drop_fraction = dropped / total}
+ * With no routes every output is 0. */
+void oracle_routing_stats(int32_t T, int32_t N, int32_t k, const int32_t* topk_idx,
+                          double capacity_factor, int32_t* load, int32_t* ints, double* reals);
+
+/* Expert-choice routing ("Mixture-of-experts routing and LLM repeatability":
+ * each expert takes its highest-scoring tokens of the batch; "Mixture-of-
+ * Experts Routing at Inference Time", section "Integration: where routing
+ * lives in a serving stack", the comparison of routing variants: each expert
+ * picks the tokens it will take, up to its capacity).  Scores are the softmax
+ * probabilities over the N experts.  Routes are r = t*N + e.
+ *   key[t,e] = (l[t,e] - m) - log(sum_e exp(l[t,e] - m))   (fp64, the log
+ *              of the probability; m = max non-NaN logit, the sum in
+ *              ascending e, NaN logits left out of it and given a NaN key)
+ *   expert e takes the `capacity` tokens with the largest key (NaN lowest,
+ *   equal keys: lower token index first); capacity is clipped to T.
+ *   selected [T*N] 1 if expert e took token t;  probs [T*N] = exp(key). */
+void oracle_expert_choice(int32_t T, int32_t N, int32_t capacity, const float* logits,
+                          uint8_t* selected, double* probs);
+
+/* Capacity of expert-choice routing: ceil(cf*T*k/N) with cf = 1 when cf <= 0,
+ * clipped to T. */
+int32_t oracle_ec_capacity(int32_t T, int32_t N, int32_t k, double capacity_factor);
+
 /* SwiGLU expert on one token row, fp64 accumulation:
  *   g = x . W13[:, 0:I], u = x . W13[:, I:2I], a = bf16(silu(g) * u), y = a . W2
  * x [H] bf16, w13 [H, 2I], w2 [I, H]; y [H] fp64; a_out [I] bf16 bits or NULL. */
@@ -79,9 +125,14 @@ void oracle_combine_rows(int32_t n, const int32_t* tokens, int32_t H, int32_t k,
 
 /* Whole layer for all T tokens (small shapes): router, top-k, capacity,
  * alignment, routed and shared SwiGLU experts, combine.  w13s/w2s may be NULL
- * (no shared expert).  out [T,H] bf16 bits. */
+ * (no shared expert).  overflow_policy 0 drops overflowing routes, 1 reroutes
+ * them (oracle_reroute; the route keeps its slot's gate).  routing 0 is
+ * token choice (top-k), 1 is expert choice (oracle_expert_choice; a token's
+ * routes are its N slots e = 0..N-1, gate = probability, summed in ascending
+ * e).  out [T,H] bf16 bits. */
 void oracle_moe_forward(int32_t T, int32_t H, int32_t N, int32_t k, int32_t I, int32_t B,
-                        double capacity_factor, int32_t Is, const uint16_t* h,
+                        double capacity_factor, int32_t overflow_policy, int32_t routing,
+                        int32_t Is, const uint16_t* h,
                         const uint16_t* w_gate, const float* bias, const uint16_t* w13,
                         const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s,
                         uint16_t* out, int32_t nthreads);
