@@ -50,18 +50,48 @@
 extern "C" {
 #endif
 
+/* Overflow policy for routes past an expert's capacity ("Mixture-of-Experts
+ * Routing at Inference Time", Figure 2): drop (the route adds nothing; the
+ * token keeps its residual and its other routes) or reroute (the route moves
+ * to the token's best-ranked expert that still has room and that the token
+ * does not use yet; it keeps its slot's gate). */
+#define MOE_OVERFLOW_DROP 0
+#define MOE_OVERFLOW_REROUTE 1
+/* Routing: token choice (each token takes its top-k experts) or expert choice
+ * (each expert takes its top-C tokens of the batch by softmax probability;
+ * "Mixture-of-experts routing and LLM repeatability"). */
+#define MOE_ROUTING_TOKEN_CHOICE 0
+#define MOE_ROUTING_EXPERT_CHOICE 1
+
 /* Layer shape.  Supported: H % 128 == 0, I % 128 == 0, Is % 128 == 0,
  * 1 <= N <= 256, 1 <= k <= min(N, 16), B % 8 == 0 and 8 <= B <= 128 with
- * 128 % B == 0, T <= 1,048,576 and T*k < 2^31. */
+ * 128 % B == 0, T <= 1,048,576 and T*S < 2^31, S = route slots per token
+ * (k for token choice, N for expert choice).  Zero-initialise the struct:
+ * zero is the default of every field. */
 typedef struct moe_config {
   int32_t hidden;              /* H */
   int32_t num_experts;         /* N routed experts */
-  int32_t top_k;               /* k */
+  int32_t top_k;               /* k (expert choice: average experts per token) */
   int32_t intermediate;        /* I, routed expert FFN width */
   int32_t block_size;          /* B, rows per padded expert block */
-  float capacity_factor;       /* > 0: capacity ceil(cf*T*k/N) per expert; <= 0: no limit */
+  float capacity_factor;       /* > 0: capacity ceil(cf*T*k/N) per expert; <= 0: no limit
+                                  (expert choice: cf = 1, capacity clipped to T) */
   int32_t shared_intermediate; /* Is of the always-on shared expert; 0: none */
+  int32_t overflow_policy;     /* MOE_OVERFLOW_DROP or MOE_OVERFLOW_REROUTE (token choice) */
+  int32_t routing;             /* MOE_ROUTING_TOKEN_CHOICE or MOE_ROUTING_EXPERT_CHOICE */
 } moe_config;
+
+/* Output of moe_routing_stats (device memory, 40 bytes). */
+typedef struct moe_route_stats {
+  int32_t max_expert_load;  /* routes naming the busiest expert */
+  int32_t min_expert_load;  /* routes naming the idlest expert */
+  int32_t capacity;         /* probe capacity floor(mean load * capacity_factor) */
+  int32_t dropped_tokens;   /* sum over experts of max(0, load - capacity) */
+  int32_t total_routes;     /* routes with an expert id in [0, N) */
+  int32_t reserved;         /* 0 */
+  double imbalance_ratio;   /* max load / mean load */
+  double drop_fraction;     /* dropped_tokens / total_routes */
+} moe_route_stats;
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -86,12 +116,15 @@ moe_status moe_check_config(const moe_config* cfg);
 
 /* Expert capacity for a batch of T tokens: ceil(cf*T*k/N), or -1 (no limit).
  * Capacity per "Mixture-of-experts routing and LLM repeatability" (tokens per
- * expert times a capacity factor), rounded up. */
+ * expert times a capacity factor), rounded up.  Expert choice: the tokens
+ * each expert takes, min(ceil(cf*T*k/N), T) with cf = 1 when cf <= 0. */
 int32_t moe_capacity(const moe_config* cfg, int32_t T);
 
 /* Upper bounds used to size caller buffers for T tokens:
  *   rows of sorted_route_ids (and of y_perm):  T*k + N*(B-1)
- *   entries of block_expert:                   (T*k)/B + N                */
+ *   entries of block_expert:                   (T*k)/B + N
+ * Expert choice: N*P rows and N*P/B blocks exactly, P = moe_capacity rounded
+ * up to a multiple of B. */
 int64_t moe_max_padded_rows(const moe_config* cfg, int32_t T);
 int64_t moe_max_blocks(const moe_config* cfg, int32_t T);
 
@@ -117,6 +150,13 @@ size_t moe_workspace_bytes(const moe_config* cfg, int32_t max_tokens);
 moe_status moe_route(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w_gate,
                      const float* router_bias, int32_t* topk_idx, float* topk_gate,
                      float* logits_out, void* ws, size_t ws_bytes, void* stream);
+
+/* The router logits alone: logits_out [T, N] fp32, every expert, in the
+ * fixed order of moe_route (CUDA cores).  Input of expert-choice routing,
+ * overflow reroute and the router margin. */
+moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h,
+                             const uint16_t* w_gate, const float* router_bias, float* logits_out,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /* Router paths.  With logits_out != NULL, when N is not a multiple of 128, or
  * when H > 8192, moe_route computes every logit in the canonical order on CUDA cores.
@@ -169,10 +209,76 @@ moe_status moe_dispatch_align(const moe_config* cfg, int32_t T, const int32_t* t
                               uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                               int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                               int32_t* num_dropped, void* ws, size_t ws_bytes, void* stream);
+/* moe_dispatch_align implements the drop policy only: with
+ * cfg->overflow_policy == MOE_OVERFLOW_REROUTE and a capacity in force, or with
+ * expert-choice routing, it returns MOE_ERR_INVALID_ARG rather than dropping
+ * routes the caller asked to keep (use the two entry points below). */
+
+/* Capacity dispatch with the reroute overflow policy, then the same stable
+ * alignment.  Phase one is moe_dispatch_align's capacity rule.  Phase two
+ * takes the routes it would drop in ascending route id; each goes to the
+ * best-ranked expert of its token (the router's order on logits [T, N], the
+ * fp32 logits of every expert, e.g. from moe_router_logits) that has room left
+ * and that the token does not use yet (its k chosen experts and the targets of
+ * its earlier slots).  A route with no such expert is dropped.  The rerouted
+ * route keeps its slot j and gate; moe_combine needs nothing else.
+ * Outputs as moe_dispatch_align, plus
+ *   route_expert [T*k] int32, expert each route is sent to, -1 if dropped
+ *   num_rerouted [1] int32;  num_dropped counts the routes left dropped;
+ *   expert_counts counts all routes each expert processes.
+ * Integer results only: identical bits on every run.  cfg->overflow_policy is
+ * not consulted (this entry point is the reroute policy). */
+moe_status moe_dispatch_align_reroute(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                                      const float* logits, uint8_t* route_kept, int32_t* route_expert,
+                                      int32_t* route_pos, int32_t* sorted_route_ids,
+                                      int32_t* block_expert, int32_t* num_padded,
+                                      int32_t* expert_counts, int32_t* num_dropped,
+                                      int32_t* num_rerouted, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert-choice routing with its padded layout (cfg->routing must be
+ * MOE_ROUTING_EXPERT_CHOICE).  From logits [T, N] (moe_router_logits) every
+ * expert takes its C = moe_capacity(cfg, T) tokens of largest probability:
+ * the key is log p = (l - m) - log(sum_e exp(l_e - m)) in fp64 (m = largest
+ * logit, sum in ascending e; NaN logits rank last), equal keys by lower token
+ * index.  A token may be taken by no expert (its output is then h plus the
+ * shared expert).  Routes are r = t*N + e:
+ *   gates       [T*N] fp32 out, softmax probability of every (t, e)
+ *   route_kept  [T*N] uint8 out, 1 if expert e took token t
+ *   route_pos   [T*N] int32 out, row in sorted_route_ids, -1 if not taken
+ *   sorted_route_ids [moe_max_padded_rows], block_expert [moe_max_blocks],
+ *   num_padded [1], expert_counts [N] (= C for every expert): as in
+ *   moe_dispatch_align, expert e's tokens in ascending t, padded with T*N.
+ * moe_expert_ffn and moe_combine then run with N slots per token. */
+moe_status moe_route_expert_choice(const moe_config* cfg, int32_t T, const float* logits,
+                                   float* gates, uint8_t* route_kept, int32_t* route_pos,
+                                   int32_t* sorted_route_ids, int32_t* block_expert,
+                                   int32_t* num_padded, int32_t* expert_counts, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* The routing_stats probe of "Mixture-of-Experts Routing at Inference Time"
+ * (section "The hard part: token dropping is a silent correctness bug") on
+ * topk_idx [T, k] (token choice): expert_load [N] int32 out (routes naming
+ * each expert), stats (device) out.  capacity_factor sets the probe's own
+ * capacity floor(mean * cf) (1.25 in the page's probe); it is independent of
+ * the layer's capacity.  fp64 results are single IEEE operations on the
+ * integer counts.  Asynchronous; ids outside [0, N) are not counted. */
+moe_status moe_routing_stats(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                             double capacity_factor, int32_t* expert_load, moe_route_stats* stats,
+                             void* stream);
+
+/* Router margin per token ("Mixture-of-experts routing and LLM
+ * repeatability"): margin [T] fp64 out = l_(k) - l_(k+1), the k-th and
+ * (k+1)-th logits of logits [T, N] under the router's ranking, as the fp64
+ * difference of the two fp32 values; +inf when k = N, NaN if either is NaN.
+ * A small margin marks a token whose experts a small numerical change can
+ * flip. */
+moe_status moe_router_margin(const moe_config* cfg, int32_t T, const float* logits, double* margin,
+                             void* stream);
 
 /* Grouped SwiGLU expert FFN over the padded blocks, on tcgen05 tensor cores:
  *   for every padded row p of expert e = block_expert[p / B] with route r:
- *     x = h[r / k] (zero for the sentinel), [g | u] = x . W13_e,
+ *     x = h[r / S] (S = k, or N for expert choice; zero for the sentinel),
+ *     [g | u] = x . W13_e,
  *     a = bf16(silu(g) * u), y_perm[p] = a . W2_e  (fp32)
  *   and, when cfg->shared_intermediate > 0, y_shared[t] = SwiGLU_shared(h[t]).
  *   w13 [N, H, 2I] bf16 (gate columns 0..I-1, up columns I..2I-1),
@@ -190,16 +296,22 @@ moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const uint16_t* h, c
                           float* y_shared, void* ws, size_t ws_bytes, void* stream);
 
 /* Gate-weighted combine into the residual:
- *   out[t] = bf16( h[t] + sum_{j ascending, kept} topk_gate[t,j] * y_perm[route_pos[t*k+j]]
+ *   out[t] = bf16( h[t] + sum_{j ascending, kept} topk_gate[t,j] * y_perm[route_pos[t*S+j]]
  *                  + y_shared[t] )
- * accumulated in fp32 in that fixed order.  y_shared may be NULL.  out [T,H] bf16. */
+ * accumulated in fp32 in that fixed order; S = k slots per token (N for
+ * expert choice, whose gates are the [T, N] probabilities).  y_shared may be
+ * NULL.  out [T,H] bf16. */
 moe_status moe_combine(const moe_config* cfg, int32_t T, const uint16_t* h, const float* topk_gate,
                        const uint8_t* route_kept, const int32_t* route_pos, const float* y_perm,
                        const float* y_shared, uint16_t* out, void* stream);
 
 /* The whole layer: moe_route -> moe_dispatch_align -> moe_expert_ffn ->
  * moe_combine on `stream`, intermediates in the workspace.  No host
- * synchronisation and no device-to-host copy. */
+ * synchronisation and no device-to-host copy.  With the reroute policy (and
+ * a capacity) the router computes every logit canonically and the dispatch is
+ * moe_dispatch_align_reroute; with expert-choice routing it is
+ * moe_router_logits -> moe_route_expert_choice -> moe_expert_ffn ->
+ * moe_combine. */
 moe_status moe_forward(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w_gate,
                        const float* router_bias, const uint16_t* w13, const uint16_t* w2,
                        const uint16_t* w13_shared, const uint16_t* w2_shared, uint16_t* out,

@@ -30,13 +30,25 @@ MOE_ERR_DEVICE = 5
 MOE_DEV_ERR_EXPERT_RANGE = 0x1
 MOE_DEV_ERR_TIMEOUT = 0x2
 MOE_DEV_ERR_BAD_BLOCKS = 0x4
+MOE_OVERFLOW_DROP = 0
+MOE_OVERFLOW_REROUTE = 1
+MOE_ROUTING_TOKEN_CHOICE = 0
+MOE_ROUTING_EXPERT_CHOICE = 1
 
 
 class moe_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
-                ("shared_intermediate", ctypes.c_int32)]
+                ("shared_intermediate", ctypes.c_int32), ("overflow_policy", ctypes.c_int32),
+                ("routing", ctypes.c_int32)]
+
+
+class moe_route_stats(ctypes.Structure):
+    _fields_ = [("max_expert_load", ctypes.c_int32), ("min_expert_load", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("dropped_tokens", ctypes.c_int32),
+                ("total_routes", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("imbalance_ratio", ctypes.c_double), ("drop_fraction", ctypes.c_double)]
 
 
 class MoEError(RuntimeError):
@@ -67,6 +79,11 @@ _SIGS = {
     "moe_route_filtered": ([_cfgp, _i32] + [_vp] * 6 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_router_tc_logits": ([_cfgp, _i32] + [_vp] * 3 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_dispatch_align_noalloc": ([_cfgp, _i32] + [_vp] * 9 + [_vp], ctypes.c_int),
+    "moe_router_logits": ([_cfgp, _i32] + [_vp] * 4 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_dispatch_align_reroute": ([_cfgp, _i32] + [_vp] * 11 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_route_expert_choice": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
+    "moe_routing_stats": ([_cfgp, _i32, _vp, ctypes.c_double, _vp, _vp, _vp], ctypes.c_int),
+    "moe_router_margin": ([_cfgp, _i32, _vp, _vp, _vp], ctypes.c_int),
     "moe_get_device_status": ([_vp, ctypes.POINTER(_i32), _vp], ctypes.c_int),
     "moe_clear_device_status": ([_vp, _vp], ctypes.c_int),
 }
@@ -79,9 +96,10 @@ EXPORTED = tuple(_SIGS)
 
 
 def make_config(hidden, num_experts, top_k, intermediate, block_size, capacity_factor=0.0,
-                shared_intermediate=0) -> moe_config:
+                shared_intermediate=0, overflow_policy=MOE_OVERFLOW_DROP,
+                routing=MOE_ROUTING_TOKEN_CHOICE) -> moe_config:
     return moe_config(hidden, num_experts, top_k, intermediate, block_size, capacity_factor,
-                      shared_intermediate)
+                      shared_intermediate, overflow_policy, routing)
 
 
 def _cfg(cfg) -> moe_config:
@@ -160,6 +178,53 @@ def moe_dispatch_align_noalloc(cfg, topk_idx, route_kept, route_pos, sorted_rout
         ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), _ptr(route_kept), _ptr(route_pos),
         _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded), _ptr(expert_counts),
         _ptr(num_dropped), _ptr(status_out), _stream(stream)))
+
+
+def moe_router_logits(cfg, h, w_gate, router_bias, logits_out, ws, stream=None):
+    T = h.shape[0]
+    _check("moe_router_logits", _lib.moe_router_logits(
+        ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w_gate), _ptr(router_bias), _ptr(logits_out),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_align_reroute(cfg, topk_idx, logits, route_kept, route_expert, route_pos,
+                               sorted_route_ids, block_expert, num_padded, expert_counts,
+                               num_dropped, num_rerouted, ws, stream=None):
+    T = topk_idx.shape[0]
+    _check("moe_dispatch_align_reroute", _lib.moe_dispatch_align_reroute(
+        ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), _ptr(logits), _ptr(route_kept),
+        _ptr(route_expert), _ptr(route_pos), _ptr(sorted_route_ids), _ptr(block_expert),
+        _ptr(num_padded), _ptr(expert_counts), _ptr(num_dropped), _ptr(num_rerouted), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_route_expert_choice(cfg, logits, gates, route_kept, route_pos, sorted_route_ids,
+                            block_expert, num_padded, expert_counts, ws, stream=None):
+    T = logits.shape[0]
+    _check("moe_route_expert_choice", _lib.moe_route_expert_choice(
+        ctypes.byref(_cfg(cfg)), T, _ptr(logits), _ptr(gates), _ptr(route_kept), _ptr(route_pos),
+        _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded), _ptr(expert_counts),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_routing_stats(cfg, topk_idx, capacity_factor, expert_load, stats, stream=None):
+    """stats: a device uint8 tensor of at least 40 bytes (moe_route_stats);
+    read it with route_stats_from_bytes."""
+    T = topk_idx.shape[0]
+    _check("moe_routing_stats", _lib.moe_routing_stats(
+        ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), float(capacity_factor), _ptr(expert_load),
+        _ptr(stats), _stream(stream)))
+
+
+def route_stats_from_bytes(raw: bytes) -> dict:
+    st = moe_route_stats.from_buffer_copy(bytes(raw)[:ctypes.sizeof(moe_route_stats)])
+    return {name: getattr(st, name) for name, _ in moe_route_stats._fields_ if name != "reserved"}
+
+
+def moe_router_margin(cfg, logits, margin, stream=None):
+    T = logits.shape[0]
+    _check("moe_router_margin", _lib.moe_router_margin(
+        ctypes.byref(_cfg(cfg)), T, _ptr(logits), _ptr(margin), _stream(stream)))
 
 
 def moe_expert_ffn(cfg, h, w13, w2, w13_shared, w2_shared, sorted_route_ids, block_expert,

@@ -3,8 +3,11 @@
 // gets h plus its kept experts' outputs scaled by their gates; a route that
 // overflowed contributes nothing.
 //
-// out[t,:] = bf16( h[t,:] + acc ),  acc = fma over kept slots j = 0..k-1 in
-// ascending order of gate[t,j] * y_perm[route_pos[t*k+j], :], then + y_shared.
+// out[t,:] = bf16( h[t,:] + acc ),  acc = fma over kept slots j = 0..S-1 in
+// ascending order of gate[t,j] * y_perm[route_pos[t*S+j], :], then + y_shared.
+// S is the number of route slots per token: k for token choice, N for expert
+// choice (slot e = expert e).  The kept slots are first listed in ascending j
+// in shared memory; skipping the others leaves the chain of fmas unchanged.
 // One CTA per token row, 4 consecutive features per thread, 128-bit loads of
 // y_perm; the order of the sum is fixed and independent of T.
 #include <cuda_bf16.h>
@@ -15,6 +18,8 @@
 namespace moe {
 namespace {
 
+constexpr int kMaxSlots = 256;
+
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ h,
                                                       const float* __restrict__ gates,
                                                       const uint8_t* __restrict__ route_kept,
@@ -24,22 +29,38 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       uint16_t* __restrict__ out, int H, int k,
                                                       long long max_rows) {
   const int t = blockIdx.x;
-  __shared__ int s_pos[16];
-  __shared__ float s_gate[16];
-  if (threadIdx.x < k) {
-    const size_t r = (size_t)t * k + threadIdx.x;
-    const int pos = route_pos[r];
-    const bool use = route_kept[r] && pos >= 0 && (long long)pos < max_rows;
-    s_pos[threadIdx.x] = use ? pos : -1;
-    s_gate[threadIdx.x] = gates[r];
+  __shared__ int s_pos[kMaxSlots];
+  __shared__ float s_gate[kMaxSlots];
+  __shared__ int s_wcnt[8];
+  // list the kept slots in ascending j (k <= 256 = blockDim.x: one slot per thread)
+  const int j = threadIdx.x, lane = j & 31, w = j >> 5;
+  bool use = false;
+  int pos = -1;
+  float g = 0.0f;
+  if (j < k) {
+    const size_t r = (size_t)t * k + j;
+    pos = route_pos[r];
+    use = route_kept[r] && pos >= 0 && (long long)pos < max_rows;
+    g = gates[r];
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, use);
+  if (lane == 0) s_wcnt[w] = __popc(m);
+  __syncthreads();
+  int before = __popc(m & ((1u << lane) - 1u)), n_used = 0;
+  for (int i = 0; i < 8; ++i) {
+    if (i < w) before += s_wcnt[i];
+    n_used += s_wcnt[i];
+  }
+  if (use) {
+    s_pos[before] = pos;
+    s_gate[before] = g;
   }
   __syncthreads();
   for (int d = threadIdx.x * 4; d < H; d += blockDim.x * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int pos = s_pos[j];
-      if (pos < 0) continue;
-      const float g = s_gate[j];
+    for (int i = 0; i < n_used; ++i) {
+      const int pos = s_pos[i];
+      const float g = s_gate[i];
       const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)pos * H + d));
       acc.x = fmaf(g, y.x, acc.x);
       acc.y = fmaf(g, y.y, acc.y);

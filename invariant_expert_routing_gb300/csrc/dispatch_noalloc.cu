@@ -70,6 +70,9 @@ extern "C" moe_status moe_dispatch_align_noalloc(const moe_config* cfg, int32_t 
   const moe_status cs = moe_check_config(cfg);
   if (cs != MOE_OK) return cs;
   if (T < 0) return MOE_ERR_INVALID_ARG;
+  // the drop policy only, as moe_dispatch_align
+  if (cfg->routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
+  if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && moe_capacity(cfg, T) >= 0) return MOE_ERR_INVALID_ARG;
   if ((int64_t)T * cfg->top_k > kMaxRoutes) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
   if (T == 0) return MOE_OK;
   if (!ok_ptr(topk_idx) || !ok_ptr(route_kept) || !ok_ptr(route_pos) || !ok_ptr(sorted_route_ids) ||

@@ -57,6 +57,24 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
                      int32_t* seg_off, int* status, cudaStream_t s);
+// phase one of launch_dispatch, overflow reroute, then the layout of the
+// final assignment (route_expert: expert per route, -1 = dropped)
+void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int B,
+                             int capacity, uint8_t* route_kept, int32_t* route_expert,
+                             int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
+                             int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
+                             int32_t* num_rerouted, int32_t* rank_in_tile, int32_t* tile_count,
+                             int32_t* seg_off, int* status, cudaStream_t s);
+// stable layout of routes that already carry their expert (-1 = none)
+void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, uint8_t* route_kept,
+                            int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
+                            int32_t* num_padded, int32_t* expert_counts, int32_t* rank_in_tile,
+                            int32_t* tile_count, int32_t* seg_off, int* status, cudaStream_t s);
+// expert choice: scores, per-expert top-C selection and the padded layout
+void launch_expert_choice(const float* logits, int T, int N, int C, int B, unsigned long long* keys,
+                          float* gates, uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                          int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                          cudaStream_t s);
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
@@ -87,7 +105,16 @@ void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CU
 void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                         const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
 
-// ---- combine
+// ---- diagnostics
+struct RoutingStats {  // same layout as moe_route_stats
+  int32_t max_expert_load, min_expert_load, capacity, dropped_tokens, total_routes, reserved;
+  double imbalance_ratio, drop_fraction;
+};
+void launch_routing_stats(const int32_t* topk_idx, long long R, int N, double capacity_factor,
+                          int32_t* load_out, RoutingStats* stats, cudaStream_t s);
+void launch_router_margin(const float* logits, int T, int N, int k, double* margin, cudaStream_t s);
+
+// ---- combine (k = route slots per token: top_k, or N for expert choice)
 void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,
                     const int32_t* route_pos, const float* y_perm, const float* y_shared,
                     uint16_t* out, int T, int H, int k, int64_t max_rows, cudaStream_t s);

@@ -33,25 +33,53 @@ moe_status check_cfg(const moe_config* c) {
   if (c->num_experts > 256) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > c->num_experts || c->top_k > 16) return MOE_ERR_UNSUPPORTED;
   if (c->block_size % 8 || c->block_size > 128 || 128 % c->block_size) return MOE_ERR_UNSUPPORTED;
+  if (c->overflow_policy != MOE_OVERFLOW_DROP && c->overflow_policy != MOE_OVERFLOW_REROUTE)
+    return MOE_ERR_INVALID_ARG;
+  if (c->routing != MOE_ROUTING_TOKEN_CHOICE && c->routing != MOE_ROUTING_EXPERT_CHOICE)
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
+
+bool expert_choice(const moe_config* c) { return c->routing == MOE_ROUTING_EXPERT_CHOICE; }
+
+// Route slots per token: k (token choice) or N (expert choice, slot e = expert e).
+int slots_of(const moe_config* c) { return expert_choice(c) ? c->num_experts : c->top_k; }
 
 moe_status check_T(const moe_config* c, int32_t T) {
   if (T < 0) return MOE_ERR_INVALID_ARG;
-  if (T > (1 << 20) || (int64_t)T * c->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T > (1 << 20) || (int64_t)T * slots_of(c) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
+// Token choice: ceil(cf*T*k/N) or -1 (no limit).  Expert choice: tokens per
+// expert, min(ceil(cf*T*k/N), T) with cf = 1 when unset.
 int32_t capacity_of(const moe_config* c, int32_t T) {
+  if (expert_choice(c)) {
+    const double cf = c->capacity_factor > 0.0f ? (double)c->capacity_factor : 1.0;
+    const double v = std::ceil(cf * (double)T * (double)c->top_k / (double)c->num_experts);
+    return v >= (double)T ? T : (int32_t)v;
+  }
   if (!(c->capacity_factor > 0.0f)) return -1;
   return (int32_t)std::ceil((double)c->capacity_factor * (double)T * (double)c->top_k /
                             (double)c->num_experts);
 }
 
+bool reroute_active(const moe_config* c, int32_t T) {
+  return !expert_choice(c) && c->overflow_policy == MOE_OVERFLOW_REROUTE && capacity_of(c, T) >= 0;
+}
+
+// Expert choice: every expert takes exactly C tokens, segment P = C rounded up to B.
+int64_t ec_segment_rows(const moe_config* c, int32_t T) {
+  const int64_t C = capacity_of(c, T);
+  return (C + c->block_size - 1) / c->block_size * c->block_size;
+}
+
 int64_t max_rows_of(const moe_config* c, int32_t T) {
+  if (expert_choice(c)) return (int64_t)c->num_experts * ec_segment_rows(c, T);
   return (int64_t)T * c->top_k + (int64_t)c->num_experts * (c->block_size - 1);
 }
 int64_t max_blocks_of(const moe_config* c, int32_t T) {
+  if (expert_choice(c)) return max_rows_of(c, T) / c->block_size;
   return (int64_t)T * c->top_k / c->block_size + c->num_experts;
 }
 int64_t max_gemm_tiles_of(const moe_config* c, int32_t T, int tile_rows) {
@@ -62,13 +90,12 @@ int64_t max_gemm_tiles_of(const moe_config* c, int32_t T, int tile_rows) {
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
   size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
-      num_padded, counts, dropped, gemm_tiles, num_gemm_tiles, gemm_tiles2, num_gemm_tiles2, x_perm,
-      a, y, a_sh, y_sh, h_stage,
-      out_stage, total;
+      num_padded, counts, dropped, route_expert, rerouted, ec_keys, gemm_tiles, num_gemm_tiles,
+      gemm_tiles2, num_gemm_tiles2, x_perm, a, y, a_sh, y_sh, h_stage, out_stage, total;
 };
 
 Layout layout_of(const moe_config* c, int32_t T) {
-  const size_t R = (size_t)T * c->top_k, N = c->num_experts, H = c->hidden;
+  const size_t R = (size_t)T * slots_of(c), N = c->num_experts, H = c->hidden;
   const size_t rows = (size_t)max_rows_of(c, T);
   const size_t dtiles = (R + moe::kDispatchTile - 1) / moe::kDispatchTile;
   Layout L{};
@@ -94,6 +121,9 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.num_padded = take(sizeof(int32_t));
   L.counts = take(sizeof(int32_t) * N);
   L.dropped = take(sizeof(int32_t));
+  L.route_expert = take(c->overflow_policy == MOE_OVERFLOW_REROUTE ? sizeof(int32_t) * R : 0);
+  L.rerouted = take(sizeof(int32_t));
+  L.ec_keys = take(expert_choice(c) ? sizeof(unsigned long long) * N * T : 0);
   // tile lists of the W13 (128-row) and W2 (256-row) GEMMs
   L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW13TileRows));
   L.num_gemm_tiles = take(sizeof(int32_t));
@@ -235,6 +265,28 @@ moe_status dispatch_impl(const moe_config* c, int32_t T, const int32_t* idx, uin
   return last_cuda();
 }
 
+moe_status reroute_impl(const moe_config* c, int32_t T, const int32_t* idx, const float* logits,
+                        uint8_t* kept, int32_t* route_expert, int32_t* pos, int32_t* sorted,
+                        int32_t* blocks, int32_t* num_padded, int32_t* counts, int32_t* dropped,
+                        int32_t* rerouted, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  moe::launch_dispatch_reroute(idx, logits, T, c->num_experts, c->top_k, c->block_size, capacity_of(c, T),
+                               kept, route_expert, pos, sorted, blocks, num_padded, counts, dropped,
+                               rerouted, at<int32_t>(ws, L.rank), at<int32_t>(ws, L.tile_count),
+                               at<int32_t>(ws, L.seg_off), at<int>(ws, L.status), s);
+  return last_cuda();
+}
+
+moe_status expert_choice_impl(const moe_config* c, int32_t T, const float* logits, float* gates,
+                              uint8_t* kept, int32_t* pos, int32_t* sorted, int32_t* blocks,
+                              int32_t* num_padded, int32_t* counts, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  moe::launch_expert_choice(logits, T, c->num_experts, capacity_of(c, T), c->block_size,
+                            at<unsigned long long>(ws, L.ec_keys), gates, kept, pos, sorted, blocks,
+                            num_padded, counts, s);
+  return last_cuda();
+}
+
 struct Marks;
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
@@ -247,7 +299,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
                     void* ws, cudaStream_t s, const Marks* mk) {
   const Layout L = layout_of(c, T);
-  const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = c->top_k;
+  const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = slots_of(c);
   const int64_t rows = max_rows_of(c, T);
   const int max_tiles13 = (int)max_gemm_tiles_of(c, T, moe::kW13TileRows);
   const int max_tiles2 = (int)max_gemm_tiles_of(c, T, moe::kW2TileRows);
@@ -361,18 +413,35 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   int32_t* num_padded = at<int32_t>(ws, L.num_padded);
   float* y = at<float>(ws, L.y);
   float* ysh = c->shared_intermediate ? at<float>(ws, L.y_sh) : nullptr;
+  float* logits = at<float>(ws, L.logits);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  moe_status st = MOE_OK;
   mk.at(0);
-  moe_status st = route_impl(c, T, h, wg, bias, idx, gates, at<float>(ws, L.logits), false, ws, s);
-  if (st != MOE_OK) return st;
-  mk.at(1);
-  st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, at<int32_t>(ws, L.counts),
-                     at<int32_t>(ws, L.dropped), ws, s);
+  if (expert_choice(c)) {
+    // every logit in the canonical order, then each expert takes its tokens
+    moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
+    mk.at(1);
+    st = expert_choice_impl(c, T, logits, gates, kept, pos, sorted, blocks, num_padded, counts, ws, s);
+  } else if (reroute_active(c, T)) {
+    // rerouting ranks every expert of an overflowing token: canonical logits
+    st = route_impl(c, T, h, wg, bias, idx, gates, logits, true, ws, s);
+    if (st != MOE_OK) return st;
+    mk.at(1);
+    st = reroute_impl(c, T, idx, logits, kept, at<int32_t>(ws, L.route_expert), pos, sorted, blocks,
+                      num_padded, counts, at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.rerouted), ws, s);
+  } else {
+    st = route_impl(c, T, h, wg, bias, idx, gates, logits, false, ws, s);
+    if (st != MOE_OK) return st;
+    mk.at(1);
+    st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
+                       ws, s);
+  }
   if (st != MOE_OK) return st;
   mk.at(2);
   st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk);
   if (st != MOE_OK) return st;
   mk.at(6);
-  moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, c->top_k, max_rows_of(c, T), s);
+  moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, slots_of(c), max_rows_of(c, T), s);
   mk.at(7);
   return last_cuda();
 }
@@ -468,9 +537,114 @@ moe_status moe_dispatch_align(const moe_config* cfg, int32_t T, const int32_t* t
   MOE_TRY(need(num_padded));
   MOE_TRY(need(expert_counts));
   MOE_TRY(need(num_dropped));
+  // the drop policy only: never drop routes the configuration asks to keep
+  if (expert_choice(cfg) || reroute_active(cfg, T)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
   return dispatch_impl(cfg, T, topk_idx, route_kept, route_pos, sorted_route_ids, block_expert,
                        num_padded, expert_counts, num_dropped, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dispatch_align_reroute(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                                      const float* logits, uint8_t* route_kept, int32_t* route_expert,
+                                      int32_t* route_pos, int32_t* sorted_route_ids,
+                                      int32_t* block_expert, int32_t* num_padded,
+                                      int32_t* expert_counts, int32_t* num_dropped,
+                                      int32_t* num_rerouted, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (expert_choice(cfg)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(logits));
+  MOE_TRY(need(route_kept));
+  MOE_TRY(need(route_expert));
+  MOE_TRY(need(route_pos));
+  MOE_TRY(need(sorted_route_ids));
+  MOE_TRY(need(block_expert));
+  MOE_TRY(need(num_padded));
+  MOE_TRY(need(expert_counts));
+  MOE_TRY(need(num_dropped));
+  MOE_TRY(need(num_rerouted));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (capacity_of(cfg, T) < 0) {
+    // no capacity: nothing overflows; every route keeps its expert
+    MOE_TRY(dispatch_impl(cfg, T, topk_idx, route_kept, route_pos, sorted_route_ids, block_expert,
+                          num_padded, expert_counts, num_dropped, ws, s));
+    if (cudaMemcpyAsync(route_expert, topk_idx, sizeof(int32_t) * (size_t)T * cfg->top_k,
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+        cudaMemsetAsync(num_rerouted, 0, sizeof(int32_t), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  return reroute_impl(cfg, T, topk_idx, logits, route_kept, route_expert, route_pos, sorted_route_ids,
+                      block_expert, num_padded, expert_counts, num_dropped, num_rerouted, ws, s);
+}
+
+moe_status moe_route_expert_choice(const moe_config* cfg, int32_t T, const float* logits, float* gates,
+                                   uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                                   int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (!expert_choice(cfg)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(logits));
+  MOE_TRY(need(gates));
+  MOE_TRY(need(route_kept));
+  MOE_TRY(need(route_pos));
+  MOE_TRY(need(sorted_route_ids));
+  MOE_TRY(need(block_expert));
+  MOE_TRY(need(num_padded));
+  MOE_TRY(need(expert_counts));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  return expert_choice_impl(cfg, T, logits, gates, route_kept, route_pos, sorted_route_ids, block_expert,
+                            num_padded, expert_counts, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w_gate,
+                             const float* router_bias, float* logits_out, void* ws, size_t ws_bytes,
+                             void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(h));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(opt(router_bias));
+  MOE_TRY(need(logits_out));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  moe::launch_router_logits(h, w_gate, router_bias, logits_out, T, cfg->hidden, cfg->num_experts,
+                            static_cast<cudaStream_t>(stream));
+  return last_cuda();
+}
+
+moe_status moe_routing_stats(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
+                             double capacity_factor, int32_t* expert_load, moe_route_stats* stats,
+                             void* stream) {
+  static_assert(sizeof(moe_route_stats) == sizeof(moe::RoutingStats), "stats layout");
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (std::isnan(capacity_factor) || capacity_factor < 0.0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(expert_load));
+  MOE_TRY(need(stats));
+  moe::launch_routing_stats(topk_idx, (long long)T * cfg->top_k, cfg->num_experts, capacity_factor,
+                            expert_load, reinterpret_cast<moe::RoutingStats*>(stats),
+                            static_cast<cudaStream_t>(stream));
+  return last_cuda();
+}
+
+moe_status moe_router_margin(const moe_config* cfg, int32_t T, const float* logits, double* margin,
+                             void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(logits));
+  MOE_TRY(need(margin));
+  moe::launch_router_margin(logits, T, cfg->num_experts, cfg->top_k, margin,
+                            static_cast<cudaStream_t>(stream));
+  return last_cuda();
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w13,
@@ -511,7 +685,7 @@ moe_status moe_combine(const moe_config* cfg, int32_t T, const uint16_t* h, cons
   MOE_TRY(opt(y_shared));
   MOE_TRY(need(out));
   moe::launch_combine(h, topk_gate, route_kept, route_pos, y_perm, y_shared, out, T, cfg->hidden,
-                      cfg->top_k, max_rows_of(cfg, T), static_cast<cudaStream_t>(stream));
+                      slots_of(cfg), max_rows_of(cfg, T), static_cast<cudaStream_t>(stream));
   return last_cuda();
 }
 
@@ -561,11 +735,21 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
 
 int32_t moe_forward_launch_count(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
-  // router (CUDA cores: logits + top-k = 2; tensor cores: transpose, norms,
-  // GEMM, certified select = 4) + dispatch 3 + tile lists 2 + row gather 1
-  // + W13 + W2 + combine 1 (+ shared W13, W2)
-  const int router = use_tc_router(cfg) ? 4 : 2;
-  return router + 3 + 2 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
+  // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
+  // combine 1 (+ shared W13, W2).  Router: CUDA cores logits + top-k = 2,
+  // tensor cores transpose, norms, GEMM, certified select = 4.  Dispatch:
+  // count, scan, scatter = 3; with reroute count, scan, reroute, count,
+  // scan, scatter = 6 after the CUDA-core router.  Expert choice: logits,
+  // scores, selection = 3 in all.
+  int front = 0;
+  if (expert_choice(cfg)) {
+    front = 3;
+  } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0f) {
+    front = 2 + 6;
+  } else {
+    front = (use_tc_router(cfg) ? 4 : 2) + 3;
+  }
+  return front + 2 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }
 
 moe_status moe_router_tc_logits(const moe_config* cfg, int32_t T, const uint16_t* h,

@@ -119,3 +119,64 @@ def test_binding_refuses_to_import_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import invariant_expert_routing_gb300"],
                        cwd=tmp_path, capture_output=True, text=True)
     assert r.returncode != 0 and "no CPU fallback" in r.stderr
+
+
+@pytest.mark.parametrize("bad", [dict(overflow_policy=2), dict(overflow_policy=-1), dict(routing=2)])
+def test_policy_and_routing_validation(moe, bad):
+    assert moe.moe_check_config(dict(TINY, **bad)) == 1
+    assert moe.moe_check_config(dict(TINY, overflow_policy=1, routing=1)) == 0
+
+
+def test_expert_choice_capacity_and_bounds_match_the_oracle(moe):
+    import oracle
+    for T, N, k, cf, B in [(64, 8, 2, 0.0, 8), (100, 8, 2, 1.25, 16), (5, 2, 2, 1.5, 8),
+                           (8192, 128, 8, 1.0, 16), (1, 256, 8, 0.0, 16)]:
+        cfg = dict(hidden=128, num_experts=N, top_k=k, intermediate=128, block_size=B,
+                   capacity_factor=cf, routing=1)
+        C = oracle.ec_capacity(T, N, k, cf)
+        assert moe.moe_capacity(cfg, T) == C
+        P = (C + B - 1) // B * B
+        assert moe.moe_max_padded_rows(cfg, T) == N * P
+        assert moe.moe_max_blocks(cfg, T) == N * P // B
+        assert moe.moe_workspace_bytes(cfg, T) > 0
+
+
+def test_launch_counts(moe):
+    mix = dict(hidden=4096, num_experts=8, top_k=2, intermediate=14336, block_size=64)
+    qw = dict(hidden=2048, num_experts=128, top_k=8, intermediate=768, block_size=16)
+    assert moe.moe_forward_launch_count(mix) == 2 + 3 + 6
+    assert moe.moe_forward_launch_count(qw) == 4 + 3 + 6
+    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1)) == 8 + 6
+    assert moe.moe_forward_launch_count(dict(qw, routing=1)) == 3 + 6
+    assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128)) == 2 + 3 + 6 + 2
+
+
+def test_drop_only_dispatch_refuses_reroute_and_expert_choice(moe):
+    # moe_dispatch_align would drop routes the configuration asks to keep:
+    # it refuses before launching anything
+    fake = [0x10000 + 0x1000 * i for i in range(8)]
+    for extra, code in [(dict(capacity_factor=1.0, overflow_policy=1), 1), (dict(routing=1), 1)]:
+        cfg = dict(TINY, **extra)
+        c = moe.make_config(**cfg)
+        ws = moe.moe_workspace_bytes(cfg, 64)
+        assert moe._lib.moe_dispatch_align(ctypes.byref(c), 64, *fake, 0x90000, ws, None) == code
+        st = moe._lib.moe_dispatch_align_noalloc(ctypes.byref(c), 64, *fake, None, None)
+        assert st == code
+    # the expert-choice entry refuses a token-choice configuration, and the
+    # reroute entry an expert-choice one
+    c = moe.make_config(**TINY)
+    assert moe._lib.moe_route_expert_choice(ctypes.byref(c), 64, *fake, 0x90000,
+                                            moe.moe_workspace_bytes(TINY, 64), None) == 1
+    ce = moe.make_config(**dict(TINY, routing=1))
+    assert moe._lib.moe_dispatch_align_reroute(ctypes.byref(ce), 64, *(fake + fake[:3]), 0x90000,
+                                               1 << 30, None) == 1
+
+
+def test_diagnostic_argument_errors(moe):
+    c = moe.make_config(**TINY)
+    assert moe._lib.moe_routing_stats(ctypes.byref(c), 64, 0x10000, -1.0, 0x20000, 0x30000, None) == 1
+    assert moe._lib.moe_routing_stats(ctypes.byref(c), 0, 0x10000, 1.25, 0x20000, 0x30000, None) == 0
+    assert moe._lib.moe_routing_stats(ctypes.byref(c), 64, None, 1.25, 0x20000, 0x30000, None) == 1
+    assert moe._lib.moe_router_margin(ctypes.byref(c), 64, 0x10004, 0x20000, None) == 1
+    assert moe._lib.moe_router_margin(ctypes.byref(c), 0, None, None, None) == 0
+    assert ctypes.sizeof(moe.moe_route_stats) == 40

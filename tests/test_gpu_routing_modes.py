@@ -1,0 +1,334 @@
+"""GPU parity of the overflow reroute policy, the routing diagnostics and
+expert-choice routing, through the C ABI, against the CPU oracle.
+
+Integer results (reroute assignments, layouts, expert-choice selections,
+routing_stats counts) must match bit for bit; the fp64 diagnostics (imbalance
+ratio, drop fraction, router margin) too, since both sides make the same IEEE
+operations on the same inputs; gates and layer outputs within the tolerances
+of tests/checks.py.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import workloads as W
+from tests.checks import check_dispatch, check_equal, check_gates, check_outputs
+
+pytestmark = pytest.mark.gpu
+
+_cases = {}
+
+
+def case(name):
+    from tests.layer_case import LayerCase
+    if name not in _cases:
+        _cases.clear()
+        _cases[name] = LayerCase(W.WORKLOADS[name])
+    return _cases[name]
+
+
+def _logits_and_topk(moe, cfg, c, h_d, ws):
+    import torch
+    T, N, k = h_d.shape[0], cfg["num_experts"], cfg["top_k"]
+    idx = torch.empty((T, k), dtype=torch.int32, device=h_d.device)
+    g = torch.empty((T, k), dtype=torch.float32, device=h_d.device)
+    lg = torch.empty((T, N), dtype=torch.float32, device=h_d.device)
+    moe.moe_route(cfg, h_d, c.wg_d, c.bias_d, idx, g, lg, ws)
+    lg2 = torch.empty_like(lg)
+    moe.moe_router_logits(cfg, h_d, c.wg_d, c.bias_d, lg2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(lg.view(torch.int32), lg2.view(torch.int32))
+    return idx, g, lg
+
+
+def _reroute_on_gpu(moe, cfg, idx, lg, ws):
+    import torch
+    from tests.gpu_util import host
+    T, k = idx.shape
+    N = cfg["num_experts"]
+    d = idx.device
+    R = T * k
+    rows, nblk = moe.moe_max_padded_rows(cfg, T), moe.moe_max_blocks(cfg, T)
+    kept = torch.empty(R, dtype=torch.uint8, device=d)
+    rexp = torch.full((R,), -9, dtype=torch.int32, device=d)
+    pos = torch.empty(R, dtype=torch.int32, device=d)
+    srt = torch.full((rows,), -9, dtype=torch.int32, device=d)
+    blk = torch.full((nblk,), -9, dtype=torch.int32, device=d)
+    npad = torch.zeros(1, dtype=torch.int32, device=d)
+    counts = torch.empty(N, dtype=torch.int32, device=d)
+    nd = torch.full((1,), -1, dtype=torch.int32, device=d)
+    nr = torch.full((1,), -1, dtype=torch.int32, device=d)
+    moe.moe_dispatch_align_reroute(cfg, idx, lg, kept, rexp, pos, srt, blk, npad, counts, nd, nr, ws)
+    torch.cuda.synchronize()
+    P = int(host(npad)[0])
+    B = cfg["block_size"]
+    return dict(route_kept=host(kept), route_expert=host(rexp), route_pos=host(pos),
+                sorted_route_ids=host(srt)[:P], block_expert=host(blk)[:P // B], num_padded=P,
+                expert_counts=host(counts), num_dropped=int(host(nd)[0]),
+                num_rerouted=int(host(nr)[0]))
+
+
+def _ref_reroute(l, idx, N, B, cap):
+    re, nr, nd = oracle.reroute(l, idx, cap)
+    d = oracle.dispatch_routes(re, N, B, idx.shape[1])
+    d["num_dropped"] = nd
+    return re, nr, d
+
+
+REROUTE_CASES = [("tiny", 64, 0.5), ("tiny", 61, 0.75), ("tiny", 1, 0.5), ("cap", 8192, 1.0),
+                 ("cap", 2000, 0.8), ("qw", 512, 1.0), ("qw", 8192, 1.0), ("qw", 777, 0.6),
+                 ("ds", 200, 1.0), ("mix", 128, 4.0)]
+
+
+@pytest.mark.parametrize("name,T,cf", REROUTE_CASES)
+def test_reroute_dispatch_is_bit_exact(name, T, cf):
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16, host
+    c = case(name)
+    cfg = dict(c.cfg, capacity_factor=cf, overflow_policy=1)
+    N, k, B = cfg["num_experts"], cfg["top_k"], cfg["block_size"]
+    h = W.make_h(c.wl, T, seed=21)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    idx, _, lg = _logits_and_topk(moe, cfg, c, dev_bf16(h), ws)
+    l_ref = oracle.router_logits(h, c.wg, c.bias)
+    check_equal("logits", host(lg).view(np.uint32), l_ref.view(np.uint32))
+    idx_ref, _ = oracle.select_topk(l_ref, k)
+    check_equal("topk_idx", host(idx), idx_ref)
+    got = _reroute_on_gpu(moe, cfg, idx, lg, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    cap = oracle.capacity(T, N, k, cf)
+    re, nr, d = _ref_reroute(l_ref, idx_ref, N, B, cap)
+    check_equal("route_expert", got["route_expert"], re)
+    assert got["num_rerouted"] == nr
+    check_dispatch(got, d)
+    if name in ("cap", "qw") and cf <= 1.0:
+        assert nr > 0                 # the case exercises the reroute phase
+
+
+def test_reroute_without_capacity_keeps_every_route():
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16, host
+    c = case("tiny")
+    cfg = dict(c.cfg, capacity_factor=0.0, overflow_policy=1)
+    h = W.make_h(c.wl, 50, seed=2)
+    ws = moe.workspace(cfg, 50)
+    idx, _, lg = _logits_and_topk(moe, cfg, c, dev_bf16(h), ws)
+    got = _reroute_on_gpu(moe, cfg, idx, lg, ws)
+    assert (got["route_expert"] == host(idx).reshape(-1)).all()
+    assert got["num_rerouted"] == 0 and got["num_dropped"] == 0
+    assert got["route_kept"].all()
+    del torch
+
+
+@pytest.mark.parametrize("name,T,cf", [("tiny", 64, 0.5), ("cap", 2048, 1.0), ("qw", 512, 0.8)])
+def test_reroute_forward_matches_oracle(name, T, cf):
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16, host_bf16
+    c = case(name)
+    cfg = dict(c.cfg, capacity_factor=cf, overflow_policy=1)
+    N, k, B = cfg["num_experts"], cfg["top_k"], cfg["block_size"]
+    h = W.make_h(c.wl, T, seed=4)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    out = torch.empty((T, c.wl.hidden), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(cfg, dev_bf16(h), c.wg_d, c.bias_d, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, out, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    got = host_bf16(out)
+    l = oracle.router_logits(h, c.wg, c.bias)
+    idx, gates = oracle.select_topk(l, k)
+    re, nr, nd = oracle.reroute(l, idx, oracle.capacity(T, N, k, cf))
+    assert nr > 0
+    moved = np.flatnonzero((re >= 0) & (re != idx.reshape(-1)))
+    rng = np.random.default_rng(T)
+    toks = np.unique(np.concatenate([moved[:24] // k, rng.choice(T, 16, replace=False)]))
+    # the oracle's layer output for those tokens: expert per route from the
+    # reroute, the slot's gate, kept iff the route has an expert
+    kept = (re >= 0).astype(np.uint8)
+    pairs_t = np.repeat(toks, k)
+    pairs_r = (toks[:, None] * k + np.arange(k)[None, :]).reshape(-1)
+    use = kept[pairs_r].astype(bool)
+    y = np.zeros((len(pairs_t), c.wl.hidden))
+    y[use] = c.ref_expert_rows(h, pairs_t[use], re[pairs_r][use])
+    ref = oracle.combine_rows(toks, h, gates, kept, y.reshape(len(toks), k, c.wl.hidden))
+    check_outputs(got[toks], ref)
+    if name == "tiny":
+        full = oracle.moe_forward(cfg, h, c.wg, c.bias, c.w13, c.w2)
+        check_outputs(got, full)
+
+
+@pytest.mark.parametrize("name,T,cf", [("mix", 4096, 1.25), ("qw", 8192, 1.25), ("cap", 8192, 1.0),
+                                       ("ds", 333, 1.0), ("tiny", 1, 1.25)])
+def test_routing_stats_bit_exact(name, T, cf):
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev, host
+    c = case(name)
+    N, k = c.wl.num_experts, c.wl.top_k
+    h = W.make_h(c.wl, T, seed=6)
+    idx, _ = oracle.select_topk(oracle.router_logits(h, c.wg, c.bias), k)
+    load = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    raw = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    moe.moe_routing_stats(c.cfg, dev(idx), cf, load, raw)
+    torch.cuda.synchronize()
+    got = moe.route_stats_from_bytes(host(raw).tobytes())
+    ref_load, ref = oracle.routing_stats(idx, N, cf)
+    check_equal("expert_load", host(load), ref_load)
+    for key in ("max_expert_load", "min_expert_load", "capacity", "dropped_tokens", "total_routes"):
+        assert got[key] == ref[key], key
+    for key in ("imbalance_ratio", "drop_fraction"):
+        assert np.float64(got[key]).tobytes() == np.float64(ref[key]).tobytes(), key
+
+
+@pytest.mark.parametrize("name,T", [("qw", 8192), ("mix", 4096), ("tiny", 64), ("ds", 100)])
+def test_router_margin_bit_exact(name, T):
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev, host
+    c = case(name)
+    k = c.wl.top_k
+    h = W.make_h(c.wl, T, seed=7)
+    l = oracle.router_logits(h, c.wg, c.bias)
+    ref = oracle.router_margin(l, k)
+    m = torch.empty(T, dtype=torch.float64, device="cuda")
+    moe.moe_router_margin(c.cfg, dev(l), m)
+    torch.cuda.synchronize()
+    check_equal("margin", host(m).view(np.uint64), ref.view(np.uint64))
+    if name == "qw":
+        assert (ref == 0).sum() > 0       # the zero tokens tie exactly at the cut
+
+
+def test_router_margin_special_values():
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev, host
+    rng = np.random.default_rng(1)
+    N = 40
+    l = rng.standard_normal((12, N)).astype(np.float32)
+    l[0, 5] = np.nan
+    l[1, :] = 1.0                     # all tied
+    l[2, :3] = np.inf
+    l[3, :] = np.nan
+    l[4, 7] = -0.0
+    l[4, 8] = 0.0
+    for k in (1, 3, N):
+        cfg = dict(hidden=128, num_experts=N, top_k=k, intermediate=128, block_size=8)
+        m = torch.empty(12, dtype=torch.float64, device="cuda")
+        moe.moe_router_margin(cfg, dev(l), m)
+        torch.cuda.synchronize()
+        ref = oracle.router_margin(l, k)
+        check_equal(f"margin k={k}", host(m).view(np.uint64), ref.view(np.uint64))
+
+
+def _ec_on_gpu(moe, cfg, lg, ws):
+    import torch
+    from tests.gpu_util import host
+    T, N = lg.shape
+    d = lg.device
+    R = T * N
+    rows, nblk = moe.moe_max_padded_rows(cfg, T), moe.moe_max_blocks(cfg, T)
+    gates = torch.empty(R, dtype=torch.float32, device=d)
+    kept = torch.empty(R, dtype=torch.uint8, device=d)
+    pos = torch.empty(R, dtype=torch.int32, device=d)
+    srt = torch.full((rows,), -9, dtype=torch.int32, device=d)
+    blk = torch.full((nblk,), -9, dtype=torch.int32, device=d)
+    npad = torch.zeros(1, dtype=torch.int32, device=d)
+    counts = torch.empty(N, dtype=torch.int32, device=d)
+    moe.moe_route_expert_choice(cfg, lg, gates, kept, pos, srt, blk, npad, counts, ws)
+    torch.cuda.synchronize()
+    P = int(host(npad)[0])
+    B = cfg["block_size"]
+    return dict(gates=host(gates), route_kept=host(kept), route_pos=host(pos),
+                sorted_route_ids=host(srt)[:P], block_expert=host(blk)[:P // B], num_padded=P,
+                expert_counts=host(counts), num_dropped=0)
+
+
+EC_CASES = [("tiny", 64, 0.0), ("tiny", 3, 0.0), ("tiny", 61, 1.5), ("mix", 128, 1.0),
+            ("mix", 4096, 1.0), ("qw", 512, 1.0), ("qw", 8192, 1.25), ("ds", 300, 1.0),
+            ("cap", 1000, 1.0)]
+
+
+@pytest.mark.parametrize("name,T,cf", EC_CASES)
+def test_expert_choice_selection_is_bit_exact(name, T, cf):
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16
+    c = case(name)
+    cfg = dict(c.cfg, capacity_factor=cf, routing=1)
+    N, k, B = cfg["num_experts"], cfg["top_k"], cfg["block_size"]
+    h = W.make_h(c.wl, T, seed=13)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    import torch
+    lg = torch.empty((T, N), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(cfg, dev_bf16(h), c.wg_d, c.bias_d, lg, ws)
+    got = _ec_on_gpu(moe, cfg, lg, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    l = oracle.router_logits(h, c.wg, c.bias)
+    C = oracle.ec_capacity(T, N, k, cf)
+    sel, probs = oracle.expert_choice(l, C)
+    re = np.where(sel.reshape(-1) == 1, np.tile(np.arange(N), T), -1).astype(np.int32)
+    d = oracle.dispatch_routes(re, N, B, N)
+    check_dispatch(got, d)
+    assert (got["expert_counts"] == C).all()
+    check_gates(got["gates"], probs.reshape(-1))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 64), ("mix", 256), ("qw", 512), ("ds", 40)])
+def test_expert_choice_forward_matches_oracle(name, T):
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16, host_bf16
+    c = case(name)
+    cfg = dict(c.cfg, capacity_factor=0.0, routing=1)
+    N, k = cfg["num_experts"], cfg["top_k"]
+    h = W.make_h(c.wl, T, seed=17)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    out = torch.empty((T, c.wl.hidden), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(cfg, dev_bf16(h), c.wg_d, c.bias_d, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, out, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    got = host_bf16(out)
+    l = oracle.router_logits(h, c.wg, c.bias)
+    sel, probs = oracle.expert_choice(l, oracle.ec_capacity(T, N, k, 0.0))
+    rng = np.random.default_rng(T)
+    n_sample = 6 if c.w13 is None else 24       # host-regenerated experts are slow
+    toks = np.arange(T) if T <= n_sample else np.sort(rng.choice(T, n_sample, replace=False))
+    # include tokens no expert took (they get h plus the shared expert only)
+    none = np.flatnonzero(sel.sum(axis=1) == 0)
+    toks = np.unique(np.concatenate([toks, none[:4]])).astype(np.int32)
+    pairs_t = np.repeat(toks, N)
+    pairs_e = np.tile(np.arange(N, dtype=np.int32), len(toks))
+    use = sel[toks].reshape(-1).astype(bool)
+    y = np.zeros((len(pairs_t), c.wl.hidden))
+    y[use] = c.ref_expert_rows(h, pairs_t[use], pairs_e[use])
+    ysh = None
+    if c.wl.shared_intermediate:
+        ysh = oracle.expert_rows(toks, np.zeros(len(toks), np.int32), h, c.w13s[None], c.w2s[None])
+    ref = oracle.combine_rows(toks, h, probs, sel.reshape(-1), y.reshape(len(toks), N, c.wl.hidden),
+                              ysh)
+    check_outputs(got[toks], ref)
+    if name == "tiny":
+        check_outputs(got, oracle.moe_forward(cfg, h, c.wg, c.bias, c.w13, c.w2))
+
+
+def test_expert_choice_ties_go_to_the_lowest_token():
+    # identical token rows: every expert takes the first C of them
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16, host
+    c = case("qw")
+    cfg = dict(c.cfg, capacity_factor=1.0, routing=1)
+    T, N = 300, c.wl.num_experts
+    h = np.tile(W.make_h(c.wl, 1, seed=3), (T, 1))
+    ws = moe.workspace(cfg, T)
+    lg = torch.empty((T, N), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits(cfg, dev_bf16(h), c.wg_d, c.bias_d, lg, ws)
+    got = _ec_on_gpu(moe, cfg, lg, ws)
+    C = oracle.ec_capacity(T, N, c.wl.top_k, 1.0)
+    kept = got["route_kept"].reshape(T, N)
+    assert (kept[:C] == 1).all() and not kept[C:].any()
+    del host
