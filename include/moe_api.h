@@ -74,8 +74,9 @@ typedef struct moe_config {
   int32_t top_k;               /* k (expert choice: average experts per token) */
   int32_t intermediate;        /* I, routed expert FFN width */
   int32_t block_size;          /* B, rows per padded expert block */
-  float capacity_factor;       /* > 0: capacity ceil(cf*T*k/N) per expert; <= 0: no limit
-                                  (expert choice: cf = 1, capacity clipped to T) */
+  double capacity_factor;      /* > 0: capacity ceil(cf*T*k/N) per expert, in fp64 as
+                                  ceil(((cf*T)*k)/N); <= 0: no limit (expert choice:
+                                  cf = 1, capacity clipped to T) */
   int32_t shared_intermediate; /* Is of the always-on shared expert; 0: none */
   int32_t overflow_policy;     /* MOE_OVERFLOW_DROP or MOE_OVERFLOW_REROUTE (token choice) */
   int32_t routing;             /* MOE_ROUTING_TOKEN_CHOICE or MOE_ROUTING_EXPERT_CHOICE */

@@ -39,7 +39,7 @@ MOE_ROUTING_EXPERT_CHOICE = 1
 class moe_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("intermediate", ctypes.c_int32),
-                ("block_size", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("block_size", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
                 ("shared_intermediate", ctypes.c_int32), ("overflow_policy", ctypes.c_int32),
                 ("routing", ctypes.c_int32)]
 

@@ -55,12 +55,12 @@ moe_status check_T(const moe_config* c, int32_t T) {
 // expert, min(ceil(cf*T*k/N), T) with cf = 1 when unset.
 int32_t capacity_of(const moe_config* c, int32_t T) {
   if (expert_choice(c)) {
-    const double cf = c->capacity_factor > 0.0f ? (double)c->capacity_factor : 1.0;
+    const double cf = c->capacity_factor > 0.0 ? c->capacity_factor : 1.0;
     const double v = std::ceil(cf * (double)T * (double)c->top_k / (double)c->num_experts);
     return v >= (double)T ? T : (int32_t)v;
   }
-  if (!(c->capacity_factor > 0.0f)) return -1;
-  return (int32_t)std::ceil((double)c->capacity_factor * (double)T * (double)c->top_k /
+  if (!(c->capacity_factor > 0.0)) return -1;
+  return (int32_t)std::ceil(c->capacity_factor * (double)T * (double)c->top_k /
                             (double)c->num_experts);
 }
 
@@ -744,7 +744,7 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   int front = 0;
   if (expert_choice(cfg)) {
     front = 3;
-  } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0f) {
+  } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = 2 + 6;
   } else {
     front = (use_tc_router(cfg) ? 4 : 2) + 3;

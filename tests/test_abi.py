@@ -64,8 +64,9 @@ def test_good_configs(moe):
 
 def test_capacity_matches_the_oracle(moe):
     import oracle
+    # 0.8 is not an fp32 value: carried in fp32 it would make ceil(0.8*2000*2/8) 401
     for T, N, k, cf in [(8192, 8, 2, 1.0), (10, 8, 2, 1.0), (4096, 8, 2, 1.25), (7, 3, 1, 1.0),
-                        (64, 8, 2, 0.0), (333, 128, 8, 0.7)]:
+                        (64, 8, 2, 0.0), (333, 128, 8, 0.7), (2000, 8, 2, 0.8), (777, 128, 8, 0.6)]:
         cfg = dict(hidden=128, num_experts=N, top_k=k, intermediate=128, block_size=8,
                    capacity_factor=cf)
         assert moe.moe_capacity(cfg, T) == oracle.capacity(T, N, k, cf)
