@@ -220,7 +220,12 @@ def test_router_margin_special_values():
         moe.moe_router_margin(cfg, dev(l), m)
         torch.cuda.synchronize()
         ref = oracle.router_margin(l, k)
-        check_equal(f"margin k={k}", host(m).view(np.uint64), ref.view(np.uint64))
+        got = host(m)
+        # a NaN result (inf - inf, NaN logits) is a NaN on both sides; its sign
+        # and payload are the hardware's choice
+        nan = np.isnan(ref)
+        assert (np.isnan(got) == nan).all()
+        check_equal(f"margin k={k}", got[~nan].view(np.uint64), ref[~nan].view(np.uint64))
 
 
 def _ec_on_gpu(moe, cfg, lg, ws):
