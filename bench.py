@@ -253,12 +253,20 @@ WORKLOAD_NAMES = {"tiny": "tiny MoE layer", "mix": "mixtral-like MoE layer",
                   "ds": "deepseek-v3-like MoE layer (+1 shared expert)"}
 
 
-def workload_config(wl, T, world):
+def workload_config(wl, T, world, cfg=None):
+    cfg = cfg or wl.cfg
     shared = f", shared expert {wl.shared_intermediate}" if wl.shared_intermediate else ""
-    cap = f", capacity factor {wl.capacity_factor}" if wl.capacity_factor > 0 else ""
+    cf = cfg.get("capacity_factor", 0.0)
+    cap = f", capacity factor {cf}" if cf > 0 else ""
+    mode = ""
+    if cfg.get("routing", 0) == 1:
+        mode = ", expert-choice routing"
+    elif cfg.get("overflow_policy", 0) == 1 and cf > 0:
+        mode = ", overflow reroute"
     return {"workload": (f"{WORKLOAD_NAMES.get(wl.name, wl.name)} forward: hidden {wl.hidden}, "
                          f"{wl.num_experts} experts, top-{wl.top_k}, SwiGLU intermediate "
-                         f"{wl.intermediate}{shared}, block {wl.block_size}{cap}, T={T} tokens per GPU"),
+                         f"{wl.intermediate}{shared}, block {wl.block_size}{cap}{mode}, "
+                         f"T={T} tokens per GPU"),
             "tokens_per_gpu": T, "global_batch": T * world, "seed": 0,
             "l2": (f"inputs larger than L2: {wl.weight_bytes() / 1e9:.1f} GB of expert weights, "
                    "the touched experts' weights are read every step"),
@@ -266,24 +274,44 @@ def workload_config(wl, T, world):
 
 
 def batch_counts(moe, cfg, wl, h_d, wg_d, bias_d, ws, device):
-    """Kept routes and touched experts of one batch (for the algorithmic work)."""
-    import numpy as np
+    """Kept routes, touched experts and dropped routes of one batch (for the
+    algorithmic work), through the stage entry points of the layer's mode.
+    Expert choice drops no route; its third number is the tokens no expert
+    took."""
     import torch
     T = h_d.shape[0]
-    R, N = T * wl.top_k, wl.num_experts
-    idx = torch.empty((T, wl.top_k), dtype=torch.int32, device=device)
-    gates = torch.empty((T, wl.top_k), dtype=torch.float32, device=device)
-    moe.moe_route(cfg, h_d, wg_d, bias_d, idx, gates, None, ws)
+    N = wl.num_experts
+    ec = cfg.get("routing", 0) == 1
+    slots = N if ec else wl.top_k
+    R = T * slots
     kept = torch.empty(R, dtype=torch.uint8, device=device)
     pos = torch.empty(R, dtype=torch.int32, device=device)
     srt = torch.empty(moe.moe_max_padded_rows(cfg, T), dtype=torch.int32, device=device)
     blk = torch.empty(moe.moe_max_blocks(cfg, T), dtype=torch.int32, device=device)
     npad = torch.empty(1, dtype=torch.int32, device=device)
     counts = torch.empty(N, dtype=torch.int32, device=device)
-    dropped = torch.empty(1, dtype=torch.int32, device=device)
-    moe.moe_dispatch_align(cfg, idx, kept, pos, srt, blk, npad, counts, dropped, ws)
+    dropped = torch.zeros(1, dtype=torch.int32, device=device)
+    logits = torch.empty((T, N), dtype=torch.float32, device=device)
+    if ec:
+        gates = torch.empty(R, dtype=torch.float32, device=device)
+        moe.moe_router_logits(cfg, h_d, wg_d, bias_d, logits, ws)
+        moe.moe_route_expert_choice(cfg, logits, gates, kept, pos, srt, blk, npad, counts, ws)
+        third = int((kept.view(T, N).sum(dim=1) == 0).sum().item())
+    else:
+        idx = torch.empty((T, wl.top_k), dtype=torch.int32, device=device)
+        gates = torch.empty((T, wl.top_k), dtype=torch.float32, device=device)
+        reroute = cfg.get("overflow_policy", 0) == 1 and cfg.get("capacity_factor", 0.0) > 0
+        moe.moe_route(cfg, h_d, wg_d, bias_d, idx, gates, logits if reroute else None, ws)
+        if reroute:
+            rexp = torch.empty(R, dtype=torch.int32, device=device)
+            nrer = torch.zeros(1, dtype=torch.int32, device=device)
+            moe.moe_dispatch_align_reroute(cfg, idx, logits, kept, rexp, pos, srt, blk, npad, counts,
+                                           dropped, nrer, ws)
+        else:
+            moe.moe_dispatch_align(cfg, idx, kept, pos, srt, blk, npad, counts, dropped, ws)
+        third = int(dropped.item())
     c = counts.cpu().numpy()
-    return int(c.sum()), int((c > 0).sum()), int(dropped.item())
+    return int(c.sum()), int((c > 0).sum()), third
 
 
 def time_graph(fwd, n):
@@ -342,7 +370,13 @@ def run_gpu(args):
 
     wl = W.WORKLOADS[args.workload]
     T = args.tokens
-    cfg = wl.cfg
+    cfg = dict(wl.cfg)
+    if args.capacity_factor is not None:
+        cfg["capacity_factor"] = args.capacity_factor
+    cfg["overflow_policy"] = 1 if args.policy == "reroute" else 0
+    cfg["routing"] = 1 if args.routing == "expert" else 0
+    default_mode = (cfg["overflow_policy"] == 0 and cfg["routing"] == 0
+                    and cfg["capacity_factor"] == wl.capacity_factor)
     wg, bias = W.make_router(wl)
     wg_d = dev_bf16(wg, device)
     bias_d = None if bias is None else dev(bias, device)
@@ -418,6 +452,8 @@ def run_gpu(args):
     w13_bytes = 4.0 * wl.hidden * wl.intermediate * touched + 4.0 * kept_routes * wl.hidden
     ridge = peak_tf * 1e12 / (peak_gb * 1e9)
     traffic, traffic_src = profiled_traffic("expert_w13_gemm", f"{wl.name}_T{T}")
+    if not default_mode:
+        traffic, traffic_src = None, "no ncu summary for this routing mode"
     if w13_flops / w13_bytes >= ridge:
         roof = {"bound": "tensor", "achieved": w13_flops / w13_s / 1e12, "peak": peak_tf,
                 "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16 burst",
@@ -438,15 +474,39 @@ def run_gpu(args):
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded counter-based generator; no checkpoints)",
-            "config": workload_config(wl, T, world), "roofline": roof,
+            "config": workload_config(wl, T, world, cfg), "roofline": roof,
             "layer_roofline": {"algorithmic_gflop": flops / 1e9, "algorithmic_gb": bytes_ / 1e9,
-                               "kept_routes": kept_routes, "dropped_routes": dropped,
+                               "kept_routes": kept_routes,
+                               ("tokens_without_expert" if cfg["routing"] == 1
+                                else "dropped_routes"): dropped,
                                "touched_experts": touched, "tflops": layer_tf,
                                "frac_of_bf16_peak": layer_tf / peak_tf, "gbs": layer_gb,
                                "frac_of_hbm": layer_gb / peak_gb},
             "stage_ms": {n: float(v) for n, v in zip(names, stage_ms)},
             "gpu_launches": moe.moe_forward_launch_count(cfg) * K,
             "clocks": clocks.summary(t_wall0, t_wall1)}
+
+    # ---- routing diagnostics on this batch: the routing_stats probe and the
+    # router margin (device time per call, 50 calls each)
+    if cfg["routing"] == 0:
+        idx_d = torch.empty((T, wl.top_k), dtype=torch.int32, device=device)
+        gate_d = torch.empty((T, wl.top_k), dtype=torch.float32, device=device)
+        logit_d = torch.empty((T, wl.num_experts), dtype=torch.float32, device=device)
+        moe.moe_route(cfg, h_d, wg_d, bias_d, idx_d, gate_d, logit_d, ws)
+        load_d = torch.empty(wl.num_experts, dtype=torch.int32, device=device)
+        stats_d = torch.empty(64, dtype=torch.uint8, device=device)
+        margin_d = torch.empty(T, dtype=torch.float64, device=device)
+        ms_stats = time_forwards(moe, lambda: moe.moe_routing_stats(cfg, idx_d, 1.25, load_d, stats_d),
+                                 50, stream)
+        ms_margin = time_forwards(moe, lambda: moe.moe_router_margin(cfg, logit_d, margin_d), 50, stream)
+        st = moe.route_stats_from_bytes(stats_d.cpu().numpy().tobytes())
+        m = margin_d.cpu().numpy()
+        line["diagnostics"] = {"routing_stats_us": 1e3 * ms_stats, "router_margin_us": 1e3 * ms_margin,
+                               "routing_stats_cf_1.25": st,
+                               "margin_quantiles": {q: float(v) for q, v in
+                                                    zip(("p01", "p10", "p50"),
+                                                        np.quantile(m, [0.01, 0.1, 0.5]))},
+                               "tokens_with_zero_margin": int((m == 0).sum())}
 
     # ---- the workload's other batch sizes (secondary lines, same layer)
     sweep = []
@@ -496,8 +556,8 @@ def run_gpu(args):
         raise RuntimeError("host-buffer path and device path disagree")
 
     # ---- CPU oracle on the host cores (rank 0, N = 1)
-    if (rank == 0 and world == 1 and not args.no_cpu_baseline and wl.capacity_factor <= 0
-            and wl.weight_bytes() < (8 << 30)):
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and cfg["capacity_factor"] <= 0
+            and default_mode and wl.weight_bytes() < (8 << 30)):
         line["cpu_baseline"] = cpu_baseline(wl, h, wg, bias, host_bf16(out_d))
 
     if world > 1:
@@ -550,6 +610,12 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=["tiny", "mix", "qw", "cap", "ds"])
     ap.add_argument("--tokens", type=int, default=TOKENS)
+    ap.add_argument("--capacity-factor", type=float, default=None,
+                    help="override the workload's capacity factor")
+    ap.add_argument("--policy", default="drop", choices=["drop", "reroute"],
+                    help="overflow policy for routes past an expert's capacity")
+    ap.add_argument("--routing", default="token", choices=["token", "expert"],
+                    help="token choice (top-k) or expert choice (top-C tokens per expert)")
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up + steps forwards of the main workload (for ncu)")
     args = ap.parse_args()
