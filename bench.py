@@ -84,7 +84,7 @@ def load_peaks():
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for name in ("expert_gemm.cu", "ptx.cuh", "kernels.h"):
+    for name in ("expert_gemm.cu", "ptx.cuh", "gemm.h"):
         with open(os.path.join(ROOT, "invariant_expert_routing_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

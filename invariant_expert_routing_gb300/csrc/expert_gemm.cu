@@ -27,7 +27,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
-#include "kernels.h"
+#include "gemm.h"
 #include "ptx.cuh"
 
 namespace moe {

@@ -1,0 +1,62 @@
+// Grouped tcgen05 GEMM of the expert FFN (and of the router's tensor-core
+// logits): tile shapes, the tile list, the launch arguments.  Internal, not
+// part of the C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// Status word bits (mirrors include/moe_api.h).
+constexpr int kDevErrExpertRange = 0x1;
+constexpr int kDevErrTimeout = 0x2;
+constexpr int kDevErrBadBlocks = 0x4;
+
+// Rows of one grouped-GEMM token tile (the N of every tcgen05 MMA), one
+// fixed value per GEMM for every layer and every T: one tile shape, one K
+// order.  W2 takes 256-row tiles (fewer shared-memory bytes per flop); W13
+// keeps 128 rows so that its gate and up accumulators stay double-buffered in
+// the 512 TMEM columns and the epilogue overlaps the next tile's MMAs; the
+// router's tensor-core logits use 128.
+constexpr int kW13TileRows = 128;
+constexpr int kW2TileRows = 256;
+constexpr int kRouterTileRows = 128;
+constexpr int kMaxTileRows = 256;
+// Output features of one grouped-GEMM tile (the M of every MMA).
+constexpr int kTileFeat = 128;
+
+struct GemmTile {
+  int32_t expert;
+  int32_t row0;   // first padded row of the tile
+  int32_t rows;   // valid rows (<= the tile size)
+  int32_t first;  // index of the first tile of this expert in the list
+  int32_t count;  // tiles of this expert
+  int32_t pad[3];
+};
+
+// ---- grouped expert GEMMs (tcgen05)
+struct GemmArgs {
+  int K;               // reduction length (H for W13, I for W2)
+  int n_feat_tiles;    // output features / kTileFeat (I for W13, H for W2)
+  int w_rows_per_e;    // rows of one expert in the 2-D weight map (= K)
+  int up_col;          // column offset of the "up" half in W13 (= I)
+  const GemmTile* tiles;     // routed mode: tile list on the device
+  const int32_t* num_tiles;  // routed mode: device count
+  int identity_T;            // identity mode (shared expert): rows 0..T-1, else 0
+  void* out;           // W13: bf16 a [rows, I]; W2: fp32 y [rows, H]
+  int out_ld;          // elements per output row
+  int* status;
+  int concurrent;      // work units resident at once (set by the launcher)
+};
+
+bool gemm_smem_ok();
+// x_small: the same token tensor with a 32-row box (tiles with <= 32 rows)
+void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
+void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                    const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
+void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
+                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
+
+}  // namespace moe
