@@ -9,7 +9,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 SOURCES = ["route.cu", "dispatch.cu", "expert_gemm.cu", "combine.cu", "moe_api.cu",
-           "dispatch_noalloc.cu", "diag.cu", "expert_choice.cu"]
+           "dispatch_noalloc.cu", "diag.cu", "expert_choice.cu", "reroute.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 

@@ -146,168 +146,6 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
   }
 }
 
-// Overflow reroute ("Mixture-of-Experts Routing at Inference Time", Figure 2,
-// the reroute branch of the overflow policy).  Phase one is the drop rule
-// above: route r keeps its expert if its rank among that expert's routes is
-// below C.  Phase two visits the overflowing routes in ascending r; each takes
-// the best-ranked expert of its token (larger logit, then lower index, NaN
-// last) that has room left and that the token does not use yet (its k chosen
-// experts and the targets of its earlier slots), or stays dropped.
-//
-// One CTA.  Routes are scanned in batches of 1024; the overflowing routes of
-// a batch are compacted in order, then resolved 32 at a time, one warp each:
-// every warp proposes its route's best expert given the room left, and warp 0
-// commits the longest prefix of proposals that the sequential rule would
-// also make (no earlier unresolved slot of the same token, and fewer earlier
-// proposals for the same expert than its room).  The first unresolved route
-// always qualifies, so each round commits at least one route and a group
-// ends within 32 rounds.  Integer decisions only: the result is the
-// sequential assignment, bit for bit.
-constexpr int kRerouteThreads = 1024;
-
-// Ranking key: larger is better; NaN below every number, -0 equal to +0,
-// equal logits ordered by lower expert index.  0 means "no expert".
-__device__ __forceinline__ unsigned long long reroute_key(float l, int e) {
-  uint32_t key = 0u;
-  if (!isnan(l)) {
-    uint32_t u = __float_as_uint(l);
-    if (u == 0x80000000u) u = 0u;
-    key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  }
-  return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
-}
-
-__global__ void __launch_bounds__(kRerouteThreads) reroute_kernel(
-    const int32_t* __restrict__ topk_idx, const float* __restrict__ logits, int T, int N, int k,
-    int capacity, const int32_t* __restrict__ rank_in_tile, const int32_t* __restrict__ tile_base,
-    const int32_t* __restrict__ kept_count, int32_t* __restrict__ route_expert,
-    int32_t* __restrict__ num_dropped, int32_t* __restrict__ num_rerouted) {
-  __shared__ int room[kMaxN];
-  __shared__ int list[kRerouteThreads];
-  __shared__ int wsum[32];
-  __shared__ int tent[32];
-  __shared__ int done[32];
-  __shared__ int s_total, s_all_done, s_rer, s_drop;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const long long R = (long long)T * k;
-  for (int e = tid; e < N; e += blockDim.x) room[e] = capacity - kept_count[e];
-  if (tid == 0) {
-    s_rer = 0;
-    s_drop = 0;
-  }
-  __syncthreads();
-  for (long long base = 0; base < R; base += kRerouteThreads) {
-    const long long r = base + tid;
-    bool over = false;
-    if (r < R) {
-      const int e = topk_idx[r];
-      int out = -1;
-      if (e >= 0 && e < N) {
-        const int rank = tile_base[(size_t)(r / kDispatchTile) * N + e] + rank_in_tile[r];
-        if (rank < capacity) out = e;
-        else over = true;
-      }
-      route_expert[r] = out;
-    }
-    const unsigned om = __ballot_sync(0xffffffffu, over);
-    if (lane == 0) wsum[w] = __popc(om);
-    __syncthreads();
-    if (w == 0) {
-      const int c = wsum[lane];
-      int incl = c;
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      wsum[lane] = incl - c;
-      if (lane == 31) s_total = incl;
-    }
-    __syncthreads();
-    if (over) list[wsum[w] + __popc(om & ((1u << lane) - 1u))] = tid;
-    __syncthreads();
-    const int total = s_total;
-    for (int c0 = 0; c0 < total; c0 += 32) {
-      const int n = min(32, total - c0);
-      if (tid < 32) done[tid] = tid < n ? 0 : 1;
-      // this warp's route: token t, slot j, and the experts the token uses
-      // among the experts lane, lane+32, ... (bit s = expert lane + 32 s)
-      long long rr = 0;
-      int t = 0;
-      uint32_t used = 0;
-      if (w < n) {
-        rr = base + list[c0 + w];
-        t = (int)(rr / k);
-        const int j = (int)(rr - (long long)t * k);
-        for (int q = 0; q < k; ++q) {
-          const long long rq = (long long)t * k + q;
-          const int e1 = topk_idx[rq];
-          if (e1 >= 0 && e1 < N && (e1 & 31) == lane) used |= 1u << (e1 >> 5);
-        }
-      }
-      __syncthreads();
-      for (int round = 0; round <= 32; ++round) {
-        if (w < n && !done[w]) {
-          const int j = (int)(rr - (long long)t * k);
-          uint32_t excl = used;
-          for (int q = 0; q < j; ++q) {   // targets of the token's earlier slots
-            const int e2 = route_expert[(long long)t * k + q];
-            if (e2 >= 0 && e2 < N && (e2 & 31) == lane) excl |= 1u << (e2 >> 5);
-          }
-          unsigned long long best = 0ull;
-          for (int e = lane, sl = 0; e < N; e += 32, ++sl) {
-            if (((excl >> sl) & 1u) || room[e] <= 0) continue;
-            const unsigned long long key = reroute_key(logits[(size_t)t * N + e], e);
-            best = key > best ? key : best;
-          }
-          for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
-          }
-          if (lane == 0)
-            tent[w] = best ? (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull)) : -1;
-        }
-        __syncthreads();
-        if (w == 0) {
-          const bool unres = lane < n && !done[lane];
-          const int te = unres ? tent[lane] : -2;
-          const long long myr = unres ? base + list[c0 + lane] : -1;
-          const int tok = unres ? (int)(myr / k) : -1 - lane;
-          const unsigned unres_m = __ballot_sync(0xffffffffu, unres);
-          const unsigned lt = (1u << lane) - 1u;
-          const bool clash = (__match_any_sync(0xffffffffu, tok) & unres_m & lt) != 0u;
-          const int occ = __popc(__match_any_sync(0xffffffffu, te) & unres_m & lt);
-          const bool valid = unres && !clash && (te < 0 || occ < room[te]);
-          const unsigned bad = __ballot_sync(0xffffffffu, unres && !valid);
-          const unsigned below = bad ? ((1u << (__ffs(bad) - 1)) - 1u) : 0xffffffffu;
-          const bool commit = unres && ((below >> lane) & 1u);
-          if (commit) {
-            if (te >= 0) route_expert[myr] = te;
-            done[lane] = 1;
-          }
-          const unsigned grp = __match_any_sync(0xffffffffu, commit ? te : -3 - lane);
-          if (commit && te >= 0 && (grp & lt) == 0u) room[te] -= __popc(grp);
-          const unsigned cr = __ballot_sync(0xffffffffu, commit && te >= 0);
-          const unsigned cd = __ballot_sync(0xffffffffu, commit && te < 0);
-          const unsigned left = __ballot_sync(0xffffffffu, unres && !commit);
-          if (lane == 0) {
-            s_rer += __popc(cr);
-            s_drop += __popc(cd);
-            s_all_done = left == 0u;
-          }
-        }
-        __syncthreads();
-        if (s_all_done) break;
-      }
-      __syncthreads();
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
-    *num_dropped = s_drop;
-    *num_rerouted = s_rer;
-  }
-}
-
 // Grouped-GEMM tile list from the padded blocks: each expert segment is cut
 // into tiles of tile_rows rows from its start.  Rejects (no tiles, status
 // bit) a block list that is not sorted by expert or out of range.
@@ -446,7 +284,7 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
                              int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
                              int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
                              int32_t* num_rerouted, int32_t* rank_in_tile, int32_t* tile_count,
-                             int32_t* seg_off, int* status, cudaStream_t s) {
+                             int32_t* seg_off, const RerouteScratch& sc, int* status, cudaStream_t s) {
   const int R = T * k;
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   // phase one: ranks and the per-expert kept counts of the drop rule
@@ -455,9 +293,8 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
   dispatch_scan_kernel<<<1, 256, 0, s>>>(tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
                                          num_padded, nullptr, block_expert, sorted_route_ids);
   // phase two, then the stable layout of the final assignment
-  reroute_kernel<<<1, kRerouteThreads, 0, s>>>(topk_idx, logits, T, N, k, capacity, rank_in_tile,
-                                               tile_count, expert_counts, route_expert, num_dropped,
-                                               num_rerouted);
+  launch_reroute(topk_idx, logits, T, N, k, capacity, rank_in_tile, tile_count, expert_counts, sc,
+                 route_expert, num_dropped, num_rerouted, s);
   launch_dispatch_routes(route_expert, R, N, B, route_kept, route_pos, sorted_route_ids, block_expert,
                          num_padded, expert_counts, rank_in_tile, tile_count, seg_off, status, s);
 }

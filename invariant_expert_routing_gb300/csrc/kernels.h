@@ -33,6 +33,25 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
                      int32_t* seg_off, int* status, cudaStream_t s);
+// Scratch of the overflow reroute (R routes, N experts).
+constexpr int kRerouteListLen = 32;   // cached best experts per overflowing route
+struct RerouteScratch {
+  int32_t* list;    // [R] overflowing route ids, ascending
+  int32_t* hold;    // [R] per list position: expert held, -1 none, -2 none possible
+  int32_t* cand;    // [R] per list position: this round's candidate
+  int32_t* ptr;     // [R] per list position: next cached preference to try
+  uint8_t* prefs;   // [R * kRerouteListLen] cached preferences, by route id
+  int32_t* acc;     // [N] overflowing routes each expert holds at the end
+  int32_t* worst;   // [N] largest route id each expert holds (-1 none)
+  int32_t* flag;    // [1] non-zero: recompute with the sequential kernel
+  int32_t* count;   // [1] overflowing routes
+};
+// phase two of the reroute: route_expert for every route (kept: its expert,
+// overflowing: its new expert or -1), num_dropped / num_rerouted
+void launch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int capacity,
+                    const int32_t* rank_in_tile, const int32_t* tile_base, const int32_t* kept_count,
+                    const RerouteScratch& sc, int32_t* route_expert, int32_t* num_dropped,
+                    int32_t* num_rerouted, cudaStream_t s);
 // phase one of launch_dispatch, overflow reroute, then the layout of the
 // final assignment (route_expert: expert per route, -1 = dropped)
 void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int B,
@@ -40,7 +59,7 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
                              int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
                              int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
                              int32_t* num_rerouted, int32_t* rank_in_tile, int32_t* tile_count,
-                             int32_t* seg_off, int* status, cudaStream_t s);
+                             int32_t* seg_off, const RerouteScratch& sc, int* status, cudaStream_t s);
 // stable layout of routes that already carry their expert (-1 = none)
 void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, uint8_t* route_kept,
                             int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,

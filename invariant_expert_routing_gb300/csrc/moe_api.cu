@@ -90,7 +90,8 @@ int64_t max_gemm_tiles_of(const moe_config* c, int32_t T, int tile_rows) {
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
   size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
-      num_padded, counts, dropped, route_expert, rerouted, ec_keys, gemm_tiles, num_gemm_tiles,
+      num_padded, counts, dropped, route_expert, rerouted, rr_list, rr_hold, rr_cand, rr_ptr, rr_prefs,
+      rr_acc, rr_worst, rr_flag, rr_count, ec_keys, gemm_tiles, num_gemm_tiles,
       gemm_tiles2, num_gemm_tiles2, x_perm, a, y, a_sh, y_sh, h_stage, out_stage, total;
 };
 
@@ -121,8 +122,18 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.num_padded = take(sizeof(int32_t));
   L.counts = take(sizeof(int32_t) * N);
   L.dropped = take(sizeof(int32_t));
-  L.route_expert = take(c->overflow_policy == MOE_OVERFLOW_REROUTE ? sizeof(int32_t) * R : 0);
+  const bool rr = c->overflow_policy == MOE_OVERFLOW_REROUTE && !expert_choice(c);
+  L.route_expert = take(rr ? sizeof(int32_t) * R : 0);
   L.rerouted = take(sizeof(int32_t));
+  L.rr_list = take(rr ? sizeof(int32_t) * R : 0);
+  L.rr_hold = take(rr ? sizeof(int32_t) * R : 0);
+  L.rr_cand = take(rr ? sizeof(int32_t) * R : 0);
+  L.rr_ptr = take(rr ? sizeof(int32_t) * R : 0);
+  L.rr_prefs = take(rr ? R * moe::kRerouteListLen : 0);
+  L.rr_acc = take(sizeof(int32_t) * N);
+  L.rr_worst = take(sizeof(int32_t) * N);
+  L.rr_flag = take(sizeof(int32_t));
+  L.rr_count = take(sizeof(int32_t));
   L.ec_keys = take(expert_choice(c) ? sizeof(unsigned long long) * N * T : 0);
   // tile lists of the W13 (128-row) and W2 (256-row) GEMMs
   L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW13TileRows));
@@ -269,11 +280,18 @@ moe_status reroute_impl(const moe_config* c, int32_t T, const int32_t* idx, cons
                         uint8_t* kept, int32_t* route_expert, int32_t* pos, int32_t* sorted,
                         int32_t* blocks, int32_t* num_padded, int32_t* counts, int32_t* dropped,
                         int32_t* rerouted, void* ws, cudaStream_t s) {
-  const Layout L = layout_of(c, T);
+  // the reroute scratch is laid out for the reroute policy whatever cfg says
+  moe_config cr = *c;
+  cr.overflow_policy = MOE_OVERFLOW_REROUTE;
+  const Layout L = layout_of(&cr, T);
+  moe::RerouteScratch sc{at<int32_t>(ws, L.rr_list), at<int32_t>(ws, L.rr_hold), at<int32_t>(ws, L.rr_cand),
+                         at<int32_t>(ws, L.rr_ptr), at<uint8_t>(ws, L.rr_prefs), at<int32_t>(ws, L.rr_acc),
+                         at<int32_t>(ws, L.rr_worst), at<int32_t>(ws, L.rr_flag),
+                         at<int32_t>(ws, L.rr_count)};
   moe::launch_dispatch_reroute(idx, logits, T, c->num_experts, c->top_k, c->block_size, capacity_of(c, T),
                                kept, route_expert, pos, sorted, blocks, num_padded, counts, dropped,
                                rerouted, at<int32_t>(ws, L.rank), at<int32_t>(ws, L.tile_count),
-                               at<int32_t>(ws, L.seg_off), at<int>(ws, L.status), s);
+                               at<int32_t>(ws, L.seg_off), sc, at<int>(ws, L.status), s);
   return last_cuda();
 }
 
@@ -565,7 +583,9 @@ moe_status moe_dispatch_align_reroute(const moe_config* cfg, int32_t T, const in
   MOE_TRY(need(expert_counts));
   MOE_TRY(need(num_dropped));
   MOE_TRY(need(num_rerouted));
-  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  moe_config cr = *cfg;
+  cr.overflow_policy = MOE_OVERFLOW_REROUTE;
+  MOE_TRY(check_ws(&cr, T, ws, ws_bytes));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (capacity_of(cfg, T) < 0) {
     // no capacity: nothing overflows; every route keeps its expert
@@ -738,14 +758,15 @@ int32_t moe_forward_launch_count(const moe_config* cfg) {
   // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
   // combine 1 (+ shared W13, W2).  Router: CUDA cores logits + top-k = 2,
   // tensor cores transpose, norms, GEMM, certified select = 4.  Dispatch:
-  // count, scan, scatter = 3; with reroute count, scan, reroute, count,
-  // scan, scatter = 6 after the CUDA-core router.  Expert choice: logits,
-  // scores, selection = 3 in all.
+  // count, scan, scatter = 3; with reroute count, scan, preference lists,
+  // deferred acceptance, check, sequential fallback (returns at once unless
+  // the check failed), count, scan, scatter = 9 after the CUDA-core router.
+  // Expert choice: logits, scores, selection = 3 in all.
   int front = 0;
   if (expert_choice(cfg)) {
     front = 3;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
-    front = 2 + 6;
+    front = 2 + 9;
   } else {
     front = (use_tc_router(cfg) ? 4 : 2) + 3;
   }

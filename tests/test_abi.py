@@ -147,7 +147,7 @@ def test_launch_counts(moe):
     qw = dict(hidden=2048, num_experts=128, top_k=8, intermediate=768, block_size=16)
     assert moe.moe_forward_launch_count(mix) == 2 + 3 + 6
     assert moe.moe_forward_launch_count(qw) == 4 + 3 + 6
-    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1)) == 8 + 6
+    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1)) == 11 + 6
     assert moe.moe_forward_launch_count(dict(qw, routing=1)) == 3 + 6
     assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128)) == 2 + 3 + 6 + 2
 

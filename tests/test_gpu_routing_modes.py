@@ -338,3 +338,21 @@ def test_expert_choice_ties_go_to_the_lowest_token():
     kept = got["route_kept"].reshape(T, N)
     assert (kept[:C] == 1).all() and not kept[C:].any()
     del host
+
+
+def test_reroute_sequential_path_is_bit_exact():
+    # the sequential kernel (the fallback of the deferred-acceptance pass) on
+    # its own: a process with MOE_REROUTE_SEQUENTIAL=1 runs only it
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from tests import test_gpu_routing_modes as m\n"
+            "for case in [('tiny', 61, 0.75), ('cap', 2000, 0.8), ('qw', 777, 0.6)]:\n"
+            "    m.test_reroute_dispatch_is_bit_exact(*case)\n"
+            "print('sequential ok')\n") % root
+    env = dict(os.environ, MOE_REROUTE_SEQUENTIAL="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0 and "sequential ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
