@@ -34,7 +34,7 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
                      int32_t* seg_off, int* status, cudaStream_t s);
 // Scratch of the overflow reroute (R routes, N experts).
-constexpr int kRerouteListLen = 32;   // cached best experts per overflowing route
+constexpr int kRerouteListLen = 128;  // cached best experts per overflowing route
 struct RerouteScratch {
   int32_t* list;    // [R] overflowing route ids, ascending
   int32_t* hold;    // [R] per list position: expert held, -1 none, -2 none possible

@@ -219,12 +219,16 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
       sc.ptr[i] = p;
       if (chosen < 0 && !lists_complete) {
         // the cached list is used up: scan every expert
+        uint32_t own[kMaxN / 32];
+        for (int x = 0; x < kMaxN / 32; ++x) own[x] = 0u;
+        for (int q = 0; q < k; ++q) {
+          const int e1 = topk_idx[(long long)t * k + q];
+          if (e1 >= 0 && e1 < N) own[e1 >> 5] |= 1u << (e1 & 31);
+        }
+        for (int x = 0; x < nh; ++x) own[held[x] >> 5] |= 1u << (held[x] & 31);
         unsigned long long best = 0ull;
         for (int e = 0; e < N; ++e) {
-          bool ex = false;
-          for (int q = 0; q < k; ++q) ex |= topk_idx[(long long)t * k + q] == e;
-          for (int x = 0; x < nh; ++x) ex |= held[x] == e;
-          if (ex || !(cnt[e] < room[e] || worst[e] > r)) continue;
+          if (((own[e >> 5] >> (e & 31)) & 1u) || !(cnt[e] < room[e] || worst[e] > r)) continue;
           const unsigned long long key = reroute_key(logits[(size_t)t * N + e], e);
           best = key > best ? key : best;
         }
