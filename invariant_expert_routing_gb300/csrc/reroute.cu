@@ -49,10 +49,6 @@ __device__ __forceinline__ unsigned long long reroute_key(float l, int e) {
   return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
 }
 
-__device__ __forceinline__ int prefs_at(const uint8_t* __restrict__ prefs, int r, int L, int p) {
-  return prefs[(size_t)r * L + p];
-}
-
 __device__ __forceinline__ int key_expert(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
@@ -155,6 +151,8 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
     int32_t* __restrict__ route_expert, int32_t* __restrict__ num_dropped,
     int32_t* __restrict__ num_rerouted) {
   __shared__ int room[kMaxN], cnt[kMaxN], worst[kMaxN], acc[kMaxN], nworst[kMaxN];
+  // thresh[e]: expert e can still take route r iff r < thresh[e] (INT_MAX while it has room)
+  __shared__ int thresh[kMaxN];
   __shared__ int tab[32][kMaxN + 1];
   __shared__ int wbuf[33];
   __shared__ int s_unplaced;
@@ -167,6 +165,7 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
     room[e] = capacity - kept_count[e];
     cnt[e] = 0;
     worst[e] = -1;
+    thresh[e] = room[e] > 0 ? 0x7FFFFFFF : -1;
   }
   // phase one for every route; the overflowing ones listed in route order
   int M = 0;
@@ -207,13 +206,19 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
         if (sc.hold[q] >= 0) held[nh++] = sc.hold[q];
       int chosen = -1;
       int p = sc.ptr[i];
-      for (; p < Leff; ++p) {
-        const int e = prefs_at(sc.prefs, r, L, p);
-        bool ex = false;
-        for (int x = 0; x < nh; ++x) ex |= held[x] == e;
-        if (!ex && (cnt[e] < room[e] || worst[e] > r)) {
-          chosen = e;
-          break;
+      // walk the cached list 16 entries (one 16-byte load) at a time
+      const uint4* row = reinterpret_cast<const uint4*>(sc.prefs + (size_t)r * L);
+      while (p < Leff && chosen < 0) {
+        const uint4 v = row[p >> 4];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int b = p & 15; b < 16 && p < Leff; ++b, ++p) {
+          const int e = (int)((wv[b >> 2] >> (8 * (b & 3))) & 0xFFu);
+          bool ex = false;
+          for (int x = 0; x < nh; ++x) ex |= held[x] == e;
+          if (!ex && r < thresh[e]) {
+            chosen = e;
+            break;
+          }
         }
       }
       sc.ptr[i] = p;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
         for (int x = 0; x < nh; ++x) own[held[x] >> 5] |= 1u << (held[x] & 31);
         unsigned long long best = 0ull;
         for (int e = 0; e < N; ++e) {
-          if (((own[e >> 5] >> (e & 31)) & 1u) || !(cnt[e] < room[e] || worst[e] > r)) continue;
+          if (((own[e >> 5] >> (e & 31)) & 1u) || !(r < thresh[e])) continue;
           const unsigned long long key = reroute_key(logits[(size_t)t * N + e], e);
           best = key > best ? key : best;
         }
@@ -291,6 +296,7 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
     for (int e = tid; e < N; e += blockDim.x) {
       cnt[e] = min(acc[e], room[e]);
       worst[e] = nworst[e];
+      thresh[e] = cnt[e] < room[e] ? 0x7FFFFFFF : worst[e];
     }
     __syncthreads();
     settled = s_unplaced == 0;
