@@ -40,6 +40,7 @@ struct RerouteScratch {
   int32_t* hold;    // [R] per list position: expert held, -1 none, -2 none possible
   int32_t* cand;    // [R] per list position: this round's candidate
   int32_t* ptr;     // [R] per list position: next cached preference to try
+  int32_t* first;   // [R] per list position: list position of the token's first overflowing slot
   uint8_t* prefs;   // [R * kRerouteListLen] cached preferences, by route id
   int32_t* acc;     // [N] overflowing routes each expert holds at the end
   int32_t* worst;   // [N] largest route id each expert holds (-1 none)

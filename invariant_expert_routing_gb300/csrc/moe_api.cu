@@ -90,7 +90,8 @@ int64_t max_gemm_tiles_of(const moe_config* c, int32_t T, int tile_rows) {
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
   size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
-      num_padded, counts, dropped, route_expert, rerouted, rr_list, rr_hold, rr_cand, rr_ptr, rr_prefs,
+      num_padded, counts, dropped, route_expert, rerouted, rr_list, rr_hold, rr_cand, rr_ptr, rr_first,
+      rr_prefs,
       rr_acc, rr_worst, rr_flag, rr_count, ec_keys, gemm_tiles, num_gemm_tiles,
       gemm_tiles2, num_gemm_tiles2, x_perm, a, y, a_sh, y_sh, h_stage, out_stage, total;
 };
@@ -129,6 +130,7 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.rr_hold = take(rr ? sizeof(int32_t) * R : 0);
   L.rr_cand = take(rr ? sizeof(int32_t) * R : 0);
   L.rr_ptr = take(rr ? sizeof(int32_t) * R : 0);
+  L.rr_first = take(rr ? sizeof(int32_t) * R : 0);
   L.rr_prefs = take(rr ? R * moe::kRerouteListLen : 0);
   L.rr_acc = take(sizeof(int32_t) * N);
   L.rr_worst = take(sizeof(int32_t) * N);
@@ -285,7 +287,8 @@ moe_status reroute_impl(const moe_config* c, int32_t T, const int32_t* idx, cons
   cr.overflow_policy = MOE_OVERFLOW_REROUTE;
   const Layout L = layout_of(&cr, T);
   moe::RerouteScratch sc{at<int32_t>(ws, L.rr_list), at<int32_t>(ws, L.rr_hold), at<int32_t>(ws, L.rr_cand),
-                         at<int32_t>(ws, L.rr_ptr), at<uint8_t>(ws, L.rr_prefs), at<int32_t>(ws, L.rr_acc),
+                         at<int32_t>(ws, L.rr_ptr), at<int32_t>(ws, L.rr_first), at<uint8_t>(ws, L.rr_prefs),
+                         at<int32_t>(ws, L.rr_acc),
                          at<int32_t>(ws, L.rr_worst), at<int32_t>(ws, L.rr_flag),
                          at<int32_t>(ws, L.rr_count)};
   moe::launch_dispatch_reroute(idx, logits, T, c->num_experts, c->top_k, c->block_size, capacity_of(c, T),

@@ -177,12 +177,21 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
       over = phase_one_overflow(topk_idx, rank_in_tile, tile_base, N, capacity, r, &kept_e);
       route_expert[r] = kept_e;
     }
+    int nprev = 0;   // earlier overflowing slots of the same token
+    if (over) {
+      const long long t0 = (r / k) * k;
+      for (long long q = t0; q < r; ++q) {
+        int kq = -1;
+        nprev += phase_one_overflow(topk_idx, rank_in_tile, tile_base, N, capacity, q, &kq) ? 1 : 0;
+      }
+    }
     int total = 0;
     const int pos = block_scan_1024(over ? 1 : 0, wbuf, &total);
     if (over) {
       sc.list[M + pos] = (int32_t)r;
       sc.hold[M + pos] = -1;
       sc.ptr[M + pos] = 0;
+      sc.first[M + pos] = M + pos - nprev;
     }
     M += total;
   }
@@ -202,8 +211,10 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
       const int t = r / k;
       int held[16];
       int nh = 0;
-      for (int q = i - 1; q >= 0 && sc.list[q] / k == t && nh < 16; --q)
-        if (sc.hold[q] >= 0) held[nh++] = sc.hold[q];
+      for (int q = sc.first[i]; q < i; ++q) {   // the token's earlier overflowing slots
+        const int hq = sc.hold[q];
+        if (hq >= 0) held[nh++] = hq;
+      }
       int chosen = -1;
       int p = sc.ptr[i];
       // walk the cached list 16 entries (one 16-byte load) at a time
@@ -254,13 +265,9 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_da_kernel(
       if (i < M) {
         c = sc.cand[i];
         r = sc.list[i];
-        const int t = r / k;
         if (c >= 0)   // a token's later slot yields to an earlier slot's candidate
-          for (int q = i - 1; q >= 0 && sc.list[q] / k == t; --q)
-            if (sc.cand[q] == c) {
-              c = -1;
-              break;
-            }
+          for (int q = sc.first[i]; q < i; ++q)
+            if (sc.cand[q] == c) c = -1;
       }
       for (int x = tid; x < 32 * (kMaxN + 1); x += blockDim.x) (&tab[0][0])[x] = 0;
       __syncthreads();
