@@ -364,6 +364,295 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// The same GEMM on pairs of CTAs (a cluster of two, one per SM) whose tensor
+// cores run one cta_group::2 MMA of M = 256 features x N = 256 token rows:
+// each CTA loads its own 128 features of the weights (gate and up for W13)
+// and half of the token tile (128 rows), and its TMEM receives its 128
+// features for all 256 rows.  Per SM this halves the token bytes per flop,
+// the operand traffic that bounds the one-CTA kernel.  One shape for every
+// tile and every batch, K from 0 to the end: the arithmetic of a token's row
+// does not depend on the batch or on which half of the tile holds it.
+//
+// Synchronisation: the even CTA's producer expects the bytes of both CTAs on
+// its full barrier, and both CTAs' TMA loads complete there; the even CTA's
+// MMA thread commits to the empty and tmem_full barriers of both CTAs; the
+// epilogue warps of both CTAs arrive on the even CTA's tmem_empty.  Every
+// wait is bounded, and both CTAs of a pair follow the same control flow up to
+// the final cluster barrier.
+constexpr int kPairRows = 256;      // token rows per pair tile (the MMA's N)
+constexpr int kPairFeat = 256;      // features per pair tile (the MMA's M)
+
+template <bool kW13>
+struct PairCfg {
+  static constexpr int kRowsCta = kPairRows / 2;
+  static constexpr uint32_t kABytes = kW13 ? 4 * kBoxBytes : 2 * kBoxBytes;
+  static constexpr uint32_t kBTileBytes = kRowsCta * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
+  static constexpr int kStages = (int)(kStageBudget / kStageBytes) < 6 ? (int)(kStageBudget / kStageBytes) : 6;
+  static constexpr uint32_t kAccCols = kW13 ? 2 * kPairRows : kPairRows;
+  static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kBarBytes = 256;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairFeat, kPairRows, true, false);
+};
+
+template <bool kW13>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
+                            const __grid_constant__ CUtensorMap x_map,
+                            const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
+  using C = PairCfg<kW13>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+
+  const uint32_t rank = cluster_ctarank();            // 0: issues the MMAs
+  const bool lead = rank == 0;
+  const int num_tiles = args.identity_T ? (args.identity_T + kPairRows - 1) / kPairRows : *args.num_tiles;
+  const int nfe = args.n_feat_tiles;                  // pair feature tiles of 256
+  const int pair0 = (int)(blockIdx.x >> 1);
+  const int pairs = (int)(gridDim.x >> 1);
+  const int total = num_tiles * nfe;
+  if (pair0 >= total) return;  // the same verdict in both CTAs of the pair
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t tfull0 = empty0 + 8 * C::kStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = args.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(full0 + 8 * st, 1);
+      mbar_init(empty0 + 8 * st, 1);
+    }
+    for (int b = 0; b < C::kNumAcc; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 2 * kEpiWarps);   // one arrival per epilogue warp of each CTA
+    }
+    mbar_init(drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&s_tmem_base), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&w_map);
+    prefetch_tmap(&x_map);
+    prefetch_tmap(&x_map_small);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before either signals the other
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    const uint64_t pol_w = policy_evict_normal();
+    const uint64_t pol_x = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed = 0;
+    bool ok = true;
+    for (int item = pair0; item < total && ok; item += pairs) {
+      const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
+      const TileInfo t = wk.t;
+      const int wrow0 = t.expert * args.w_rows_per_e;
+      const int fcol = wk.f * kPairFeat + (int)rank * kTileFeat;     // this CTA's 128 features
+      const int brow0 = t.row0 + (int)rank * C::kRowsCta;             // this CTA's half of the rows
+      const bool small = t.rows <= kSmallRows;
+      const int b_rows = small ? kSmallRows : C::kRowsCta;
+      const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, &s_abort) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = smem + stage * C::kStageBytes;
+        uint8_t* sB = sA + C::kABytes;
+        const uint32_t fb = mapa_shared(full0 + 8 * stage, 0);   // the even CTA's full barrier
+        const int k0 = ks * kBK;
+        if (lane == 0) {
+          if (lead) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * cta_tx);
+          tma_load_2d_pair(smem_u32(sA), &w_map, fcol, wrow0 + k0, fb, pol_w);
+          tma_load_2d_pair(smem_u32(sA + kBoxBytes), &w_map, fcol + 64, wrow0 + k0, fb, pol_w);
+          if (kW13) {
+            tma_load_2d_pair(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
+            tma_load_2d_pair(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb,
+                             pol_w);
+          }
+          tma_load_2d_pair(smem_u32(sB), small ? &x_map_small : &x_map, k0, brow0, fb, pol_x);
+        }
+        __syncwarp();
+        armed = min(armed + 1, C::kStages);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      s_abort = 1;
+      if (lane == 0) atomicOr(args.status, kDevErrTimeout);
+    }
+    if (s_abort && lane == 0) {
+      if (lead) {
+        // copies already issued (ours and the odd CTA's) complete on our full
+        // barriers: let them land before exit
+        volatile int no_abort = 0;
+        int st = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < armed; ++i) {
+          if (--st < 0) {
+            st = C::kStages - 1;
+            ph ^= 1u;
+          }
+          mbar_wait_cluster(full0 + 8 * st, ph, &no_abort);
+        }
+      } else {
+        // the odd CTA's copies complete on the even CTA's barriers: give any
+        // still in flight time to land in our shared memory
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lead && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int item = pair0; item < total && ok; item += pairs) {
+        if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem + acc * C::kAccCols;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!mbar_wait_cluster(full0 + 8 * stage, phase, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t b_base = a_base + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
+            const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
+            mma_bf16_pair(d0, adesc, bdesc, C::kIdesc, accum);
+            if (kW13) {
+              const uint64_t adesc_up = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+              mma_bf16_pair(d0 + kPairRows, adesc_up, bdesc, C::kIdesc, accum);
+            }
+          }
+          mma_commit_pair(empty0 + 8 * stage, 0x3);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull0 + 8 * acc, 0x3);
+        if (++acc == C::kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(args.status, kDevErrTimeout);
+      }
+      mma_commit_pair(drain, 0x1);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int feat_local = quarter * 32 + lane;
+    const int col0 = ((warp - 2) / 4) * (kPairRows / 2), col1 = col0 + kPairRows / 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = pair0; item < total; item += pairs) {
+      const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
+      const TileInfo t = wk.t;
+      int got = 1;
+      if (lane == 0) got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, &s_abort) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) {
+          s_abort = 1;
+          atomicOr(args.status, kDevErrTimeout);
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
+      const int feat = wk.f * kPairFeat + (int)rank * kTileFeat + feat_local;
+      for (int c = col0; c < col1 && c < t.rows; c += 16) {
+        float g[16];
+        tmem_ld16(tbase + c, g);
+        if (kW13) {
+          float u[16];
+          tmem_ld16(tbase + kPairRows + c, u);
+          tmem_wait_ld();
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.rows) {
+              const float x = g[jj];
+              const float v = (x / (1.0f + expf(-x))) * u[jj];
+              out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v);
+            }
+          }
+        } else {
+          tmem_wait_ld();
+          float* out = reinterpret_cast<float*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.rows) out[(size_t)(t.row0 + j) * args.out_ld + feat] = g[jj];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
+      if (++acc == C::kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // nothing of either CTA still targets the other's shared memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, C::kTmemCols);
+}
+
 template <bool kW13, int BN>
 void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
             GemmArgs a, int max_tiles, int num_sms, cudaStream_t s) {
@@ -383,6 +672,55 @@ void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMa
   kernel<<<grid, kThreads, smem, s>>>(w_map, x_map, x_small, a);
 }
 
+// Pairs of CTAs that can be resident at once (one CTA per SM; a pair needs
+// two SMs of one GPC), looked up once per device and kernel.
+template <bool kW13>
+int resident_pairs(int num_sms) {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<kW13>::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  n = n < num_sms / 2 ? n : num_sms / 2;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+template <bool kW13>
+void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small, GemmArgs a,
+                 int max_tiles, int num_sms, cudaStream_t s) {
+  auto kernel = expert_gemm_pair_kernel<kW13>;
+  const int smem = (int)PairCfg<kW13>::kSmemBytes;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const long long items = (long long)max_tiles * a.n_feat_tiles;
+  if (items <= 0) return;
+  const int cap = resident_pairs<kW13>(num_sms);
+  const int pairs = (int)(items < cap ? items : cap);
+  a.concurrent = pairs;
+  kernel<<<2 * pairs, kThreads, smem, s>>>(w_map, x_map, x_small, a);
+}
+
 }  // namespace
 
 bool gemm_smem_ok() {
@@ -391,17 +729,26 @@ bool gemm_smem_ok() {
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   return optin >= (int)GemmCfg<true, kW13TileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kW2TileRows>::kSmemBytes &&
-         optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes;
+         optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes &&
+         optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes;
 }
+
+bool gemm_pair_ok(int features) { return features % kPairFeat == 0; }
 
 void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                      const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
-  launch<true, kW13TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  if (a.pair)
+    launch_pair<true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  else
+    launch<true, kW13TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
 }
 
 void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
-  launch<false, kW2TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  if (a.pair)
+    launch_pair<false>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  else
+    launch<false, kW2TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
 }
 
 void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,

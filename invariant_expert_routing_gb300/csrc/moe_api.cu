@@ -341,66 +341,79 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
   mark(mk, 3);
 
+  // CTA-pair kernels where the output features are a multiple of 256 (a
+  // property of the layer, the same for every T); they take the 256-row tile
+  // list and load 128-row token boxes per CTA
+  const bool pair13 = moe::gemm_pair_ok(I), pair2 = moe::gemm_pair_ok(H);
+  const int box13 = pair13 ? moe::kPairBoxRows : moe::kW13TileRows;
+  const int box2 = pair2 ? moe::kPairBoxRows : moe::kW2TileRows;
   CUtensorMap m_w13, m_x, m_xs, m_w2, m_a, m_as;
   if (!map_2d(&m_w13, w13, 2ull * I, (uint64_t)N * H, 64, 64) ||
-      !token_maps(&m_x, &m_xs, x_perm, (uint64_t)H, (uint64_t)(rows + moe::kMaxTileRows), moe::kW13TileRows) ||
+      !token_maps(&m_x, &m_xs, x_perm, (uint64_t)H, (uint64_t)(rows + moe::kMaxTileRows), box13) ||
       !map_2d(&m_w2, w2, (uint64_t)H, (uint64_t)N * I, 64, 64) ||
-      !token_maps(&m_a, &m_as, a, (uint64_t)I, (uint64_t)(rows + moe::kMaxTileRows), moe::kW2TileRows))
+      !token_maps(&m_a, &m_as, a, (uint64_t)I, (uint64_t)(rows + moe::kMaxTileRows), box2))
     return MOE_ERR_CUDA;
 
   moe::GemmArgs g13{};
   g13.K = H;
-  g13.n_feat_tiles = I / moe::kTileFeat;
+  g13.n_feat_tiles = pair13 ? I / moe::kPairTileRows : I / moe::kTileFeat;
   g13.w_rows_per_e = H;
   g13.up_col = I;
-  g13.tiles = tiles13;
-  g13.num_tiles = ntiles13;
+  g13.tiles = pair13 ? tiles2 : tiles13;
+  g13.num_tiles = pair13 ? ntiles2 : ntiles13;
   g13.identity_T = 0;
   g13.out = a;
   g13.out_ld = I;
   g13.status = status;
-  moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, max_tiles13, sms, s);
+  g13.pair = pair13 ? 1 : 0;
+  moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, pair13 ? max_tiles2 : max_tiles13, sms, s);
   mark(mk, 4);
 
   moe::GemmArgs g2 = g13;
   g2.K = I;
-  g2.n_feat_tiles = H / moe::kTileFeat;
+  g2.n_feat_tiles = pair2 ? H / moe::kPairTileRows : H / moe::kTileFeat;
   g2.w_rows_per_e = I;
   g2.up_col = 0;
   g2.tiles = tiles2;
   g2.num_tiles = ntiles2;
   g2.out = y_perm;
   g2.out_ld = H;
+  g2.pair = pair2 ? 1 : 0;
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
   const int Is = c->shared_intermediate;
   if (Is > 0) {
     uint16_t* ash = at<uint16_t>(ws, L.a_sh);
+    const bool spair13 = moe::gemm_pair_ok(Is);
+    const int sbox13 = spair13 ? moe::kPairBoxRows : moe::kW13TileRows;
+    const int srows13 = spair13 ? moe::kPairTileRows : moe::kW13TileRows;
     CUtensorMap m_w13s, m_w2s, m_ash, m_ashs, m_h, m_hs;
     // the last tile of h may run past row T-1: TMA fills those rows with zeros
-    if (!token_maps(&m_h, &m_hs, h, (uint64_t)H, (uint64_t)T, moe::kW13TileRows) ||
+    if (!token_maps(&m_h, &m_hs, h, (uint64_t)H, (uint64_t)T, sbox13) ||
         !map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
         !map_2d(&m_w2s, w2s, (uint64_t)H, (uint64_t)Is, 64, 64) ||
-        !token_maps(&m_ash, &m_ashs, ash, (uint64_t)Is, (uint64_t)T + moe::kMaxTileRows, moe::kW2TileRows))
+        !token_maps(&m_ash, &m_ashs, ash, (uint64_t)Is, (uint64_t)T + moe::kMaxTileRows, box2))
       return MOE_ERR_CUDA;
     moe::GemmArgs s13{};
     s13.K = H;
-    s13.n_feat_tiles = Is / moe::kTileFeat;
+    s13.n_feat_tiles = spair13 ? Is / moe::kPairTileRows : Is / moe::kTileFeat;
     s13.w_rows_per_e = H;
     s13.up_col = Is;
     s13.identity_T = T;
     s13.out = ash;
     s13.out_ld = Is;
     s13.status = status;
-    moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + moe::kW13TileRows - 1) / moe::kW13TileRows, sms, s);
+    s13.pair = spair13 ? 1 : 0;
+    moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + srows13 - 1) / srows13, sms, s);
     moe::GemmArgs s2 = s13;
     s2.K = Is;
-    s2.n_feat_tiles = H / moe::kTileFeat;
+    s2.n_feat_tiles = pair2 ? H / moe::kPairTileRows : H / moe::kTileFeat;
     s2.w_rows_per_e = Is;
     s2.up_col = 0;
     s2.out = y_shared;
     s2.out_ld = H;
+    s2.pair = pair2 ? 1 : 0;
     moe::launch_w2_gemm(m_w2s, m_ash, m_ashs, s2, (T + moe::kW2TileRows - 1) / moe::kW2TileRows, sms, s);
   }
   return last_cuda();
