@@ -365,14 +365,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ CTA pairs
-// The same GEMM on pairs of CTAs (a cluster of two, one per SM) whose tensor
-// cores run one cta_group::2 MMA of M = 256 features x N = 256 token rows:
-// each CTA loads its own 128 features of the weights (gate and up for W13)
-// and half of the token tile (128 rows), and its TMEM receives its 128
-// features for all 256 rows.  Per SM this halves the token bytes per flop,
-// the operand traffic that bounds the one-CTA kernel.  One shape for every
-// tile and every batch, K from 0 to the end: the arithmetic of a token's row
-// does not depend on the batch or on which half of the tile holds it.
+// The same GEMMs on pairs of CTAs (a cluster of two, one per SM) whose tensor
+// cores run one cta_group::2 MMA of M = 256 rows x N = 256 token rows: each
+// CTA loads its own 128 rows of the weight tile and half of the token tile
+// (128 rows), and its TMEM receives its 128 rows of the result for all 256
+// tokens.  Per SM this halves the token bytes per flop, the operand traffic
+// that bounds the one-CTA kernel, and keeps both accumulators of a CTA
+// (2 x 256 TMEM columns) so that the epilogue of one tile overlaps the MMAs
+// of the next.
+//   W2 : a CTA's 128 rows are 128 output features (a pair tile: 256).
+//   W13: a CTA's 128 rows are 64 gate features followed by the same 64 up
+//        features (a pair tile: 128 features).  TMEM lanes 0..63 hold g,
+//        lanes 64..127 u; the epilogue warps of lane quarters 2 and 3 pass u
+//        through shared memory to the warps of quarters 0 and 1, which store
+//        a = silu(g) * u.
+// One shape for every tile and every batch, K from 0 to the end: the
+// arithmetic of a token's row does not depend on the batch or on which half
+// of the tile holds it.
 //
 // Synchronisation: the even CTA's producer expects the bytes of both CTAs on
 // its full barrier, and both CTAs' TMA loads complete there; the even CTA's
@@ -381,22 +390,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 // wait is bounded, and both CTAs of a pair follow the same control flow up to
 // the final cluster barrier.
 constexpr int kPairRows = 256;      // token rows per pair tile (the MMA's N)
-constexpr int kPairFeat = 256;      // features per pair tile (the MMA's M)
+constexpr int kPairM = 256;         // weight rows per pair (the MMA's M)
 
 template <bool kW13>
 struct PairCfg {
   static constexpr int kRowsCta = kPairRows / 2;
-  static constexpr uint32_t kABytes = kW13 ? 4 * kBoxBytes : 2 * kBoxBytes;
+  static constexpr int kFeatCta = kW13 ? 64 : 128;           // output features per CTA
+  static constexpr int kFeatTile = 2 * kFeatCta;             // output features per pair tile
+  static constexpr uint32_t kABytes = 2 * kBoxBytes;         // 128 weight rows x 64 K
   static constexpr uint32_t kBTileBytes = kRowsCta * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
   static constexpr int kStages = (int)(kStageBudget / kStageBytes) < 6 ? (int)(kStageBudget / kStageBytes) : 6;
-  static constexpr uint32_t kAccCols = kW13 ? 2 * kPairRows : kPairRows;
-  static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;
+  static constexpr uint32_t kAccCols = kPairRows;
+  static constexpr int kNumAcc = 2;
   static constexpr uint32_t kTmemCols = 512;
+  // W13: u handed from the up warps to the gate warps, 4 warp pairs x 2
+  // buffers x 32 lanes x 16 fp32
+  static constexpr uint32_t kXchgBytes = kW13 ? 4 * 2 * 32 * 16 * 4 : 0;
   static constexpr uint32_t kBarBytes = 256;
-  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
-  static constexpr uint32_t kIdesc = idesc_bf16(kPairFeat, kPairRows, true, false);
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kXchgBytes + kBarBytes + 1024;
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairM, kPairRows, true, false);
 };
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 template <bool kW13>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -411,14 +429,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();            // 0: issues the MMAs
   const bool lead = rank == 0;
   const int num_tiles = args.identity_T ? (args.identity_T + kPairRows - 1) / kPairRows : *args.num_tiles;
-  const int nfe = args.n_feat_tiles;                  // pair feature tiles of 256
+  const int nfe = args.n_feat_tiles;                  // pair feature tiles (C::kFeatTile features)
   const int pair0 = (int)(blockIdx.x >> 1);
   const int pairs = (int)(gridDim.x >> 1);
   const int total = num_tiles * nfe;
   if (pair0 >= total) return;  // the same verdict in both CTAs of the pair
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kXchgBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * C::kStages;
   const uint32_t tfull0 = empty0 + 8 * C::kStages;
@@ -468,8 +487,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
       const int wrow0 = t.expert * args.w_rows_per_e;
-      const int fcol = wk.f * kPairFeat + (int)rank * kTileFeat;     // this CTA's 128 features
-      const int brow0 = t.row0 + (int)rank * C::kRowsCta;             // this CTA's half of the rows
+      const int fcol = wk.f * C::kFeatTile + (int)rank * C::kFeatCta;   // this CTA's features
+      const int brow0 = t.row0 + (int)rank * C::kRowsCta;                // this CTA's half of the rows
       const bool small = t.rows <= kSmallRows;
       const int b_rows = small ? kSmallRows : C::kRowsCta;
       const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
@@ -487,13 +506,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int k0 = ks * kBK;
         if (lane == 0) {
           if (lead) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * cta_tx);
+          // rows 0..63 and 64..127 of this CTA's weight tile: two 64-wide boxes
+          const int c_hi = kW13 ? args.up_col + fcol : fcol + 64;
           tma_load_2d_pair(smem_u32(sA), &w_map, fcol, wrow0 + k0, fb, pol_w);
-          tma_load_2d_pair(smem_u32(sA + kBoxBytes), &w_map, fcol + 64, wrow0 + k0, fb, pol_w);
-          if (kW13) {
-            tma_load_2d_pair(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
-            tma_load_2d_pair(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb,
-                             pol_w);
-          }
+          tma_load_2d_pair(smem_u32(sA + kBoxBytes), &w_map, c_hi, wrow0 + k0, fb, pol_w);
           tma_load_2d_pair(smem_u32(sB), small ? &x_map_small : &x_map, k0, brow0, fb, pol_x);
         }
         __syncwarp();
@@ -557,12 +573,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
             const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
-            const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16_pair(d0, adesc, bdesc, C::kIdesc, accum);
-            if (kW13) {
-              const uint64_t adesc_up = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
-              mma_bf16_pair(d0 + kPairRows, adesc_up, bdesc, C::kIdesc, accum);
-            }
+            mma_bf16_pair(d0, adesc, bdesc, C::kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == C::kStages) {
@@ -588,11 +599,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int quarter = warp & 3;
-    const int feat_local = quarter * 32 + lane;
-    const int col0 = ((warp - 2) / 4) * (kPairRows / 2), col1 = col0 + kPairRows / 2;
+    const int quarter = warp & 3;                       // TMEM lanes this warp may access
+    const int half = (warp - 2) / 4;                    // its half of the 256 columns
+    const int col0 = half * (kPairRows / 2), col1 = col0 + kPairRows / 2;
+    // W13: quarters 0,1 hold g (features 0..63 of the CTA), quarters 2,3 hold u
+    const bool up_warp = kW13 && quarter >= 2;
+    const int xpair = (quarter & 1) + 2 * half;         // W13: the (gate, up) warp pair
+    float* xbuf = xchg + (size_t)xpair * 2 * 32 * 16;   // two buffers of 32 lanes x 16
     int acc = 0;
     uint32_t acc_phase = 0;
+    int chunk = 0;                                      // W13: exchange buffer parity
     for (int item = pair0; item < total; item += pairs) {
       const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
@@ -608,31 +624,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
-      const int feat = wk.f * kPairFeat + (int)rank * kTileFeat + feat_local;
+      const int feat = wk.f * C::kFeatTile + (int)rank * C::kFeatCta + (kW13 ? (quarter & 1) * 32 : quarter * 32) + lane;
       for (int c = col0; c < col1 && c < t.rows; c += 16) {
-        float g[16];
-        tmem_ld16(tbase + c, g);
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_wait_ld();
         if (kW13) {
-          float u[16];
-          tmem_ld16(tbase + kPairRows + c, u);
-          tmem_wait_ld();
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+          float* buf = xbuf + (chunk & 1) * (32 * 16) + lane * 16;
+          if (up_warp) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = c + jj;
-            if (j < t.rows) {
-              const float x = g[jj];
-              const float v = (x / (1.0f + expf(-x))) * u[jj];
-              out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v);
+            for (int jj = 0; jj < 16; ++jj) buf[jj] = v[jj];
+            named_bar_sync(1 + xpair, 64);
+          } else {
+            named_bar_sync(1 + xpair, 64);
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = c + jj;
+              if (j < t.rows) {
+                // sentinel rows have x = 0, hence g = u = 0 and a = 0
+                const float x = v[jj];
+                const float a = (x / (1.0f + expf(-x))) * buf[jj];
+                out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(a);
+              }
             }
           }
+          ++chunk;
         } else {
-          tmem_wait_ld();
           float* out = reinterpret_cast<float*>(args.out);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c + jj;
-            if (j < t.rows) out[(size_t)(t.row0 + j) * args.out_ld + feat] = g[jj];
+            if (j < t.rows) out[(size_t)(t.row0 + j) * args.out_ld + feat] = v[jj];
           }
         }
       }
@@ -733,7 +756,9 @@ bool gemm_smem_ok() {
          optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes;
 }
 
-bool gemm_pair_ok(int features) { return features % kPairFeat == 0; }
+bool gemm_pair_ok(bool w13, int features) {
+  return features % (w13 ? PairCfg<true>::kFeatTile : PairCfg<false>::kFeatTile) == 0;
+}
 
 void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                      const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {

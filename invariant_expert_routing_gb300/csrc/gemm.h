@@ -48,16 +48,19 @@ struct GemmArgs {
   int out_ld;          // elements per output row
   int* status;
   int concurrent;      // work units resident at once (set by the launcher)
-  int pair;            // 1: CTA-pair kernel (256 features x 256 token rows per tile,
-                       //    n_feat_tiles in units of 256, token maps with 128-row boxes)
+  int pair;            // 1: CTA-pair kernel (256 token rows per tile, token maps with
+                       //    128-row boxes; n_feat_tiles in units of kPairFeatW13 / kPairFeatW2)
 };
 
-// Rows of a CTA-pair token tile and the token box each CTA of the pair loads.
+// Rows of a CTA-pair token tile, the token box each CTA of the pair loads,
+// and the output features of one pair tile.
 constexpr int kPairTileRows = 256;
 constexpr int kPairBoxRows = 128;
-// The pair kernel covers layers whose output features are a multiple of 256;
-// which kernel a GEMM uses depends on the layer's shape only, never on T.
-bool gemm_pair_ok(int features);
+constexpr int kPairFeatW13 = 128;
+constexpr int kPairFeatW2 = 256;
+// Whether the pair kernel covers a GEMM with this many output features: a
+// property of the layer's shape, never of T.
+bool gemm_pair_ok(bool w13, int features);
 
 bool gemm_smem_ok();
 // x_small: the same token tensor with a 32-row box (tiles with <= 32 rows)

@@ -344,7 +344,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   // CTA-pair kernels where the output features are a multiple of 256 (a
   // property of the layer, the same for every T); they take the 256-row tile
   // list and load 128-row token boxes per CTA
-  const bool pair13 = moe::gemm_pair_ok(I), pair2 = moe::gemm_pair_ok(H);
+  const bool pair13 = moe::gemm_pair_ok(true, I), pair2 = moe::gemm_pair_ok(false, H);
   const int box13 = pair13 ? moe::kPairBoxRows : moe::kW13TileRows;
   const int box2 = pair2 ? moe::kPairBoxRows : moe::kW2TileRows;
   CUtensorMap m_w13, m_x, m_xs, m_w2, m_a, m_as;
@@ -356,7 +356,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
 
   moe::GemmArgs g13{};
   g13.K = H;
-  g13.n_feat_tiles = pair13 ? I / moe::kPairTileRows : I / moe::kTileFeat;
+  g13.n_feat_tiles = pair13 ? I / moe::kPairFeatW13 : I / moe::kTileFeat;
   g13.w_rows_per_e = H;
   g13.up_col = I;
   g13.tiles = pair13 ? tiles2 : tiles13;
@@ -371,7 +371,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
 
   moe::GemmArgs g2 = g13;
   g2.K = I;
-  g2.n_feat_tiles = pair2 ? H / moe::kPairTileRows : H / moe::kTileFeat;
+  g2.n_feat_tiles = pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat;
   g2.w_rows_per_e = I;
   g2.up_col = 0;
   g2.tiles = tiles2;
@@ -385,7 +385,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   const int Is = c->shared_intermediate;
   if (Is > 0) {
     uint16_t* ash = at<uint16_t>(ws, L.a_sh);
-    const bool spair13 = moe::gemm_pair_ok(Is);
+    const bool spair13 = moe::gemm_pair_ok(true, Is);
     const int sbox13 = spair13 ? moe::kPairBoxRows : moe::kW13TileRows;
     const int srows13 = spair13 ? moe::kPairTileRows : moe::kW13TileRows;
     CUtensorMap m_w13s, m_w2s, m_ash, m_ashs, m_h, m_hs;
@@ -397,7 +397,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
       return MOE_ERR_CUDA;
     moe::GemmArgs s13{};
     s13.K = H;
-    s13.n_feat_tiles = spair13 ? Is / moe::kPairTileRows : Is / moe::kTileFeat;
+    s13.n_feat_tiles = spair13 ? Is / moe::kPairFeatW13 : Is / moe::kTileFeat;
     s13.w_rows_per_e = H;
     s13.up_col = Is;
     s13.identity_T = T;
@@ -408,7 +408,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
     moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + srows13 - 1) / srows13, sms, s);
     moe::GemmArgs s2 = s13;
     s2.K = Is;
-    s2.n_feat_tiles = pair2 ? H / moe::kPairTileRows : H / moe::kTileFeat;
+    s2.n_feat_tiles = pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat;
     s2.w_rows_per_e = Is;
     s2.up_col = 0;
     s2.out = y_shared;
