@@ -630,10 +630,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld16(tbase + c, v);
         tmem_wait_ld();
         if (kW13) {
-          float* buf = xbuf + (chunk & 1) * (32 * 16) + lane * 16;
+          // [column][lane] order: the 32 lanes touch 32 consecutive words
+          float* buf = xbuf + (chunk & 1) * (32 * 16) + lane;
           if (up_warp) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) buf[jj] = v[jj];
+            for (int jj = 0; jj < 16; ++jj) buf[jj * 32] = v[jj];
             named_bar_sync(1 + xpair, 64);
           } else {
             named_bar_sync(1 + xpair, 64);
@@ -644,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (j < t.rows) {
                 // sentinel rows have x = 0, hence g = u = 0 and a = 0
                 const float x = v[jj];
-                const float a = (x / (1.0f + expf(-x))) * buf[jj];
+                const float a = (x / (1.0f + expf(-x))) * buf[jj * 32];
                 out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(a);
               }
             }
