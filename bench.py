@@ -489,7 +489,7 @@ def run_gpu(args):
                                "frac_of_bf16_peak": layer_tf / peak_tf, "gbs": layer_gb,
                                "frac_of_hbm": layer_gb / peak_gb},
             "stage_ms": {n: float(v) for n, v in zip(names, stage_ms)},
-            "gpu_launches": moe.moe_forward_launch_count(cfg) * K,
+            "gpu_launches": moe.moe_forward_launch_count(cfg, T) * K,
             "clocks": clocks.summary(t_wall0, t_wall1)}
 
     # ---- routing diagnostics on this batch: the routing_stats probe and the

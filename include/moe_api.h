@@ -343,8 +343,9 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
                              const uint16_t* w2_shared, uint16_t* out, void* ws, size_t ws_bytes,
                              void* const* events, int32_t n_events, void* stream);
 
-/* Number of kernel launches one moe_forward makes for this configuration. */
-int32_t moe_forward_launch_count(const moe_config* cfg);
+/* Number of kernel launches one moe_forward of T tokens makes for this
+ * configuration (a batch of at most 16 tokens is routed in one launch). */
+int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T);
 
 /* moe_dispatch_align for callers that cannot allocate device memory (for
  * example a serving loop whose memory is fixed at start-up, or code running

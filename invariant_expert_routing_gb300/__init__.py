@@ -74,7 +74,7 @@ _SIGS = {
     "moe_forward": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_forward_hostio": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_forward_timed": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp, _i32, _vp], ctypes.c_int),
-    "moe_forward_launch_count": ([_cfgp], _i32),
+    "moe_forward_launch_count": ([_cfgp, _i32], _i32),
     "moe_router_cert_beta": ([_i32], ctypes.c_float),
     "moe_route_filtered": ([_cfgp, _i32] + [_vp] * 6 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_router_tc_logits": ([_cfgp, _i32] + [_vp] * 3 + [_vp, _sz, _vp], ctypes.c_int),
@@ -297,8 +297,8 @@ def moe_router_tc_logits(cfg, h, w_gate, logits_out, ws, stream=None):
         _stream(stream)))
 
 
-def moe_forward_launch_count(cfg) -> int:
-    return int(_lib.moe_forward_launch_count(ctypes.byref(_cfg(cfg))))
+def moe_forward_launch_count(cfg, T: int) -> int:
+    return int(_lib.moe_forward_launch_count(ctypes.byref(_cfg(cfg)), T))
 
 
 def moe_get_device_status(ws, stream=None) -> int:

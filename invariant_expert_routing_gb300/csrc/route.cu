@@ -173,22 +173,19 @@ __device__ __forceinline__ void write_slots_and_gates(int (&sel)[16], float (&se
   }
 }
 
-// One warp per token: k rounds of a warp-shuffle tournament over the N
-// logits, slots sorted by expert index, gates = softmax over the selected.
-__global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict__ logits,
-                                                         int32_t* __restrict__ topk_idx,
-                                                         float* __restrict__ gates, int T, int N,
-                                                         int k) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
+// One warp: k rounds of a warp-shuffle tournament over the N logits of one
+// token (lrow, global or shared memory), slots sorted by expert index, gates
+// = softmax over the selected.
+__device__ __forceinline__ void topk_select_warp(const float* lrow, int N, int k, int lane,
+                                                 int32_t* __restrict__ idx_out,
+                                                 float* __restrict__ gate_out) {
   float v[8];
   uint32_t used = 0;
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const int e = lane + 32 * s;
     if (e < N) {
-      v[s] = logits[(size_t)t * N + e];
+      v[s] = lrow[e];
     } else {
       v[s] = 0.0f;
       used |= 1u << s;
@@ -219,7 +216,63 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
     selv[j] = bv;
     if ((bi & 31) == lane) used |= 1u << (bi >> 5);
   }
-  write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
+  write_slots_and_gates(sel, selv, k, idx_out, gate_out, lane);
+}
+
+// One warp per token.
+__global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict__ logits,
+                                                         int32_t* __restrict__ topk_idx,
+                                                         float* __restrict__ gates, int T, int N,
+                                                         int k) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_select_warp(logits + (size_t)t * N, N, k, lane, topk_idx + (size_t)t * k, gates + (size_t)t * k);
+}
+
+// Router for a few tokens (decode): one CTA per token does the whole route.
+// Thread (e, c) runs the in-order fma chain of chunk c for expert e (the
+// chains are independent, so a token's N x chunks chains run in parallel
+// instead of a tile of tokens sharing each weight load); the chunk sums of
+// each expert are added in ascending chunk order, then the bias, exactly as
+// in router_logits_kernel; warp 0 then selects the top-k with the same
+// tournament and gate code as topk_gates_kernel.  Same bits as the tiled
+// router for every token.
+constexpr int kSmallRouterThreads = 512;
+
+__global__ void __launch_bounds__(kSmallRouterThreads) router_small_kernel(
+    const uint16_t* __restrict__ h, const uint16_t* __restrict__ wg, const float* __restrict__ bias,
+    float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ gates, int H, int N,
+    int k) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  const int t = blockIdx.x;
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+  float* hs = reinterpret_cast<float*>(rsm);                 // [H] the token row, widened
+  float* part = hs + H;                                      // [chunks][N] chunk sums
+  float* lrow = part + (size_t)chunks * N;                   // [N] logits
+  const uint16_t* hrow = h + (size_t)t * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) hs[i] = __uint_as_float((uint32_t)hrow[i] << 16);
+  __syncthreads();
+  for (int item = threadIdx.x; item < chunks * N; item += blockDim.x) {
+    const int e = item % N, c = item / N;
+    const int i0 = c * kRouterChunk, i1 = min(H, i0 + kRouterChunk);
+    const uint16_t* wcol = wg + e;
+    float p = 0.0f;
+#pragma unroll 8
+    for (int i = i0; i < i1; ++i) p = fmaf(hs[i], __uint_as_float((uint32_t)__ldg(wcol + (size_t)i * N) << 16), p);
+    part[(size_t)c * N + e] = p;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    float total = 0.0f;
+    for (int c = 0; c < chunks; ++c) total = total + part[(size_t)c * N + e];
+    if (bias) total = total + bias[e];
+    lrow[e] = total;
+    if (logits) logits[(size_t)t * N + e] = total;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32)
+    topk_select_warp(lrow, N, k, threadIdx.x, topk_idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
 
@@ -493,6 +546,22 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
                             int32_t* topk_idx, float* gates, int32_t* n_cand, cudaStream_t s) {
   route_certified_kernel<<<(T + kCertWarps - 1) / kCertWarps, kCertWarps * 32, 0, s>>>(
       logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
+}
+
+bool router_small_ok(int T, int H) { return T <= kSmallRouterMaxT && H <= 8192; }
+
+void launch_router_small(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
+                         int32_t* topk_idx, float* gates, int T, int H, int N, int k, cudaStream_t s) {
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+  const size_t smem = sizeof(float) * ((size_t)H + (size_t)chunks * N + N);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  router_small_kernel<<<T, kSmallRouterThreads, smem, s>>>(h, w_gate, bias, logits, topk_idx, gates, H, N, k);
 }
 
 void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,

@@ -145,11 +145,17 @@ def test_expert_choice_capacity_and_bounds_match_the_oracle(moe):
 def test_launch_counts(moe):
     mix = dict(hidden=4096, num_experts=8, top_k=2, intermediate=14336, block_size=64)
     qw = dict(hidden=2048, num_experts=128, top_k=8, intermediate=768, block_size=16)
-    assert moe.moe_forward_launch_count(mix) == 2 + 3 + 6
-    assert moe.moe_forward_launch_count(qw) == 4 + 3 + 6
-    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1)) == 11 + 6
-    assert moe.moe_forward_launch_count(dict(qw, routing=1)) == 3 + 6
-    assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128)) == 2 + 3 + 6 + 2
+    T = 4096
+    assert moe.moe_forward_launch_count(mix, T) == 2 + 3 + 6
+    assert moe.moe_forward_launch_count(qw, T) == 4 + 3 + 6
+    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 6
+    assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 3 + 6
+    assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 6 + 2
+    # up to 16 tokens are routed in one launch, whatever the router path
+    assert moe.moe_forward_launch_count(mix, 1) == 1 + 3 + 6
+    assert moe.moe_forward_launch_count(qw, 16) == 1 + 3 + 6
+    assert moe.moe_forward_launch_count(qw, 17) == 4 + 3 + 6
+    assert moe.moe_forward_launch_count(mix, 0) == 0
 
 
 def test_drop_only_dispatch_refuses_reroute_and_expert_choice(moe):
