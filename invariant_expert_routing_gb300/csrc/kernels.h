@@ -21,7 +21,7 @@ void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int
 // a few tokens (decode): logits (optional), top-k and gates in one launch,
 // the same bits as launch_router_logits + launch_topk_gates
 constexpr int kSmallRouterMaxT = 16;
-bool router_small_ok(int T, int H);
+bool router_small_ok(int T, int H, int N);
 void launch_router_small(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
                          int32_t* topk_idx, float* gates, int T, int H, int N, int k, cudaStream_t s);
 // tensor-core router with a certified candidate filter (N % 128 == 0)

@@ -253,12 +253,15 @@ moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const u
                       const float* bias, int32_t* idx, float* gates, float* logits, bool canonical_logits,
                       void* ws, cudaStream_t s, int32_t* n_cand = nullptr) {
   const int H = c->hidden, N = c->num_experts, k = c->top_k;
-  if (moe::router_small_ok(T, H) && !n_cand) {
+  if (moe::router_small_ok(T, H, N) && !n_cand) {
     // a few tokens: one launch, the same bits as either path below
     moe::launch_router_small(h, wg, bias, canonical_logits ? logits : nullptr, idx, gates, T, H, N, k, s);
     return last_cuda();
   }
-  if (!canonical_logits && use_tc_router(c) && moe::gemm_smem_ok()) {
+  // the certified tensor-core path pays off on batches; a few tokens route
+  // faster on the CUDA cores (same bits either way)
+  if (!canonical_logits && use_tc_router(c) && moe::gemm_smem_ok() &&
+      (T > moe::kSmallRouterMaxT || n_cand)) {
     const Layout L = layout_of(c, T);
     uint16_t* wgT = at<uint16_t>(ws, L.wgT);
     float* norm_w = at<float>(ws, L.norm_w);
@@ -784,14 +787,14 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   // deferred acceptance, check, sequential fallback (returns at once unless
   // the check failed), count, scan, scatter = 9 after the CUDA-core router.
   // Expert choice: logits, scores, selection = 3 in all.
-  const int router = moe::router_small_ok(T, cfg->hidden) ? 1 : 2;   // small batches: one launch
+  const bool small = moe::router_small_ok(T, cfg->hidden, cfg->num_experts);   // one launch
   int front = 0;
   if (expert_choice(cfg)) {
     front = 3;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
-    front = router + 9;
+    front = (small ? 1 : 2) + 9;
   } else {
-    front = (moe::router_small_ok(T, cfg->hidden) ? 1 : (use_tc_router(cfg) ? 4 : 2)) + 3;
+    front = (small ? 1 : (use_tc_router(cfg) && T > moe::kSmallRouterMaxT ? 4 : 2)) + 3;
   }
   return front + 2 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }

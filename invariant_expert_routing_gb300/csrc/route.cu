@@ -548,7 +548,12 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
       logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
 }
 
-bool router_small_ok(int T, int H) { return T <= kSmallRouterMaxT && H <= 8192; }
+// One CTA per token reads all of W_g: worth it while W_g is small (a 64 K
+// element router such as H 4096 x N 16); larger routers keep the tiled or
+// certified paths, whose CTAs share the weight reads.
+bool router_small_ok(int T, int H, int N) {
+  return T <= kSmallRouterMaxT && H <= 8192 && (long long)H * N <= 65536;
+}
 
 void launch_router_small(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
                          int32_t* topk_idx, float* gates, int T, int H, int N, int k, cudaStream_t s) {

@@ -151,9 +151,11 @@ def test_launch_counts(moe):
     assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 6
     assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 3 + 6
     assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 6 + 2
-    # up to 16 tokens are routed in one launch, whatever the router path
+    # up to 16 tokens are routed in one launch when W_g is small
     assert moe.moe_forward_launch_count(mix, 1) == 1 + 3 + 6
-    assert moe.moe_forward_launch_count(qw, 16) == 1 + 3 + 6
+    assert moe.moe_forward_launch_count(mix, 16) == 1 + 3 + 6
+    assert moe.moe_forward_launch_count(mix, 17) == 2 + 3 + 6
+    assert moe.moe_forward_launch_count(qw, 1) == 2 + 3 + 6
     assert moe.moe_forward_launch_count(qw, 17) == 4 + 3 + 6
     assert moe.moe_forward_launch_count(mix, 0) == 0
 
