@@ -235,6 +235,146 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
 }
 
+// Dispatch, alignment and both GEMM tile lists of a batch of at most 1024
+// routes in one CTA (decode): the same integers as dispatch_count, _scan,
+// _scatter and build_tiles (ranks by warp match, per-warp counts added in
+// warp order, segment and tile offsets by ordered scans), in one launch.
+constexpr int kSmallDispatchMaxR = 1024;
+
+// Exclusive scan of v over experts 0..N-1 by warp 0 (N <= 256, 8 per lane);
+// out[e] = sum of v[0..e-1], returns the total (to lane 0..31).
+__device__ int warp_scan_experts(const int* v, int* out, int N, int lane) {
+  int loc[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * 8 + i;
+    loc[i] = e < N ? v[e] : 0;
+    sum += loc[i];
+  }
+  int incl = sum;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * 8 + i;
+    if (e < N) out[e] = run;
+    run += loc[i];
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+__global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
+    const int32_t* __restrict__ topk_idx, int R, int N, int B, int capacity,
+    uint8_t* __restrict__ route_kept, int32_t* __restrict__ route_pos,
+    int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
+    int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts,
+    int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
+    int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
+    int max_b, int* status) {
+  __shared__ int wc[32][kMaxN + 1];
+  __shared__ int kept_s[kMaxN], pad_s[kMaxN], drop_s[kMaxN], nta[kMaxN], ntb[kMaxN];
+  __shared__ int seg[kMaxN], offa[kMaxN], offb[kMaxN];
+  __shared__ int s_rows, s_drop, s_ta, s_tb;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 32 * (kMaxN + 1); i += blockDim.x) (&wc[0][0])[i] = 0;
+  __syncthreads();
+  const int r = tid;
+  const int e = (r < R) ? topk_idx[r] : -1;
+  const bool valid = (r < R) && e >= 0 && e < N;
+  if (r < R && !valid) atomicOr(status, kDevErrExpertRange);
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank == 0) wc[w][e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < N; x += blockDim.x) {
+    int run = 0;
+    for (int ww = 0; ww < 32; ++ww) {
+      const int c = wc[ww][x];
+      wc[ww][x] = run;
+      run += c;
+    }
+    const int kept = capacity < 0 ? run : min(run, capacity);
+    const int padded = (kept + B - 1) / B * B;
+    kept_s[x] = kept;
+    pad_s[x] = padded;
+    drop_s[x] = run - kept;
+    nta[x] = (padded + rows_a - 1) / rows_a;
+    ntb[x] = (padded + rows_b - 1) / rows_b;
+    expert_counts[x] = kept;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int rows = warp_scan_experts(pad_s, seg, N, lane);
+    const int ta = warp_scan_experts(nta, offa, N, lane);
+    const int tb = warp_scan_experts(ntb, offb, N, lane);
+    int dsum = 0;
+    for (int x = lane; x < N; x += 32) dsum += drop_s[x];
+    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    if (lane == 0) {
+      s_rows = rows;
+      s_drop = dsum;
+      s_ta = ta;
+      s_tb = tb;
+    }
+  }
+  __syncthreads();
+  if (r < R) {
+    if (valid) {
+      const int rk = wc[w][e] + rank;
+      const bool kept = capacity < 0 || rk < capacity;
+      route_kept[r] = kept ? 1 : 0;
+      if (kept) {
+        route_pos[r] = seg[e] + rk;
+        sorted_route_ids[seg[e] + rk] = r;
+      } else {
+        route_pos[r] = -1;
+      }
+    } else {
+      route_kept[r] = 0;
+      route_pos[r] = -1;
+    }
+  }
+  for (int x = tid; x < N; x += blockDim.x) {
+    for (int j = kept_s[x]; j < pad_s[x]; ++j) sorted_route_ids[seg[x] + j] = R;
+    for (int b = seg[x] / B; b < (seg[x] + pad_s[x]) / B; ++b) block_expert[b] = x;
+    for (int j = 0; j < nta[x]; ++j) {
+      const int idx = offa[x] + j;
+      if (idx < max_a) {
+        GemmTile tl;
+        tl.expert = x;
+        tl.row0 = seg[x] + j * rows_a;
+        tl.rows = min(rows_a, pad_s[x] - j * rows_a);
+        tl.first = offa[x];
+        tl.count = nta[x];
+        tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+        tiles_a[idx] = tl;
+      }
+    }
+    for (int j = 0; j < ntb[x]; ++j) {
+      const int idx = offb[x] + j;
+      if (idx < max_b) {
+        GemmTile tl;
+        tl.expert = x;
+        tl.row0 = seg[x] + j * rows_b;
+        tl.rows = min(rows_b, pad_s[x] - j * rows_b);
+        tl.first = offb[x];
+        tl.count = ntb[x];
+        tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+        tiles_b[idx] = tl;
+      }
+    }
+  }
+  if (tid == 0) {
+    *num_padded = s_rows;
+    *num_dropped = s_drop;
+    *ntiles_a = min(s_ta, max_a);
+    *ntiles_b = min(s_tb, max_b);
+  }
+}
+
 }  // namespace
 
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
@@ -297,6 +437,18 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
                  route_expert, num_dropped, num_rerouted, s);
   launch_dispatch_routes(route_expert, R, N, B, route_kept, route_pos, sorted_route_ids, block_expert,
                          num_padded, expert_counts, rank_in_tile, tile_count, seg_off, status, s);
+}
+
+bool dispatch_small_ok(long long R) { return R <= kSmallDispatchMaxR; }
+
+void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* route_kept,
+                           int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
+                           int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
+                           GemmTile* tiles_a, int32_t* ntiles_a, int rows_a, int max_a, GemmTile* tiles_b,
+                           int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s) {
+  dispatch_small_kernel<<<1, kSmallDispatchMaxR, 0, s>>>(
+      topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert, num_padded,
+      expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, status);
 }
 
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,

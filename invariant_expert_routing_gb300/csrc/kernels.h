@@ -77,6 +77,14 @@ void launch_expert_choice(const float* logits, int T, int N, int C, int B, unsig
                           float* gates, uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                           int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                           cudaStream_t s);
+// a batch of at most 1024 routes: launch_dispatch + both launch_build_tiles
+// (tile_rows rows_a and rows_b) in one launch, the same integers
+bool dispatch_small_ok(long long R);
+void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* route_kept,
+                           int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
+                           int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
+                           GemmTile* tiles_a, int32_t* ntiles_a, int rows_a, int max_a, GemmTile* tiles_b,
+                           int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s);
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,

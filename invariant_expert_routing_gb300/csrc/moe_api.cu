@@ -320,13 +320,13 @@ struct Marks;
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
-                    void* ws, cudaStream_t s, const Marks* mk = nullptr);
+                    void* ws, cudaStream_t s, const Marks* mk = nullptr, bool tiles_ready = false);
 void mark(const Marks* mk, int i);
 
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
-                    void* ws, cudaStream_t s, const Marks* mk) {
+                    void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready) {
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = slots_of(c);
   const int64_t rows = max_rows_of(c, T);
@@ -342,10 +342,12 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* a = at<uint16_t>(ws, L.a);
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
-  moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW13TileRows, tiles13, ntiles13,
-                          max_tiles13, status, s);
-  moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW2TileRows, tiles2, ntiles2,
-                          max_tiles2, status, s);
+  if (!tiles_ready) {   // else the small-batch dispatch built both lists
+    moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW13TileRows, tiles13, ntiles13,
+                            max_tiles13, status, s);
+    moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW2TileRows, tiles2, ntiles2,
+                            max_tiles2, status, s);
+  }
   moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
   mark(mk, 3);
 
@@ -458,6 +460,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   float* logits = at<float>(ws, L.logits);
   int32_t* counts = at<int32_t>(ws, L.counts);
   moe_status st = MOE_OK;
+  bool tiles_ready = false;
   mk.at(0);
   if (expert_choice(c)) {
     // every logit in the canonical order, then each expert takes its tokens
@@ -475,12 +478,25 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
     st = route_impl(c, T, h, wg, bias, idx, gates, logits, false, ws, s);
     if (st != MOE_OK) return st;
     mk.at(1);
-    st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
-                       ws, s);
+    if (moe::dispatch_small_ok((long long)T * c->top_k)) {
+      // a few routes: dispatch, alignment and both tile lists in one launch
+      moe::launch_dispatch_small(idx, T * c->top_k, c->num_experts, c->block_size, capacity_of(c, T), kept, pos,
+                                 sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
+                                 at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles),
+                                 moe::kW13TileRows, (int)max_gemm_tiles_of(c, T, moe::kW13TileRows),
+                                 at<GemmTile>(ws, L.gemm_tiles2), at<int32_t>(ws, L.num_gemm_tiles2),
+                                 moe::kW2TileRows, (int)max_gemm_tiles_of(c, T, moe::kW2TileRows),
+                                 at<int>(ws, L.status), s);
+      tiles_ready = true;
+      st = last_cuda();
+    } else {
+      st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
+                         ws, s);
+    }
   }
   if (st != MOE_OK) return st;
   mk.at(2);
-  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk);
+  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk, tiles_ready);
   if (st != MOE_OK) return st;
   mk.at(6);
   moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, slots_of(c), max_rows_of(c, T), s);
@@ -781,18 +797,23 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
   if (T == 0) return 0;
   // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
-  // combine 1 (+ shared W13, W2).  Router: CUDA cores logits + top-k = 2,
-  // tensor cores transpose, norms, GEMM, certified select = 4.  Dispatch:
-  // count, scan, scatter = 3; with reroute count, scan, preference lists,
-  // deferred acceptance, check, sequential fallback (returns at once unless
-  // the check failed), count, scan, scatter = 9 after the CUDA-core router.
-  // Expert choice: logits, scores, selection = 3 in all.
+  // combine 1 (+ shared W13, W2).  Router: one launch for at most 16 tokens
+  // with a small W_g, else CUDA cores logits + top-k = 2, or for more than 16
+  // tokens on the tensor cores transpose, norms, GEMM, certified select = 4.
+  // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
+  // launch that also builds both tile lists; with reroute count, scan,
+  // preference lists, deferred acceptance, check, sequential fallback
+  // (returns at once unless the check failed), count, scan, scatter = 9
+  // after the CUDA-core router.  Expert choice: logits, scores, selection = 3.
   const bool small = moe::router_small_ok(T, cfg->hidden, cfg->num_experts);   // one launch
   int front = 0;
   if (expert_choice(cfg)) {
     front = 3;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = (small ? 1 : 2) + 9;
+  } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {
+    // dispatch and both tile lists in one launch
+    front = (small ? 1 : (use_tc_router(cfg) && T > moe::kSmallRouterMaxT ? 4 : 2)) + 1 - 2;
   } else {
     front = (small ? 1 : (use_tc_router(cfg) && T > moe::kSmallRouterMaxT ? 4 : 2)) + 3;
   }

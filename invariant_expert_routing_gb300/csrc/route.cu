@@ -230,14 +230,15 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
   topk_select_warp(logits + (size_t)t * N, N, k, lane, topk_idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
-// Router for a few tokens (decode): one CTA per token does the whole route.
-// Thread (e, c) runs the in-order fma chain of chunk c for expert e (the
-// chains are independent, so a token's N x chunks chains run in parallel
-// instead of a tile of tokens sharing each weight load); the chunk sums of
-// each expert are added in ascending chunk order, then the bias, exactly as
-// in router_logits_kernel; warp 0 then selects the top-k with the same
-// tournament and gate code as topk_gates_kernel.  Same bits as the tiled
-// router for every token.
+// Router for a few tokens (decode) of a small router matrix: one CTA per
+// token does the whole route.  The CTA copies W_g (at most 64 K elements) and
+// the token row into shared memory with 16-byte loads, then thread (e, c)
+// runs the in-order fma chain of chunk c for expert e from shared memory (a
+// token's N x chunks chains run in parallel instead of a tile of tokens
+// sharing each weight load); the chunk sums of each expert are added in
+// ascending chunk order, then the bias, exactly as in router_logits_kernel;
+// warp 0 then selects the top-k with the same tournament and gate code as
+// topk_gates_kernel.  Same bits as the tiled router for every token.
 constexpr int kSmallRouterThreads = 512;
 
 __global__ void __launch_bounds__(kSmallRouterThreads) router_small_kernel(
@@ -247,19 +248,23 @@ __global__ void __launch_bounds__(kSmallRouterThreads) router_small_kernel(
   extern __shared__ __align__(16) uint8_t rsm[];
   const int t = blockIdx.x;
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  float* hs = reinterpret_cast<float*>(rsm);                 // [H] the token row, widened
-  float* part = hs + H;                                      // [chunks][N] chunk sums
-  float* lrow = part + (size_t)chunks * N;                   // [N] logits
+  uint16_t* ws = reinterpret_cast<uint16_t*>(rsm);                          // [H][N] W_g
+  float* hs = reinterpret_cast<float*>(rsm + (((size_t)H * N * 2 + 15) & ~(size_t)15));  // [H] token row
+  float* part = hs + H;                                                     // [chunks][N] chunk sums
+  float* lrow = part + (size_t)chunks * N;                                  // [N] logits
+  const size_t wvec = (size_t)H * N / 8;                                    // H % 128 == 0: whole uint4s
+  const uint4* wsrc = reinterpret_cast<const uint4*>(wg);
+  uint4* wdst = reinterpret_cast<uint4*>(ws);
+  for (size_t i = threadIdx.x; i < wvec; i += blockDim.x) wdst[i] = __ldg(wsrc + i);
   const uint16_t* hrow = h + (size_t)t * H;
   for (int i = threadIdx.x; i < H; i += blockDim.x) hs[i] = __uint_as_float((uint32_t)hrow[i] << 16);
   __syncthreads();
   for (int item = threadIdx.x; item < chunks * N; item += blockDim.x) {
     const int e = item % N, c = item / N;
     const int i0 = c * kRouterChunk, i1 = min(H, i0 + kRouterChunk);
-    const uint16_t* wcol = wg + e;
     float p = 0.0f;
 #pragma unroll 8
-    for (int i = i0; i < i1; ++i) p = fmaf(hs[i], __uint_as_float((uint32_t)__ldg(wcol + (size_t)i * N) << 16), p);
+    for (int i = i0; i < i1; ++i) p = fmaf(hs[i], __uint_as_float((uint32_t)ws[(size_t)i * N + e] << 16), p);
     part[(size_t)c * N + e] = p;
   }
   __syncthreads();
@@ -558,12 +563,13 @@ bool router_small_ok(int T, int H, int N) {
 void launch_router_small(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
                          int32_t* topk_idx, float* gates, int T, int H, int N, int k, cudaStream_t s) {
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const size_t smem = sizeof(float) * ((size_t)H + (size_t)chunks * N + N);
+  const size_t smem = (((size_t)H * N * 2 + 15) & ~(size_t)15) +
+                      sizeof(float) * ((size_t)H + (size_t)chunks * N + N);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   router_small_kernel<<<T, kSmallRouterThreads, smem, s>>>(h, w_gate, bias, logits, topk_idx, gates, H, N, k);
