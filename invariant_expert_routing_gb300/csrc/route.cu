@@ -446,36 +446,27 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
     for (int qb = g; active && qb < nq; qb += 4 * G) {
       int ce[4];
       float acc[4];
-      const uint4* wp[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int q = qb + u * G;
         ce[u] = (q < nq) ? sm.cidx[wib][q0 + q] : -1;
         acc[u] = 0.0f;
-        // a missing candidate reads candidate 0's row and its sum is dropped:
-        // the loop has no branches, so the loads of later steps can be issued early
-        wp[u] = reinterpret_cast<const uint4*>(wgT + (size_t)(ce[u] >= 0 ? ce[u] : ce[0]) * H + i0);
       }
-      const uint4* hp = reinterpret_cast<const uint4*>(hrow + i0);
       // 16 elements (two full 32-byte sectors) per step; chunk lengths are
       // multiples of 128
-#pragma unroll 2
       for (int i = 0; i < len; i += 16) {
-        const uint4 hv0 = __ldg(hp + i / 8), hv1 = __ldg(hp + i / 8 + 1);
-        uint4 wv[4][2];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wv[u][0] = __ldg(wp[u] + i / 8);
-          wv[u][1] = __ldg(wp[u] + i / 8 + 1);
-        }
+        const uint4 hv0 = __ldg(reinterpret_cast<const uint4*>(hrow + i0 + i));
+        const uint4 hv1 = __ldg(reinterpret_cast<const uint4*>(hrow + i0 + i + 8));
         const uint32_t hw[8] = {hv0.x, hv0.y, hv0.z, hv0.w, hv1.x, hv1.y, hv1.z, hv1.w};
         float hx[16];
 #pragma unroll
         for (int ii = 0; ii < 16; ++ii) hx[ii] = (ii & 1) ? bf16_hi(hw[ii >> 1]) : bf16_lo(hw[ii >> 1]);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t ww[8] = {wv[u][0].x, wv[u][0].y, wv[u][0].z, wv[u][0].w,
-                                  wv[u][1].x, wv[u][1].y, wv[u][1].z, wv[u][1].w};
+          if (ce[u] < 0) continue;
+          const uint4* wp = reinterpret_cast<const uint4*>(wgT + (size_t)ce[u] * H + i0 + i);
+          const uint4 wv0 = __ldg(wp), wv1 = __ldg(wp + 1);
+          const uint32_t ww[8] = {wv0.x, wv0.y, wv0.z, wv0.w, wv1.x, wv1.y, wv1.z, wv1.w};
 #pragma unroll
           for (int ii = 0; ii < 16; ++ii) {
             const float wx = (ii & 1) ? bf16_hi(ww[ii >> 1]) : bf16_lo(ww[ii >> 1]);
