@@ -411,14 +411,23 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
   // l_tc < V - 2 delta is out.  (N >= 128 here: every lane holds experts.)
   float V = 0.0f;
   {
-    int rank = 0;  // lanes whose best ranks before mine
-    for (int o = 0; o < 32; ++o) {
-      const float ov = __shfl_sync(full, lane_best, o);
-      const int oe = __shfl_sync(full, lane_best_e, o);
-      rank += (oe >= 0 && ranks_before(ov, oe, lane_best, lane_best_e)) ? 1 : 0;
+    // k rounds of a warp tournament over the lane bests; the k-th winner is V
+    bool out = false;
+    for (int j = 0; j < k; ++j) {
+      float bv = out ? 0.0f : lane_best;
+      int bi = out ? -1 : lane_best_e;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(full, bv, off);
+        const int oi = __shfl_xor_sync(full, bi, off);
+        if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      V = bv;
+      if (bi == lane_best_e) out = true;
     }
-    const unsigned who = __ballot_sync(full, rank == k - 1);
-    V = __shfl_sync(full, lane_best, __ffs(who) - 1);
   }
   const float cut = V - 2.0f * delta;
   int nc = 0;
@@ -488,24 +497,39 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
     }
     __syncwarp();
   }
-  // top-k among the candidates: each candidate's rank = number of candidates
-  // that beat it; ranks 0..k-1 are selected
+  // top-k among the candidates: k rounds of a warp tournament (the same
+  // ranking; candidates past the first 32 per lane are folded in by a loop)
   int sel[16];
   float selv[16];
-  for (int q = lane; q < nc; q += 32) {
-    const int e = sm.cidx[wib][q];
-    const float cv = sm.cval[wib][q];
-    int rank = 0;
-    for (int o = 0; o < nc; ++o) rank += ranks_before(sm.cval[wib][o], sm.cidx[wib][o], cv, e) ? 1 : 0;
-    if (rank < k) {
-      sm.part[wib][rank] = cv;                 // reuse the partials buffer for the winners
-      reinterpret_cast<int*>(sm.part[wib])[kCertPass * 32 - 16 + rank] = e;
-    }
-  }
-  __syncwarp();
+  uint32_t taken = 0;   // bit s: candidate lane + 32 s already selected (nc <= 256)
   for (int j = 0; j < k; ++j) {
-    selv[j] = sm.part[wib][j];
-    sel[j] = reinterpret_cast<const int*>(sm.part[wib])[kCertPass * 32 - 16 + j];
+    float bv = 0.0f;
+    int bi = -1, bs = -1;
+    for (int q = lane, sl = 0; q < nc; q += 32, ++sl) {
+      if ((taken >> sl) & 1u) continue;
+      const int e = sm.cidx[wib][q];
+      const float cv = sm.cval[wib][q];
+      if (bi < 0 || ranks_before(cv, e, bv, bi)) {
+        bv = cv;
+        bi = e;
+        bs = sl;
+      }
+    }
+    int bq = bs >= 0 ? lane + 32 * bs : -1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(full, bv, off);
+      const int oi = __shfl_xor_sync(full, bi, off);
+      const int oq = __shfl_xor_sync(full, bq, off);
+      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+        bq = oq;
+      }
+    }
+    sel[j] = bi;
+    selv[j] = bv;
+    if (bq >= 0 && (bq & 31) == lane) taken |= 1u << (bq >> 5);
   }
   write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
   if (n_cand && lane == 0) n_cand[t] = nc;
