@@ -400,7 +400,10 @@ struct PairCfg {
   static constexpr uint32_t kABytes = 2 * kBoxBytes;         // 128 weight rows x 64 K
   static constexpr uint32_t kBTileBytes = kRowsCta * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
-  static constexpr int kStages = (int)(kStageBudget / kStageBytes) < 6 ? (int)(kStageBudget / kStageBytes) : 6;
+  // W2 fits a seventh 32 KB stage in the 227 KB of shared memory; W13 needs
+  // 16 KB for the u exchange
+  static constexpr uint32_t kPairBudget = kW13 ? kStageBudget : 224 * 1024;
+  static constexpr int kStages = (int)(kPairBudget / kStageBytes) < 7 ? (int)(kPairBudget / kStageBytes) : 7;
   static constexpr uint32_t kAccCols = kPairRows;
   static constexpr int kNumAcc = 2;
   static constexpr uint32_t kTmemCols = 512;
