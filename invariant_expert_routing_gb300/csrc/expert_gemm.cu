@@ -760,8 +760,11 @@ bool gemm_smem_ok() {
          optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes;
 }
 
-bool gemm_pair_ok(bool w13, int features) {
-  return features % (w13 ? PairCfg<true>::kFeatTile : PairCfg<false>::kFeatTile) == 0;
+bool gemm_pair_ok(bool w13, int features, int K) {
+  if (features % (w13 ? PairCfg<true>::kFeatTile : PairCfg<false>::kFeatTile) != 0) return false;
+  // W13 pairs carry half the features per CTA of the one-CTA kernel: with a
+  // short reduction (K < 4096) the one-CTA kernel measured faster
+  return !w13 || K >= 4096;
 }
 
 void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,

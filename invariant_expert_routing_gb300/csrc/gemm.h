@@ -58,9 +58,9 @@ constexpr int kPairTileRows = 256;
 constexpr int kPairBoxRows = 128;
 constexpr int kPairFeatW13 = 128;
 constexpr int kPairFeatW2 = 256;
-// Whether the pair kernel covers a GEMM with this many output features: a
-// property of the layer's shape, never of T.
-bool gemm_pair_ok(bool w13, int features);
+// Whether a GEMM with this many output features and reduction length K runs
+// on CTA pairs: a property of the layer's shape, never of T.
+bool gemm_pair_ok(bool w13, int features, int K);
 
 bool gemm_smem_ok();
 // x_small: the same token tensor with a 32-row box (tiles with <= 32 rows)

@@ -354,7 +354,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   // CTA-pair kernels where the output features are a multiple of 256 (a
   // property of the layer, the same for every T); they take the 256-row tile
   // list and load 128-row token boxes per CTA
-  const bool pair13 = moe::gemm_pair_ok(true, I), pair2 = moe::gemm_pair_ok(false, H);
+  const bool pair13 = moe::gemm_pair_ok(true, I, H), pair2 = moe::gemm_pair_ok(false, H, I);
   const int box13 = pair13 ? moe::kPairBoxRows : moe::kW13TileRows;
   const int box2 = pair2 ? moe::kPairBoxRows : moe::kW2TileRows;
   CUtensorMap m_w13, m_x, m_xs, m_w2, m_a, m_as;
@@ -395,7 +395,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   const int Is = c->shared_intermediate;
   if (Is > 0) {
     uint16_t* ash = at<uint16_t>(ws, L.a_sh);
-    const bool spair13 = moe::gemm_pair_ok(true, Is);
+    const bool spair13 = moe::gemm_pair_ok(true, Is, H);
     const int sbox13 = spair13 ? moe::kPairBoxRows : moe::kW13TileRows;
     const int srows13 = spair13 ? moe::kPairTileRows : moe::kW13TileRows;
     CUtensorMap m_w13s, m_w2s, m_ash, m_ashs, m_h, m_hs;
