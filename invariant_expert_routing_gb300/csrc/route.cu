@@ -26,22 +26,23 @@ constexpr int kRouterWarps = 8;
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// CTA tile: TT = 4*G tokens x NE = 2*P experts (NE <= 32).  Lane l of a warp
-// owns the expert pair p = l % P and the token quad g = l / P (P*G = 32).
+// CTA tile: TT = TQ*G tokens x NE = 2*P experts (NE <= 32).  Lane l of a warp
+// owns the expert pair p = l % P and the token group g = l / P (P*G = 32) of
+// TQ tokens.
 // Warp w sums chunks w, w+8, ...: it first copies the chunk's W_g slice
 // [256 x NE] and the TT token rows [TT x 256] into its shared-memory stage with
 // one burst of independent loads, then runs the in-order fma chains from
 // shared memory.  After each round of 8 chunks the partial sums are added, in
 // ascending chunk order, to running totals held by the threads that own each
 // (token, expert).
-template <bool kEvenN>
+template <bool kEvenN, int TQ>
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ h,
                                                             const uint16_t* __restrict__ wg,
                                                             const float* __restrict__ bias,
                                                             float* __restrict__ logits, int T, int H,
                                                             int N, int P, int G) {
   extern __shared__ __align__(16) uint8_t rsm[];
-  const int NE = 2 * P, TT = 4 * G;
+  const int NE = 2 * P, TT = TQ * G;
   const int t0 = blockIdx.x * TT, e0 = blockIdx.y * NE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = lane % P, g = lane / P;
@@ -80,19 +81,19 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
                                  : make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
-      float acc[4][2];
+      float acc[TQ][2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.0f;
+      for (int q = 0; q < TQ; ++q) acc[q][0] = acc[q][1] = 0.0f;
       for (int i = 0; i < len; i += 8) {
-        uint4 hv[4];
+        uint4 hv[TQ];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) hv[q] = sh[(4 * g + q) * 32 + i / 8];
+        for (int q = 0; q < TQ; ++q) hv[q] = sh[(TQ * g + q) * 32 + i / 8];
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii) {
           const uint32_t w2 = sw[(i + ii) * P + p];
           const float wa = bf16_lo(w2), wb = bf16_hi(w2);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < TQ; ++q) {
             const uint32_t word = (ii < 2) ? hv[q].x : (ii < 4) ? hv[q].y : (ii < 6) ? hv[q].z : hv[q].w;
             const float hx = (ii & 1) ? bf16_hi(word) : bf16_lo(word);
             acc[q][0] = fmaf(hx, wa, acc[q][0]);
@@ -101,8 +102,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float* dst = part + (size_t)warp * slot + (size_t)(4 * g + q) * NE + 2 * p;
+      for (int q = 0; q < TQ; ++q) {
+        float* dst = part + (size_t)warp * slot + (size_t)(TQ * g + q) * NE + 2 * p;
         dst[0] = acc[q][0];
         dst[1] = acc[q][1];
       }
@@ -539,21 +540,29 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
 
 void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
                           int T, int H, int N, cudaStream_t s) {
-  // NE experts per CTA (power of two, 8..32), P = NE/2 pairs, G = 32/P token
-  // quads: the tile shape depends on N only, never on T.
+  // NE experts per CTA (power of two, 8..16), P = NE/2 pairs, G = 32/P token
+  // groups of two: about 100 KB of shared memory, two CTAs per SM.  Any tile
+  // shape gives the same bits (each logit's order is fixed by its own chunks).
+  constexpr int TQ = 2;
   int NE = 8;
-  while (NE < N && NE < 32) NE *= 2;
-  const int P = NE / 2, G = 32 / P, TT = 4 * G;
+  while (NE < N && NE < 16) NE *= 2;
+  const int P = NE / 2, G = 32 / P, TT = TQ * G;
   const size_t stage = (size_t)kRouterChunk * NE * 2 + (size_t)TT * kRouterChunk * 2;
   const size_t smem = kRouterWarps * stage + (size_t)kRouterWarps * TT * NE * sizeof(float);
   dim3 grid((T + TT - 1) / TT, (N + NE - 1) / NE);
-  if (N % 2 == 0) {
-    cudaFuncSetAttribute(router_logits_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    router_logits_kernel<true><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
-  } else {
-    cudaFuncSetAttribute(router_logits_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    router_logits_kernel<false><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
+  static bool attr_set[64][2] = {{false}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int even = N % 2 == 0 ? 1 : 0;
+  if (dev < 0 || dev >= 64 || !attr_set[dev][even]) {
+    cudaFuncSetAttribute(even ? router_logits_kernel<true, TQ> : router_logits_kernel<false, TQ>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    if (dev >= 0 && dev < 64) attr_set[dev][even] = true;
   }
+  if (even)
+    router_logits_kernel<true, TQ><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
+  else
+    router_logits_kernel<false, TQ><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
 }
 
 void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
