@@ -356,3 +356,87 @@ def test_reroute_sequential_path_is_bit_exact():
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
                        text=True, timeout=900)
     assert r.returncode == 0 and "sequential ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def _nan_logits(rng, T, N, ties=True):
+    l = (rng.standard_normal((T, N)) - 1.2 * np.log(np.arange(N) + 1.0)).astype(np.float32)
+    if ties:
+        l[::5] = np.round(l[::5])          # exact ties inside a token
+        l[7] = l[3]                        # two identical tokens
+    l[2, 1] = np.nan
+    l[9, :] = np.nan                       # a token of NaN logits
+    l[11, 0] = -np.inf
+    return l
+
+
+@pytest.mark.parametrize("T,N,k,cf", [(200, 8, 2, 0.7), (300, 32, 4, 0.8), (129, 256, 8, 1.0)])
+def test_reroute_with_nan_and_tied_logits(T, N, k, cf):
+    # crafted logits (NaN, -inf, exact ties) fed straight to the reroute
+    # dispatch: NaN ranks last, ties go to the lower index, on both sides
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev
+    rng = np.random.default_rng(T + N)
+    l = _nan_logits(rng, T, N)
+    idx, _ = oracle.select_topk(l, k)
+    cfg = dict(hidden=128, num_experts=N, top_k=k, intermediate=128, block_size=8,
+               capacity_factor=cf, overflow_policy=1)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    got = _reroute_on_gpu(moe, cfg, dev(idx), dev(l), ws)
+    assert moe.moe_get_device_status(ws) == 0
+    re, nr, d = _ref_reroute(l, idx, N, 8, oracle.capacity(T, N, k, cf))
+    check_equal("route_expert", got["route_expert"], re)
+    assert got["num_rerouted"] == nr and nr > 0
+    check_dispatch(got, d)
+    del torch
+
+
+@pytest.mark.parametrize("T,N,cf", [(100, 8, 1.0), (257, 64, 0.5), (40, 256, 2.0)])
+def test_expert_choice_with_nan_and_tied_logits(T, N, cf):
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev
+    rng = np.random.default_rng(T * N)
+    l = _nan_logits(rng, T, N)
+    cfg = dict(hidden=128, num_experts=N, top_k=2, intermediate=128, block_size=8,
+               capacity_factor=cf, routing=1)
+    ws = moe.workspace(cfg, T)
+    got = _ec_on_gpu(moe, cfg, dev(l), ws)
+    C = oracle.ec_capacity(T, N, 2, cf)
+    sel, probs = oracle.expert_choice(l, C)
+    re = np.where(sel.reshape(-1) == 1, np.tile(np.arange(N), T), -1).astype(np.int32)
+    check_dispatch(got, oracle.dispatch_routes(re, N, 8, N))
+    ok = ~np.isnan(probs.reshape(-1))
+    check_gates(got["gates"][ok], probs.reshape(-1)[ok])
+    assert np.isnan(got["gates"][~ok]).all()
+    del torch
+
+
+def test_timed_and_host_buffer_forwards_give_the_same_bits():
+    # moe_forward_timed and moe_forward_hostio run the same launches as
+    # moe_forward: identical outputs, bit for bit
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16, host_bf16
+    c = case("mix")
+    T = 640
+    h = W.make_h(c.wl, T, seed=27)
+    h_d = dev_bf16(h)
+    ws = moe.workspace(c.cfg, T)
+    out = torch.empty((T, c.wl.hidden), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(c.cfg, h_d, c.wg_d, c.bias_d, c.w13_d, c.w2_d, None, None, out, ws)
+    ref = host_bf16(out)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    for e in ev:
+        e.record()
+    out2 = torch.empty_like(out)
+    moe.moe_forward_timed(c.cfg, h_d, c.wg_d, c.bias_d, c.w13_d, c.w2_d, None, None, out2, ws, ev)
+    h_host = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((T, c.wl.hidden), dtype=torch.bfloat16).pin_memory()
+    moe.moe_forward_hostio(c.cfg, h_host, c.wg_d, c.bias_d, c.w13_d, c.w2_d, None, None, out_host, ws)
+    torch.cuda.synchronize()
+    assert (host_bf16(out2) == ref).all()
+    assert (host_bf16(out_host) == ref).all()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(7)]
+    assert all(t >= 0 for t in times) and times[3] > 0      # the W13 stage took time
