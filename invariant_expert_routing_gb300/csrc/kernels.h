@@ -40,18 +40,30 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
                      int32_t* seg_off, int* status, cudaStream_t s);
 // Scratch of the overflow reroute (R routes, N experts).
-constexpr int kRerouteListLen = 128;  // cached best experts per overflowing route
+constexpr int kRerouteListLen = 128;  // cached best experts per token with an overflowing slot
+// ints of one buffer of the per-round exchange of the grid-wide reroute
+// rounds with G CTAs: 16-bit counts [N + 2][G rounded up to 8] (candidates
+// per expert, then unplaceable and listed routes), and the exclusive prefix
+// of the candidate counts over experts [G][N].
+__host__ __device__ inline size_t reroute_exchange_ints(int G, int N) {
+  const size_t gs = (size_t)(G + 7) / 8 * 8;
+  return ((size_t)(N + 2) * gs / 2 + (size_t)G * N + 3) / 4 * 4;
+}
 struct RerouteScratch {
   int32_t* list;    // [R] overflowing route ids, ascending
   int32_t* hold;    // [R] per list position: expert held, -1 none, -2 none possible
   int32_t* cand;    // [R] per list position: this round's candidate
   int32_t* ptr;     // [R] per list position: next cached preference to try
   int32_t* first;   // [R] per list position: list position of the token's first overflowing slot
-  uint8_t* prefs;   // [R * kRerouteListLen] cached preferences, by route id
+  uint8_t* prefs;   // [T * kRerouteListLen] cached preferences, by token
   int32_t* acc;     // [N] overflowing routes each expert holds at the end
   int32_t* worst;   // [N] largest route id each expert holds (-1 none)
   int32_t* flag;    // [1] non-zero: recompute with the sequential kernel
   int32_t* count;   // [1] overflowing routes
+  // grid-wide version (many overflowing routes)
+  uint32_t* gsync;  // [4] barrier arrivals, generation, error
+  int32_t* lcount;  // [2][reroute_exchange_ints(CTAs, N)] per-CTA counts exchanged each round
+  int32_t* lrank;   // [2][R] per-CTA candidate route ids ordered by (expert, rank)
 };
 // phase two of the reroute: route_expert for every route (kept: its expert,
 // overflowing: its new expert or -1), num_dropped / num_rerouted

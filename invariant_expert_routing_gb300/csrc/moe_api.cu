@@ -92,7 +92,7 @@ struct Layout {
   size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
       num_padded, counts, dropped, route_expert, rerouted, rr_list, rr_hold, rr_cand, rr_ptr, rr_first,
       rr_prefs,
-      rr_acc, rr_worst, rr_flag, rr_count, ec_keys, gemm_tiles, num_gemm_tiles,
+      rr_acc, rr_worst, rr_flag, rr_count, rr_gsync, rr_lcount, rr_lrank, ec_keys, gemm_tiles, num_gemm_tiles,
       gemm_tiles2, num_gemm_tiles2, x_perm, a, y, a_sh, y_sh, h_stage, out_stage, total;
 };
 
@@ -131,11 +131,16 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.rr_cand = take(rr ? sizeof(int32_t) * R : 0);
   L.rr_ptr = take(rr ? sizeof(int32_t) * R : 0);
   L.rr_first = take(rr ? sizeof(int32_t) * R : 0);
-  L.rr_prefs = take(rr ? R * moe::kRerouteListLen : 0);
+  L.rr_prefs = take(rr ? (size_t)T * moe::kRerouteListLen : 0);
   L.rr_acc = take(sizeof(int32_t) * N);
   L.rr_worst = take(sizeof(int32_t) * N);
   L.rr_flag = take(sizeof(int32_t));
   L.rr_count = take(sizeof(int32_t));
+  // the grid-wide rounds use at most R / 1009 + 1 CTAs (chunks of >= 1009 routes)
+  const size_t rr_ctas = R / 1000 + 2;
+  L.rr_gsync = take(4 * sizeof(uint32_t));
+  L.rr_lcount = take(rr ? sizeof(int32_t) * 2 * moe::reroute_exchange_ints((int)rr_ctas, (int)N) : 0);
+  L.rr_lrank = take(rr ? sizeof(int32_t) * 2 * R : 0);
   L.ec_keys = take(expert_choice(c) ? sizeof(unsigned long long) * N * T : 0);
   // tile lists of the W13 (128-row) and W2 (256-row) GEMMs
   L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW13TileRows));
@@ -298,7 +303,8 @@ moe_status reroute_impl(const moe_config* c, int32_t T, const int32_t* idx, cons
                          at<int32_t>(ws, L.rr_ptr), at<int32_t>(ws, L.rr_first), at<uint8_t>(ws, L.rr_prefs),
                          at<int32_t>(ws, L.rr_acc),
                          at<int32_t>(ws, L.rr_worst), at<int32_t>(ws, L.rr_flag),
-                         at<int32_t>(ws, L.rr_count)};
+                         at<int32_t>(ws, L.rr_count), at<uint32_t>(ws, L.rr_gsync),
+                         at<int32_t>(ws, L.rr_lcount), at<int32_t>(ws, L.rr_lrank)};
   moe::launch_dispatch_reroute(idx, logits, T, c->num_experts, c->top_k, c->block_size, capacity_of(c, T),
                                kept, route_expert, pos, sorted, blocks, num_padded, counts, dropped,
                                rerouted, at<int32_t>(ws, L.rank), at<int32_t>(ws, L.tile_count),

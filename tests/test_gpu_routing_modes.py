@@ -340,22 +340,42 @@ def test_expert_choice_ties_go_to_the_lowest_token():
     del host
 
 
-def test_reroute_sequential_path_is_bit_exact():
-    # the sequential kernel (the fallback of the deferred-acceptance pass) on
-    # its own: a process with MOE_REROUTE_SEQUENTIAL=1 runs only it
+_FORCED_PATHS = {
+    # the sequential kernel (the fallback of the deferred-acceptance rounds) alone
+    "sequential": ({"MOE_REROUTE_SEQUENTIAL": "1"},
+                   "[('tiny', 61, 0.75), ('cap', 2000, 0.8), ('qw', 777, 0.6)]", ""),
+    # the grid-wide rounds on small batches (one list tile, ragged tails)
+    "grid": ({"MOE_REROUTE_GRID": "1"},
+             "[('tiny', 61, 0.75), ('tiny', 1, 0.5), ('cap', 2000, 0.8), ('qw', 777, 0.6), ('ds', 200, 1.0)]",
+             "for a in [(200, 8, 2, 0.7), (300, 32, 4, 0.8), (129, 256, 8, 1.0)]:\n"
+             "    m.test_reroute_with_nan_and_tied_logits(*a)\n"),
+    # the grid-wide rounds with several 1024-route chunks per CTA
+    "grid_chunks": ({"MOE_REROUTE_GRID": "1", "MOE_REROUTE_GRID_CTAS": "12"},
+                    "[('qw', 777, 0.6), ('cap', 8192, 1.0), ('qw', 8192, 1.0)]", ""),
+    # the one-CTA rounds on batches that default to the grid
+    "cta": ({"MOE_REROUTE_GRID": "0"}, "[('cap', 8192, 1.0), ('qw', 8192, 1.0)]", ""),
+}
+
+
+@pytest.mark.parametrize("path", sorted(_FORCED_PATHS))
+def test_reroute_forced_path_is_bit_exact(path):
+    # each way of computing the reroute on its own, in a process whose
+    # environment selects it
     import os
     import subprocess
     import sys
+    env_add, cases, extra = _FORCED_PATHS[path]
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = ("import sys; sys.path.insert(0, %r)\n"
             "from tests import test_gpu_routing_modes as m\n"
-            "for case in [('tiny', 61, 0.75), ('cap', 2000, 0.8), ('qw', 777, 0.6)]:\n"
+            "for case in %s:\n"
             "    m.test_reroute_dispatch_is_bit_exact(*case)\n"
-            "print('sequential ok')\n") % root
-    env = dict(os.environ, MOE_REROUTE_SEQUENTIAL="1")
+            "%s"
+            "print('path ok')\n") % (root, cases, extra)
+    env = dict(os.environ, **env_add)
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
                        text=True, timeout=900)
-    assert r.returncode == 0 and "sequential ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+    assert r.returncode == 0 and "path ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
 
 
 def _nan_logits(rng, T, N, ties=True):
