@@ -8,8 +8,11 @@
 // S is the number of route slots per token: k for token choice, N for expert
 // choice (slot e = expert e).  The kept slots are first listed in ascending j
 // in shared memory; skipping the others leaves the chain of fmas unchanged.
-// One CTA per token row, 4 consecutive features per thread, 128-bit loads of
-// y_perm; the order of the sum is fixed and independent of T.
+// A token row is split over gridDim.y CTAs (more when there are few tokens,
+// so that a lone token's row is spread over several SMs), 4 consecutive
+// features per thread, 128-bit loads of y_perm issued eight slots at a time
+// before their fmas; the order of the sum is fixed and independent of T and
+// of the grid.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -56,16 +59,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     s_gate[before] = g;
   }
   __syncthreads();
-  for (int d = threadIdx.x * 4; d < H; d += blockDim.x * 4) {
+  for (int d = (blockIdx.y * blockDim.x + threadIdx.x) * 4; d < H; d += gridDim.y * blockDim.x * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n_used; ++i) {
-      const int pos = s_pos[i];
-      const float g = s_gate[i];
-      const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)pos * H + d));
-      acc.x = fmaf(g, y.x, acc.x);
-      acc.y = fmaf(g, y.y, acc.y);
-      acc.z = fmaf(g, y.z, acc.z);
-      acc.w = fmaf(g, y.w, acc.w);
+    for (int i0 = 0; i0 < n_used; i0 += 8) {
+      float4 y[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (i0 + q < n_used)
+          y[q] = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)s_pos[i0 + q] * H + d));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (i0 + q < n_used) {
+          const float g = s_gate[i0 + q];
+          acc.x = fmaf(g, y[q].x, acc.x);
+          acc.y = fmaf(g, y[q].y, acc.y);
+          acc.z = fmaf(g, y[q].z, acc.z);
+          acc.w = fmaf(g, y[q].w, acc.w);
+        }
+      }
     }
     if (y_shared) {
       const float4 ys = __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * H + d));
@@ -91,8 +102,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,
                     const int32_t* route_pos, const float* y_perm, const float* y_shared,
                     uint16_t* out, int T, int H, int k, int64_t max_rows, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
-                                   (long long)max_rows);
+  // enough CTAs for about two per SM, at most one per 1024 features of a row
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int per_row = (H + 1023) / 1024;
+  const int want = T > 0 ? (2 * (sms > 0 ? sms : 1) + T - 1) / T : 1;
+  const dim3 grid((unsigned)T, (unsigned)(want < per_row ? (want > 0 ? want : 1) : per_row));
+  combine_kernel<<<grid, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
+                                      (long long)max_rows);
 }
 
 }  // namespace moe

@@ -150,7 +150,9 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
 // into tiles of tile_rows rows from its start.  Rejects (no tiles, status
 // bit) a block list that is not sorted by expert or out of range.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
-                                                          const int32_t* __restrict__ num_padded, int N,
+                                                          const int32_t* __restrict__ num_padded,
+                                                          const int32_t* __restrict__ sorted_route_ids,
+                                                          int R, int N,
                                                           int B, long long max_rows, int tile_rows,
                                                           GemmTile* __restrict__ tiles,
                                                           int32_t* __restrict__ num_tiles, int max_tiles,
@@ -191,6 +193,13 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     last = lo;
   }
   const int rows = (last - first) * B;
+  // rows up to the segment's last route (the padding sentinels trail it)
+  int used = rows;
+  while (used > 0) {
+    const int r = sorted_route_ids[first * B + used - 1];
+    if (r >= 0 && r < R) break;
+    --used;
+  }
   const int nt = (rows + tile_rows - 1) / tile_rows;
   int total = 0;
   const int off = block_exclusive_scan(nt, buf, &total);
@@ -203,7 +212,8 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
       tl.rows = min(tile_rows, rows - j * tile_rows);
       tl.first = off;
       tl.count = nt;
-      tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+      tl.valid = max(0, min(tl.rows, used - j * tile_rows));
+      tl.pad[0] = tl.pad[1] = 0;
       tiles[idx] = tl;
     }
   }
@@ -349,7 +359,8 @@ __global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
         tl.rows = min(rows_a, pad_s[x] - j * rows_a);
         tl.first = offa[x];
         tl.count = nta[x];
-        tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+        tl.valid = max(0, min(tl.rows, kept_s[x] - j * rows_a));
+        tl.pad[0] = tl.pad[1] = 0;
         tiles_a[idx] = tl;
       }
     }
@@ -362,7 +373,8 @@ __global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
         tl.rows = min(rows_b, pad_s[x] - j * rows_b);
         tl.first = offb[x];
         tl.count = ntb[x];
-        tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+        tl.valid = max(0, min(tl.rows, kept_s[x] - j * rows_b));
+        tl.pad[0] = tl.pad[1] = 0;
         tiles_b[idx] = tl;
       }
     }
@@ -451,11 +463,12 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
       expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, status);
 }
 
-void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
-                        int64_t max_rows, int tile_rows, GemmTile* tiles, int32_t* num_tiles,
-                        int max_tiles, int* status, cudaStream_t s) {
-  build_tiles_kernel<<<1, 256, 0, s>>>(block_expert, num_padded, N, B, (long long)max_rows, tile_rows,
-                                       tiles, num_tiles, max_tiles, status);
+void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
+                        const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
+                        int tile_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles, int* status,
+                        cudaStream_t s) {
+  build_tiles_kernel<<<1, 256, 0, s>>>(block_expert, num_padded, sorted_route_ids, R, N, B,
+                                       (long long)max_rows, tile_rows, tiles, num_tiles, max_tiles, status);
 }
 
 }  // namespace moe

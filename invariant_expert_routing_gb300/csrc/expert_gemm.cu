@@ -37,7 +37,7 @@ constexpr int kBK = 64;                             // K per stage: one 128-byte
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // 64 K rows x 64 features of bf16
 constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter, one column half each
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr int kSmallRows = 32;                      // token box used when a tile has <= 32 rows
+constexpr int kSmallRows = 32;                      // token box when a tile has <= 32 routed rows
 constexpr uint32_t kStageBudget = 192 * 1024;       // shared memory for the operand stages
 
 constexpr uint32_t pow2_at_least(uint32_t x) {
@@ -61,10 +61,11 @@ struct GemmCfg {
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
   // M = 128 features, N = BN token rows; A (weights) MN-major, B (tokens) K-major.
   static constexpr uint32_t kIdesc = idesc_bf16(kTileFeat, BN, true, false);
+  static constexpr uint32_t kIdescSmall = idesc_bf16(kTileFeat, kSmallRows, true, false);
 };
 
 struct TileInfo {
-  int expert, row0, rows;
+  int expert, row0, rows, valid;
 };
 
 template <int BN>
@@ -74,11 +75,13 @@ __device__ __forceinline__ TileInfo tile_of(const GemmArgs& a, int ti) {
     t.expert = 0;
     t.row0 = ti * BN;
     t.rows = min(BN, a.identity_T - t.row0);
+    t.valid = t.rows;
   } else {
     const GemmTile g = a.tiles[ti];
     t.expert = g.expert;
     t.row0 = g.row0;
     t.rows = g.rows;
+    t.valid = g.valid;
   }
   return t;
 }
@@ -182,10 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int f = wk.f;
       const int wrow0 = t.expert * args.w_rows_per_e;
       const int fcol = f * kTileFeat;
-      // A tile with few rows (decode) loads a 32-row token box: the rows past
-      // it keep stale data, which only feeds MMA columns that are never
-      // stored (columns of an MMA are independent).
-      const bool small = t.rows <= kSmallRows;
+      // A tile with at most 32 rows holding routes (decode) loads a 32-row
+      // token box and runs N = 32 MMAs (columns of an MMA are independent:
+      // each token column's sum over K runs in the same order for any N).
+      const bool small = t.valid <= kSmallRows;
       const int b_rows = small ? kSmallRows : BN;
       const uint32_t stage_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
@@ -246,6 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int item = unit0; item < total && ok; item += units) {
+        const bool small = work_of<BN>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
+        const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
           ok = false;
           break;
@@ -268,10 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 1 KB apart (SBO); a K=16 step is 16 rows = 2 KB.
             const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
             const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16(d0, adesc, bdesc, C::kIdesc, accum);
+            mma_bf16(d0, adesc, bdesc, idesc, accum);
             if (kW13) {
               const uint64_t adesc_up = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
-              mma_bf16(d0 + BN, adesc_up, bdesc, C::kIdesc, accum);
+              mma_bf16(d0 + BN, adesc_up, bdesc, idesc, accum);
             }
           }
           mma_commit(empty0 + 8 * stage);
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
       const int feat = f * kTileFeat + feat_local;
-      for (int c = col0; c < col1 && c < t.rows; c += 16) {
+      for (int c = col0; c < col1 && c < t.valid; c += 16) {
         float g[16];
         tmem_ld16(tbase + c, g);
         if (kW13) {
@@ -332,8 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c + jj;
-            if (j < t.rows) {
-              // sentinel rows have x = 0, hence g = u = 0 and a = 0
+            if (j < t.valid) {   // padding rows are not stored: nothing reads them
               const float x = g[jj];
               const float v = (x / (1.0f + expf(-x))) * u[jj];
               out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v);
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c + jj;
-            if (j < t.rows) out[(size_t)(t.row0 + j) * args.out_ld + feat] = g[jj];
+            if (j < t.valid) out[(size_t)(t.row0 + j) * args.out_ld + feat] = g[jj];
           }
         }
       }
@@ -379,9 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 //        lanes 64..127 u; the epilogue warps of lane quarters 2 and 3 pass u
 //        through shared memory to the warps of quarters 0 and 1, which store
 //        a = silu(g) * u.
-// One shape for every tile and every batch, K from 0 to the end: the
-// arithmetic of a token's row does not depend on the batch or on which half
-// of the tile holds it.
+// One weight tile shape and one K order (from 0 to the end, 64 per stage, 16
+// per MMA) for every tile and every batch.  The MMA's N (token columns) is
+// 256, or 64 for a tile with at most 32 routed rows (decode): the columns of
+// an MMA are independent dot products over the same K steps, so a token row's
+// arithmetic does not depend on the batch, on N, or on which half of the
+// tile holds it (the GPU batch-invariance tests compare rows computed with
+// N = 64 against the same rows computed with N = 256, bit for bit).
 //
 // Synchronisation: the even CTA's producer expects the bytes of both CTAs on
 // its full barrier, and both CTAs' TMA loads complete there; the even CTA's
@@ -413,6 +421,9 @@ struct PairCfg {
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kXchgBytes + kBarBytes + 1024;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, kPairRows, true, false);
+  // tiles with at most kSmallRows routed rows: N = 2 x kSmallRows (each CTA
+  // supplies kSmallRows token rows)
+  static constexpr uint32_t kIdescSmall = idesc_bf16(kPairM, 2 * kSmallRows, true, false);
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
@@ -491,9 +502,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const TileInfo t = wk.t;
       const int wrow0 = t.expert * args.w_rows_per_e;
       const int fcol = wk.f * C::kFeatTile + (int)rank * C::kFeatCta;   // this CTA's features
-      const int brow0 = t.row0 + (int)rank * C::kRowsCta;                // this CTA's half of the rows
-      const bool small = t.rows <= kSmallRows;
+      // tiles with at most kSmallRows routed rows (decode): a kSmallRows-row
+      // token box per CTA and N = 2 kSmallRows MMAs; the odd CTA's rows are
+      // padding or beyond the tile, in columns that are never stored
+      const bool small = t.valid <= kSmallRows;
       const int b_rows = small ? kSmallRows : C::kRowsCta;
+      const int brow0 = t.row0 + (int)rank * b_rows;                     // this CTA's half of the rows
       const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
         int got = 1;
@@ -558,6 +572,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int item = pair0; item < total && ok; item += pairs) {
+        const bool small = work_of<kPairRows>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
+        const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
           ok = false;
           break;
@@ -576,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
             const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
-            mma_bf16_pair(d0, adesc, bdesc, C::kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_pair(d0, adesc, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == C::kStages) {
@@ -628,7 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
       const int feat = wk.f * C::kFeatTile + (int)rank * C::kFeatCta + (kW13 ? (quarter & 1) * 32 : quarter * 32) + lane;
-      for (int c = col0; c < col1 && c < t.rows; c += 16) {
+      for (int c = col0; c < col1 && c < t.valid; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
         tmem_wait_ld();
@@ -645,8 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int j = c + jj;
-              if (j < t.rows) {
-                // sentinel rows have x = 0, hence g = u = 0 and a = 0
+              if (j < t.valid) {   // padding rows are not stored: nothing reads them
                 const float x = v[jj];
                 const float a = (x / (1.0f + expf(-x))) * buf[jj * 32];
                 out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(a);
@@ -659,7 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c + jj;
-            if (j < t.rows) out[(size_t)(t.row0 + j) * args.out_ld + feat] = v[jj];
+            if (j < t.valid) out[(size_t)(t.row0 + j) * args.out_ld + feat] = v[jj];
           }
         }
       }

@@ -29,10 +29,11 @@ constexpr int kTileFeat = 128;
 struct GemmTile {
   int32_t expert;
   int32_t row0;   // first padded row of the tile
-  int32_t rows;   // valid rows (<= the tile size)
+  int32_t rows;   // padded rows of the expert's segment in this tile (<= the tile size)
   int32_t first;  // index of the first tile of this expert in the list
   int32_t count;  // tiles of this expert
-  int32_t pad[3];
+  int32_t valid;  // rows holding a route: rows [row0, row0 + valid) (<= rows); the rest is padding
+  int32_t pad[2];
 };
 
 // ---- grouped expert GEMMs (tcgen05)

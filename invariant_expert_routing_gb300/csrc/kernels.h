@@ -18,12 +18,16 @@ void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float
                           int T, int H, int N, cudaStream_t s);
 void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,
                        cudaStream_t s);
-// a few tokens (decode): logits (optional), top-k and gates in one launch,
-// the same bits as launch_router_logits + launch_topk_gates
-constexpr int kSmallRouterMaxT = 16;
-bool router_small_ok(int T, int H, int N);
-void launch_router_small(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
-                         int32_t* topk_idx, float* gates, int T, int H, int N, int k, cudaStream_t s);
+// a few tokens (decode): chunk sums in parallel over (chunk, 32 experts, 8
+// tokens), then logits (optional), top-k and gates (optional: topk_idx null
+// for logits alone); the same bits as launch_router_logits +
+// launch_topk_gates.  part: decode_router_part_floats floats.
+constexpr int kDecodeRouterMaxT = 64;
+bool decode_router_ok(int T);
+size_t decode_router_part_floats(int T, int H, int N);
+void launch_router_decode(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
+                          float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
+                          cudaStream_t s);
 // tensor-core router with a certified candidate filter (N % 128 == 0)
 void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
                       cudaStream_t s);
@@ -99,9 +103,13 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
                            int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s);
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
-void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded, int N, int B,
-                        int64_t max_rows, int tile_rows, GemmTile* tiles, int32_t* num_tiles,
-                        int max_tiles, int* status, cudaStream_t s);
+// Tile list of one GEMM: tile_rows-row tiles over each expert's padded
+// segment; a tile's valid rows end at the segment's last route (sorted ids
+// in [0, R)).
+void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
+                        const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
+                        int tile_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles, int* status,
+                        cudaStream_t s);
 
 // ---- diagnostics
 struct RoutingStats {  // same layout as moe_route_stats

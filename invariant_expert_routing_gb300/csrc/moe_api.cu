@@ -89,7 +89,7 @@ int64_t max_gemm_tiles_of(const moe_config* c, int32_t T, int tile_rows) {
 // ----------------------------------------------------------------- workspace
 // Regions, each 256-byte aligned; the status word is always at offset 0.
 struct Layout {
-  size_t status, logits, wgT, norm_w, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
+  size_t status, logits, wgT, norm_w, rpart, topk, gates, kept, pos, rank, tile_count, seg_off, sorted, blocks,
       num_padded, counts, dropped, route_expert, rerouted, rr_list, rr_hold, rr_cand, rr_ptr, rr_first,
       rr_prefs,
       rr_acc, rr_worst, rr_flag, rr_count, rr_gsync, rr_lcount, rr_lrank, ec_keys, gemm_tiles, num_gemm_tiles,
@@ -111,6 +111,7 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.logits = take(sizeof(float) * T * N);
   L.wgT = take(sizeof(uint16_t) * N * H);
   L.norm_w = take(sizeof(float) * N);
+  L.rpart = take(sizeof(float) * moe::decode_router_part_floats(T, (int)H, (int)N));
   L.topk = take(sizeof(int32_t) * R);
   L.gates = take(sizeof(float) * R);
   L.kept = take(R);
@@ -258,15 +259,16 @@ moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const u
                       const float* bias, int32_t* idx, float* gates, float* logits, bool canonical_logits,
                       void* ws, cudaStream_t s, int32_t* n_cand = nullptr) {
   const int H = c->hidden, N = c->num_experts, k = c->top_k;
-  if (moe::router_small_ok(T, H, N) && !n_cand) {
-    // a few tokens: one launch, the same bits as either path below
-    moe::launch_router_small(h, wg, bias, canonical_logits ? logits : nullptr, idx, gates, T, H, N, k, s);
+  if (moe::decode_router_ok(T) && !n_cand) {
+    // a few tokens: chunk sums spread over many CTAs, the same bits as either
+    // path below
+    const Layout L = layout_of(c, T);
+    moe::launch_router_decode(h, wg, bias, at<float>(ws, L.rpart), logits, idx, gates, T, H, N, k, s);
     return last_cuda();
   }
-  // the certified tensor-core path pays off on batches; a few tokens route
-  // faster on the CUDA cores (same bits either way)
-  if (!canonical_logits && use_tc_router(c) && moe::gemm_smem_ok() &&
-      (T > moe::kSmallRouterMaxT || n_cand)) {
+  // the certified tensor-core path pays off on batches (same bits as the
+  // CUDA-core path)
+  if (!canonical_logits && use_tc_router(c) && moe::gemm_smem_ok()) {
     const Layout L = layout_of(c, T);
     uint16_t* wgT = at<uint16_t>(ws, L.wgT);
     float* norm_w = at<float>(ws, L.norm_w);
@@ -326,13 +328,60 @@ struct Marks;
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
-                    void* ws, cudaStream_t s, const Marks* mk = nullptr, bool tiles_ready = false);
+                    void* ws, cudaStream_t s, const Marks* mk = nullptr, bool tiles_ready = false,
+                    bool skip_shared = false);
 void mark(const Marks* mk, int i);
+
+// The shared expert (identity mode over h; every token, no routing): W13 then
+// W2 into y_shared.  It depends on h alone, so the forward runs it on a
+// second stream alongside routing, dispatch and the routed GEMMs.
+moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13s,
+                           const uint16_t* w2s, float* y_shared, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(c, T);
+  const int H = c->hidden, Is = c->shared_intermediate;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  int* status = at<int>(ws, L.status);
+  const bool pair2 = moe::gemm_pair_ok(false, H, Is);
+  const int box2 = pair2 ? moe::kPairBoxRows : moe::kW2TileRows;
+  uint16_t* ash = at<uint16_t>(ws, L.a_sh);
+  const bool spair13 = moe::gemm_pair_ok(true, Is, H);
+  const int sbox13 = spair13 ? moe::kPairBoxRows : moe::kW13TileRows;
+  const int srows13 = spair13 ? moe::kPairTileRows : moe::kW13TileRows;
+  CUtensorMap m_w13s, m_w2s, m_ash, m_ashs, m_h, m_hs;
+  // the last tile of h may run past row T-1: TMA fills those rows with zeros
+  if (!token_maps(&m_h, &m_hs, h, (uint64_t)H, (uint64_t)T, sbox13) ||
+      !map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
+      !map_2d(&m_w2s, w2s, (uint64_t)H, (uint64_t)Is, 64, 64) ||
+      !token_maps(&m_ash, &m_ashs, ash, (uint64_t)Is, (uint64_t)T + moe::kMaxTileRows, box2))
+    return MOE_ERR_CUDA;
+  moe::GemmArgs s13{};
+  s13.K = H;
+  s13.n_feat_tiles = spair13 ? Is / moe::kPairFeatW13 : Is / moe::kTileFeat;
+  s13.w_rows_per_e = H;
+  s13.up_col = Is;
+  s13.identity_T = T;
+  s13.out = ash;
+  s13.out_ld = Is;
+  s13.status = status;
+  s13.pair = spair13 ? 1 : 0;
+  moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + srows13 - 1) / srows13, sms, s);
+  moe::GemmArgs s2 = s13;
+  s2.K = Is;
+  s2.n_feat_tiles = pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat;
+  s2.w_rows_per_e = Is;
+  s2.up_col = 0;
+  s2.out = y_shared;
+  s2.out_ld = H;
+  s2.pair = pair2 ? 1 : 0;
+  moe::launch_w2_gemm(m_w2s, m_ash, m_ashs, s2, (T + moe::kW2TileRows - 1) / moe::kW2TileRows, sms, s);
+  return last_cuda();
+}
 
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
-                    void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready) {
+                    void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready, bool skip_shared) {
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = slots_of(c);
   const int64_t rows = max_rows_of(c, T);
@@ -349,10 +398,10 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
   if (!tiles_ready) {   // else the small-batch dispatch built both lists
-    moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW13TileRows, tiles13, ntiles13,
-                            max_tiles13, status, s);
-    moe::launch_build_tiles(blocks, num_padded, N, c->block_size, rows, moe::kW2TileRows, tiles2, ntiles2,
-                            max_tiles2, status, s);
+    moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, moe::kW13TileRows,
+                            tiles13, ntiles13, max_tiles13, status, s);
+    moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, moe::kW2TileRows,
+                            tiles2, ntiles2, max_tiles2, status, s);
   }
   moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
   mark(mk, 3);
@@ -398,39 +447,9 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
-  const int Is = c->shared_intermediate;
-  if (Is > 0) {
-    uint16_t* ash = at<uint16_t>(ws, L.a_sh);
-    const bool spair13 = moe::gemm_pair_ok(true, Is, H);
-    const int sbox13 = spair13 ? moe::kPairBoxRows : moe::kW13TileRows;
-    const int srows13 = spair13 ? moe::kPairTileRows : moe::kW13TileRows;
-    CUtensorMap m_w13s, m_w2s, m_ash, m_ashs, m_h, m_hs;
-    // the last tile of h may run past row T-1: TMA fills those rows with zeros
-    if (!token_maps(&m_h, &m_hs, h, (uint64_t)H, (uint64_t)T, sbox13) ||
-        !map_2d(&m_w13s, w13s, 2ull * Is, (uint64_t)H, 64, 64) ||
-        !map_2d(&m_w2s, w2s, (uint64_t)H, (uint64_t)Is, 64, 64) ||
-        !token_maps(&m_ash, &m_ashs, ash, (uint64_t)Is, (uint64_t)T + moe::kMaxTileRows, box2))
-      return MOE_ERR_CUDA;
-    moe::GemmArgs s13{};
-    s13.K = H;
-    s13.n_feat_tiles = spair13 ? Is / moe::kPairFeatW13 : Is / moe::kTileFeat;
-    s13.w_rows_per_e = H;
-    s13.up_col = Is;
-    s13.identity_T = T;
-    s13.out = ash;
-    s13.out_ld = Is;
-    s13.status = status;
-    s13.pair = spair13 ? 1 : 0;
-    moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + srows13 - 1) / srows13, sms, s);
-    moe::GemmArgs s2 = s13;
-    s2.K = Is;
-    s2.n_feat_tiles = pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat;
-    s2.w_rows_per_e = Is;
-    s2.up_col = 0;
-    s2.out = y_shared;
-    s2.out_ld = H;
-    s2.pair = pair2 ? 1 : 0;
-    moe::launch_w2_gemm(m_w2s, m_ash, m_ashs, s2, (T + moe::kW2TileRows - 1) / moe::kW2TileRows, sms, s);
+  if (!skip_shared && c->shared_intermediate > 0) {
+    const moe_status st = shared_ffn_impl(c, T, h, w13s, w2s, y_shared, ws, s);
+    if (st != MOE_OK) return st;
   }
   return last_cuda();
 }
@@ -446,6 +465,37 @@ struct Marks {
 
 void mark(const Marks* mk, int i) {
   if (mk) mk->at(i);
+}
+
+// Second stream of a device for the shared expert, with the fork and join
+// events.  One forward at a time enqueues on it (the events are reused).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+std::mutex& side_mutex() {
+  static std::mutex m;
+  return m;
+}
+
+// Called with side_mutex() held.
+bool side_stream(SideStream* out) {
+  static SideStream cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  SideStream& c = cache[dev];
+  if (!c.stream) {
+    if (cudaStreamCreateWithFlags(&c.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      c = SideStream{};
+      return false;
+    }
+  }
+  *out = c;
+  return true;
 }
 
 moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* wg,
@@ -468,23 +518,44 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   moe_status st = MOE_OK;
   bool tiles_ready = false;
   mk.at(0);
+  // the shared expert needs h alone: it runs on a second stream from here
+  // and joins before the combine
+  std::unique_lock<std::mutex> side_lock;
+  SideStream side;
+  const bool fork = c->shared_intermediate > 0;
+  if (fork) {
+    side_lock = std::unique_lock<std::mutex>(side_mutex());
+    if (!side_stream(&side)) return MOE_ERR_CUDA;
+    if (cudaEventRecord(side.fork, s) != cudaSuccess || cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
+      return last_cuda();
+    st = shared_ffn_impl(c, T, h, w13s, w2s, ysh, ws, side.stream);
+    if (st == MOE_OK && cudaEventRecord(side.join, side.stream) != cudaSuccess) st = last_cuda();
+    if (st != MOE_OK) {
+      cudaStreamWaitEvent(s, side.join, 0);   // leave no branch of a capture unjoined
+      return st;
+    }
+  }
   if (expert_choice(c)) {
     // every logit in the canonical order, then each expert takes its tokens
-    moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
+    if (moe::decode_router_ok(T))
+      moe::launch_router_decode(h, wg, bias, at<float>(ws, L.rpart), logits, nullptr, nullptr, T, c->hidden,
+                                c->num_experts, c->top_k, s);
+    else
+      moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
     mk.at(1);
     st = expert_choice_impl(c, T, logits, gates, kept, pos, sorted, blocks, num_padded, counts, ws, s);
   } else if (reroute_active(c, T)) {
     // rerouting ranks every expert of an overflowing token: canonical logits
     st = route_impl(c, T, h, wg, bias, idx, gates, logits, true, ws, s);
-    if (st != MOE_OK) return st;
     mk.at(1);
-    st = reroute_impl(c, T, idx, logits, kept, at<int32_t>(ws, L.route_expert), pos, sorted, blocks,
-                      num_padded, counts, at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.rerouted), ws, s);
+    if (st == MOE_OK)
+      st = reroute_impl(c, T, idx, logits, kept, at<int32_t>(ws, L.route_expert), pos, sorted, blocks,
+                        num_padded, counts, at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.rerouted), ws, s);
   } else {
     st = route_impl(c, T, h, wg, bias, idx, gates, logits, false, ws, s);
-    if (st != MOE_OK) return st;
     mk.at(1);
-    if (moe::dispatch_small_ok((long long)T * c->top_k)) {
+    // (an error is reported below, after the shared-expert branch has joined)
+    if (st == MOE_OK && moe::dispatch_small_ok((long long)T * c->top_k)) {
       // a few routes: dispatch, alignment and both tile lists in one launch
       moe::launch_dispatch_small(idx, T * c->top_k, c->num_experts, c->block_size, capacity_of(c, T), kept, pos,
                                  sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
@@ -495,14 +566,19 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
                                  at<int>(ws, L.status), s);
       tiles_ready = true;
       st = last_cuda();
-    } else {
+    } else if (st == MOE_OK) {
       st = dispatch_impl(c, T, idx, kept, pos, sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
                          ws, s);
     }
   }
-  if (st != MOE_OK) return st;
+  if (st != MOE_OK) {
+    if (fork) cudaStreamWaitEvent(s, side.join, 0);
+    return st;
+  }
   mk.at(2);
-  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk, tiles_ready);
+  st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk, tiles_ready,
+                /*skip_shared=*/fork);
+  if (fork && cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess && st == MOE_OK) st = last_cuda();
   if (st != MOE_OK) return st;
   mk.at(6);
   moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, slots_of(c), max_rows_of(c, T), s);
@@ -679,8 +755,13 @@ moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h
   MOE_TRY(opt(router_bias));
   MOE_TRY(need(logits_out));
   MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
-  moe::launch_router_logits(h, w_gate, router_bias, logits_out, T, cfg->hidden, cfg->num_experts,
-                            static_cast<cudaStream_t>(stream));
+  if (moe::decode_router_ok(T))
+    moe::launch_router_decode(h, w_gate, router_bias, at<float>(ws, layout_of(cfg, T).rpart), logits_out,
+                              nullptr, nullptr, T, cfg->hidden, cfg->num_experts, cfg->top_k,
+                              static_cast<cudaStream_t>(stream));
+  else
+    moe::launch_router_logits(h, w_gate, router_bias, logits_out, T, cfg->hidden, cfg->num_experts,
+                              static_cast<cudaStream_t>(stream));
   return last_cuda();
 }
 
@@ -803,25 +884,27 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
   if (T == 0) return 0;
   // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
-  // combine 1 (+ shared W13, W2).  Router: one launch for at most 16 tokens
-  // with a small W_g, else CUDA cores logits + top-k = 2, or for more than 16
-  // tokens on the tensor cores transpose, norms, GEMM, certified select = 4.
+  // combine 1 (+ shared W13, W2).  Router: for at most 64 tokens chunk sums
+  // + reduce/top-k = 2, else on the tensor cores transpose, norms, GEMM,
+  // certified select = 4, or CUDA-core logits + top-k = 2.
   // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
   // launch that also builds both tile lists; with reroute count, scan,
   // preference lists, deferred acceptance, check, sequential fallback
   // (returns at once unless the check failed), count, scan, scatter = 9
-  // after the CUDA-core router.  Expert choice: logits, scores, selection = 3.
-  const bool small = moe::router_small_ok(T, cfg->hidden, cfg->num_experts);   // one launch
+  // after the CUDA-core router.  Expert choice: logits (2 launches for at most
+  // 64 tokens, else 1), scores, selection.
+  const bool decode = moe::decode_router_ok(T);   // chunk sums + reduce/top-k: 2 launches
+  const int router = decode ? 2 : (use_tc_router(cfg) ? 4 : 2);
   int front = 0;
   if (expert_choice(cfg)) {
-    front = 3;
+    front = (decode ? 2 : 1) + 2;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
-    front = (small ? 1 : 2) + 9;
+    front = 2 + 9;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {
     // dispatch and both tile lists in one launch
-    front = (small ? 1 : (use_tc_router(cfg) && T > moe::kSmallRouterMaxT ? 4 : 2)) + 1 - 2;
+    front = router + 1 - 2;
   } else {
-    front = (small ? 1 : (use_tc_router(cfg) && T > moe::kSmallRouterMaxT ? 4 : 2)) + 3;
+    front = router + 3;
   }
   return front + 2 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }

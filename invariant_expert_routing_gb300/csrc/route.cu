@@ -231,56 +231,100 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
   topk_select_warp(logits + (size_t)t * N, N, k, lane, topk_idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
-// Router for a few tokens (decode) of a small router matrix: one CTA per
-// token does the whole route.  The CTA copies W_g (at most 64 K elements) and
-// the token row into shared memory with 16-byte loads, then thread (e, c)
-// runs the in-order fma chain of chunk c for expert e from shared memory (a
-// token's N x chunks chains run in parallel instead of a tile of tokens
-// sharing each weight load); the chunk sums of each expert are added in
-// ascending chunk order, then the bias, exactly as in router_logits_kernel;
-// warp 0 then selects the top-k with the same tournament and gate code as
-// topk_gates_kernel.  Same bits as the tiled router for every token.
-constexpr int kSmallRouterThreads = 512;
+// Router for a few tokens (decode): two launches.
+//
+// router_partials_kernel: one CTA per (256-element chunk c of H, 32 experts,
+// 8 tokens).  The CTA copies the chunk's W_g rows for its experts and its
+// tokens' row slices into shared memory (cp.async, one round trip), then
+// warp w, lane l runs the in-order fma chain of chunk c for token t0 + w and
+// expert e0 + l, and writes the chunk sum.  The H x N weights are read once
+// per 8 tokens by many CTAs in parallel, instead of by one CTA per token.
+// router_reduce_kernel: one CTA per token adds the chunk sums in ascending
+// chunk order, then the bias, exactly as in router_logits_kernel, and (unless
+// only logits are wanted) selects the top-k with the tournament and gate code
+// of topk_gates_kernel.  Same bits as the tiled router for every token.
+constexpr int kDecodeTok = 8;    // tokens per CTA (one warp each)
+constexpr int kDecodeExp = 32;   // experts per CTA (one lane each)
 
-__global__ void __launch_bounds__(kSmallRouterThreads) router_small_kernel(
-    const uint16_t* __restrict__ h, const uint16_t* __restrict__ wg, const float* __restrict__ bias,
-    float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ gates, int H, int N,
-    int k) {
-  extern __shared__ __align__(16) uint8_t rsm[];
-  const int t = blockIdx.x;
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kDecodeTok * 32) router_partials_kernel(
+    const uint16_t* __restrict__ h, const uint16_t* __restrict__ wg, int T, int H, int N,
+    float* __restrict__ part) {
+  __shared__ __align__(16) uint16_t sw[kRouterChunk][kDecodeExp];   // W_g rows of the chunk
+  __shared__ __align__(16) uint16_t sx[kDecodeTok][kRouterChunk];   // token row slices
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  uint16_t* ws = reinterpret_cast<uint16_t*>(rsm);                          // [H][N] W_g
-  float* hs = reinterpret_cast<float*>(rsm + (((size_t)H * N * 2 + 15) & ~(size_t)15));  // [H] token row
-  float* part = hs + H;                                                     // [chunks][N] chunk sums
-  float* lrow = part + (size_t)chunks * N;                                  // [N] logits
-  const size_t wvec = (size_t)H * N / 8;                                    // H % 128 == 0: whole uint4s
-  const uint4* wsrc = reinterpret_cast<const uint4*>(wg);
-  uint4* wdst = reinterpret_cast<uint4*>(ws);
-  for (size_t i = threadIdx.x; i < wvec; i += blockDim.x) wdst[i] = __ldg(wsrc + i);
-  const uint16_t* hrow = h + (size_t)t * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) hs[i] = __uint_as_float((uint32_t)hrow[i] << 16);
-  __syncthreads();
-  for (int item = threadIdx.x; item < chunks * N; item += blockDim.x) {
-    const int e = item % N, c = item / N;
-    const int i0 = c * kRouterChunk, i1 = min(H, i0 + kRouterChunk);
-    float p = 0.0f;
-#pragma unroll 8
-    for (int i = i0; i < i1; ++i) p = fmaf(hs[i], __uint_as_float((uint32_t)ws[(size_t)i * N + e] << 16), p);
-    part[(size_t)c * N + e] = p;
+  const int c = blockIdx.x, e0 = blockIdx.y * kDecodeExp, t0 = blockIdx.z * kDecodeTok;
+  const int i0 = c * kRouterChunk, len = min(H, i0 + kRouterChunk) - i0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ne = min(kDecodeExp, N - e0);
+  if (kVec) {   // N % 8 == 0 and 16-byte aligned W_g: 16-byte pieces of 8 experts
+    const int per_row = ne / 8;
+    for (int idx = tid; idx < len * per_row; idx += blockDim.x) {
+      const int r = idx / per_row, q = idx % per_row;
+      cp_async_16(&sw[r][8 * q], wg + (size_t)(i0 + r) * N + e0 + 8 * q);
+    }
+  } else {
+    for (int idx = tid; idx < len * kDecodeExp; idx += blockDim.x) {
+      const int r = idx / kDecodeExp, e = idx % kDecodeExp;
+      sw[r][e] = e < ne ? wg[(size_t)(i0 + r) * N + e0 + e] : (uint16_t)0;
+    }
   }
+  if (kVec) {   // 16-byte aligned token rows, H % 8 == 0
+    const int vec = len / 8;
+    for (int idx = tid; idx < kDecodeTok * vec; idx += blockDim.x) {
+      const int q = idx / vec, v = idx % vec;
+      if (t0 + q < T) cp_async_16(&sx[q][8 * v], h + (size_t)(t0 + q) * H + i0 + 8 * v);
+    }
+  } else {
+    for (int idx = tid; idx < kDecodeTok * len; idx += blockDim.x) {
+      const int q = idx / len, i = idx % len;
+      if (t0 + q < T) sx[q][i] = h[(size_t)(t0 + q) * H + i0 + i];
+    }
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncthreads();
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+  const int t = t0 + warp, e = e0 + lane;
+  if (t >= T || lane >= ne) return;
+  float p = 0.0f;
+#pragma unroll 16
+  for (int i = 0; i < len; ++i)
+    p = fmaf(__uint_as_float((uint32_t)sx[warp][i] << 16), __uint_as_float((uint32_t)sw[i][lane] << 16), p);
+  part[((size_t)t * chunks + c) * N + e] = p;
+}
+
+__global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ part,
+                                                            const float* __restrict__ bias, int T, int N,
+                                                            int chunks, int k, float* __restrict__ logits,
+                                                            int32_t* __restrict__ topk_idx,
+                                                            float* __restrict__ gates) {
+  // one CTA per token, one thread per expert: the chunk sums are loaded eight
+  // at a time (independent loads), then added in ascending chunk order
+  __shared__ float lrow[256];
+  const int t = blockIdx.x, e = threadIdx.x;
+  if (e < N) {
+    const float* pe = part + (size_t)t * chunks * N + e;
     float total = 0.0f;
-    for (int c = 0; c < chunks; ++c) total = total + part[(size_t)c * N + e];
+    for (int c0 = 0; c0 < chunks; c0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < chunks ? pe[(size_t)(c0 + j) * N] : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < chunks) total = total + v[j];
+    }
     if (bias) total = total + bias[e];
     lrow[e] = total;
     if (logits) logits[(size_t)t * N + e] = total;
   }
   __syncthreads();
-  if (threadIdx.x < 32)
+  if (topk_idx && threadIdx.x < 32)
     topk_select_warp(lrow, N, k, threadIdx.x, topk_idx + (size_t)t * k, gates + (size_t)t * k);
 }
-
 
 // ------------------------------------------------------------------------
 // Tensor-core router with a certified candidate filter.
@@ -586,26 +630,26 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
       logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
 }
 
-// One CTA per token reads all of W_g: worth it while W_g is small (a 64 K
-// element router such as H 4096 x N 16); larger routers keep the tiled or
-// certified paths, whose CTAs share the weight reads.
-bool router_small_ok(int T, int H, int N) {
-  return T <= kSmallRouterMaxT && H <= 8192 && (long long)H * N <= 65536;
+bool decode_router_ok(int T) { return T <= kDecodeRouterMaxT; }
+
+size_t decode_router_part_floats(int T, int H, int N) {
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+  return (size_t)(T < kDecodeRouterMaxT ? T : kDecodeRouterMaxT) * chunks * N;
 }
 
-void launch_router_small(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
-                         int32_t* topk_idx, float* gates, int T, int H, int N, int k, cudaStream_t s) {
+void launch_router_decode(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
+                          float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
+                          cudaStream_t s) {
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const size_t smem = (((size_t)H * N * 2 + 15) & ~(size_t)15) +
-                      sizeof(float) * ((size_t)H + (size_t)chunks * N + N);
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  router_small_kernel<<<T, kSmallRouterThreads, smem, s>>>(h, w_gate, bias, logits, topk_idx, gates, H, N, k);
+  const dim3 grid((unsigned)chunks, (unsigned)((N + kDecodeExp - 1) / kDecodeExp),
+                  (unsigned)((T + kDecodeTok - 1) / kDecodeTok));
+  const bool vec = N % 8 == 0 && H % 8 == 0 && (reinterpret_cast<uintptr_t>(w_gate) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
+  if (vec)
+    router_partials_kernel<true><<<grid, kDecodeTok * 32, 0, s>>>(h, w_gate, T, H, N, part);
+  else
+    router_partials_kernel<false><<<grid, kDecodeTok * 32, 0, s>>>(h, w_gate, T, H, N, part);
+  router_reduce_kernel<<<T, (N + 31) / 32 * 32, 0, s>>>(part, bias, T, N, chunks, k, logits, topk_idx, gates);
 }
 
 void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,

@@ -151,15 +151,18 @@ def test_launch_counts(moe):
     assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 6
     assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 3 + 6
     assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 6 + 2
-    # up to 16 tokens are routed in one launch when W_g is small, and up to
-    # 1024 routes are dispatched with both tile lists in one launch
-    assert moe.moe_forward_launch_count(mix, 1) == 1 + 1 + 4
-    assert moe.moe_forward_launch_count(mix, 16) == 1 + 1 + 4
-    assert moe.moe_forward_launch_count(mix, 17) == 2 + 1 + 4
+    # up to 64 tokens are routed in two launches (chunk sums, reduce + top-k),
+    # and up to 1024 routes are dispatched with both tile lists in one launch
+    assert moe.moe_forward_launch_count(mix, 1) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(mix, 64) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(mix, 65) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 512) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 513) == 2 + 3 + 6
     assert moe.moe_forward_launch_count(qw, 1) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(qw, 64) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(qw, 65) == 4 + 1 + 4
     assert moe.moe_forward_launch_count(qw, 128) == 4 + 1 + 4
+    assert moe.moe_forward_launch_count(dict(qw, routing=1), 64) == 4 + 6
     assert moe.moe_forward_launch_count(mix, 0) == 0
 
 
