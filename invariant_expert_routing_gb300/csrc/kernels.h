@@ -18,16 +18,18 @@ void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float
                           int T, int H, int N, cudaStream_t s);
 void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,
                        cudaStream_t s);
-// a few tokens (decode): chunk sums in parallel over (chunk, 32 experts, 8
+// Chunked CUDA-core router: chunk sums in parallel over (chunk, experts,
 // tokens), then logits (optional), top-k and gates (optional: topk_idx null
 // for logits alone); the same bits as launch_router_logits +
-// launch_topk_gates.  part: decode_router_part_floats floats.
+// launch_topk_gates.  Used for at most kDecodeRouterMaxT tokens, and for
+// batches when H x N <= 2^19 (unless a tensor-core router exists for the
+// shape and T x H x N > 2^29).  part: chunked_router_part_floats floats.
 constexpr int kDecodeRouterMaxT = 64;
-bool decode_router_ok(int T);
-size_t decode_router_part_floats(int T, int H, int N);
-void launch_router_decode(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
-                          float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
-                          cudaStream_t s);
+bool chunked_router_ok(int T, int H, int N, bool tc_router);
+size_t chunked_router_part_floats(int T, int H, int N);
+void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
+                           float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
+                           cudaStream_t s);
 // tensor-core router with a certified candidate filter (N % 128 == 0)
 void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
                       cudaStream_t s);

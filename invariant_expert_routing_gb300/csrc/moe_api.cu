@@ -111,7 +111,7 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.logits = take(sizeof(float) * T * N);
   L.wgT = take(sizeof(uint16_t) * N * H);
   L.norm_w = take(sizeof(float) * N);
-  L.rpart = take(sizeof(float) * moe::decode_router_part_floats(T, (int)H, (int)N));
+  L.rpart = take(sizeof(float) * moe::chunked_router_part_floats(T, (int)H, (int)N));
   L.topk = take(sizeof(int32_t) * R);
   L.gates = take(sizeof(float) * R);
   L.kept = take(R);
@@ -259,11 +259,11 @@ moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const u
                       const float* bias, int32_t* idx, float* gates, float* logits, bool canonical_logits,
                       void* ws, cudaStream_t s, int32_t* n_cand = nullptr) {
   const int H = c->hidden, N = c->num_experts, k = c->top_k;
-  if (moe::decode_router_ok(T) && !n_cand) {
-    // a few tokens: chunk sums spread over many CTAs, the same bits as either
-    // path below
+  if (moe::chunked_router_ok(T, H, N, use_tc_router(c) && !canonical_logits) && !n_cand) {
+    // a few tokens, or a small W_g: chunk sums spread over many CTAs, the
+    // same bits as either path below
     const Layout L = layout_of(c, T);
-    moe::launch_router_decode(h, wg, bias, at<float>(ws, L.rpart), logits, idx, gates, T, H, N, k, s);
+    moe::launch_router_chunked(h, wg, bias, at<float>(ws, L.rpart), logits, idx, gates, T, H, N, k, s);
     return last_cuda();
   }
   // the certified tensor-core path pays off on batches (same bits as the
@@ -537,9 +537,9 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   }
   if (expert_choice(c)) {
     // every logit in the canonical order, then each expert takes its tokens
-    if (moe::decode_router_ok(T))
-      moe::launch_router_decode(h, wg, bias, at<float>(ws, L.rpart), logits, nullptr, nullptr, T, c->hidden,
-                                c->num_experts, c->top_k, s);
+    if (moe::chunked_router_ok(T, c->hidden, c->num_experts, /*tc_router=*/false))
+      moe::launch_router_chunked(h, wg, bias, at<float>(ws, L.rpart), logits, nullptr, nullptr, T, c->hidden,
+                                 c->num_experts, c->top_k, s);
     else
       moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
     mk.at(1);
@@ -755,10 +755,10 @@ moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h
   MOE_TRY(opt(router_bias));
   MOE_TRY(need(logits_out));
   MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
-  if (moe::decode_router_ok(T))
-    moe::launch_router_decode(h, w_gate, router_bias, at<float>(ws, layout_of(cfg, T).rpart), logits_out,
-                              nullptr, nullptr, T, cfg->hidden, cfg->num_experts, cfg->top_k,
-                              static_cast<cudaStream_t>(stream));
+  if (moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, /*tc_router=*/false))
+    moe::launch_router_chunked(h, w_gate, router_bias, at<float>(ws, layout_of(cfg, T).rpart), logits_out,
+                               nullptr, nullptr, T, cfg->hidden, cfg->num_experts, cfg->top_k,
+                               static_cast<cudaStream_t>(stream));
   else
     moe::launch_router_logits(h, w_gate, router_bias, logits_out, T, cfg->hidden, cfg->num_experts,
                               static_cast<cudaStream_t>(stream));
@@ -884,20 +884,21 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
   if (T == 0) return 0;
   // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
-  // combine 1 (+ shared W13, W2).  Router: for at most 64 tokens chunk sums
-  // + reduce/top-k = 2, else on the tensor cores transpose, norms, GEMM,
-  // certified select = 4, or CUDA-core logits + top-k = 2.
+  // combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2 for
+  // at most 64 tokens or a small W_g, else on the tensor cores transpose,
+  // norms, GEMM, certified select = 4, or CUDA-core logits + top-k = 2.
   // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
   // launch that also builds both tile lists; with reroute count, scan,
   // preference lists, deferred acceptance, check, sequential fallback
   // (returns at once unless the check failed), count, scan, scatter = 9
-  // after the CUDA-core router.  Expert choice: logits (2 launches for at most
-  // 64 tokens, else 1), scores, selection.
-  const bool decode = moe::decode_router_ok(T);   // chunk sums + reduce/top-k: 2 launches
-  const int router = decode ? 2 : (use_tc_router(cfg) ? 4 : 2);
+  // after the CUDA-core router.  Expert choice: logits (2 launches on the
+  // chunked router, else 1), scores, selection.
+  // chunk sums + reduce/top-k: 2 launches
+  const bool chunked = moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg));
+  const int router = chunked ? 2 : (use_tc_router(cfg) ? 4 : 2);
   int front = 0;
-  if (expert_choice(cfg)) {
-    front = (decode ? 2 : 1) + 2;
+  if (expert_choice(cfg)) {   // logits only: no tensor-core router
+    front = (moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, false) ? 2 : 1) + 2;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = 2 + 9;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {

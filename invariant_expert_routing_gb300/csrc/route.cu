@@ -231,70 +231,83 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
   topk_select_warp(logits + (size_t)t * N, N, k, lane, topk_idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
-// Router for a few tokens (decode): two launches.
+// Chunked router on the CUDA cores: two launches, for a few tokens (decode)
+// and for batches when W_g is small.
 //
-// router_partials_kernel: one CTA per (256-element chunk c of H, 32 experts,
-// 8 tokens).  The CTA copies the chunk's W_g rows for its experts and its
-// tokens' row slices into shared memory (cp.async, one round trip), then
-// warp w, lane l runs the in-order fma chain of chunk c for token t0 + w and
-// expert e0 + l, and writes the chunk sum.  The H x N weights are read once
-// per 8 tokens by many CTAs in parallel, instead of by one CTA per token.
+// router_partials_kernel: one CTA per (256-element chunk c of H, LE experts,
+// TB tokens).  The CTA copies the chunk's W_g rows for its experts and its
+// tokens' row slices into shared memory (cp.async, one round trip); lane l of
+// a warp serves expert l % LE for token group l / LE, and each thread runs
+// the in-order fma chains of chunk c for TQ tokens (interleaved, so that the
+// token groups of a warp read different banks), writing the chunk sums.
 // router_reduce_kernel: one CTA per token adds the chunk sums in ascending
 // chunk order, then the bias, exactly as in router_logits_kernel, and (unless
 // only logits are wanted) selects the top-k with the tournament and gate code
 // of topk_gates_kernel.  Same bits as the tiled router for every token.
-constexpr int kDecodeTok = 8;    // tokens per CTA (one warp each)
-constexpr int kDecodeExp = 32;   // experts per CTA (one lane each)
+constexpr int kPartWarps = 8;
+constexpr int kPartRow = kRouterChunk + 8;   // token row stride in shared memory (528 B)
 
 __device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
   const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kDecodeTok * 32) router_partials_kernel(
+template <bool kVec, int LE, int TQ>
+__global__ void __launch_bounds__(kPartWarps * 32) router_partials_kernel(
     const uint16_t* __restrict__ h, const uint16_t* __restrict__ wg, int T, int H, int N,
     float* __restrict__ part) {
-  __shared__ __align__(16) uint16_t sw[kRouterChunk][kDecodeExp];   // W_g rows of the chunk
-  __shared__ __align__(16) uint16_t sx[kDecodeTok][kRouterChunk];   // token row slices
+  constexpr int G = 32 / LE;                 // token groups per warp
+  constexpr int TB = kPartWarps * G * TQ;    // tokens per CTA
+  extern __shared__ __align__(16) uint16_t psm[];
+  uint16_t* sw = psm;                        // [256][LE] W_g rows of the chunk
+  uint16_t* sx = psm + kRouterChunk * LE;    // [TB][kPartRow] token row slices
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const int c = blockIdx.x, e0 = blockIdx.y * kDecodeExp, t0 = blockIdx.z * kDecodeTok;
+  const int c = blockIdx.x, e0 = blockIdx.y * LE, t0 = blockIdx.z * TB;
   const int i0 = c * kRouterChunk, len = min(H, i0 + kRouterChunk) - i0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ne = min(kDecodeExp, N - e0);
-  if (kVec) {   // N % 8 == 0 and 16-byte aligned W_g: 16-byte pieces of 8 experts
+  const int ne = min(LE, N - e0);
+  const int nt = min(TB, T - t0);
+  if (kVec) {   // N % 8 == 0, H % 8 == 0, 16-byte aligned W_g and h: 16-byte pieces
     const int per_row = ne / 8;
     for (int idx = tid; idx < len * per_row; idx += blockDim.x) {
       const int r = idx / per_row, q = idx % per_row;
-      cp_async_16(&sw[r][8 * q], wg + (size_t)(i0 + r) * N + e0 + 8 * q);
+      cp_async_16(sw + r * LE + 8 * q, wg + (size_t)(i0 + r) * N + e0 + 8 * q);
     }
-  } else {
-    for (int idx = tid; idx < len * kDecodeExp; idx += blockDim.x) {
-      const int r = idx / kDecodeExp, e = idx % kDecodeExp;
-      sw[r][e] = e < ne ? wg[(size_t)(i0 + r) * N + e0 + e] : (uint16_t)0;
-    }
-  }
-  if (kVec) {   // 16-byte aligned token rows, H % 8 == 0
     const int vec = len / 8;
-    for (int idx = tid; idx < kDecodeTok * vec; idx += blockDim.x) {
+    for (int idx = tid; idx < nt * vec; idx += blockDim.x) {
       const int q = idx / vec, v = idx % vec;
-      if (t0 + q < T) cp_async_16(&sx[q][8 * v], h + (size_t)(t0 + q) * H + i0 + 8 * v);
+      cp_async_16(sx + q * kPartRow + 8 * v, h + (size_t)(t0 + q) * H + i0 + 8 * v);
     }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   } else {
-    for (int idx = tid; idx < kDecodeTok * len; idx += blockDim.x) {
+    for (int idx = tid; idx < len * LE; idx += blockDim.x) {
+      const int r = idx / LE, e = idx % LE;
+      sw[r * LE + e] = e < ne ? wg[(size_t)(i0 + r) * N + e0 + e] : (uint16_t)0;
+    }
+    for (int idx = tid; idx < nt * len; idx += blockDim.x) {
       const int q = idx / len, i = idx % len;
-      if (t0 + q < T) sx[q][i] = h[(size_t)(t0 + q) * H + i0 + i];
+      sx[q * kPartRow + i] = h[(size_t)(t0 + q) * H + i0 + i];
     }
   }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncthreads();
-  const int t = t0 + warp, e = e0 + lane;
-  if (t >= T || lane >= ne) return;
-  float p = 0.0f;
-#pragma unroll 16
-  for (int i = 0; i < len; ++i)
-    p = fmaf(__uint_as_float((uint32_t)sx[warp][i] << 16), __uint_as_float((uint32_t)sw[i][lane] << 16), p);
-  part[((size_t)t * chunks + c) * N + e] = p;
+  const int el = lane % LE, tg = lane / LE;
+  if (el >= ne) return;
+  const int tb = warp * G * TQ + tg;         // this thread's tokens: tb + G * q
+  float p[TQ];
+#pragma unroll
+  for (int q = 0; q < TQ; ++q) p[q] = 0.0f;
+#pragma unroll 8
+  for (int i = 0; i < len; ++i) {
+    const float w = __uint_as_float((uint32_t)sw[i * LE + el] << 16);
+#pragma unroll
+    for (int q = 0; q < TQ; ++q)
+      p[q] = fmaf(__uint_as_float((uint32_t)sx[(tb + G * q) * kPartRow + i] << 16), w, p[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < TQ; ++q) {
+    const int tl = tb + G * q;
+    if (tl < nt) part[((size_t)(t0 + tl) * chunks + c) * N + e0 + el] = p[q];
+  }
 }
 
 __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ part,
@@ -630,25 +643,59 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
       logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
 }
 
-bool decode_router_ok(int T) { return T <= kDecodeRouterMaxT; }
-
-size_t decode_router_part_floats(int T, int H, int N) {
-  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  return (size_t)(T < kDecodeRouterMaxT ? T : kDecodeRouterMaxT) * chunks * N;
+// The chunked router: for a few tokens always (many CTAs share the weight
+// reads of a decode step); for larger batches while W_g is small (H x N <=
+// 2^19) and either no tensor-core router exists for the shape or the batch's
+// T x H x N fused multiply-adds (at most 2^29) stay below the tensor-core
+// path's costs.  Every path gives the same bits.
+bool chunked_router_ok(int T, int H, int N, bool tc_router) {
+  if (T <= kDecodeRouterMaxT) return true;
+  const long long hn = (long long)H * N;
+  return hn <= (1ll << 19) && (!tc_router || hn * T <= (1ll << 29));
 }
 
-void launch_router_decode(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
-                          float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
-                          cudaStream_t s) {
+size_t chunked_router_part_floats(int T, int H, int N) {
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const dim3 grid((unsigned)chunks, (unsigned)((N + kDecodeExp - 1) / kDecodeExp),
-                  (unsigned)((T + kDecodeTok - 1) / kDecodeTok));
+  const int tt = (long long)H * N <= (1ll << 19) ? T : (T < kDecodeRouterMaxT ? T : kDecodeRouterMaxT);
+  return (size_t)tt * chunks * N;
+}
+
+template <int LE, int TQ>
+void launch_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int T, int H, int N, bool vec,
+                     cudaStream_t s) {
+  constexpr int TB = kPartWarps * (32 / LE) * TQ;
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+  const dim3 grid((unsigned)chunks, (unsigned)((N + LE - 1) / LE), (unsigned)((T + TB - 1) / TB));
+  const size_t smem = sizeof(uint16_t) * ((size_t)kRouterChunk * LE + (size_t)TB * kPartRow);
+  auto kernel = vec ? router_partials_kernel<true, LE, TQ> : router_partials_kernel<false, LE, TQ>;
+  static bool attr_set[64][2] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev][vec ? 1 : 0]) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (dev >= 0 && dev < 64) attr_set[dev][vec ? 1 : 0] = true;
+  }
+  kernel<<<grid, kPartWarps * 32, smem, s>>>(h, w_gate, T, H, N, part);
+}
+
+void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
+                           float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
+                           cudaStream_t s) {
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
   const bool vec = N % 8 == 0 && H % 8 == 0 && (reinterpret_cast<uintptr_t>(w_gate) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
-  if (vec)
-    router_partials_kernel<true><<<grid, kDecodeTok * 32, 0, s>>>(h, w_gate, T, H, N, part);
-  else
-    router_partials_kernel<false><<<grid, kDecodeTok * 32, 0, s>>>(h, w_gate, T, H, N, part);
+  // a few tokens: one token per thread (more CTAs); batches: four
+  const bool few = T <= kDecodeRouterMaxT;
+  if (N <= 8) {
+    if (few) launch_partials<8, 1>(h, w_gate, part, T, H, N, vec, s);
+    else launch_partials<8, 4>(h, w_gate, part, T, H, N, vec, s);
+  } else if (N <= 16) {
+    if (few) launch_partials<16, 1>(h, w_gate, part, T, H, N, vec, s);
+    else launch_partials<16, 4>(h, w_gate, part, T, H, N, vec, s);
+  } else {
+    if (few) launch_partials<32, 1>(h, w_gate, part, T, H, N, vec, s);
+    else launch_partials<32, 4>(h, w_gate, part, T, H, N, vec, s);
+  }
   router_reduce_kernel<<<T, (N + 31) / 32 * 32, 0, s>>>(part, bias, T, N, chunks, k, logits, topk_idx, gates);
 }
 

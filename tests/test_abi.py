@@ -145,14 +145,19 @@ def test_expert_choice_capacity_and_bounds_match_the_oracle(moe):
 def test_launch_counts(moe):
     mix = dict(hidden=4096, num_experts=8, top_k=2, intermediate=14336, block_size=64)
     qw = dict(hidden=2048, num_experts=128, top_k=8, intermediate=768, block_size=16)
+    ds = dict(hidden=7168, num_experts=256, top_k=8, intermediate=2048, block_size=16)
     T = 4096
     assert moe.moe_forward_launch_count(mix, T) == 2 + 3 + 6
     assert moe.moe_forward_launch_count(qw, T) == 4 + 3 + 6
+    assert moe.moe_forward_launch_count(qw, 2048) == 2 + 3 + 6   # chunked router: W_g is small
     assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 6
-    assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 3 + 6
+    assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 4 + 6
+    assert moe.moe_forward_launch_count(dict(ds, routing=1), T) == 3 + 6
+    assert moe.moe_forward_launch_count(ds, T) == 4 + 3 + 6
     assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 6 + 2
-    # up to 64 tokens are routed in two launches (chunk sums, reduce + top-k),
-    # and up to 1024 routes are dispatched with both tile lists in one launch
+    # up to 64 tokens (or any batch for a small W_g) are routed in two
+    # launches (chunk sums, reduce + top-k), and up to 1024 routes are
+    # dispatched with both tile lists in one launch
     assert moe.moe_forward_launch_count(mix, 1) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 64) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 65) == 2 + 1 + 4
@@ -160,9 +165,11 @@ def test_launch_counts(moe):
     assert moe.moe_forward_launch_count(mix, 513) == 2 + 3 + 6
     assert moe.moe_forward_launch_count(qw, 1) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(qw, 64) == 2 + 1 + 4
-    assert moe.moe_forward_launch_count(qw, 65) == 4 + 1 + 4
-    assert moe.moe_forward_launch_count(qw, 128) == 4 + 1 + 4
+    assert moe.moe_forward_launch_count(qw, 65) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(qw, 128) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(dict(qw, routing=1), 64) == 4 + 6
+    assert moe.moe_forward_launch_count(ds, 64) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(ds, 65) == 4 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 0) == 0
 
 
