@@ -14,16 +14,12 @@ constexpr int kRouterChunk = 256;
 constexpr int kDispatchTile = 1024;
 
 // ---- router
-void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
-                          int T, int H, int N, cudaStream_t s);
-void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,
-                       cudaStream_t s);
 // Chunked CUDA-core router: chunk sums in parallel over (chunk, experts,
-// tokens), then logits (optional), top-k and gates (optional: topk_idx null
-// for logits alone); the same bits as launch_router_logits +
-// launch_topk_gates.  Used for at most kDecodeRouterMaxT tokens, and for
-// batches when H x N <= 2^19 (unless a tensor-core router exists for the
-// shape and T x H x N > 2^29).  part: chunked_router_part_floats floats.
+// tokens), then logits in the canonical chunked order (optional), top-k and
+// gates (optional: topk_idx null for logits alone).  Used for at most
+// kDecodeRouterMaxT tokens, and for batches unless the tensor-core router
+// serves the call and W_g has more than 2^19 elements or T x H x N > 2^29.
+// part: chunked_router_part_floats floats.
 constexpr int kDecodeRouterMaxT = 64;
 bool chunked_router_ok(int T, int H, int N, bool tc_router);
 size_t chunked_router_part_floats(int T, int H, int N);

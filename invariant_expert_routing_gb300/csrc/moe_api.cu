@@ -278,8 +278,9 @@ moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const u
     moe::launch_route_certified(logits, bias, h, wgT, norm_w, T, H, N, k, idx, gates, n_cand, s);
     return last_cuda();
   }
-  moe::launch_router_logits(h, wg, bias, logits, T, H, N, s);
-  moe::launch_topk_gates(logits, idx, gates, T, N, k, s);
+  // the tensor-core path is unavailable: the chunked router serves any batch
+  const Layout L = layout_of(c, T);
+  moe::launch_router_chunked(h, wg, bias, at<float>(ws, L.rpart), logits, idx, gates, T, H, N, k, s);
   return last_cuda();
 }
 
@@ -537,11 +538,8 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   }
   if (expert_choice(c)) {
     // every logit in the canonical order, then each expert takes its tokens
-    if (moe::chunked_router_ok(T, c->hidden, c->num_experts, /*tc_router=*/false))
-      moe::launch_router_chunked(h, wg, bias, at<float>(ws, L.rpart), logits, nullptr, nullptr, T, c->hidden,
-                                 c->num_experts, c->top_k, s);
-    else
-      moe::launch_router_logits(h, wg, bias, logits, T, c->hidden, c->num_experts, s);
+    moe::launch_router_chunked(h, wg, bias, at<float>(ws, L.rpart), logits, nullptr, nullptr, T, c->hidden,
+                               c->num_experts, c->top_k, s);
     mk.at(1);
     st = expert_choice_impl(c, T, logits, gates, kept, pos, sorted, blocks, num_padded, counts, ws, s);
   } else if (reroute_active(c, T)) {
@@ -755,13 +753,9 @@ moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h
   MOE_TRY(opt(router_bias));
   MOE_TRY(need(logits_out));
   MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
-  if (moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, /*tc_router=*/false))
-    moe::launch_router_chunked(h, w_gate, router_bias, at<float>(ws, layout_of(cfg, T).rpart), logits_out,
-                               nullptr, nullptr, T, cfg->hidden, cfg->num_experts, cfg->top_k,
-                               static_cast<cudaStream_t>(stream));
-  else
-    moe::launch_router_logits(h, w_gate, router_bias, logits_out, T, cfg->hidden, cfg->num_experts,
-                              static_cast<cudaStream_t>(stream));
+  moe::launch_router_chunked(h, w_gate, router_bias, at<float>(ws, layout_of(cfg, T).rpart), logits_out,
+                             nullptr, nullptr, T, cfg->hidden, cfg->num_experts, cfg->top_k,
+                             static_cast<cudaStream_t>(stream));
   return last_cuda();
 }
 
@@ -884,21 +878,21 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
   if (T == 0) return 0;
   // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
-  // combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2 for
-  // at most 64 tokens or a small W_g, else on the tensor cores transpose,
-  // norms, GEMM, certified select = 4, or CUDA-core logits + top-k = 2.
+  // combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2
+  // (chunked router), or on the tensor cores transpose, norms, GEMM,
+  // certified select = 4.
   // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
   // launch that also builds both tile lists; with reroute count, scan,
   // preference lists, deferred acceptance, check, sequential fallback
   // (returns at once unless the check failed), count, scan, scatter = 9
-  // after the CUDA-core router.  Expert choice: logits (2 launches on the
-  // chunked router, else 1), scores, selection.
+  // after the CUDA-core router.  Expert choice: logits (2 launches), scores,
+  // selection.
   // chunk sums + reduce/top-k: 2 launches
   const bool chunked = moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg));
   const int router = chunked ? 2 : (use_tc_router(cfg) ? 4 : 2);
   int front = 0;
-  if (expert_choice(cfg)) {   // logits only: no tensor-core router
-    front = (moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, false) ? 2 : 1) + 2;
+  if (expert_choice(cfg)) {   // logits (chunked router, 2), scores, selection
+    front = 2 + 2;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = 2 + 9;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {

@@ -10,9 +10,12 @@
 // ("Why temperature=0 Still Gives Different Answers: Batch Invariance",
 // Tier 2: a reduction cut into constant 256-element pieces added in one
 // order).  bf16 x bf16 products are exact in fp32, so the fma rounds exactly
-// like the separate add.  Chunks are spread over the warps of a CTA and their partial sums are
-// combined in ascending chunk order through shared memory; no split crosses a
-// CTA and nothing depends on T.
+// like the separate add.  Two implementations give these bits: the chunked
+// CUDA-core router (router_partials_kernel + router_reduce_kernel: chunk sums
+// in parallel CTAs, added in ascending chunk order per token) and the
+// certified tensor-core router (route_certified_kernel recomputes the
+// candidates' logits in the same order); the split of work never changes a
+// logit's order and nothing depends on T.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -21,118 +24,8 @@
 namespace moe {
 namespace {
 
-constexpr int kRouterWarps = 8;
-
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-// CTA tile: TT = TQ*G tokens x NE = 2*P experts (NE <= 32).  Lane l of a warp
-// owns the expert pair p = l % P and the token group g = l / P (P*G = 32) of
-// TQ tokens.
-// Warp w sums chunks w, w+8, ...: it first copies the chunk's W_g slice
-// [256 x NE] and the TT token rows [TT x 256] into its shared-memory stage with
-// one burst of independent loads, then runs the in-order fma chains from
-// shared memory.  After each round of 8 chunks the partial sums are added, in
-// ascending chunk order, to running totals held by the threads that own each
-// (token, expert).
-template <bool kEvenN, int TQ>
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ h,
-                                                            const uint16_t* __restrict__ wg,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits, int T, int H,
-                                                            int N, int P, int G) {
-  extern __shared__ __align__(16) uint8_t rsm[];
-  const int NE = 2 * P, TT = TQ * G;
-  const int t0 = blockIdx.x * TT, e0 = blockIdx.y * NE;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = lane % P, g = lane / P;
-  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const size_t stage_bytes = (size_t)kRouterChunk * NE * 2 + (size_t)TT * kRouterChunk * 2;
-  uint32_t* sw = reinterpret_cast<uint32_t*>(rsm + warp * stage_bytes);  // [256][P] expert pairs
-  uint4* sh = reinterpret_cast<uint4*>(rsm + warp * stage_bytes + (size_t)kRouterChunk * NE * 2);  // [TT][32]
-  float* part = reinterpret_cast<float*>(rsm + kRouterWarps * stage_bytes);  // [8][TT][NE]
-  const int slot = TT * NE;
-  constexpr int kMaxOwn = 2;  // (token, expert) pairs per thread: TT*NE <= 512
-  float total[kMaxOwn] = {0.0f, 0.0f};
-  for (int round = 0; round < chunks; round += kRouterWarps) {
-    const int c = round + warp;
-    if (c < chunks) {
-      const int i0 = c * kRouterChunk, len = min(H, i0 + kRouterChunk) - i0;
-      // W_g[i0 .. i0+len, e0 .. e0+NE) as expert pairs; experts >= N read as 0
-      for (int idx = lane; idx < len * P; idx += 32) {
-        const int row = idx / P, pp = idx % P;
-        const int e = e0 + 2 * pp;
-        const size_t off = (size_t)(i0 + row) * N + e;
-        uint32_t v = 0;
-        if (kEvenN) {
-          if (e < N) v = __ldg(reinterpret_cast<const unsigned int*>(wg + off));
-        } else {
-          if (e < N) v = (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(wg + off));
-          if (e + 1 < N) v |= (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(wg + off + 1)) << 16;
-        }
-        sw[row * P + pp] = v;
-      }
-      // token rows t0 .. t0+TT, columns i0 .. i0+len (missing tokens read as 0)
-      const int vec = len / 8;
-      for (int idx = lane; idx < TT * vec; idx += 32) {
-        const int q = idx / vec, v = idx % vec;
-        const int t = t0 + q;
-        sh[q * 32 + v] = (t < T) ? __ldg(reinterpret_cast<const uint4*>(h + (size_t)t * H + i0) + v)
-                                 : make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-      float acc[TQ][2];
-#pragma unroll
-      for (int q = 0; q < TQ; ++q) acc[q][0] = acc[q][1] = 0.0f;
-      for (int i = 0; i < len; i += 8) {
-        uint4 hv[TQ];
-#pragma unroll
-        for (int q = 0; q < TQ; ++q) hv[q] = sh[(TQ * g + q) * 32 + i / 8];
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii) {
-          const uint32_t w2 = sw[(i + ii) * P + p];
-          const float wa = bf16_lo(w2), wb = bf16_hi(w2);
-#pragma unroll
-          for (int q = 0; q < TQ; ++q) {
-            const uint32_t word = (ii < 2) ? hv[q].x : (ii < 4) ? hv[q].y : (ii < 6) ? hv[q].z : hv[q].w;
-            const float hx = (ii & 1) ? bf16_hi(word) : bf16_lo(word);
-            acc[q][0] = fmaf(hx, wa, acc[q][0]);
-            acc[q][1] = fmaf(hx, wb, acc[q][1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < TQ; ++q) {
-        float* dst = part + (size_t)warp * slot + (size_t)(TQ * g + q) * NE + 2 * p;
-        dst[0] = acc[q][0];
-        dst[1] = acc[q][1];
-      }
-      __syncwarp();
-    }
-    __syncthreads();
-    const int nc = min(kRouterWarps, chunks - round);
-#pragma unroll
-    for (int o = 0; o < kMaxOwn; ++o) {
-      const int idx = threadIdx.x + o * blockDim.x;
-      if (idx < slot)
-        for (int w = 0; w < nc; ++w) total[o] = total[o] + part[(size_t)w * slot + idx];
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int o = 0; o < kMaxOwn; ++o) {
-    const int idx = threadIdx.x + o * blockDim.x;
-    if (idx < slot) {
-      const int tl = idx / NE, el = idx % NE;
-      const int t = t0 + tl, e = e0 + el;
-      if (t < T && e < N) {
-        float v = total[o];
-        if (bias) v = v + bias[e];
-        logits[(size_t)t * N + e] = v;
-      }
-    }
-  }
-}
 
 // Ranking: a number beats NaN; larger beats smaller; equal -> lower index.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
@@ -220,17 +113,6 @@ __device__ __forceinline__ void topk_select_warp(const float* lrow, int N, int k
   write_slots_and_gates(sel, selv, k, idx_out, gate_out, lane);
 }
 
-// One warp per token.
-__global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict__ logits,
-                                                         int32_t* __restrict__ topk_idx,
-                                                         float* __restrict__ gates, int T, int N,
-                                                         int k) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  topk_select_warp(logits + (size_t)t * N, N, k, lane, topk_idx + (size_t)t * k, gates + (size_t)t * k);
-}
-
 // Chunked router on the CUDA cores: two launches, for a few tokens (decode)
 // and for batches when W_g is small.
 //
@@ -241,9 +123,8 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
 // the in-order fma chains of chunk c for TQ tokens (interleaved, so that the
 // token groups of a warp read different banks), writing the chunk sums.
 // router_reduce_kernel: one CTA per token adds the chunk sums in ascending
-// chunk order, then the bias, exactly as in router_logits_kernel, and (unless
-// only logits are wanted) selects the top-k with the tournament and gate code
-// of topk_gates_kernel.  Same bits as the tiled router for every token.
+// chunk order, then the bias, and (unless only logits are wanted) selects
+// the top-k with the warp tournament of topk_select_warp.
 constexpr int kPartWarps = 8;
 constexpr int kPartRow = kRouterChunk + 8;   // token row stride in shared memory (528 B)
 
@@ -354,7 +235,7 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
 // additions of the canonical order.  If L_k is the k-th largest l_tc, every
 // expert with l_tc < L_k - 2 delta_t has a canonical logit strictly below the
 // canonical k-th value, so only the remaining candidates get their canonical
-// logits computed (in the exact order of router_logits_kernel), and the
+// logits computed (in the canonical chunked order), and the
 // top-k and gates are chosen from those.  The indices and gates are
 // therefore bit-identical to the CUDA-core router's; only the work differs.
 // Every decision depends on the token's own values alone.
@@ -595,33 +476,6 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
 
 }  // namespace
 
-void launch_router_logits(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* logits,
-                          int T, int H, int N, cudaStream_t s) {
-  // NE experts per CTA (power of two, 8..16), P = NE/2 pairs, G = 32/P token
-  // groups of two: about 100 KB of shared memory, two CTAs per SM.  Any tile
-  // shape gives the same bits (each logit's order is fixed by its own chunks).
-  constexpr int TQ = 2;
-  int NE = 8;
-  while (NE < N && NE < 16) NE *= 2;
-  const int P = NE / 2, G = 32 / P, TT = TQ * G;
-  const size_t stage = (size_t)kRouterChunk * NE * 2 + (size_t)TT * kRouterChunk * 2;
-  const size_t smem = kRouterWarps * stage + (size_t)kRouterWarps * TT * NE * sizeof(float);
-  dim3 grid((T + TT - 1) / TT, (N + NE - 1) / NE);
-  static bool attr_set[64][2] = {{false}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int even = N % 2 == 0 ? 1 : 0;
-  if (dev < 0 || dev >= 64 || !attr_set[dev][even]) {
-    cudaFuncSetAttribute(even ? router_logits_kernel<true, TQ> : router_logits_kernel<false, TQ>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
-    if (dev >= 0 && dev < 64) attr_set[dev][even] = true;
-  }
-  if (even)
-    router_logits_kernel<true, TQ><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
-  else
-    router_logits_kernel<false, TQ><<<grid, 256, smem, s>>>(h, w_gate, bias, logits, T, H, N, P, G);
-}
-
 void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
                       cudaStream_t s) {
   dim3 grid((N + 31) / 32, (H + 31) / 32), block(32, 8);
@@ -644,20 +498,19 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
 }
 
 // The chunked router: for a few tokens always (many CTAs share the weight
-// reads of a decode step); for larger batches while W_g is small (H x N <=
-// 2^19) and either no tensor-core router exists for the shape or the batch's
-// T x H x N fused multiply-adds (at most 2^29) stay below the tensor-core
-// path's costs.  Every path gives the same bits.
+// reads of a decode step); for larger batches unless the certified
+// tensor-core router is available and the batch's T x H x N fused
+// multiply-adds exceed 2^29 (or W_g exceeds 2^19 elements), where the
+// tensor-core path costs less.  Every path gives the same bits.
 bool chunked_router_ok(int T, int H, int N, bool tc_router) {
-  if (T <= kDecodeRouterMaxT) return true;
+  if (T <= kDecodeRouterMaxT || !tc_router) return true;
   const long long hn = (long long)H * N;
-  return hn <= (1ll << 19) && (!tc_router || hn * T <= (1ll << 29));
+  return hn <= (1ll << 19) && hn * T <= (1ll << 29);
 }
 
 size_t chunked_router_part_floats(int T, int H, int N) {
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
-  const int tt = (long long)H * N <= (1ll << 19) ? T : (T < kDecodeRouterMaxT ? T : kDecodeRouterMaxT);
-  return (size_t)tt * chunks * N;
+  return (size_t)T * chunks * N;
 }
 
 template <int LE, int TQ>
@@ -697,12 +550,6 @@ void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const floa
     else launch_partials<32, 4>(h, w_gate, part, T, H, N, vec, s);
   }
   router_reduce_kernel<<<T, (N + 31) / 32 * 32, 0, s>>>(part, bias, T, N, chunks, k, logits, topk_idx, gates);
-}
-
-void launch_topk_gates(const float* logits, int32_t* topk_idx, float* gates, int T, int N, int k,
-                       cudaStream_t s) {
-  const int warps = 8;
-  topk_gates_kernel<<<(T + warps - 1) / warps, warps * 32, 0, s>>>(logits, topk_idx, gates, T, N, k);
 }
 
 }  // namespace moe

@@ -152,7 +152,7 @@ def test_launch_counts(moe):
     assert moe.moe_forward_launch_count(qw, 2048) == 2 + 3 + 6   # chunked router: W_g is small
     assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 6
     assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 4 + 6
-    assert moe.moe_forward_launch_count(dict(ds, routing=1), T) == 3 + 6
+    assert moe.moe_forward_launch_count(dict(ds, routing=1), T) == 4 + 6
     assert moe.moe_forward_launch_count(ds, T) == 4 + 3 + 6
     assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 6 + 2
     # up to 64 tokens (or any batch for a small W_g) are routed in two
