@@ -10,9 +10,9 @@
 // in shared memory; skipping the others leaves the chain of fmas unchanged.
 // A token row is split over gridDim.y CTAs (more when there are few tokens,
 // so that a lone token's row is spread over several SMs), 4 consecutive
-// features per thread, 128-bit loads of y_perm issued eight slots at a time
-// before their fmas; the order of the sum is fixed and independent of T and
-// of the grid.
+// features per thread, 128-bit loads of y_perm (with few tokens issued eight
+// slots at a time before their fmas); the order of the sum is fixed and
+// independent of T and of the grid.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kMaxSlots = 256;
 
+template <bool kBatch>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ h,
                                                       const float* __restrict__ gates,
                                                       const uint8_t* __restrict__ route_kept,
@@ -61,21 +62,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   __syncthreads();
   for (int d = (blockIdx.y * blockDim.x + threadIdx.x) * 4; d < H; d += gridDim.y * blockDim.x * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < n_used; i0 += 8) {
-      float4 y[8];
+    if (kBatch) {   // few tokens: eight slots' loads in flight before their fmas
+      for (int i0 = 0; i0 < n_used; i0 += 8) {
+        float4 y[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (i0 + q < n_used)
-          y[q] = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)s_pos[i0 + q] * H + d));
+        for (int q = 0; q < 8; ++q)
+          if (i0 + q < n_used)
+            y[q] = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)s_pos[i0 + q] * H + d));
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (i0 + q < n_used) {
-          const float g = s_gate[i0 + q];
-          acc.x = fmaf(g, y[q].x, acc.x);
-          acc.y = fmaf(g, y[q].y, acc.y);
-          acc.z = fmaf(g, y[q].z, acc.z);
-          acc.w = fmaf(g, y[q].w, acc.w);
+        for (int q = 0; q < 8; ++q) {
+          if (i0 + q < n_used) {
+            const float g = s_gate[i0 + q];
+            acc.x = fmaf(g, y[q].x, acc.x);
+            acc.y = fmaf(g, y[q].y, acc.y);
+            acc.z = fmaf(g, y[q].z, acc.z);
+            acc.w = fmaf(g, y[q].w, acc.w);
+          }
         }
+      }
+    } else {        // many tokens: occupancy hides the latency (fewer registers)
+      for (int i = 0; i < n_used; ++i) {
+        const float g = s_gate[i];
+        const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)s_pos[i] * H + d));
+        acc.x = fmaf(g, y.x, acc.x);
+        acc.y = fmaf(g, y.y, acc.y);
+        acc.z = fmaf(g, y.z, acc.z);
+        acc.w = fmaf(g, y.w, acc.w);
       }
     }
     if (y_shared) {
@@ -109,8 +121,12 @@ void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_
   const int per_row = (H + 1023) / 1024;
   const int want = T > 0 ? (2 * (sms > 0 ? sms : 1) + T - 1) / T : 1;
   const dim3 grid((unsigned)T, (unsigned)(want < per_row ? (want > 0 ? want : 1) : per_row));
-  combine_kernel<<<grid, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
-                                      (long long)max_rows);
+  if (grid.y > 1)
+    combine_kernel<true><<<grid, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
+                                              (long long)max_rows);
+  else
+    combine_kernel<false><<<grid, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
+                                               (long long)max_rows);
 }
 
 }  // namespace moe
