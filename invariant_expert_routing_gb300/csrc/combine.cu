@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -32,6 +33,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ y_shared,
                                                       uint16_t* __restrict__ out, int H, int k,
                                                       long long max_rows) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
   const int t = blockIdx.x;
   __shared__ int s_pos[kMaxSlots];
   __shared__ float s_gate[kMaxSlots];
@@ -122,10 +124,10 @@ void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_
   const int want = T > 0 ? (2 * (sms > 0 ? sms : 1) + T - 1) / T : 1;
   const dim3 grid((unsigned)T, (unsigned)(want < per_row ? (want > 0 ? want : 1) : per_row));
   if (grid.y > 1)
-    combine_kernel<true><<<grid, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
+    launch_pdl(combine_kernel<true>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
                                               (long long)max_rows);
   else
-    combine_kernel<false><<<grid, 256, 0, s>>>(h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
+    launch_pdl(combine_kernel<false>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
                                                (long long)max_rows);
 }
 

@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -29,6 +30,8 @@ __global__ void __launch_bounds__(1024) dispatch_count_kernel(const int32_t* __r
                                                               int32_t* __restrict__ rank_in_tile,
                                                               int32_t* __restrict__ tile_count,
                                                               int* status) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   __shared__ int32_t wc[32][kMaxN + 1];
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 32 * (kMaxN + 1); i += blockDim.x) (&wc[0][0])[i] = 0;
@@ -79,6 +82,8 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
     int32_t* __restrict__ seg_off, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_padded,
     int32_t* __restrict__ num_dropped, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ sorted_route_ids) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   __shared__ int buf[256];
   __shared__ int blk_off[kMaxN + 1];
   const int e = threadIdx.x;
@@ -126,6 +131,8 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
     const int32_t* __restrict__ rank_in_tile, const int32_t* __restrict__ tile_base,
     const int32_t* __restrict__ seg_off, uint8_t* __restrict__ route_kept,
     int32_t* __restrict__ route_pos, int32_t* __restrict__ sorted_route_ids) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   const int r = blockIdx.x * kDispatchTile + threadIdx.x;
   if (r >= R) return;
   const int e = topk_idx[r];
@@ -157,6 +164,8 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
                                                           GemmTile* __restrict__ tiles,
                                                           int32_t* __restrict__ num_tiles, int max_tiles,
                                                           int* status) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   __shared__ int buf[256];
   __shared__ int s_bad;
   const int P = *num_padded;
@@ -228,6 +237,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ num_padded, int k,
                                                           int R, int H, long long max_rows,
                                                           uint16_t* __restrict__ x_perm) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  // no early trigger: the next kernel is a GEMM or the combine, whose CTAs
+  // would hold SMs idle while they wait
   const long long P = min((long long)*num_padded, max_rows);
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
@@ -284,6 +296,8 @@ __global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
     int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
     int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
     int max_b, int* status) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   __shared__ int wc[32][kMaxN + 1];
   __shared__ int kept_s[kMaxN], pad_s[kMaxN], drop_s[kMaxN], nta[kMaxN], ntb[kMaxN];
   __shared__ int seg[kMaxN], offa[kMaxN], offb[kMaxN];
@@ -397,7 +411,7 @@ void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, cons
   const long long want = (max_rows + 7) / 8;
   const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
   const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-  gather_rows_kernel<<<grid, 256, 0, s>>>(h, sorted_route_ids, num_padded, k, R, H, (long long)max_rows,
+  launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, h, sorted_route_ids, num_padded, k, R, H, (long long)max_rows,
                                           x_perm);
 }
 
@@ -408,11 +422,11 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      int32_t* seg_off, int* status, cudaStream_t s) {
   const int R = T * k;
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
-  dispatch_count_kernel<<<ntiles, kDispatchTile, 0, s>>>(topk_idx, R, N, 0, rank_in_tile, tile_count,
+  launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, 0, rank_in_tile, tile_count,
                                                          status);
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
                                          num_padded, num_dropped, block_expert, sorted_route_ids);
-  dispatch_scatter_kernel<<<ntiles, kDispatchTile, 0, s>>>(topk_idx, R, N, capacity, rank_in_tile,
+  launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, capacity, rank_in_tile,
                                                            tile_count, seg_off, route_kept, route_pos,
                                                            sorted_route_ids);
 }
@@ -422,11 +436,11 @@ void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, ui
                             int32_t* num_padded, int32_t* expert_counts, int32_t* rank_in_tile,
                             int32_t* tile_count, int32_t* seg_off, int* status, cudaStream_t s) {
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
-  dispatch_count_kernel<<<ntiles, kDispatchTile, 0, s>>>(route_expert, R, N, 1, rank_in_tile, tile_count,
+  launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, 1, rank_in_tile, tile_count,
                                                          status);
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(tile_count, ntiles, N, B, -1, R, seg_off, expert_counts,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, -1, R, seg_off, expert_counts,
                                          num_padded, nullptr, block_expert, sorted_route_ids);
-  dispatch_scatter_kernel<<<ntiles, kDispatchTile, 0, s>>>(route_expert, R, N, -1, rank_in_tile,
+  launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, -1, rank_in_tile,
                                                            tile_count, seg_off, route_kept, route_pos,
                                                            sorted_route_ids);
 }
@@ -440,9 +454,9 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
   const int R = T * k;
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   // phase one: ranks and the per-expert kept counts of the drop rule
-  dispatch_count_kernel<<<ntiles, kDispatchTile, 0, s>>>(topk_idx, R, N, 0, rank_in_tile, tile_count,
+  launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, 0, rank_in_tile, tile_count,
                                                          status);
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
                                          num_padded, nullptr, block_expert, sorted_route_ids);
   // phase two, then the stable layout of the final assignment
   launch_reroute(topk_idx, logits, T, N, k, capacity, rank_in_tile, tile_count, expert_counts, sc,
@@ -458,7 +472,7 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
                            int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
                            GemmTile* tiles_a, int32_t* ntiles_a, int rows_a, int max_a, GemmTile* tiles_b,
                            int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s) {
-  dispatch_small_kernel<<<1, kSmallDispatchMaxR, 0, s>>>(
+  launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallDispatchMaxR), 0, s, 
       topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert, num_padded,
       expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, status);
 }
@@ -467,7 +481,7 @@ void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
                         const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
                         int tile_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles, int* status,
                         cudaStream_t s) {
-  build_tiles_kernel<<<1, 256, 0, s>>>(block_expert, num_padded, sorted_route_ids, R, N, B,
+  launch_pdl(build_tiles_kernel, dim3(1), dim3(256), 0, s, block_expert, num_padded, sorted_route_ids, R, N, B,
                                        (long long)max_rows, tile_rows, tiles, num_tiles, max_tiles, status);
 }
 

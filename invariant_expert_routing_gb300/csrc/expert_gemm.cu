@@ -28,6 +28,7 @@
 #include <cstdint>
 
 #include "gemm.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -121,6 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
                        const __grid_constant__ CUtensorMap x_map,
                        const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  // no early trigger: CTAs of the next kernel would hold SMs idle while they wait
   using C = GemmCfg<kW13, BN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
@@ -435,6 +438,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
                             const __grid_constant__ CUtensorMap x_map,
                             const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  // no early trigger: CTAs of the next kernel would hold SMs idle while they wait
   using C = PairCfg<kW13>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
@@ -711,7 +716,7 @@ void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMa
   if (items <= 0) return;
   const int grid = (int)(items < num_sms ? items : num_sms);
   a.concurrent = grid;
-  kernel<<<grid, kThreads, smem, s>>>(w_map, x_map, x_small, a);
+  launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, w_map, x_map, x_small, a);
 }
 
 // Pairs of CTAs that can be resident at once (one CTA per SM; a pair needs
@@ -760,7 +765,7 @@ void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUten
   const int cap = resident_pairs<kW13>(num_sms);
   const int pairs = (int)(items < cap ? items : cap);
   a.concurrent = pairs;
-  kernel<<<2 * pairs, kThreads, smem, s>>>(w_map, x_map, x_small, a);
+  launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, w_map, x_map, x_small, a);
 }
 
 }  // namespace

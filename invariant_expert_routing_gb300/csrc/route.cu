@@ -20,6 +20,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -137,6 +138,8 @@ template <bool kVec, int LE, int TQ>
 __global__ void __launch_bounds__(kPartWarps * 32) router_partials_kernel(
     const uint16_t* __restrict__ h, const uint16_t* __restrict__ wg, int T, int H, int N,
     float* __restrict__ part) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   constexpr int G = 32 / LE;                 // token groups per warp
   constexpr int TB = kPartWarps * G * TQ;    // tokens per CTA
   extern __shared__ __align__(16) uint16_t psm[];
@@ -196,6 +199,8 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
                                                             int chunks, int k, float* __restrict__ logits,
                                                             int32_t* __restrict__ topk_idx,
                                                             float* __restrict__ gates) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   // one CTA per token, one thread per expert: the chunk sums are loaded eight
   // at a time (independent loads), then added in ascending chunk order
   __shared__ float lrow[256];
@@ -242,6 +247,8 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
 
 __global__ void __launch_bounds__(256) gate_transpose_kernel(const uint16_t* __restrict__ wg,
                                                              uint16_t* __restrict__ wgT, int H, int N) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   __shared__ uint16_t tile[32][33];
   const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += blockDim.y) {
@@ -258,6 +265,8 @@ __global__ void __launch_bounds__(256) gate_transpose_kernel(const uint16_t* __r
 // norm_w[e] >= ||W_g[:, e]||_2 (fp32 sum of squares scaled up to cover its rounding).
 __global__ void __launch_bounds__(256) gate_norm_kernel(const uint16_t* __restrict__ wgT,
                                                         float* __restrict__ norm_w, int H, int N) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (e >= N) return;
@@ -293,6 +302,8 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
     const float* __restrict__ logits_tc, const float* __restrict__ bias, const uint16_t* __restrict__ h,
     const uint16_t* __restrict__ wgT, const float* __restrict__ norm_w, int T, int H, int N, int k,
     float beta, int32_t* __restrict__ topk_idx, float* __restrict__ gates, int32_t* __restrict__ n_cand) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   __shared__ CertSmem sm;
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kCertWarps + wib;
@@ -479,8 +490,8 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
 void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
                       cudaStream_t s) {
   dim3 grid((N + 31) / 32, (H + 31) / 32), block(32, 8);
-  gate_transpose_kernel<<<grid, block, 0, s>>>(w_gate, wgT, H, N);
-  gate_norm_kernel<<<(N + 7) / 8, 256, 0, s>>>(wgT, norm_w, H, N);
+  launch_pdl(gate_transpose_kernel, dim3(grid), dim3(block), 0, s, w_gate, wgT, H, N);
+  launch_pdl(gate_norm_kernel, dim3((N + 7) / 8), dim3(256), 0, s, wgT, norm_w, H, N);
 }
 
 float router_cert_beta(int H) {
@@ -493,7 +504,7 @@ bool route_certified_ok(int H) { return H <= kCertMaxH; }
 void launch_route_certified(const float* logits_tc, const float* bias, const uint16_t* h,
                             const uint16_t* wgT, const float* norm_w, int T, int H, int N, int k,
                             int32_t* topk_idx, float* gates, int32_t* n_cand, cudaStream_t s) {
-  route_certified_kernel<<<(T + kCertWarps - 1) / kCertWarps, kCertWarps * 32, 0, s>>>(
+  launch_pdl(route_certified_kernel, dim3((T + kCertWarps - 1) / kCertWarps), dim3(kCertWarps * 32), 0, s, 
       logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
 }
 
@@ -528,7 +539,7 @@ void launch_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (dev >= 0 && dev < 64) attr_set[dev][vec ? 1 : 0] = true;
   }
-  kernel<<<grid, kPartWarps * 32, smem, s>>>(h, w_gate, T, H, N, part);
+  launch_pdl(kernel, dim3(grid), dim3(kPartWarps * 32), smem, s, h, w_gate, T, H, N, part);
 }
 
 void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
@@ -549,7 +560,7 @@ void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const floa
     if (few) launch_partials<32, 1>(h, w_gate, part, T, H, N, vec, s);
     else launch_partials<32, 4>(h, w_gate, part, T, H, N, vec, s);
   }
-  router_reduce_kernel<<<T, (N + 31) / 32 * 32, 0, s>>>(part, bias, T, N, chunks, k, logits, topk_idx, gates);
+  launch_pdl(router_reduce_kernel, dim3(T), dim3((N + 31) / 32 * 32), 0, s, part, bias, T, N, chunks, k, logits, topk_idx, gates);
 }
 
 }  // namespace moe
