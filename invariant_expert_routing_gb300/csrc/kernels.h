@@ -18,8 +18,8 @@ constexpr int kDispatchTile = 1024;
 // tokens), then logits in the canonical chunked order (optional), top-k and
 // gates (optional: topk_idx null for logits alone).  Used for at most
 // kDecodeRouterMaxT tokens, and for batches unless the tensor-core router
-// serves the call and W_g has more than 2^19 elements or T x H x N > 2^29.
-// part: chunked_router_part_floats floats.
+// serves the call and W_g has more than 2^19 elements.  part:
+// chunked_router_part_floats floats.
 constexpr int kDecodeRouterMaxT = 64;
 bool chunked_router_ok(int T, int H, int N, bool tc_router);
 size_t chunked_router_part_floats(int T, int H, int N);

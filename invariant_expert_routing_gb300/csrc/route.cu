@@ -18,6 +18,8 @@
 // logit's order and nothing depends on T.
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "kernels.h"
 #include "pdl.cuh"
@@ -134,13 +136,14 @@ __device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
-template <bool kVec, int LE, int TQ>
+template <bool kVec, int LE, int TQ, int EQ>
 __global__ void __launch_bounds__(kPartWarps * 32) router_partials_kernel(
     const uint16_t* __restrict__ h, const uint16_t* __restrict__ wg, int T, int H, int N,
     float* __restrict__ part) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   pdl_trigger();
-  constexpr int G = 32 / LE;                 // token groups per warp
+  constexpr int EG = LE / EQ;                // expert groups of EQ per warp row
+  constexpr int G = 32 / EG;                 // token groups per warp
   constexpr int TB = kPartWarps * G * TQ;    // tokens per CTA
   extern __shared__ __align__(16) uint16_t psm[];
   uint16_t* sw = psm;                        // [256][LE] W_g rows of the chunk
@@ -174,23 +177,55 @@ __global__ void __launch_bounds__(kPartWarps * 32) router_partials_kernel(
     }
   }
   __syncthreads();
-  const int el = lane % LE, tg = lane / LE;
+  const int el = (lane % EG) * EQ, tg = lane / EG;
   if (el >= ne) return;
   const int tb = warp * G * TQ + tg;         // this thread's tokens: tb + G * q
-  float p[TQ];
+  float p[TQ][EQ];
 #pragma unroll
-  for (int q = 0; q < TQ; ++q) p[q] = 0.0f;
-#pragma unroll 8
-  for (int i = 0; i < len; ++i) {
-    const float w = __uint_as_float((uint32_t)sw[i * LE + el] << 16);
+  for (int q = 0; q < TQ; ++q)
 #pragma unroll
-    for (int q = 0; q < TQ; ++q)
-      p[q] = fmaf(__uint_as_float((uint32_t)sx[(tb + G * q) * kPartRow + i] << 16), w, p[q]);
+    for (int u = 0; u < EQ; ++u) p[q][u] = 0.0f;
+  // two elements per step (chunk lengths are multiples of 128); each chain
+  // takes element i, then i + 1
+#pragma unroll 4
+  for (int i = 0; i < len; i += 2) {
+    float w0[EQ], w1[EQ];
+    if (EQ == 4) {
+      const uint2 a0 = *reinterpret_cast<const uint2*>(sw + i * LE + el);
+      const uint2 a1 = *reinterpret_cast<const uint2*>(sw + (i + 1) * LE + el);
+      w0[0] = bf16_lo(a0.x);
+      w0[1 % EQ] = bf16_hi(a0.x);
+      w0[2 % EQ] = bf16_lo(a0.y);
+      w0[3 % EQ] = bf16_hi(a0.y);
+      w1[0] = bf16_lo(a1.x);
+      w1[1 % EQ] = bf16_hi(a1.x);
+      w1[2 % EQ] = bf16_lo(a1.y);
+      w1[3 % EQ] = bf16_hi(a1.y);
+    } else {
+#pragma unroll
+      for (int u = 0; u < EQ; ++u) {
+        w0[u] = __uint_as_float((uint32_t)sw[i * LE + el + u] << 16);
+        w1[u] = __uint_as_float((uint32_t)sw[(i + 1) * LE + el + u] << 16);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < TQ; ++q) {
+      const uint32_t hw = *reinterpret_cast<const uint32_t*>(sx + (tb + G * q) * kPartRow + i);
+      const float h0 = bf16_lo(hw), h1 = bf16_hi(hw);
+#pragma unroll
+      for (int u = 0; u < EQ; ++u) {
+        p[q][u] = fmaf(h0, w0[u], p[q][u]);
+        p[q][u] = fmaf(h1, w1[u], p[q][u]);
+      }
+    }
   }
 #pragma unroll
   for (int q = 0; q < TQ; ++q) {
     const int tl = tb + G * q;
-    if (tl < nt) part[((size_t)(t0 + tl) * chunks + c) * N + e0 + el] = p[q];
+    if (tl >= nt) continue;
+#pragma unroll
+    for (int u = 0; u < EQ; ++u)
+      if (el + u < ne) part[((size_t)(t0 + tl) * chunks + c) * N + e0 + el + u] = p[q][u];
   }
 }
 
@@ -509,14 +544,21 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
 }
 
 // The chunked router: for a few tokens always (many CTAs share the weight
-// reads of a decode step); for larger batches unless the certified
-// tensor-core router is available and the batch's T x H x N fused
-// multiply-adds exceed 2^29 (or W_g exceeds 2^19 elements), where the
-// tensor-core path costs less.  Every path gives the same bits.
+// reads of a decode step), and for batches unless the certified tensor-core
+// router is available and W_g has more than 2^19 elements (measured: the
+// Qwen-like router at 4096 / 8192 tokens takes 0.078 / 0.148 ms chunked
+// against 0.110 / 0.178 on the tensor cores; the DeepSeek-like one ties at
+// 4096 tokens and its tensor-core work grows more slowly with T).  Every
+// path gives the same bits.
+// MOE_ROUTER_PATH=tc / chunked forces one path where the tensor-core router
+// can serve the call (read at each call; tests compare the two).
 bool chunked_router_ok(int T, int H, int N, bool tc_router) {
-  if (T <= kDecodeRouterMaxT || !tc_router) return true;
-  const long long hn = (long long)H * N;
-  return hn <= (1ll << 19) && hn * T <= (1ll << 29);
+  if (!tc_router) return true;
+  const char* force = std::getenv("MOE_ROUTER_PATH");
+  if (force && std::strcmp(force, "tc") == 0) return false;
+  if (force && std::strcmp(force, "chunked") == 0) return true;
+  if (T <= kDecodeRouterMaxT) return true;
+  return (long long)H * N <= (1ll << 19);
 }
 
 size_t chunked_router_part_floats(int T, int H, int N) {
@@ -524,14 +566,14 @@ size_t chunked_router_part_floats(int T, int H, int N) {
   return (size_t)T * chunks * N;
 }
 
-template <int LE, int TQ>
+template <int LE, int TQ, int EQ = 1>
 void launch_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int T, int H, int N, bool vec,
                      cudaStream_t s) {
-  constexpr int TB = kPartWarps * (32 / LE) * TQ;
+  constexpr int TB = kPartWarps * (32 / (LE / EQ)) * TQ;
   const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
   const dim3 grid((unsigned)chunks, (unsigned)((N + LE - 1) / LE), (unsigned)((T + TB - 1) / TB));
   const size_t smem = sizeof(uint16_t) * ((size_t)kRouterChunk * LE + (size_t)TB * kPartRow);
-  auto kernel = vec ? router_partials_kernel<true, LE, TQ> : router_partials_kernel<false, LE, TQ>;
+  auto kernel = vec ? router_partials_kernel<true, LE, TQ, EQ> : router_partials_kernel<false, LE, TQ, EQ>;
   static bool attr_set[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -557,8 +599,10 @@ void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const floa
     if (few) launch_partials<16, 1>(h, w_gate, part, T, H, N, vec, s);
     else launch_partials<16, 4>(h, w_gate, part, T, H, N, vec, s);
   } else {
+    // batches: 4 experts x 4 tokens per thread (16 chains; 8-byte weight
+    // loads, token pairs per 4-byte load)
     if (few) launch_partials<32, 1>(h, w_gate, part, T, H, N, vec, s);
-    else launch_partials<32, 4>(h, w_gate, part, T, H, N, vec, s);
+    else launch_partials<32, 4, 4>(h, w_gate, part, T, H, N, vec, s);
   }
   launch_pdl(router_reduce_kernel, dim3(T), dim3((N + 31) / 32 * 32), 0, s, part, bias, T, N, chunks, k, logits, topk_idx, gates);
 }

@@ -17,6 +17,9 @@ pytestmark = pytest.mark.gpu
 
 
 def _route_both(moe, cfg, h_d, wg_d, bias_d, ws):
+    # with logits: the chunked CUDA-core router (every logit in the canonical
+    # order); without: the tensor-core path, forced for any batch size
+    import os
     import torch
     T, N, k = h_d.shape[0], cfg["num_experts"], cfg["top_k"]
     dev = h_d.device
@@ -25,13 +28,21 @@ def _route_both(moe, cfg, h_d, wg_d, bias_d, ws):
         idx = torch.empty((T, k), dtype=torch.int32, device=dev)
         g = torch.empty((T, k), dtype=torch.float32, device=dev)
         lg = torch.empty((T, N), dtype=torch.float32, device=dev) if with_logits else None
-        moe.moe_route(cfg, h_d, wg_d, bias_d, idx, g, lg, ws)
+        old = os.environ.get("MOE_ROUTER_PATH")
+        os.environ["MOE_ROUTER_PATH"] = "chunked" if with_logits else "tc"
+        try:
+            moe.moe_route(cfg, h_d, wg_d, bias_d, idx, g, lg, ws)
+        finally:
+            if old is None:
+                del os.environ["MOE_ROUTER_PATH"]
+            else:
+                os.environ["MOE_ROUTER_PATH"] = old
         out.append((idx, g, lg))
     torch.cuda.synchronize()
     return out
 
 
-@pytest.mark.parametrize("name,T", [("qw", 1), ("qw", 700), ("qw", 8192), ("ds", 5), ("ds", 3000)])
+@pytest.mark.parametrize("name,T", [("qw", 1), ("qw", 65), ("qw", 700), ("qw", 8192), ("ds", 5), ("ds", 3000)])
 def test_tensor_core_router_matches_canonical_router(name, T):
     import torch
     import invariant_expert_routing_gb300 as moe
