@@ -160,9 +160,10 @@ moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h
                              void* ws, size_t ws_bytes, void* stream);
 
 /* Router paths.  With logits_out != NULL, when N is not a multiple of 128,
- * when H > 8192, or for at most 16 tokens, moe_route computes every logit in
- * the canonical order on CUDA cores (one launch with the top-k for at most
- * 16 tokens when H * N <= 65536).
+ * when H > 8192, for at most 64 tokens, or when H * N <= 2^19, moe_route
+ * computes every logit in the canonical order on CUDA cores (the chunked
+ * router: 256-element chunk sums in parallel CTAs, then an in-order reduce
+ * with the top-k; two launches).
  * Otherwise (moe_forward, or moe_route without logits_out, N % 128 == 0) it
  * first computes l_tc = h . W_g on the tensor cores, bounds |l_tc - l| by
  * delta_t = beta(H) * ||h_t|| * max_e ||W_g[:,e]|| (+ bias rounding), keeps
@@ -346,8 +347,9 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
                              void* const* events, int32_t n_events, void* stream);
 
 /* Number of kernel launches one moe_forward of T tokens makes for this
- * configuration (a batch of at most 16 tokens is routed in one launch when
- * H * N <= 65536). */
+ * configuration (the router takes two on CUDA cores or four on the tensor
+ * cores; at most 1024 routes are dispatched and cut into both GEMM tile lists
+ * in one launch). */
 int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T);
 
 /* moe_dispatch_align for callers that cannot allocate device memory (for
