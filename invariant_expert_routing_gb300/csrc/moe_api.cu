@@ -519,39 +519,46 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   moe_status st = MOE_OK;
   bool tiles_ready = false;
   mk.at(0);
-  // the shared expert needs h alone: it runs on a second stream from here
-  // and joins before the combine
+  // the shared expert needs h alone: it runs on a second stream from the end
+  // of routing (the router, latency-bound, keeps the SMs to itself) and
+  // joins before the combine; it overlaps dispatch, the row gather and the
+  // routed GEMMs
   std::unique_lock<std::mutex> side_lock;
   SideStream side;
-  const bool fork = c->shared_intermediate > 0;
-  if (fork) {
+  const bool shared = c->shared_intermediate > 0;
+  bool forked = false;
+  auto fork_shared = [&]() -> moe_status {
+    if (!shared) return MOE_OK;
     side_lock = std::unique_lock<std::mutex>(side_mutex());
     if (!side_stream(&side)) return MOE_ERR_CUDA;
-    if (cudaEventRecord(side.fork, s) != cudaSuccess || cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
+    if (cudaEventRecord(side.fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
       return last_cuda();
-    st = shared_ffn_impl(c, T, h, w13s, w2s, ysh, ws, side.stream);
-    if (st == MOE_OK && cudaEventRecord(side.join, side.stream) != cudaSuccess) st = last_cuda();
-    if (st != MOE_OK) {
-      cudaStreamWaitEvent(s, side.join, 0);   // leave no branch of a capture unjoined
-      return st;
-    }
-  }
+    forked = true;
+    moe_status r = shared_ffn_impl(c, T, h, w13s, w2s, ysh, ws, side.stream);
+    if (cudaEventRecord(side.join, side.stream) != cudaSuccess && r == MOE_OK) r = last_cuda();
+    return r;
+  };
   if (expert_choice(c)) {
     // every logit in the canonical order, then each expert takes its tokens
     moe::launch_router_chunked(h, wg, bias, at<float>(ws, L.rpart), logits, nullptr, nullptr, T, c->hidden,
                                c->num_experts, c->top_k, s);
     mk.at(1);
-    st = expert_choice_impl(c, T, logits, gates, kept, pos, sorted, blocks, num_padded, counts, ws, s);
+    st = fork_shared();
+    if (st == MOE_OK)
+      st = expert_choice_impl(c, T, logits, gates, kept, pos, sorted, blocks, num_padded, counts, ws, s);
   } else if (reroute_active(c, T)) {
     // rerouting ranks every expert of an overflowing token: canonical logits
     st = route_impl(c, T, h, wg, bias, idx, gates, logits, true, ws, s);
     mk.at(1);
+    if (st == MOE_OK) st = fork_shared();
     if (st == MOE_OK)
       st = reroute_impl(c, T, idx, logits, kept, at<int32_t>(ws, L.route_expert), pos, sorted, blocks,
                         num_padded, counts, at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.rerouted), ws, s);
   } else {
     st = route_impl(c, T, h, wg, bias, idx, gates, logits, false, ws, s);
     mk.at(1);
+    if (st == MOE_OK) st = fork_shared();
     // (an error is reported below, after the shared-expert branch has joined)
     if (st == MOE_OK && moe::dispatch_small_ok((long long)T * c->top_k)) {
       // a few routes: dispatch, alignment and both tile lists in one launch
@@ -570,13 +577,13 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
     }
   }
   if (st != MOE_OK) {
-    if (fork) cudaStreamWaitEvent(s, side.join, 0);
+    if (forked) cudaStreamWaitEvent(s, side.join, 0);   // leave no branch of a capture unjoined
     return st;
   }
   mk.at(2);
   st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk, tiles_ready,
-                /*skip_shared=*/fork);
-  if (fork && cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess && st == MOE_OK) st = last_cuda();
+                /*skip_shared=*/shared);
+  if (forked && cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess && st == MOE_OK) st = last_cuda();
   if (st != MOE_OK) return st;
   mk.at(6);
   moe::launch_combine(h, gates, kept, pos, y, ysh, out, T, c->hidden, slots_of(c), max_rows_of(c, T), s);
