@@ -160,10 +160,10 @@ moe_status moe_router_logits(const moe_config* cfg, int32_t T, const uint16_t* h
                              void* ws, size_t ws_bytes, void* stream);
 
 /* Router paths.  With logits_out != NULL, when N is not a multiple of 128,
- * when H > 8192, for at most 64 tokens, or when H * N <= 2^19, moe_route
- * computes every logit in the canonical order on CUDA cores (the chunked
- * router: 256-element chunk sums in parallel CTAs, then an in-order reduce
- * with the top-k; two launches).
+ * when H > 8192, for at most 64 tokens, or when T * H * N <= 3 * 2^28,
+ * moe_route computes every logit in the canonical order on CUDA cores (the
+ * chunked router: 256-element chunk sums in parallel CTAs, then an in-order
+ * reduce with the top-k; two launches).
  * Otherwise (moe_forward, or moe_route without logits_out, N % 128 == 0) it
  * first computes l_tc = h . W_g on the tensor cores, bounds |l_tc - l| by
  * delta_t = beta(H) * ||h_t|| * max_e ||W_g[:,e]|| (+ bias rounding), keeps

@@ -18,7 +18,7 @@ constexpr int kDispatchTile = 1024;
 // tokens), then logits in the canonical chunked order (optional), top-k and
 // gates (optional: topk_idx null for logits alone).  Used for at most
 // kDecodeRouterMaxT tokens, and for batches unless the tensor-core router
-// serves the call and W_g has more than 2^19 elements.  part:
+// serves the call and T * H * N exceeds 3 * 2^28.  part:
 // chunked_router_part_floats floats.
 constexpr int kDecodeRouterMaxT = 64;
 bool chunked_router_ok(int T, int H, int N, bool tc_router);
@@ -31,9 +31,13 @@ void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int 
                       cudaStream_t s);
 float router_cert_beta(int H);
 bool route_certified_ok(int H);
+// filter, tiled recompute of the candidates' chunk sums, finalize (three
+// launches); scratch: route_certified_scratch_floats floats
+size_t route_certified_scratch_floats(int T, int H);
 void launch_route_certified(const float* logits_tc, const float* bias, const uint16_t* h,
                             const uint16_t* wgT, const float* norm_w, int T, int H, int N, int k,
-                            int32_t* topk_idx, float* gates, int32_t* n_cand, cudaStream_t s);
+                            int32_t* topk_idx, float* gates, int32_t* n_cand, float* scratch,
+                            cudaStream_t s);
 
 // ---- dispatch / alignment
 void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,

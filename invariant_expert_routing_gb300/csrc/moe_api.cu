@@ -111,7 +111,8 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.logits = take(sizeof(float) * T * N);
   L.wgT = take(sizeof(uint16_t) * N * H);
   L.norm_w = take(sizeof(float) * N);
-  L.rpart = take(sizeof(float) * moe::chunked_router_part_floats(T, (int)H, (int)N));
+  L.rpart = take(sizeof(float) * std::max(moe::chunked_router_part_floats(T, (int)H, (int)N),
+                                          moe::route_certified_scratch_floats(T, (int)H)));
   L.topk = take(sizeof(int32_t) * R);
   L.gates = take(sizeof(float) * R);
   L.kept = take(R);
@@ -275,7 +276,8 @@ moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const u
     moe::launch_gate_prep(wg, wgT, norm_w, H, N, s);
     const moe_status st = tc_logits(c, T, h, wg, logits, ws, s);
     if (st != MOE_OK) return st;
-    moe::launch_route_certified(logits, bias, h, wgT, norm_w, T, H, N, k, idx, gates, n_cand, s);
+    moe::launch_route_certified(logits, bias, h, wgT, norm_w, T, H, N, k, idx, gates, n_cand,
+                                at<float>(ws, L.rpart), s);
     return last_cuda();
   }
   // the tensor-core path is unavailable: the chunked router serves any batch
@@ -887,7 +889,7 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
   // combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2
   // (chunked router), or on the tensor cores transpose, norms, GEMM,
-  // certified select = 4.
+  // candidate filter, tiled recompute, finalize = 6.
   // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
   // launch that also builds both tile lists; with reroute count, scan,
   // preference lists, deferred acceptance, check, sequential fallback
@@ -896,7 +898,7 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   // selection.
   // chunk sums + reduce/top-k: 2 launches
   const bool chunked = moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg));
-  const int router = chunked ? 2 : (use_tc_router(cfg) ? 4 : 2);
+  const int router = chunked ? 2 : (use_tc_router(cfg) ? 6 : 2);
   int front = 0;
   if (expert_choice(cfg)) {   // logits (chunked router, 2), scores, selection
     front = 2 + 2;

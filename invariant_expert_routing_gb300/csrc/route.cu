@@ -324,6 +324,10 @@ __global__ void __launch_bounds__(256) gate_norm_kernel(const uint16_t* __restri
 constexpr int kCertWarps = 8;
 constexpr int kCertMaxH = 8192;   // rows up to 32 chunks: one chunk per lane at most
 constexpr int kCertPass = 16;     // candidates whose canonical logits one pass evaluates
+constexpr int kCertQ = 32;        // candidates per token handed to the tiled recompute
+constexpr int kCertTT = 32;       // tokens per tile of the tiled recompute
+constexpr int kCertWRows = 48;    // expert rows one pass of the tiled recompute stages
+constexpr int kCertRow = kRouterChunk * 2 + 16;   // 528-byte shared row: 16-byte pieces conflict-free
 
 // One warp per token.  Shared memory per warp: candidate list and canonical
 // values, and the chunk partial sums of one pass of candidates.
@@ -336,7 +340,8 @@ struct CertSmem {
 __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
     const float* __restrict__ logits_tc, const float* __restrict__ bias, const uint16_t* __restrict__ h,
     const uint16_t* __restrict__ wgT, const float* __restrict__ norm_w, int T, int H, int N, int k,
-    float beta, int32_t* __restrict__ topk_idx, float* __restrict__ gates, int32_t* __restrict__ n_cand) {
+    float beta, int32_t* __restrict__ topk_idx, float* __restrict__ gates, int32_t* __restrict__ n_cand,
+    int32_t* __restrict__ cand, int32_t* __restrict__ ccount) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   pdl_trigger();
   __shared__ CertSmem sm;
@@ -418,12 +423,20 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
   int nc = 0;
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    const bool cand = ((present >> s) & 1u) && (!finite || v[s] >= cut);
-    const unsigned m = __ballot_sync(full, cand);
-    if (cand) sm.cidx[wib][nc + __popc(m & ((1u << lane) - 1u))] = lane + 32 * s;
+    const bool is_cand = ((present >> s) & 1u) && (!finite || v[s] >= cut);
+    const unsigned m = __ballot_sync(full, is_cand);
+    if (is_cand) sm.cidx[wib][nc + __popc(m & ((1u << lane) - 1u))] = lane + 32 * s;
     nc += __popc(m);
   }
   __syncwarp();
+  if (n_cand && lane == 0) n_cand[t] = nc;
+  if (nc <= kCertQ) {
+    // the usual case: the tiled kernels finish this token
+    if (lane < nc) cand[(size_t)t * kCertQ + lane] = sm.cidx[wib][lane];
+    if (lane == 0) ccount[t] = nc;
+    return;
+  }
+  if (lane == 0) ccount[t] = -1;   // finished here
   // canonical logits of the candidates.  Lane (chunk c, group g): c = lane %
   // C, g = lane / C, G = 32 / C groups; it sums chunk c from +0 in ascending
   // index with fma for the pass's candidates q = g, g+G, ... (four at a time,
@@ -517,7 +530,186 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
     if (bq >= 0 && (bq & 31) == lane) taken |= 1u << (bq >> 5);
   }
   write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
-  if (n_cand && lane == 0) n_cand[t] = nc;
+}
+
+// Tiled recompute of the candidates' chunk sums.  One CTA per (chunk c,
+// tile of kCertTT tokens): the tile's h slices and the chunk-c slices of
+// the union of its tokens' candidate experts are staged in shared memory,
+// each row copied by one warp in coalesced 16-byte pieces (an expert slice serves every token of the tile that has it as a
+// candidate); then each (token, candidate) pair is summed by one thread from
+// +0 in ascending index with fma.  Pairs are bucketed by expert so that a
+// pass over kCertWRows staged experts covers a contiguous run of pairs.
+// part[(t * C + c) * kCertQ + q] receives the chunk sum.
+__global__ void __launch_bounds__(256, 3) cert_chunk_kernel(
+    const uint16_t* __restrict__ h, const uint16_t* __restrict__ wgT, const int32_t* __restrict__ cand,
+    const int32_t* __restrict__ ccount, int T, int H, float* __restrict__ part) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t csm[];
+  uint8_t* s_h = csm;                          // [kCertTT][kCertRow]
+  uint8_t* s_w = csm + kCertTT * kCertRow;     // [kCertWRows][kCertRow]
+  __shared__ int s_cand[kCertTT * kCertQ];     // the tile's candidate lists
+  __shared__ int s_pair[kCertTT * kCertQ];     // union position << 10 | token << 5 | slot, by expert
+  __shared__ int s_pos[256];                   // expert -> union position
+  __shared__ int s_uexp[256];                  // union position -> expert
+  __shared__ int s_ubeg[257];                  // union position -> first pair
+  __shared__ int s_ucur[256];
+  __shared__ int s_cnt[kCertTT];
+  __shared__ int s_nu;
+  const int C = (H + kRouterChunk - 1) / kRouterChunk;
+  const int c = blockIdx.x, t0 = blockIdx.y * kCertTT;
+  const int i0 = c * kRouterChunk, len = min(H - i0, kRouterChunk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nt = min(kCertTT, T - t0);
+  const bool piece = lane * 8 < len;   // this lane's 16-byte piece of a slice (len % 128 == 0)
+  if (piece)
+    for (int r = warp; r < nt; r += 8)
+      cp_async_16(s_h + r * kCertRow + 16 * lane, h + (size_t)(t0 + r) * H + i0 + 8 * lane);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int e = tid; e < 256; e += blockDim.x) s_ucur[e] = 0;
+  if (tid < kCertTT) s_cnt[tid] = tid < nt ? max(ccount[t0 + tid], 0) : 0;   // -1: finished by the filter
+  __syncthreads();
+  for (int p = tid; p < kCertTT * kCertQ; p += blockDim.x) {
+    const int r = p / kCertQ, q = p % kCertQ;
+    if (q < s_cnt[r]) {
+      const int e = cand[(size_t)(t0 + r) * kCertQ + q];
+      s_cand[p] = e;
+      atomicAdd(&s_ucur[e], 1);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // union positions in ascending expert order and each expert's first pair
+    // (lane l handles experts 8l .. 8l+7)
+    int pc[8], flag = 0, pairs = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      pc[j] = s_ucur[lane * 8 + j];
+      flag += pc[j] > 0;
+      pairs += pc[j];
+    }
+    int fi = flag, pi = pairs;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int fo = __shfl_up_sync(0xffffffffu, fi, off), po = __shfl_up_sync(0xffffffffu, pi, off);
+      if (lane >= off) {
+        fi += fo;
+        pi += po;
+      }
+    }
+    int u = fi - flag, pb = pi - pairs;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      if (pc[j] > 0) {
+        s_uexp[u] = e;
+        s_ubeg[u] = pb;
+        s_pos[e] = u;
+        ++u;
+        pb += pc[j];
+      }
+      s_ucur[e] = 0;
+    }
+    if (lane == 31) {
+      s_nu = fi;
+      s_ubeg[fi] = pi;
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p < kCertTT * kCertQ; p += blockDim.x) {
+    const int r = p / kCertQ, q = p % kCertQ;
+    if (q < s_cnt[r]) {
+      const int u = s_pos[s_cand[p]];
+      s_pair[s_ubeg[u] + atomicAdd(&s_ucur[u], 1)] = (u << 10) | (r << 5) | q;
+    }
+  }
+  const int nu = s_nu;
+  for (int u0 = 0; u0 < nu; u0 += kCertWRows) {
+    const int nb = min(kCertWRows, nu - u0);
+    __syncthreads();   // the pair list is complete / the previous pass is done with s_w
+    if (piece)
+      for (int r = warp; r < nb; r += 8)
+        cp_async_16(s_w + r * kCertRow + 16 * lane, wgT + (size_t)s_uexp[u0 + r] * H + i0 + 8 * lane);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int pend = s_ubeg[u0 + nb];
+    for (int pi = s_ubeg[u0] + tid; pi < pend; pi += blockDim.x) {
+      const int pr = s_pair[pi];
+      const int r = (pr >> 5) & 31, q = pr & 31;
+      const uint8_t* hr = s_h + r * kCertRow;
+      const uint8_t* wr = s_w + ((pr >> 10) - u0) * kCertRow;
+      float acc = 0.0f;
+#pragma unroll 4
+      for (int i = 0; i < len; i += 8) {
+        const uint4 hv = *reinterpret_cast<const uint4*>(hr + 2 * i);
+        const uint4 wv = *reinterpret_cast<const uint4*>(wr + 2 * i);
+        acc = fmaf(bf16_lo(hv.x), bf16_lo(wv.x), acc);
+        acc = fmaf(bf16_hi(hv.x), bf16_hi(wv.x), acc);
+        acc = fmaf(bf16_lo(hv.y), bf16_lo(wv.y), acc);
+        acc = fmaf(bf16_hi(hv.y), bf16_hi(wv.y), acc);
+        acc = fmaf(bf16_lo(hv.z), bf16_lo(wv.z), acc);
+        acc = fmaf(bf16_hi(hv.z), bf16_hi(wv.z), acc);
+        acc = fmaf(bf16_lo(hv.w), bf16_lo(wv.w), acc);
+        acc = fmaf(bf16_hi(hv.w), bf16_hi(wv.w), acc);
+      }
+      part[((size_t)(t0 + r) * C + c) * kCertQ + q] = acc;
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");   // a tile without pairs
+}
+
+// Canonical logits of the candidates (chunk sums added to +0 in ascending
+// chunk order, then the bias), then top-k and gates: one warp per token,
+// lane q holds candidate q.  Tokens the filter finished are skipped.
+__global__ void __launch_bounds__(256) cert_finalize_kernel(
+    const float* __restrict__ part, const int32_t* __restrict__ cand, const int32_t* __restrict__ ccount,
+    const float* __restrict__ bias, int T, int C, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gates) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int nc = ccount[t];
+  if (nc < 0) return;
+  const bool mine = lane < nc;
+  int e = -1;
+  float cv = 0.0f;
+  if (mine) {
+    e = cand[(size_t)t * kCertQ + lane];
+    const float* pp = part + (size_t)t * C * kCertQ + lane;
+    float total = 0.0f;
+    for (int c0 = 0; c0 < C; c0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < C ? pp[(size_t)(c0 + j) * kCertQ] : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < C) total = total + v[j];
+    }
+    cv = bias ? total + bias[e] : total;
+  }
+  int sel[16];
+  float selv[16];
+  bool taken = false;
+  for (int j = 0; j < k; ++j) {
+    float bv = cv;
+    int bi = (mine && !taken) ? e : -1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(full, bv, off);
+      const int oi = __shfl_xor_sync(full, bi, off);
+      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    sel[j] = bi;
+    selv[j] = bv;
+    if (mine && bi == e) taken = true;
+  }
+  write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
 }
 
 }  // namespace
@@ -536,29 +728,54 @@ float router_cert_beta(int H) {
 
 bool route_certified_ok(int H) { return H <= kCertMaxH; }
 
+size_t route_certified_scratch_floats(int T, int H) {
+  const size_t C = (size_t)(H + kRouterChunk - 1) / kRouterChunk;
+  return (size_t)T * C * kCertQ + (size_t)T * kCertQ + (size_t)T;
+}
+
 void launch_route_certified(const float* logits_tc, const float* bias, const uint16_t* h,
                             const uint16_t* wgT, const float* norm_w, int T, int H, int N, int k,
-                            int32_t* topk_idx, float* gates, int32_t* n_cand, cudaStream_t s) {
-  launch_pdl(route_certified_kernel, dim3((T + kCertWarps - 1) / kCertWarps), dim3(kCertWarps * 32), 0, s, 
-      logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand);
+                            int32_t* topk_idx, float* gates, int32_t* n_cand, float* scratch,
+                            cudaStream_t s) {
+  const int C = (H + kRouterChunk - 1) / kRouterChunk;
+  float* part = scratch;
+  int32_t* cand = reinterpret_cast<int32_t*>(scratch + (size_t)T * C * kCertQ);
+  int32_t* ccount = cand + (size_t)T * kCertQ;
+  launch_pdl(route_certified_kernel, dim3((T + kCertWarps - 1) / kCertWarps), dim3(kCertWarps * 32), 0, s,
+             logits_tc, bias, h, wgT, norm_w, T, H, N, k, router_cert_beta(H), topk_idx, gates, n_cand, cand,
+             ccount);
+  const size_t smem = (size_t)(kCertTT + kCertWRows) * kCertRow;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaFuncSetAttribute(cert_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  launch_pdl(cert_chunk_kernel, dim3(C, (T + kCertTT - 1) / kCertTT), dim3(256), smem, s, h, wgT,
+             (const int32_t*)cand, (const int32_t*)ccount, T, H, part);
+  launch_pdl(cert_finalize_kernel, dim3((T + 7) / 8), dim3(256), 0, s, (const float*)part,
+             (const int32_t*)cand, (const int32_t*)ccount, bias, T, C, k, topk_idx, gates);
 }
 
 // The chunked router: for a few tokens always (many CTAs share the weight
-// reads of a decode step), and for batches unless the certified tensor-core
-// router is available and W_g has more than 2^19 elements (measured: the
-// Qwen-like router at 4096 / 8192 tokens takes 0.078 / 0.148 ms chunked
-// against 0.110 / 0.178 on the tensor cores; the DeepSeek-like one ties at
-// 4096 tokens and its tensor-core work grows more slowly with T).  Every
-// path gives the same bits.
+// reads of a decode step), and for batches whose router work T * H * N is
+// at most 3 * 2^28 multiply-adds; above that the certified tensor-core
+// router, whose cost grows with T * H (measured crossings: the Qwen-like
+// router near T = 2800, 0.053 ms either way at 2048 and 0.089 chunked
+// against 0.071 at 4096; the DeepSeek-like one near T = 600, 0.132 against
+// 0.099 at 1024).  Every path gives the same bits.
 // MOE_ROUTER_PATH=tc / chunked forces one path where the tensor-core router
 // can serve the call (read at each call; tests compare the two).
+constexpr long long kChunkedRouterMaxWork = 3ll << 28;
+
 bool chunked_router_ok(int T, int H, int N, bool tc_router) {
   if (!tc_router) return true;
   const char* force = std::getenv("MOE_ROUTER_PATH");
   if (force && std::strcmp(force, "tc") == 0) return false;
   if (force && std::strcmp(force, "chunked") == 0) return true;
   if (T <= kDecodeRouterMaxT) return true;
-  return (long long)H * N <= (1ll << 19);
+  return (long long)T * H * N <= kChunkedRouterMaxWork;
 }
 
 size_t chunked_router_part_floats(int T, int H, int N) {

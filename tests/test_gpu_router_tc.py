@@ -94,3 +94,44 @@ def test_adversarial_near_identical_experts():
     assert torch.equal(i_c, i_t)
     assert torch.equal(g_c.view(torch.int32), g_t.view(torch.int32))
     assert (i_t[:4].cpu().numpy() == np.arange(k)).all()   # exact ties: lowest indices
+
+
+def test_candidate_tiles_mix_recompute_paths():
+    # Tiles of 32 tokens where some tokens have a handful of candidates, some
+    # between 17 and 32 (24 near-identical experts aligned with the token),
+    # and some every expert (h = 0: exact ties, finished by the filter warp),
+    # H with a 128-element last chunk, a ragged last tile, and random tokens
+    # whose candidate union fills more than one staging pass.
+    import torch
+    import invariant_expert_routing_gb300 as moe
+    from tests.gpu_util import dev_bf16
+    H, N, k, T = 1152, 256, 8, 200
+    cfg = dict(hidden=H, num_experts=N, top_k=k, intermediate=128, block_size=16)
+    rng = np.random.default_rng(11)
+    base = (rng.standard_normal(H) / np.sqrt(H)).astype(np.float32)
+    wg = (0.3 * rng.standard_normal((H, N)) / np.sqrt(H)).astype(np.float32)
+    near = rng.choice(N, 24, replace=False)
+    for e in near:
+        wg[:, e] = base
+        wg[rng.integers(H), e] *= np.float32(1.0 + 2.0 ** -7)
+    h = rng.standard_normal((T, H)).astype(np.float32)
+    h[0::4] = 8.0 * base + 0.01 * rng.standard_normal((len(range(0, T, 4)), H)).astype(np.float32)
+    h[6::16] = 0.0
+    h_b, wg_b = f32_to_bf16(h), f32_to_bf16(wg)
+    h_d, wg_d = dev_bf16(h_b), dev_bf16(wg_b)
+    ws = moe.workspace(cfg, T)
+    moe.moe_clear_device_status(ws)
+    (i_c, g_c, _), (i_t, g_t, _) = _route_both(moe, cfg, h_d, wg_d, None, ws)
+    assert torch.equal(i_c, i_t)
+    assert torch.equal(g_c.view(torch.int32), g_t.view(torch.int32))
+    idx = torch.empty((T, k), dtype=torch.int32, device=h_d.device)
+    g = torch.empty((T, k), dtype=torch.float32, device=h_d.device)
+    nc = torch.empty(T, dtype=torch.int32, device=h_d.device)
+    moe.moe_route_filtered(cfg, h_d, wg_d, None, idx, g, nc, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(idx, i_c)
+    n = nc.cpu().numpy()
+    assert (n[6::16] == N).all()                   # every expert: the filter warp finishes
+    assert ((n > 16) & (n <= 32)).any()            # the tiled recompute with many candidates
+    assert (n <= 12).sum() >= T // 4 and n.min() >= k   # and the usual few candidates
