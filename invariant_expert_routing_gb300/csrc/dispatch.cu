@@ -257,6 +257,44 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
 }
 
+// The same x_perm token by token: warp per token, h[t] read once from DRAM
+// and copied (from L1) to the padded row route_pos[t k + j] of each kept
+// slot; then zeros in the padding rows.  When h is larger than L2 the
+// segment-order gather fetches a token's row once per slot.
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __restrict__ h,
+                                                           const int32_t* __restrict__ route_pos,
+                                                           const int32_t* __restrict__ sorted_route_ids,
+                                                           const int32_t* __restrict__ num_padded, int k,
+                                                           int T, int H, long long max_rows,
+                                                           uint16_t* __restrict__ x_perm) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  // no early trigger: the next kernel is a GEMM
+  const long long P = min((long long)*num_padded, max_rows);
+  const long long R = (long long)T * k;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int chunks = H / 8;
+  for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < T + P;
+       item += warps) {
+    if (item < T) {
+      const uint4* src = reinterpret_cast<const uint4*>(h + (size_t)item * H);
+      for (int j = 0; j < k; ++j) {
+        const long long p = route_pos[item * k + j];
+        if (p < 0 || p >= P) continue;   // dropped
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + p * H);
+        for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+      }
+    } else {
+      const long long row = item - T;
+      const int r = sorted_route_ids[row];
+      if (r < 0 || r >= R) {
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + row * H);
+        for (int c = lane; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+}
+
 // Dispatch, alignment and both GEMM tile lists of a batch of at most 1024
 // routes in one CTA (decode): the same integers as dispatch_count, _scan,
 // _scatter and build_tiles (ranks by warp match, per-warp counts added in
@@ -413,6 +451,19 @@ void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, cons
   const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
   launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, h, sorted_route_ids, num_padded, k, R, H, (long long)max_rows,
                                           x_perm);
+}
+
+void launch_scatter_rows(const uint16_t* h, const int32_t* route_pos, const int32_t* sorted_route_ids,
+                         const int32_t* num_padded, int k, int T, int H, int64_t max_rows, uint16_t* x_perm,
+                         cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = ((long long)T + max_rows + 7) / 8;
+  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
+  const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+  launch_pdl(scatter_rows_kernel, dim3(grid), dim3(256), 0, s, h, route_pos, sorted_route_ids, num_padded, k, T,
+             H, (long long)max_rows, x_perm);
 }
 
 void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,

@@ -105,6 +105,11 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
                            int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s);
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
+// the same x_perm from the inverse map (route_pos: padded row of each route,
+// -1 dropped): each token row read once
+void launch_scatter_rows(const uint16_t* h, const int32_t* route_pos, const int32_t* sorted_route_ids,
+                         const int32_t* num_padded, int k, int T, int H, int64_t max_rows, uint16_t* x_perm,
+                         cudaStream_t s);
 // Tile list of one GEMM: tile_rows-row tiles over each expert's padded
 // segment; a tile's valid rows end at the segment's last route (sorted ids
 // in [0, R)).

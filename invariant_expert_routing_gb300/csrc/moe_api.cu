@@ -8,6 +8,8 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -327,12 +329,25 @@ moe_status expert_choice_impl(const moe_config* c, int32_t T, const float* logit
   return last_cuda();
 }
 
+// x_perm token by token (each h row read once) when h exceeds 48 MB: the
+// segment-order gather fetches a row once per slot, from DRAM when h does
+// not stay in L2 (measured on the DeepSeek-like layer, whose row copy shares
+// the SMs with the shared expert: 4.488 -> 4.452 ms at T = 4096, 11.92 ->
+// 11.87 ms at T = 16448; no change at 33 MB).  MOE_ROW_COPY=gather /
+// scatter forces one (read at each call; both write the same rows).
+bool scatter_rows_ok(int T, int H) {
+  const char* force = std::getenv("MOE_ROW_COPY");
+  if (force && std::strcmp(force, "gather") == 0) return false;
+  if (force && std::strcmp(force, "scatter") == 0) return true;
+  return (long long)T * H * 2 > (48ll << 20);
+}
+
 struct Marks;
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
                     void* ws, cudaStream_t s, const Marks* mk = nullptr, bool tiles_ready = false,
-                    bool skip_shared = false);
+                    bool skip_shared = false, const int32_t* route_pos = nullptr);
 void mark(const Marks* mk, int i);
 
 // The shared expert (identity mode over h; every token, no routing): W13 then
@@ -384,7 +399,8 @@ moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, co
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
-                    void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready, bool skip_shared) {
+                    void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready, bool skip_shared,
+                    const int32_t* route_pos) {
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = slots_of(c);
   const int64_t rows = max_rows_of(c, T);
@@ -406,7 +422,10 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
     moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, moe::kW2TileRows,
                             tiles2, ntiles2, max_tiles2, status, s);
   }
-  moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
+  if (route_pos && scatter_rows_ok(T, H))
+    moe::launch_scatter_rows(h, route_pos, sorted, num_padded, k, T, H, rows, x_perm, s);
+  else
+    moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
   mark(mk, 3);
 
   // CTA-pair kernels where the output features are a multiple of 256 (a
@@ -584,7 +603,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   }
   mk.at(2);
   st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk, tiles_ready,
-                /*skip_shared=*/shared);
+                /*skip_shared=*/shared, pos);
   if (forked && cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess && st == MOE_OK) st = last_cuda();
   if (st != MOE_OK) return st;
   mk.at(6);
