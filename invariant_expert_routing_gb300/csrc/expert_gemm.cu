@@ -403,20 +403,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kPairRows = 256;      // token rows per pair tile (the MMA's N)
 constexpr int kPairM = 256;         // weight rows per pair (the MMA's M)
 
-template <bool kW13>
+// kWide (W2 with a long reduction): a work item covers two 256-feature
+// groups, two pair MMAs per K step on the same token tile (each the same
+// M = 256 x N MMA as one plain item, so the same bits).  Per CTA 48 KB of
+// operands per K step for twice the flops: tensor-bound where the plain
+// item is bound by the operand bytes an SM takes in; its single
+// 512-column accumulator costs the overlap of the epilogue, a few per cent
+// of a 14336-deep reduction.
+template <bool kW13, bool kWide = false>
 struct PairCfg {
+  static_assert(!(kW13 && kWide), "wide items are W2 only");
+  static constexpr int kGroups = kWide ? 2 : 1;              // 256-feature groups per item
   static constexpr int kRowsCta = kPairRows / 2;
-  static constexpr int kFeatCta = kW13 ? 64 : 128;           // output features per CTA
-  static constexpr int kFeatTile = 2 * kFeatCta;             // output features per pair tile
-  static constexpr uint32_t kABytes = 2 * kBoxBytes;         // 128 weight rows x 64 K
+  static constexpr int kFeatCta = kW13 ? 64 : 128;           // output features per CTA and group
+  static constexpr int kFeatTile = 2 * kFeatCta * kGroups;   // output features per pair tile
+  static constexpr uint32_t kABytes = 2 * kBoxBytes * kGroups;   // 128 weight rows x 64 K per group
   static constexpr uint32_t kBTileBytes = kRowsCta * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
   // W2 fits a seventh 32 KB stage in the 227 KB of shared memory; W13 needs
   // 16 KB for the u exchange
   static constexpr uint32_t kPairBudget = kW13 ? kStageBudget : 224 * 1024;
   static constexpr int kStages = (int)(kPairBudget / kStageBytes) < 7 ? (int)(kPairBudget / kStageBytes) : 7;
-  static constexpr uint32_t kAccCols = kPairRows;
-  static constexpr int kNumAcc = 2;
+  static constexpr uint32_t kAccCols = kPairRows * kGroups;
+  static constexpr int kNumAcc = kWide ? 1 : 2;
   static constexpr uint32_t kTmemCols = 512;
   // W13: u handed from the up warps to the gate warps, 4 warp pairs x 2
   // buffers x 32 lanes x 16 fp32
@@ -433,14 +442,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-template <bool kW13>
+template <bool kW13, bool kWide = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
                             const __grid_constant__ CUtensorMap x_map,
                             const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   // no early trigger: CTAs of the next kernel would hold SMs idle while they wait
-  using C = PairCfg<kW13>;
+  using C = PairCfg<kW13, kWide>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
@@ -506,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
       const int wrow0 = t.expert * args.w_rows_per_e;
-      const int fcol = wk.f * C::kFeatTile + (int)rank * C::kFeatCta;   // this CTA's features
+      const int fcol = wk.f * C::kFeatTile + (int)rank * C::kFeatCta;   // this CTA's features (group 0)
       // tiles with at most kSmallRows routed rows (decode): a kSmallRows-row
       // token box per CTA and N = 2 kSmallRows MMAs; the odd CTA's rows are
       // padding or beyond the tile, in columns that are never stored
@@ -532,6 +541,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int c_hi = kW13 ? args.up_col + fcol : fcol + 64;
           tma_load_2d_pair(smem_u32(sA), &w_map, fcol, wrow0 + k0, fb, pol_w);
           tma_load_2d_pair(smem_u32(sA + kBoxBytes), &w_map, c_hi, wrow0 + k0, fb, pol_w);
+          if (kWide) {   // group 1: the next 256 features of the item
+            tma_load_2d_pair(smem_u32(sA + 2 * kBoxBytes), &w_map, fcol + 256, wrow0 + k0, fb, pol_w);
+            tma_load_2d_pair(smem_u32(sA + 3 * kBoxBytes), &w_map, fcol + 256 + 64, wrow0 + k0, fb, pol_w);
+          }
           tma_load_2d_pair(smem_u32(sB), small ? &x_map_small : &x_map, k0, brow0, fb, pol_x);
         }
         __syncwarp();
@@ -598,6 +611,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
             const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
             mma_bf16_pair(d0, adesc, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            if (kWide) {
+              const uint64_t adesc1 = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+              mma_bf16_pair(d0 + kPairRows, adesc1, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == C::kStages) {
@@ -647,8 +664,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
-      const int feat = wk.f * C::kFeatTile + (int)rank * C::kFeatCta + (kW13 ? (quarter & 1) * 32 : quarter * 32) + lane;
+      for (int grp = 0; grp < C::kGroups; ++grp) {
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols + grp * kPairRows;
+      const int feat = wk.f * C::kFeatTile + grp * 256 + (int)rank * C::kFeatCta +
+                       (kW13 ? (quarter & 1) * 32 : quarter * 32) + lane;
       for (int c = col0; c < col1 && c < t.valid; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
@@ -683,6 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }   // groups
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
@@ -721,7 +741,7 @@ void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMa
 
 // Pairs of CTAs that can be resident at once (one CTA per SM; a pair needs
 // two SMs of one GPC), looked up once per device and kernel.
-template <bool kW13>
+template <bool kW13, bool kWide = false>
 int resident_pairs(int num_sms) {
   static int cache[64] = {0};
   int dev = 0;
@@ -731,7 +751,7 @@ int resident_pairs(int num_sms) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<kW13>::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<kW13, kWide>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -739,7 +759,7 @@ int resident_pairs(int num_sms) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13, kWide>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
   }
@@ -748,11 +768,11 @@ int resident_pairs(int num_sms) {
   return n;
 }
 
-template <bool kW13>
+template <bool kW13, bool kWide = false>
 void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small, GemmArgs a,
                  int max_tiles, int num_sms, cudaStream_t s) {
-  auto kernel = expert_gemm_pair_kernel<kW13>;
-  const int smem = (int)PairCfg<kW13>::kSmemBytes;
+  auto kernel = expert_gemm_pair_kernel<kW13, kWide>;
+  const int smem = (int)PairCfg<kW13, kWide>::kSmemBytes;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -762,7 +782,7 @@ void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUten
   }
   const long long items = (long long)max_tiles * a.n_feat_tiles;
   if (items <= 0) return;
-  const int cap = resident_pairs<kW13>(num_sms);
+  const int cap = resident_pairs<kW13, kWide>(num_sms);
   const int pairs = (int)(items < cap ? items : cap);
   a.concurrent = pairs;
   launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, w_map, x_map, x_small, a);
@@ -777,7 +797,8 @@ bool gemm_smem_ok() {
   return optin >= (int)GemmCfg<true, kW13TileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kW2TileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes &&
-         optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes;
+         optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes &&
+         optin >= (int)PairCfg<false, true>::kSmemBytes;
 }
 
 bool gemm_pair_ok(bool w13, int features, int K) {
@@ -785,6 +806,10 @@ bool gemm_pair_ok(bool w13, int features, int K) {
   // W13 pairs carry half the features per CTA of the one-CTA kernel: with a
   // short reduction (K < 4096) the one-CTA kernel measured faster
   return !w13 || K >= 4096;
+}
+
+bool gemm_wide_ok(int features, int K) {
+  return features % PairCfg<false, true>::kFeatTile == 0 && K >= kWideMinK;
 }
 
 void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
@@ -797,7 +822,9 @@ void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const C
 
 void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
-  if (a.pair)
+  if (a.pair && a.wide)
+    launch_pair<false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  else if (a.pair)
     launch_pair<false>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else
     launch<false, kW2TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);

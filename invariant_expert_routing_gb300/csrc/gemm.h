@@ -51,6 +51,8 @@ struct GemmArgs {
   int concurrent;      // work units resident at once (set by the launcher)
   int pair;            // 1: CTA-pair kernel (256 token rows per tile, token maps with
                        //    128-row boxes; n_feat_tiles in units of kPairFeatW13 / kPairFeatW2)
+  int wide;            // W2 pairs only, 1: items of two 256-feature groups
+                       //    (n_feat_tiles in units of kPairFeatW2Wide)
 };
 
 // Rows of a CTA-pair token tile, the token box each CTA of the pair loads,
@@ -62,6 +64,11 @@ constexpr int kPairFeatW2 = 256;
 // Whether a GEMM with this many output features and reduction length K runs
 // on CTA pairs: a property of the layer's shape, never of T.
 bool gemm_pair_ok(bool w13, int features, int K);
+// Whether the W2 pairs take wide items (two 256-feature groups on one token
+// tile): a long reduction and 512 | features, a property of the layer.
+constexpr int kPairFeatW2Wide = 512;
+constexpr int kWideMinK = 8192;
+bool gemm_wide_ok(int features, int K);
 
 bool gemm_smem_ok();
 // x_small: the same token tensor with a 32-row box (tiles with <= 32 rows)

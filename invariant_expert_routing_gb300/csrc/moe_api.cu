@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -456,9 +457,15 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, pair13 ? max_tiles2 : max_tiles13, sms, s);
   mark(mk, 4);
 
+  // wide W2 items (two 256-feature groups per token tile, the same MMAs)
+  // where the layer has a long reduction and the batch touches enough
+  // experts to keep a quarter of the SMs busy with them (at T = 1 the
+  // Mixtral-like W2 took 0.196 ms with them against 0.167 without)
+  const long long touched = std::min<long long>(N, (long long)T * k);
+  const bool wide2 = pair2 && moe::gemm_wide_ok(H, I) && touched * (H / moe::kPairFeatW2Wide) * 4 >= sms;
   moe::GemmArgs g2 = g13;
   g2.K = I;
-  g2.n_feat_tiles = pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat;
+  g2.n_feat_tiles = wide2 ? H / moe::kPairFeatW2Wide : (pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat);
   g2.w_rows_per_e = I;
   g2.up_col = 0;
   g2.tiles = tiles2;
@@ -466,6 +473,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.out = y_perm;
   g2.out_ld = H;
   g2.pair = pair2 ? 1 : 0;
+  g2.wide = wide2 ? 1 : 0;
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
