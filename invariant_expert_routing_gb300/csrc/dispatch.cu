@@ -15,8 +15,12 @@
 // every launch shape gives the same bits.
 #include <cstdint>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "kernels.h"
 #include "pdl.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -326,16 +330,15 @@ __device__ int warp_scan_experts(const int* v, int* out, int N, int lane) {
   return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-__global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
-    const int32_t* __restrict__ topk_idx, int R, int N, int B, int capacity,
-    uint8_t* __restrict__ route_kept, int32_t* __restrict__ route_pos,
-    int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
-    int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts,
-    int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
-    int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
-    int max_b, int* status) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  pdl_trigger();
+// The body: one CTA of at least R threads (full warps), thread r handles
+// route r.  topk_idx is read with plain loads (the decode front writes it in
+// the same kernel).
+__device__ __forceinline__ void dispatch_small_block(
+    const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* __restrict__ route_kept,
+    int32_t* route_pos, int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
+    int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_dropped,
+    GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a, int rows_a, int max_a,
+    GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b, int max_b, int* status) {
   __shared__ int wc[32][kMaxN + 1];
   __shared__ int kept_s[kMaxN], pad_s[kMaxN], drop_s[kMaxN], nta[kMaxN], ntb[kMaxN];
   __shared__ int seg[kMaxN], offa[kMaxN], offb[kMaxN];
@@ -439,6 +442,69 @@ __global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
   }
 }
 
+__global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
+    const int32_t* __restrict__ topk_idx, int R, int N, int B, int capacity,
+    uint8_t* __restrict__ route_kept, int32_t* __restrict__ route_pos,
+    int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
+    int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts,
+    int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
+    int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
+    int max_b, int* status) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
+  dispatch_small_block(topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
+                       num_padded, expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b,
+                       ntiles_b, rows_b, max_b, status);
+}
+
+// ------------------------------------------------------------------------
+// Decode finish: for a few tokens, everything between the router's chunk sums
+// and the W13 GEMM in one CTA: the logits (chunk sums added in ascending
+// chunk order, then the bias, exactly as router_reduce_kernel), the same
+// top-k and gates, the same dispatch body with both tile lists, and the
+// routed token rows of x_perm.
+constexpr int kFinishThreads = 512;
+constexpr int kFinishMaxT = 2;
+
+__global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
+    const float* __restrict__ part, const uint16_t* __restrict__ h, const float* __restrict__ bias, int T, int H,
+    int N, int k, int B, int capacity, int32_t* topk_idx, float* __restrict__ gates,
+    uint8_t* __restrict__ route_kept, int32_t* route_pos, int32_t* __restrict__ sorted_route_ids,
+    int32_t* __restrict__ block_expert, int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts,
+    int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
+    int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
+    int max_b, uint16_t* __restrict__ x_perm, long long max_rows, int* status) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  // no early trigger: the next kernel is a GEMM
+  __shared__ float lrow[kFinishMaxT][kMaxN];
+  const int C = (H + kRouterChunk - 1) / kRouterChunk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int x = tid; x < T * N; x += blockDim.x) {
+    const int t = x / N, e = x % N;
+    const float* pe = part + (size_t)t * C * N + e;
+    float total = 0.0f;
+    for (int c = 0; c < C; ++c) total = total + pe[(size_t)c * N];
+    if (bias) total = total + bias[e];
+    lrow[t][e] = total;
+  }
+  __syncthreads();
+  if (warp < T) sel::topk_select_warp(lrow[warp], N, k, lane, topk_idx + (size_t)warp * k, gates + (size_t)warp * k);
+  __syncthreads();
+  const int R = T * k;
+  dispatch_small_block(topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
+                       num_padded, expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b,
+                       ntiles_b, rows_b, max_b, status);
+  __syncthreads();
+  // the routed token rows (padding rows feed only MMA columns that are never stored)
+  const int pieces = H / 8;
+  for (int x = tid; x < R * pieces; x += blockDim.x) {
+    const int r = x / pieces, q = x % pieces;
+    const long long p = route_pos[r];
+    if (p >= 0 && p < max_rows)
+      reinterpret_cast<uint4*>(x_perm + p * H)[q] = __ldg(reinterpret_cast<const uint4*>(h + (size_t)(r / k) * H) + q);
+  }
+}
+
 }  // namespace
 
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
@@ -526,6 +592,27 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
   launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallDispatchMaxR), 0, s, 
       topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert, num_padded,
       expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, status);
+}
+
+// MOE_DECODE_FRONT=0 turns the two-launch front off (read at each call; the
+// bits are the same either way).
+bool decode_front_ok(int T, int H, int N, int k) {
+  const char* v = std::getenv("MOE_DECODE_FRONT");
+  if (v && std::strcmp(v, "0") == 0) return false;
+  return T >= 1 && T <= kFinishMaxT && H % 8 == 0 && N <= kMaxN && k <= 16 && T * k <= kFinishThreads;
+}
+
+void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part, int T, int H,
+                         int N, int k, int B, int capacity, int32_t* topk_idx, float* gates, uint8_t* route_kept,
+                         int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert, int32_t* num_padded,
+                         int32_t* expert_counts, int32_t* num_dropped, GemmTile* tiles_a, int32_t* ntiles_a,
+                         int rows_a, int max_a, GemmTile* tiles_b, int32_t* ntiles_b, int rows_b, int max_b,
+                         uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s) {
+  launch_router_partials(h, w_gate, part, T, H, N, s);
+  launch_pdl(decode_finish_kernel, dim3(1), dim3(kFinishThreads), 0, s, (const float*)part, h, bias, T, H, N, k, B,
+             capacity, topk_idx, gates, route_kept, route_pos, sorted_route_ids, block_expert, num_padded,
+             expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, x_perm,
+             (long long)max_rows, status);
 }
 
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,

@@ -23,6 +23,9 @@ constexpr int kDispatchTile = 1024;
 constexpr int kDecodeRouterMaxT = 64;
 bool chunked_router_ok(int T, int H, int N, bool tc_router);
 size_t chunked_router_part_floats(int T, int H, int N);
+// the chunk sums alone (part: chunked_router_part_floats floats)
+void launch_router_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int T, int H, int N,
+                            cudaStream_t s);
 void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
                            float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
                            cudaStream_t s);
@@ -103,6 +106,18 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
                            int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
                            GemmTile* tiles_a, int32_t* ntiles_a, int rows_a, int max_a, GemmTile* tiles_b,
                            int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s);
+// decode front (at most 2 tokens, token choice): the router's chunk sums
+// (launch_router_partials), then in one CTA the logits in the canonical
+// order, top-k and gates, launch_dispatch_small's results and the routed
+// token rows of x_perm (padding rows untouched): two launches.
+bool decode_front_ok(int T, int H, int N, int k);
+void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part, int T, int H,
+                         int N, int k,
+                         int B, int capacity, int32_t* topk_idx, float* gates, uint8_t* route_kept,
+                         int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert, int32_t* num_padded,
+                         int32_t* expert_counts, int32_t* num_dropped, GemmTile* tiles_a, int32_t* ntiles_a,
+                         int rows_a, int max_a, GemmTile* tiles_b, int32_t* ntiles_b, int rows_b, int max_b,
+                         uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s);
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
 // the same x_perm from the inverse map (route_pos: padded row of each route,

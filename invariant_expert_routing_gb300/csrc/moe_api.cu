@@ -348,7 +348,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
                     void* ws, cudaStream_t s, const Marks* mk = nullptr, bool tiles_ready = false,
-                    bool skip_shared = false, const int32_t* route_pos = nullptr);
+                    bool skip_shared = false, const int32_t* route_pos = nullptr, bool rows_ready = false);
 void mark(const Marks* mk, int i);
 
 // The shared expert (identity mode over h; every token, no routing): W13 then
@@ -401,7 +401,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
                     const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
                     void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready, bool skip_shared,
-                    const int32_t* route_pos) {
+                    const int32_t* route_pos, bool rows_ready) {
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = slots_of(c);
   const int64_t rows = max_rows_of(c, T);
@@ -423,10 +423,13 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
     moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, moe::kW2TileRows,
                             tiles2, ntiles2, max_tiles2, status, s);
   }
-  if (route_pos && scatter_rows_ok(T, H))
+  if (rows_ready) {
+    // the decode front copied the routed rows
+  } else if (route_pos && scatter_rows_ok(T, H)) {
     moe::launch_scatter_rows(h, route_pos, sorted, num_padded, k, T, H, rows, x_perm, s);
-  else
+  } else {
     moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
+  }
   mark(mk, 3);
 
   // CTA-pair kernels where the output features are a multiple of 256 (a
@@ -546,7 +549,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   float* logits = at<float>(ws, L.logits);
   int32_t* counts = at<int32_t>(ws, L.counts);
   moe_status st = MOE_OK;
-  bool tiles_ready = false;
+  bool tiles_ready = false, rows_ready = false;
   mk.at(0);
   // the shared expert needs h alone: it runs on a second stream from the end
   // of routing (the router, latency-bound, keeps the SMs to itself) and
@@ -584,6 +587,23 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
     if (st == MOE_OK)
       st = reroute_impl(c, T, idx, logits, kept, at<int32_t>(ws, L.route_expert), pos, sorted, blocks,
                         num_padded, counts, at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.rerouted), ws, s);
+  } else if (moe::decode_front_ok(T, c->hidden, c->num_experts, c->top_k)) {
+    // a few tokens: the router's chunk sums, then routing, dispatch, both
+    // tile lists and the routed rows in one more launch (the same bits as
+    // the separate kernels)
+    moe::launch_decode_front(h, wg, bias, at<float>(ws, L.rpart), T, c->hidden, c->num_experts, c->top_k,
+                             c->block_size, capacity_of(c, T),
+                             idx, gates, kept, pos, sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
+                             at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles), moe::kW13TileRows,
+                             (int)max_gemm_tiles_of(c, T, moe::kW13TileRows), at<GemmTile>(ws, L.gemm_tiles2),
+                             at<int32_t>(ws, L.num_gemm_tiles2), moe::kW2TileRows,
+                             (int)max_gemm_tiles_of(c, T, moe::kW2TileRows), at<uint16_t>(ws, L.x_perm),
+                             max_rows_of(c, T), at<int>(ws, L.status), s);
+    st = last_cuda();
+    mk.at(1);
+    if (st == MOE_OK) st = fork_shared();
+    tiles_ready = true;
+    rows_ready = true;
   } else {
     st = route_impl(c, T, h, wg, bias, idx, gates, logits, false, ws, s);
     mk.at(1);
@@ -611,7 +631,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   }
   mk.at(2);
   st = ffn_impl(c, T, h, w13, w2, w13s, w2s, sorted, blocks, num_padded, y, ysh, ws, s, &mk, tiles_ready,
-                /*skip_shared=*/shared, pos);
+                /*skip_shared=*/shared, pos, rows_ready);
   if (forked && cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess && st == MOE_OK) st = last_cuda();
   if (st != MOE_OK) return st;
   mk.at(6);
@@ -931,6 +951,9 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
     front = 2 + 2;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = 2 + 9;
+  } else if (moe::decode_front_ok(T, cfg->hidden, cfg->num_experts, cfg->top_k)) {
+    // chunk sums, then routing, dispatch, tile lists and the routed rows
+    front = 2 - 2 - 1;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {
     // dispatch and both tile lists in one launch
     front = router + 1 - 2;

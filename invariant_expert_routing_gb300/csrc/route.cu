@@ -23,6 +23,7 @@
 
 #include "kernels.h"
 #include "pdl.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -30,91 +31,9 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// Ranking: a number beats NaN; larger beats smaller; equal -> lower index.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  const bool na = isnan(va), nb = isnan(vb);
-  if (na != nb) return nb;
-  if (!na && va != vb) return va > vb;
-  return ia < ib;
-}
-
-// Sorts the k selected (expert, logit) pairs by expert index and writes the
-// renormalised gates exp(l_j - m) / sum_s exp(l_s - m), m = max selected,
-// summed in slot order.  Shared by both router paths, so they agree bitwise.
-__device__ __forceinline__ void write_slots_and_gates(int (&sel)[16], float (&selv)[16], int k,
-                                                      int32_t* __restrict__ idx_out,
-                                                      float* __restrict__ gate_out, int lane) {
-  for (int a = 1; a < k; ++a) {
-    const int si = sel[a];
-    const float sv = selv[a];
-    int b = a - 1;
-    while (b >= 0 && sel[b] > si) {
-      sel[b + 1] = sel[b];
-      selv[b + 1] = selv[b];
-      --b;
-    }
-    sel[b + 1] = si;
-    selv[b + 1] = sv;
-  }
-  float m = -INFINITY;
-  for (int j = 0; j < k; ++j) m = fmaxf(m, selv[j]);
-  float ex[16];
-  float S = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    ex[j] = expf(selv[j] - m);
-    S = S + ex[j];
-  }
-  for (int j = lane; j < k; j += 32) {
-    idx_out[j] = sel[j];
-    gate_out[j] = ex[j] / S;
-  }
-}
-
-// One warp: k rounds of a warp-shuffle tournament over the N logits of one
-// token (lrow, global or shared memory), slots sorted by expert index, gates
-// = softmax over the selected.
-__device__ __forceinline__ void topk_select_warp(const float* lrow, int N, int k, int lane,
-                                                 int32_t* __restrict__ idx_out,
-                                                 float* __restrict__ gate_out) {
-  float v[8];
-  uint32_t used = 0;
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const int e = lane + 32 * s;
-    if (e < N) {
-      v[s] = lrow[e];
-    } else {
-      v[s] = 0.0f;
-      used |= 1u << s;
-    }
-  }
-  int sel[16];
-  float selv[16];
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = -1;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (!((used >> s) & 1u) && (bi < 0 || ranks_before(v[s], lane + 32 * s, bv, bi))) {
-        bv = v[s];
-        bi = lane + 32 * s;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    sel[j] = bi;
-    selv[j] = bv;
-    if ((bi & 31) == lane) used |= 1u << (bi >> 5);
-  }
-  write_slots_and_gates(sel, selv, k, idx_out, gate_out, lane);
-}
+using sel::ranks_before;
+using sel::topk_select_warp;
+using sel::write_slots_and_gates;
 
 // Chunked router on the CUDA cores: two launches, for a few tokens (decode)
 // and for batches when W_g is small.
@@ -801,10 +720,8 @@ void launch_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int
   launch_pdl(kernel, dim3(grid), dim3(kPartWarps * 32), smem, s, h, w_gate, T, H, N, part);
 }
 
-void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
-                           float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
-                           cudaStream_t s) {
-  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+void launch_router_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int T, int H, int N,
+                            cudaStream_t s) {
   const bool vec = N % 8 == 0 && H % 8 == 0 && (reinterpret_cast<uintptr_t>(w_gate) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
   // a few tokens: one token per thread (more CTAs); batches: four
@@ -821,6 +738,13 @@ void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const floa
     if (few) launch_partials<32, 1>(h, w_gate, part, T, H, N, vec, s);
     else launch_partials<32, 4, 4>(h, w_gate, part, T, H, N, vec, s);
   }
+}
+
+void launch_router_chunked(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part,
+                           float* logits, int32_t* topk_idx, float* gates, int T, int H, int N, int k,
+                           cudaStream_t s) {
+  const int chunks = (H + kRouterChunk - 1) / kRouterChunk;
+  launch_router_partials(h, w_gate, part, T, H, N, s);
   launch_pdl(router_reduce_kernel, dim3(T), dim3((N + 31) / 32 * 32), 0, s, part, bias, T, N, chunks, k, logits, topk_idx, gates);
 }
 

@@ -1,0 +1,100 @@
+// Top-k selection and renormalised gates of one token, shared by every
+// router path (the chunked CUDA-core router, the certified tensor-core
+// router and the one-launch decode front), so that all give the same bits
+// ("Mixture-of-Experts routing": softmax, top-k, gates renormalised over the
+// selected experts; ties to the lower expert index).
+#pragma once
+#include <cstdint>
+#include <cmath>
+
+namespace moe {
+namespace sel {
+
+// Ranking: a number beats NaN; larger beats smaller; equal -> lower index.
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  const bool na = isnan(va), nb = isnan(vb);
+  if (na != nb) return nb;
+  if (!na && va != vb) return va > vb;
+  return ia < ib;
+}
+
+// Sorts the k selected (expert, logit) pairs by expert index and writes the
+// renormalised gates exp(l_j - m) / sum_s exp(l_s - m), m = max selected,
+// summed in slot order.  Every router path calls it, so all agree bitwise.
+__device__ __forceinline__ void write_slots_and_gates(int (&sel)[16], float (&selv)[16], int k,
+                                                      int32_t* __restrict__ idx_out,
+                                                      float* __restrict__ gate_out, int lane) {
+  for (int a = 1; a < k; ++a) {
+    const int si = sel[a];
+    const float sv = selv[a];
+    int b = a - 1;
+    while (b >= 0 && sel[b] > si) {
+      sel[b + 1] = sel[b];
+      selv[b + 1] = selv[b];
+      --b;
+    }
+    sel[b + 1] = si;
+    selv[b + 1] = sv;
+  }
+  float m = -INFINITY;
+  for (int j = 0; j < k; ++j) m = fmaxf(m, selv[j]);
+  float ex[16];
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    ex[j] = expf(selv[j] - m);
+    S = S + ex[j];
+  }
+  for (int j = lane; j < k; j += 32) {
+    idx_out[j] = sel[j];
+    gate_out[j] = ex[j] / S;
+  }
+}
+
+// One warp: k rounds of a warp-shuffle tournament over the N logits of one
+// token (lrow, global or shared memory), slots sorted by expert index, gates
+// = softmax over the selected.
+__device__ __forceinline__ void topk_select_warp(const float* lrow, int N, int k, int lane,
+                                                 int32_t* __restrict__ idx_out,
+                                                 float* __restrict__ gate_out) {
+  float v[8];
+  uint32_t used = 0;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int e = lane + 32 * s;
+    if (e < N) {
+      v[s] = lrow[e];
+    } else {
+      v[s] = 0.0f;
+      used |= 1u << s;
+    }
+  }
+  int sel[16];
+  float selv[16];
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int bi = -1;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (!((used >> s) & 1u) && (bi < 0 || ranks_before(v[s], lane + 32 * s, bv, bi))) {
+        bv = v[s];
+        bi = lane + 32 * s;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    sel[j] = bi;
+    selv[j] = bv;
+    if ((bi & 31) == lane) used |= 1u << (bi >> 5);
+  }
+  write_slots_and_gates(sel, selv, k, idx_out, gate_out, lane);
+}
+
+}  // namespace sel
+}  // namespace moe

@@ -161,12 +161,15 @@ def test_launch_counts(moe):
     # up to 64 tokens (or any batch of small router work) are routed in two
     # launches (chunk sums, reduce + top-k), and up to 1024 routes are
     # dispatched with both tile lists in one launch
-    assert moe.moe_forward_launch_count(mix, 1) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(mix, 1) == 2 + 3   # two-launch decode front (T <= 2)
+    assert moe.moe_forward_launch_count(mix, 2) == 2 + 3
+    assert moe.moe_forward_launch_count(mix, 3) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(dict(ds, shared_intermediate=2048), 1) == 2 + 3 + 2
     assert moe.moe_forward_launch_count(mix, 64) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 65) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 512) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 513) == 2 + 3 + 6
-    assert moe.moe_forward_launch_count(qw, 1) == 2 + 1 + 4
+    assert moe.moe_forward_launch_count(qw, 1) == 2 + 3
     assert moe.moe_forward_launch_count(qw, 64) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(qw, 65) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(qw, 128) == 2 + 1 + 4
