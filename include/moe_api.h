@@ -347,9 +347,11 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
                              void* const* events, int32_t n_events, void* stream);
 
 /* Number of kernel launches one moe_forward of T tokens makes for this
- * configuration (the router takes two on CUDA cores or four on the tensor
+ * configuration (the router takes two on CUDA cores or six on the tensor
  * cores; at most 1024 routes are dispatched and cut into both GEMM tile lists
- * in one launch). */
+ * in one launch; for at most two tokens the router's chunk sums are followed
+ * by one launch that routes, dispatches and gathers the routed rows, so a
+ * forward without a shared expert is five launches). */
 int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T);
 
 /* moe_dispatch_align for callers that cannot allocate device memory (for

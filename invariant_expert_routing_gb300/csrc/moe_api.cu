@@ -942,8 +942,8 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   // preference lists, deferred acceptance, check, sequential fallback
   // (returns at once unless the check failed), count, scan, scatter = 9
   // after the CUDA-core router.  Expert choice: logits (2 launches), scores,
-  // selection.
-  // chunk sums + reduce/top-k: 2 launches
+  // selection.  At most two tokens: chunk sums, then one launch for the
+  // reduce, top-k, dispatch, tile lists and row gather.
   const bool chunked = moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg));
   const int router = chunked ? 2 : (use_tc_router(cfg) ? 6 : 2);
   int front = 0;
