@@ -10,12 +10,14 @@
 // ("Why temperature=0 Still Gives Different Answers: Batch Invariance",
 // Tier 2: a reduction cut into constant 256-element pieces added in one
 // order).  bf16 x bf16 products are exact in fp32, so the fma rounds exactly
-// like the separate add.  Two implementations give these bits: the chunked
+// like the separate add.  Three implementations give these bits: the chunked
 // CUDA-core router (router_partials_kernel + router_reduce_kernel: chunk sums
-// in parallel CTAs, added in ascending chunk order per token) and the
-// certified tensor-core router (route_certified_kernel recomputes the
-// candidates' logits in the same order); the split of work never changes a
-// logit's order and nothing depends on T.
+// in parallel CTAs, added in ascending chunk order per token), its decode
+// form (the same chunk sums, then one CTA of the dispatch code adds them in
+// the same order), and the certified tensor-core router (route_certified_kernel
+// filters the candidates, cert_chunk_kernel recomputes their chunk sums in
+// the same order from shared-memory tiles, cert_finalize_kernel adds them);
+// the split of work never changes a logit's order and nothing depends on T.
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cstdlib>
@@ -248,8 +250,13 @@ constexpr int kCertTT = 32;       // tokens per tile of the tiled recompute
 constexpr int kCertWRows = 48;    // expert rows one pass of the tiled recompute stages
 constexpr int kCertRow = kRouterChunk * 2 + 16;   // 528-byte shared row: 16-byte pieces conflict-free
 
-// One warp per token.  Shared memory per warp: candidate list and canonical
-// values, and the chunk partial sums of one pass of candidates.
+// The filter: one warp per token computes ||h_t||, the bound and the
+// candidate list.  A token with at most kCertQ candidates hands the list to
+// the tiled recompute (cand, ccount); one with more (a near-tied or
+// non-finite row) is finished here: its candidates' canonical logits in
+// passes of kCertPass (lane = chunk, four chains at a time), then the top-k.
+// Shared memory per warp: candidate list and canonical values, and the chunk
+// partial sums of one pass of candidates.
 struct CertSmem {
   int cidx[kCertWarps][256];
   float cval[kCertWarps][256];
