@@ -270,7 +270,11 @@ def workload_config(wl, T, world, cfg=None):
             "tokens_per_gpu": T, "global_batch": T * world, "seed": 0,
             "l2": (f"inputs larger than L2: {wl.weight_bytes() / 1e9:.1f} GB of expert weights, "
                    "the touched experts' weights are read every step"),
-            "parallelism": "single GPU" if world == 1 else f"{world} token-shard replicas, no collective"}
+            "parallelism": ("single GPU" if world == 1
+                            else f"{world} token shards, one all-gather of per-expert route counts per step "
+                                 "(the capacity of the whole batch)"
+                            if cf > 0 and cfg.get("overflow_policy", 0) == 0 and cfg.get("routing", 0) == 0
+                            else f"{world} token-shard replicas, no collective")}
 
 
 def batch_counts(moe, cfg, wl, h_d, wg_d, bias_d, ws, device):
@@ -415,6 +419,20 @@ def run_gpu(args):
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
+    # a capacity-limited batch sharded over ranks keeps the global batch-order
+    # capacity: every step routes, exchanges the per-expert route counts (one
+    # all-gather of N + 1 integers) and dispatches with the lower ranks' sums
+    shard_mode = (world > 1 and cfg["capacity_factor"] > 0 and cfg["overflow_policy"] == 0
+                  and cfg["routing"] == 0)
+    if shard_mode:
+        from invariant_expert_routing_gb300 import shard
+
+        def fwd_shard():
+            return shard.forward_shard(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_d, ws)
+
+        for _ in range(3):
+            fwd_shard()
+        torch.cuda.synchronize()
     clocks = ClockSampler(visible_gpu_index(local))
     clocks.start()
     time.sleep(0.6)
@@ -423,7 +441,10 @@ def run_gpu(args):
     t_wall0 = time.time()
     start.record(stream)
     for i in range(K):
-        moe.moe_forward_timed(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_d, ws, ev[i])
+        if shard_mode:
+            fwd_shard()
+        else:
+            moe.moe_forward_timed(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_d, ws, ev[i])
     end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -433,6 +454,13 @@ def run_gpu(args):
     ms_total = start.elapsed_time(end)
     ms_total = reduce_max(ms_total, device)
     ms_step = ms_total / K
+    if shard_mode:
+        # stage times for the roofline: the fused forward on this shard with a
+        # local capacity (the staged calls of the shard step have no
+        # in-kernel stage marks)
+        for i in range(K):
+            moe.moe_forward_timed(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, out_d, ws, ev[i])
+        torch.cuda.synchronize()
     stage = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(7)] for i in range(K)])
     stage_ms = stage.mean(axis=0)
     names = ["router", "dispatch_align", "tile_list_and_row_gather", "w13_gemm", "w2_gemm",
@@ -489,8 +517,13 @@ def run_gpu(args):
                                "frac_of_bf16_peak": layer_tf / peak_tf, "gbs": layer_gb,
                                "frac_of_hbm": layer_gb / peak_gb},
             "stage_ms": {n: float(v) for n, v in zip(names, stage_ms)},
-            "gpu_launches": moe.moe_forward_launch_count(cfg, T) * K,
+            "gpu_launches": (moe.moe_forward_launch_count(cfg, T) + (1 if shard_mode else 0)) * K,
             "clocks": clocks.summary(t_wall0, t_wall1)}
+    if shard_mode:
+        line["config"]["capacity_exchange"] = (
+            "capacity of the whole batch (all ranks' tokens in rank order); per step one all-gather "
+            "of each rank's per-expert route counts + token count (N + 1 ints) and "
+            "moe_dispatch_align_shard; stage_ms and the roofline from a local-capacity fused pass")
 
     # ---- routing diagnostics on this batch: the routing_stats probe and the
     # router margin (device time per call, 50 calls each)

@@ -213,6 +213,27 @@ moe_status moe_dispatch_align(const moe_config* cfg, int32_t T, const int32_t* t
                               uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                               int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                               int32_t* num_dropped, void* ws, size_t ws_bytes, void* stream);
+/* One shard of a capacity-limited batch split across GPUs (or calls) in
+ * token order: the same dispatch as moe_dispatch_align on the whole batch of
+ * global_tokens tokens, restricted to this shard's routes.  The capacity is
+ * C = moe_capacity(cfg, global_tokens); expert_offset [N] int32 (device; NULL
+ * for the first shard) holds the routes each expert received in all earlier
+ * shards (their moe_routing_stats expert_load, summed), so the shard's routes
+ * to expert e keep what the earlier ones left: a route is kept iff its rank
+ * among the shard's routes to e is below max(0, C - expert_offset[e]) — the
+ * batch-order priority of the unsharded batch ("Mixture-of-Experts Routing
+ * at Inference Time": capacity filled in batch order).  Obtaining
+ * expert_offset takes one exchange of N integers per shard (an all-gather in
+ * rank order); the layout, GEMMs and combine stay local.  Outputs as
+ * moe_dispatch_align (this shard's routes and layout; num_dropped counts the
+ * shard's dropped routes).  Drop policy and token choice only
+ * (MOE_ERR_INVALID_ARG otherwise, or when global_tokens < T). */
+moe_status moe_dispatch_align_shard(const moe_config* cfg, int32_t T, int32_t global_tokens,
+                                    const int32_t* topk_idx, const int32_t* expert_offset,
+                                    uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                                    int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                                    int32_t* num_dropped, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_dispatch_align implements the drop policy only: with
  * cfg->overflow_policy == MOE_OVERFLOW_REROUTE and a capacity in force, or with
  * expert-choice routing, it returns MOE_ERR_INVALID_ARG rather than dropping

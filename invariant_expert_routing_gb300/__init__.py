@@ -79,6 +79,7 @@ _SIGS = {
     "moe_route_filtered": ([_cfgp, _i32] + [_vp] * 6 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_router_tc_logits": ([_cfgp, _i32] + [_vp] * 3 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_dispatch_align_noalloc": ([_cfgp, _i32] + [_vp] * 9 + [_vp], ctypes.c_int),
+    "moe_dispatch_align_shard": ([_cfgp, _i32, _i32] + [_vp] * 9 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_router_logits": ([_cfgp, _i32] + [_vp] * 4 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_dispatch_align_reroute": ([_cfgp, _i32] + [_vp] * 11 + [_vp, _sz, _vp], ctypes.c_int),
     "moe_route_expert_choice": ([_cfgp, _i32] + [_vp] * 8 + [_vp, _sz, _vp], ctypes.c_int),
@@ -167,6 +168,19 @@ def moe_dispatch_align(cfg, topk_idx, route_kept, route_pos, sorted_route_ids, b
         ctypes.byref(_cfg(cfg)), T, _ptr(topk_idx), _ptr(route_kept), _ptr(route_pos),
         _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded), _ptr(expert_counts),
         _ptr(num_dropped), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_dispatch_align_shard(cfg, global_tokens, topk_idx, expert_offset, route_kept, route_pos,
+                             sorted_route_ids, block_expert, num_padded, expert_counts, num_dropped, ws,
+                             stream=None):
+    """One shard (in token order) of a capacity-limited batch of global_tokens
+    tokens; expert_offset: routes each expert received in earlier shards
+    (None for the first)."""
+    T = topk_idx.shape[0]
+    _check("moe_dispatch_align_shard", _lib.moe_dispatch_align_shard(
+        ctypes.byref(_cfg(cfg)), T, int(global_tokens), _ptr(topk_idx), _ptr(expert_offset),
+        _ptr(route_kept), _ptr(route_pos), _ptr(sorted_route_ids), _ptr(block_expert), _ptr(num_padded),
+        _ptr(expert_counts), _ptr(num_dropped), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_dispatch_align_noalloc(cfg, topk_idx, route_kept, route_pos, sorted_route_ids,

@@ -79,10 +79,19 @@ __device__ int block_exclusive_scan(int v, int* buf, int* total) {
   return incl - v;
 }
 
+// Capacity left to expert e in this batch: all of it, or for one shard of a
+// larger batch what the earlier shards (in token order) did not take
+// (expert_offset[e] routes); -1: no limit.
+__device__ __forceinline__ int capacity_left(int capacity, const int32_t* __restrict__ expert_offset, int e) {
+  if (capacity < 0) return -1;
+  return expert_offset ? max(0, capacity - expert_offset[e]) : capacity;
+}
+
 // One CTA of 256 threads; thread e owns expert e.  Turns per-tile counts into
 // per-tile bases (in place), applies the capacity, lays out the segments.
 __global__ void __launch_bounds__(256) dispatch_scan_kernel(
-    int32_t* __restrict__ tile_count, int ntiles, int N, int B, int capacity, int R,
+    int32_t* __restrict__ tile_count, int ntiles, int N, int B, int capacity,
+    const int32_t* __restrict__ expert_offset, int R,
     int32_t* __restrict__ seg_off, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_padded,
     int32_t* __restrict__ num_dropped, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ sorted_route_ids) {
@@ -99,7 +108,8 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
       load += c;
     }
   }
-  const int kept = (e < N) ? (capacity < 0 ? load : min(load, capacity)) : 0;
+  const int cap_e = (e < N) ? capacity_left(capacity, expert_offset, e) : 0;
+  const int kept = (e < N) ? (cap_e < 0 ? load : min(load, cap_e)) : 0;
   const int padded = (kept + B - 1) / B * B;
   int total_rows = 0, total_drop = 0;
   const int seg = block_exclusive_scan(padded, buf, &total_rows);
@@ -131,7 +141,7 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
 }
 
 __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
-    const int32_t* __restrict__ topk_idx, int R, int N, int capacity,
+    const int32_t* __restrict__ topk_idx, int R, int N, int capacity, const int32_t* __restrict__ expert_offset,
     const int32_t* __restrict__ rank_in_tile, const int32_t* __restrict__ tile_base,
     const int32_t* __restrict__ seg_off, uint8_t* __restrict__ route_kept,
     int32_t* __restrict__ route_pos, int32_t* __restrict__ sorted_route_ids) {
@@ -146,7 +156,8 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
     return;
   }
   const int rank = tile_base[(size_t)blockIdx.x * N + e] + rank_in_tile[r];
-  const bool kept = capacity < 0 || rank < capacity;
+  const int cap_e = capacity_left(capacity, expert_offset, e);
+  const bool kept = cap_e < 0 || rank < cap_e;
   route_kept[r] = kept ? 1 : 0;
   if (kept) {
     const int pos = seg_off[e] + rank;
@@ -536,16 +547,15 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
                      uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                      int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
-                     int32_t* seg_off, int* status, cudaStream_t s) {
+                     int32_t* seg_off, int* status, cudaStream_t s, const int32_t* expert_offset) {
   const int R = T * k;
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, 0, rank_in_tile, tile_count,
                                                          status);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
-                                         num_padded, num_dropped, block_expert, sorted_route_ids);
-  launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, capacity, rank_in_tile,
-                                                           tile_count, seg_off, route_kept, route_pos,
-                                                           sorted_route_ids);
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, expert_offset, R,
+             seg_off, expert_counts, num_padded, num_dropped, block_expert, sorted_route_ids);
+  launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, capacity,
+             expert_offset, rank_in_tile, tile_count, seg_off, route_kept, route_pos, sorted_route_ids);
 }
 
 void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, uint8_t* route_kept,
@@ -555,11 +565,10 @@ void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, ui
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, 1, rank_in_tile, tile_count,
                                                          status);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, -1, R, seg_off, expert_counts,
-                                         num_padded, nullptr, block_expert, sorted_route_ids);
-  launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, -1, rank_in_tile,
-                                                           tile_count, seg_off, route_kept, route_pos,
-                                                           sorted_route_ids);
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, -1, (const int32_t*)nullptr, R,
+             seg_off, expert_counts, num_padded, (int32_t*)nullptr, block_expert, sorted_route_ids);
+  launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, -1,
+             (const int32_t*)nullptr, rank_in_tile, tile_count, seg_off, route_kept, route_pos, sorted_route_ids);
 }
 
 void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int B,
@@ -573,8 +582,8 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
   // phase one: ranks and the per-expert kept counts of the drop rule
   launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, 0, rank_in_tile, tile_count,
                                                          status);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, R, seg_off, expert_counts,
-                                         num_padded, nullptr, block_expert, sorted_route_ids);
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, (const int32_t*)nullptr, R,
+             seg_off, expert_counts, num_padded, (int32_t*)nullptr, block_expert, sorted_route_ids);
   // phase two, then the stable layout of the final assignment
   launch_reroute(topk_idx, logits, T, N, k, capacity, rank_in_tile, tile_count, expert_counts, sc,
                  route_expert, num_dropped, num_rerouted, s);

@@ -43,11 +43,14 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
                             cudaStream_t s);
 
 // ---- dispatch / alignment
+// expert_offset (nullable, [N]): for one shard of a larger batch, the routes
+// each expert received in the earlier shards; the shard's routes then get
+// capacity - expert_offset[e] (at least 0) of expert e's capacity.
 void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,
                      uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                      int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                      int32_t* num_dropped, int32_t* rank_in_tile, int32_t* tile_count,
-                     int32_t* seg_off, int* status, cudaStream_t s);
+                     int32_t* seg_off, int* status, cudaStream_t s, const int32_t* expert_offset = nullptr);
 // Scratch of the overflow reroute (R routes, N experts).
 constexpr int kRerouteListLen = 128;  // cached best experts per token with an overflowing slot
 // ints of one buffer of the per-round exchange of the grid-wide reroute

@@ -738,6 +738,35 @@ moe_status moe_dispatch_align(const moe_config* cfg, int32_t T, const int32_t* t
                        num_padded, expert_counts, num_dropped, ws, static_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_dispatch_align_shard(const moe_config* cfg, int32_t T, int32_t global_tokens,
+                                    const int32_t* topk_idx, const int32_t* expert_offset,
+                                    uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
+                                    int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
+                                    int32_t* num_dropped, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_T(cfg, T));
+  if (global_tokens < T) return MOE_ERR_INVALID_ARG;
+  if (expert_choice(cfg) || cfg->overflow_policy == MOE_OVERFLOW_REROUTE) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(opt(expert_offset));
+  MOE_TRY(need(route_kept));
+  MOE_TRY(need(route_pos));
+  MOE_TRY(need(sorted_route_ids));
+  MOE_TRY(need(block_expert));
+  MOE_TRY(need(num_padded));
+  MOE_TRY(need(expert_counts));
+  MOE_TRY(need(num_dropped));
+  MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+  const Layout L = layout_of(cfg, T);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  moe::launch_dispatch(topk_idx, T, cfg->num_experts, cfg->top_k, cfg->block_size, capacity_of(cfg, global_tokens),
+                       route_kept, route_pos, sorted_route_ids, block_expert, num_padded, expert_counts, num_dropped,
+                       at<int32_t>(ws, L.rank), at<int32_t>(ws, L.tile_count), at<int32_t>(ws, L.seg_off),
+                       at<int>(ws, L.status), s, expert_offset);
+  return last_cuda();
+}
+
 moe_status moe_dispatch_align_reroute(const moe_config* cfg, int32_t T, const int32_t* topk_idx,
                                       const float* logits, uint8_t* route_kept, int32_t* route_expert,
                                       int32_t* route_pos, int32_t* sorted_route_ids,
