@@ -523,7 +523,8 @@ def run_gpu(args):
         line["config"]["capacity_exchange"] = (
             "capacity of the whole batch (all ranks' tokens in rank order); per step one all-gather "
             "of each rank's per-expert route counts + token count (N + 1 ints) and "
-            "moe_dispatch_align_shard; stage_ms and the roofline from a local-capacity fused pass")
+            "moe_dispatch_align_shard; stage_ms, the roofline, the sweep and e2e from local-capacity "
+            "fused forwards")
 
     # ---- routing diagnostics on this batch: the routing_stats probe and the
     # router margin (device time per call, 50 calls each)
