@@ -9,8 +9,8 @@ Each function cites the passage it follows in its C++ implementation.  Pins
 (tests/test_oracle_*.py) tie every function to something other than itself:
 brute force over expert subsets, closed forms, error bounds against exact
 arithmetic, hand-built cases and textbook reductions.  The gate values are
-compared with the GPU only within a tolerance (different exp
-implementations), so their bits are unpinned by design.
+pinned by closed forms and a hand fixture; the GPU's gates are compared with
+them within a tolerance, not bit for bit (fp32 expf on the GPU, fp64 here).
 """
 from __future__ import annotations
 
