@@ -246,7 +246,7 @@ constexpr int kCertWarps = 8;
 constexpr int kCertMaxH = 8192;   // rows up to 32 chunks: one chunk per lane at most
 constexpr int kCertPass = 16;     // candidates whose canonical logits one pass evaluates
 constexpr int kCertQ = 32;        // candidates per token handed to the tiled recompute
-constexpr int kCertTT = 32;       // tokens per tile of the tiled recompute
+constexpr int kCertTT = 32;       // tokens per tile of the tiled recompute (at most 128)
 constexpr int kCertWRows = 48;    // expert rows one pass of the tiled recompute stages
 constexpr int kCertRow = kRouterChunk * 2 + 16;   // 528-byte shared row: 16-byte pieces conflict-free
 
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(256, 3) cert_chunk_kernel(
   uint8_t* s_h = csm;                          // [kCertTT][kCertRow]
   uint8_t* s_w = csm + kCertTT * kCertRow;     // [kCertWRows][kCertRow]
   __shared__ int s_cand[kCertTT * kCertQ];     // the tile's candidate lists
-  __shared__ int s_pair[kCertTT * kCertQ];     // union position << 10 | token << 5 | slot, by expert
+  __shared__ int s_pair[kCertTT * kCertQ];     // union position << 12 | token << 5 | slot, by expert
   __shared__ int s_pos[256];                   // expert -> union position
   __shared__ int s_uexp[256];                  // union position -> expert
   __shared__ int s_ubeg[257];                  // union position -> first pair
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(256, 3) cert_chunk_kernel(
     const int r = p / kCertQ, q = p % kCertQ;
     if (q < s_cnt[r]) {
       const int u = s_pos[s_cand[p]];
-      s_pair[s_ubeg[u] + atomicAdd(&s_ucur[u], 1)] = (u << 10) | (r << 5) | q;
+      s_pair[s_ubeg[u] + atomicAdd(&s_ucur[u], 1)] = (u << 12) | (r << 5) | q;
     }
   }
   const int nu = s_nu;
@@ -561,9 +561,9 @@ __global__ void __launch_bounds__(256, 3) cert_chunk_kernel(
     const int pend = s_ubeg[u0 + nb];
     for (int pi = s_ubeg[u0] + tid; pi < pend; pi += blockDim.x) {
       const int pr = s_pair[pi];
-      const int r = (pr >> 5) & 31, q = pr & 31;
+      const int r = (pr >> 5) & 127, q = pr & 31;
       const uint8_t* hr = s_h + r * kCertRow;
-      const uint8_t* wr = s_w + ((pr >> 10) - u0) * kCertRow;
+      const uint8_t* wr = s_w + ((pr >> 12) - u0) * kCertRow;
       float acc = 0.0f;
 #pragma unroll 4
       for (int i = 0; i < len; i += 8) {
