@@ -304,31 +304,33 @@ moe_status moe_router_margin(const moe_config* cfg, int32_t T, const float* logi
  *   for every padded row p of expert e = block_expert[p / B] with route r:
  *     x = h[r / S] (S = k, or N for expert choice; zero for the sentinel),
  *     [g | u] = x . W13_e,
- *     a = bf16(silu(g) * u), y_perm[p] = a . W2_e  (fp32)
+ *     a = bf16(silu(g) * u), y_perm[p] = bf16(a . W2_e)  (fp32 accumulation)
  *   and, when cfg->shared_intermediate > 0, y_shared[t] = SwiGLU_shared(h[t]).
  *   w13 [N, H, 2I] bf16 (gate columns 0..I-1, up columns I..2I-1),
  *   w2 [N, I, H] bf16, w13_shared [H, 2Is], w2_shared [Is, H] (or NULL when
- *   Is == 0); y_perm [moe_max_padded_rows, H] fp32 out; y_shared [T, H] fp32
- *   out or NULL when Is == 0.  Rows of y_perm that hold the sentinel get
- *   x = 0 (so a = 0 and y = 0 for finite weights); rows past *num_padded are
+ *   Is == 0); y_perm [moe_max_padded_rows, H] bf16 out; y_shared [T, H] bf16
+ *   out or NULL when Is == 0 (the expert outputs are stored in bf16: half the
+ *   bytes of the W2 store and of the combine's reads; every sum stays fp32).
+ *   Rows of y_perm that hold the sentinel, and rows past *num_padded, are
  *   not written.
  * One tile shape and one K order for every T, no split-K: each y row
  * depends only on its own x row and the expert's weights. */
 moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w13,
                           const uint16_t* w2, const uint16_t* w13_shared,
                           const uint16_t* w2_shared, const int32_t* sorted_route_ids,
-                          const int32_t* block_expert, const int32_t* num_padded, float* y_perm,
-                          float* y_shared, void* ws, size_t ws_bytes, void* stream);
+                          const int32_t* block_expert, const int32_t* num_padded, uint16_t* y_perm,
+                          uint16_t* y_shared, void* ws, size_t ws_bytes, void* stream);
 
 /* Gate-weighted combine into the residual:
  *   out[t] = bf16( h[t] + sum_{j ascending, kept} topk_gate[t,j] * y_perm[route_pos[t*S+j]]
  *                  + y_shared[t] )
- * accumulated in fp32 in that fixed order; S = k slots per token (N for
- * expert choice, whose gates are the [T, N] probabilities).  y_shared may be
- * NULL.  out [T,H] bf16. */
+ * accumulated in fp32 in that fixed order (y_perm, y_shared bf16 as written
+ * by moe_expert_ffn); S = k slots per token (N for expert choice, whose
+ * gates are the [T, N] probabilities).  y_shared may be NULL.  out [T,H]
+ * bf16. */
 moe_status moe_combine(const moe_config* cfg, int32_t T, const uint16_t* h, const float* topk_gate,
-                       const uint8_t* route_kept, const int32_t* route_pos, const float* y_perm,
-                       const float* y_shared, uint16_t* out, void* stream);
+                       const uint8_t* route_kept, const int32_t* route_pos, const uint16_t* y_perm,
+                       const uint16_t* y_shared, uint16_t* out, void* stream);
 
 /* The whole layer: moe_route -> moe_dispatch_align -> moe_expert_ffn ->
  * moe_combine on `stream`, intermediates in the workspace.  No host

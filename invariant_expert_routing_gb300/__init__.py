@@ -243,6 +243,7 @@ def moe_router_margin(cfg, logits, margin, stream=None):
 
 def moe_expert_ffn(cfg, h, w13, w2, w13_shared, w2_shared, sorted_route_ids, block_expert,
                    num_padded, y_perm, y_shared, ws, stream=None):
+    """y_perm [max padded rows, H] and y_shared [T, H] (or None): bfloat16 tensors."""
     T = h.shape[0]
     _check("moe_expert_ffn", _lib.moe_expert_ffn(
         ctypes.byref(_cfg(cfg)), T, _ptr(h), _ptr(w13), _ptr(w2), _ptr(w13_shared),

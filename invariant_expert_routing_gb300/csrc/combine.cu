@@ -4,13 +4,15 @@
 // overflowed contributes nothing.
 //
 // out[t,:] = bf16( h[t,:] + acc ),  acc = fma over kept slots j = 0..S-1 in
-// ascending order of gate[t,j] * y_perm[route_pos[t*S+j], :], then + y_shared.
+// ascending order of gate[t,j] * y_perm[route_pos[t*S+j], :], then + y_shared
+// (y_perm and y_shared: the expert GEMMs' fp32 results stored as bf16; the
+// sum itself is fp32).
 // S is the number of route slots per token: k for token choice, N for expert
 // choice (slot e = expert e).  The kept slots are first listed in ascending j
 // in shared memory; skipping the others leaves the chain of fmas unchanged.
 // A token row is split over gridDim.y CTAs (more when there are few tokens,
 // so that a lone token's row is spread over several SMs), 4 consecutive
-// features per thread, 128-bit loads of y_perm (with few tokens issued eight
+// features per thread, 64-bit loads of the bf16 y_perm (with few tokens issued eight
 // slots at a time before their fmas); the order of the sum is fixed and
 // independent of T and of the grid.
 #include <cuda_bf16.h>
@@ -24,13 +26,20 @@ namespace {
 
 constexpr int kMaxSlots = 256;
 
+// Four consecutive bf16 values (8-byte aligned) widened to fp32.
+__device__ __forceinline__ float4 load_bf16x4(const uint16_t* p) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+}
+
 template <bool kBatch>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ h,
                                                       const float* __restrict__ gates,
                                                       const uint8_t* __restrict__ route_kept,
                                                       const int32_t* __restrict__ route_pos,
-                                                      const float* __restrict__ y_perm,
-                                                      const float* __restrict__ y_shared,
+                                                      const uint16_t* __restrict__ y_perm,
+                                                      const uint16_t* __restrict__ y_shared,
                                                       uint16_t* __restrict__ out, int H, int k,
                                                       long long max_rows) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
@@ -70,7 +79,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           if (i0 + q < n_used)
-            y[q] = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)s_pos[i0 + q] * H + d));
+            y[q] = load_bf16x4(y_perm + (size_t)s_pos[i0 + q] * H + d);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (i0 + q < n_used) {
@@ -85,7 +94,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     } else {        // many tokens: occupancy hides the latency (fewer registers)
       for (int i = 0; i < n_used; ++i) {
         const float g = s_gate[i];
-        const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)s_pos[i] * H + d));
+        const float4 y = load_bf16x4(y_perm + (size_t)s_pos[i] * H + d);
         acc.x = fmaf(g, y.x, acc.x);
         acc.y = fmaf(g, y.y, acc.y);
         acc.z = fmaf(g, y.z, acc.z);
@@ -93,7 +102,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
       }
     }
     if (y_shared) {
-      const float4 ys = __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * H + d));
+      const float4 ys = load_bf16x4(y_shared + (size_t)t * H + d);
       acc.x = acc.x + ys.x;
       acc.y = acc.y + ys.y;
       acc.z = acc.z + ys.z;
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 }  // namespace
 
 void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,
-                    const int32_t* route_pos, const float* y_perm, const float* y_shared,
+                    const int32_t* route_pos, const uint16_t* y_perm, const uint16_t* y_shared,
                     uint16_t* out, int T, int H, int k, int64_t max_rows, cudaStream_t s) {
   // enough CTAs for about two per SM, at most one per 1024 features of a row
   int sms = 0, dev = 0;

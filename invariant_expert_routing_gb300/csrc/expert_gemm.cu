@@ -4,7 +4,7 @@
 // ("Route-Block Membership Selects Packed-AWQ Arithmetic", "The bookkeeping
 // before the matrix multiplication"), token tiles of BN rows run
 //   W13: [g | u] = X . W13_e  ->  a = bf16(silu(g) * u)      (X = x_perm rows)
-//   W2 : y = a . W2_e         ->  y_perm (fp32)
+//   W2 : y = a . W2_e         ->  y_perm (fp32 accumulation, stored as bf16)
 // The weights are operand A (M = 128 output features, MN-major straight from
 // the [K, features] layout), the tokens operand B (N = BN rows, K-major; BN =
 // 128 for W13, 256 for W2).  Every tile of every batch runs the same
@@ -345,6 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float v = (x / (1.0f + expf(-x))) * u[jj];
               out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v);
             }
+          }
+        } else if (args.out_bf16) {
+          tmem_wait_ld();
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.valid) out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(g[jj]);
           }
         } else {
           tmem_wait_ld();
@@ -693,6 +701,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           ++chunk;
+        } else if (args.out_bf16) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.valid) out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v[jj]);
+          }
         } else {
           float* out = reinterpret_cast<float*>(args.out);
 #pragma unroll

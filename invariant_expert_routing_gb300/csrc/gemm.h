@@ -45,9 +45,11 @@ struct GemmArgs {
   const GemmTile* tiles;     // routed mode: tile list on the device
   const int32_t* num_tiles;  // routed mode: device count
   int identity_T;            // identity mode (shared expert): rows 0..T-1, else 0
-  void* out;           // W13: bf16 a [rows, I]; W2: fp32 y [rows, H]
+  void* out;           // W13: bf16 a [rows, I]; W2: y [rows, H] (bf16 with out_bf16, else fp32);
+                       // router logits: fp32 [T, N]
   int out_ld;          // elements per output row
   int* status;
+  int out_bf16;        // non-W13 outputs rounded to bf16 (the expert outputs y), else fp32
   int concurrent;      // work units resident at once (set by the launcher)
   int pair;            // 1: CTA-pair kernel (256 token rows per tile, token maps with
                        //    128-row boxes; n_feat_tiles in units of kPairFeatW13 / kPairFeatW2)

@@ -147,7 +147,7 @@ void launch_router_margin(const float* logits, int T, int N, int k, double* marg
 
 // ---- combine (k = route slots per token: top_k, or N for expert choice)
 void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_kept,
-                    const int32_t* route_pos, const float* y_perm, const float* y_shared,
+                    const int32_t* route_pos, const uint16_t* y_perm, const uint16_t* y_shared,
                     uint16_t* out, int T, int H, int k, int64_t max_rows, cudaStream_t s);
 
 }  // namespace moe

@@ -155,10 +155,10 @@ Layout layout_of(const moe_config* c, int32_t T) {
   // x_perm and a keep one tile of rows of slack so every tile load stays inside them
   L.x_perm = take(sizeof(uint16_t) * (rows + moe::kMaxTileRows) * H);
   L.a = take(sizeof(uint16_t) * (rows + moe::kMaxTileRows) * c->intermediate);
-  L.y = take(sizeof(float) * rows * H);
+  L.y = take(sizeof(uint16_t) * rows * H);
   const size_t Is = c->shared_intermediate;
   L.a_sh = take(Is ? sizeof(uint16_t) * ((size_t)T + moe::kMaxTileRows) * Is : 0);
-  L.y_sh = take(Is ? sizeof(float) * (size_t)T * H : 0);
+  L.y_sh = take(Is ? sizeof(uint16_t) * (size_t)T * H : 0);
   L.h_stage = take(sizeof(uint16_t) * (size_t)T * H);
   L.out_stage = take(sizeof(uint16_t) * (size_t)T * H);
   L.total = off;
@@ -346,7 +346,7 @@ bool scatter_rows_ok(int T, int H) {
 struct Marks;
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
-                    const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
+                    const int32_t* blocks, const int32_t* num_padded, uint16_t* y_perm, uint16_t* y_shared,
                     void* ws, cudaStream_t s, const Marks* mk = nullptr, bool tiles_ready = false,
                     bool skip_shared = false, const int32_t* route_pos = nullptr, bool rows_ready = false);
 void mark(const Marks* mk, int i);
@@ -355,7 +355,7 @@ void mark(const Marks* mk, int i);
 // W2 into y_shared.  It depends on h alone, so the forward runs it on a
 // second stream alongside routing, dispatch and the routed GEMMs.
 moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13s,
-                           const uint16_t* w2s, float* y_shared, void* ws, cudaStream_t s) {
+                           const uint16_t* w2s, uint16_t* y_shared, void* ws, cudaStream_t s) {
   const Layout L = layout_of(c, T);
   const int H = c->hidden, Is = c->shared_intermediate;
   const int sms = num_sms();
@@ -392,6 +392,7 @@ moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, co
   s2.up_col = 0;
   s2.out = y_shared;
   s2.out_ld = H;
+  s2.out_bf16 = 1;
   s2.pair = pair2 ? 1 : 0;
   moe::launch_w2_gemm(m_w2s, m_ash, m_ashs, s2, (T + moe::kW2TileRows - 1) / moe::kW2TileRows, sms, s);
   return last_cuda();
@@ -399,7 +400,7 @@ moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, co
 
 moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uint16_t* w13,
                     const uint16_t* w2, const uint16_t* w13s, const uint16_t* w2s, const int32_t* sorted,
-                    const int32_t* blocks, const int32_t* num_padded, float* y_perm, float* y_shared,
+                    const int32_t* blocks, const int32_t* num_padded, uint16_t* y_perm, uint16_t* y_shared,
                     void* ws, cudaStream_t s, const Marks* mk, bool tiles_ready, bool skip_shared,
                     const int32_t* route_pos, bool rows_ready) {
   const Layout L = layout_of(c, T);
@@ -475,6 +476,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.num_tiles = ntiles2;
   g2.out = y_perm;
   g2.out_ld = H;
+  g2.out_bf16 = 1;
   g2.pair = pair2 ? 1 : 0;
   g2.wide = wide2 ? 1 : 0;
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
@@ -544,8 +546,8 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   int32_t* sorted = at<int32_t>(ws, L.sorted);
   int32_t* blocks = at<int32_t>(ws, L.blocks);
   int32_t* num_padded = at<int32_t>(ws, L.num_padded);
-  float* y = at<float>(ws, L.y);
-  float* ysh = c->shared_intermediate ? at<float>(ws, L.y_sh) : nullptr;
+  uint16_t* y = at<uint16_t>(ws, L.y);
+  uint16_t* ysh = c->shared_intermediate ? at<uint16_t>(ws, L.y_sh) : nullptr;
   float* logits = at<float>(ws, L.logits);
   int32_t* counts = at<int32_t>(ws, L.counts);
   moe_status st = MOE_OK;
@@ -876,7 +878,7 @@ moe_status moe_router_margin(const moe_config* cfg, int32_t T, const float* logi
 moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const uint16_t* h, const uint16_t* w13,
                           const uint16_t* w2, const uint16_t* w13_shared, const uint16_t* w2_shared,
                           const int32_t* sorted_route_ids, const int32_t* block_expert,
-                          const int32_t* num_padded, float* y_perm, float* y_shared, void* ws,
+                          const int32_t* num_padded, uint16_t* y_perm, uint16_t* y_shared, void* ws,
                           size_t ws_bytes, void* stream) {
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_T(cfg, T));
@@ -898,8 +900,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, int32_t T, const uint16_t* h, c
 }
 
 moe_status moe_combine(const moe_config* cfg, int32_t T, const uint16_t* h, const float* topk_gate,
-                       const uint8_t* route_kept, const int32_t* route_pos, const float* y_perm,
-                       const float* y_shared, uint16_t* out, void* stream) {
+                       const uint8_t* route_kept, const int32_t* route_pos, const uint16_t* y_perm,
+                       const uint16_t* y_shared, uint16_t* out, void* stream) {
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_T(cfg, T));
   if (T == 0) return MOE_OK;

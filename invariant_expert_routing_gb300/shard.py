@@ -65,8 +65,8 @@ def forward_shard(cfg, h, w_gate, router_bias, w13, w2, w13_shared, w2_shared, o
     dropped = torch.empty(1, dtype=torch.int32, device=d)
     moe_dispatch_align_shard(cfg, global_tokens, idx, offset, kept, pos, srt, blk, npad, counts, dropped, ws,
                              stream)
-    y = torch.empty((rows, H), dtype=torch.float32, device=d)
-    ysh = torch.empty((T, H), dtype=torch.float32, device=d) if cfg.get("shared_intermediate", 0) else None
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device=d)
+    ysh = torch.empty((T, H), dtype=torch.bfloat16, device=d) if cfg.get("shared_intermediate", 0) else None
     moe_expert_ffn(cfg, h, w13, w2, w13_shared, w2_shared, srt, blk, npad, y, ysh, ws, stream)
     moe_combine(cfg, h, gates, kept, pos, y, ysh, out, stream)
     return global_tokens, dropped

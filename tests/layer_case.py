@@ -6,6 +6,7 @@ from __future__ import annotations
 import numpy as np
 
 import oracle
+from synth import bf16_to_f32
 from synth import workloads as W
 
 from .gpu_util import dev, dev_bf16, host, host_bf16
@@ -79,8 +80,8 @@ class LayerCase:
         counts = torch.empty(N, dtype=torch.int32, device=d)
         dropped = torch.zeros(1, dtype=torch.int32, device=d)
         moe.moe_dispatch_align(self.cfg, idx, kept, pos, srt, blk, npad, counts, dropped, ws)
-        y = torch.zeros((rows, wl.hidden), dtype=torch.float32, device=d)
-        ysh = (torch.zeros((T, wl.hidden), dtype=torch.float32, device=d)
+        y = torch.zeros((rows, wl.hidden), dtype=torch.bfloat16, device=d)
+        ysh = (torch.zeros((T, wl.hidden), dtype=torch.bfloat16, device=d)
                if wl.shared_intermediate else None)
         moe.moe_expert_ffn(self.cfg, h_d, self.w13_d, self.w2_d, self.w13s_d, self.w2s_d, srt, blk,
                            npad, y, ysh, ws)
@@ -93,8 +94,9 @@ class LayerCase:
         return dict(logits=host(logits), topk_idx=host(idx), gates=host(gates),
                     route_kept=host(kept), route_pos=host(pos), sorted_route_ids=host(srt)[:P],
                     block_expert=host(blk)[:P // B], num_padded=P, expert_counts=host(counts),
-                    num_dropped=int(host(dropped)[0]), y_perm=host(y)[:P],
-                    y_shared=None if ysh is None else host(ysh), out=host_bf16(out), status=status)
+                    num_dropped=int(host(dropped)[0]), y_perm=bf16_to_f32(host_bf16(y))[:P],
+                    y_shared=None if ysh is None else bf16_to_f32(host_bf16(ysh)), out=host_bf16(out),
+                    status=status)
 
     # ---- oracle
     def ref_routing(self, h_bits: np.ndarray):

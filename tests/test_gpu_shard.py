@@ -80,8 +80,8 @@ def test_shards_reproduce_the_unsharded_batch(name, cf, cuts):
         counts = torch.empty(N, dtype=torch.int32, device=d)
         dropped = torch.empty(1, dtype=torch.int32, device=d)
         moe.moe_dispatch_align_shard(cfg, T, idx, off_d, kept, pos, srt, blk, npad, counts, dropped, wss)
-        y = torch.empty((rows, H), dtype=torch.float32, device=d)
-        ysh = torch.empty((Ts, H), dtype=torch.float32, device=d) if wl.shared_intermediate else None
+        y = torch.empty((rows, H), dtype=torch.bfloat16, device=d)
+        ysh = torch.empty((Ts, H), dtype=torch.bfloat16, device=d) if wl.shared_intermediate else None
         moe.moe_expert_ffn(cfg, hs, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, srt, blk, npad, y, ysh, wss)
         out = torch.empty((Ts, H), dtype=torch.bfloat16, device=d)
         moe.moe_combine(cfg, hs, gates, kept, pos, y, ysh, out)
