@@ -102,10 +102,22 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
   const int e = threadIdx.x;
   int load = 0;
   if (e < N) {
-    for (int tl = 0; tl < ntiles; ++tl) {
-      const int c = tile_count[(size_t)tl * N + e];
-      tile_count[(size_t)tl * N + e] = load;
-      load += c;
+    // the counts of kScanBatch route tiles are loaded before any is
+    // overwritten by its exclusive prefix: one L2 round trip per batch
+    // instead of one per tile
+    constexpr int kScanBatch = 16;
+    for (int tl0 = 0; tl0 < ntiles; tl0 += kScanBatch) {
+      int c[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j)
+        c[j] = (tl0 + j < ntiles) ? tile_count[(size_t)(tl0 + j) * N + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (tl0 + j < ntiles) {
+          tile_count[(size_t)(tl0 + j) * N + e] = load;
+          load += c[j];
+        }
+      }
     }
   }
   const int cap_e = (e < N) ? capacity_left(capacity, expert_offset, e) : 0;
@@ -168,68 +180,79 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
   }
 }
 
-// Grouped-GEMM tile list from the padded blocks: each expert segment is cut
-// into tiles of tile_rows rows from its start.  Rejects (no tiles, status
-// bit) a block list that is not sorted by expert or out of range.
+// Grouped-GEMM tile lists from the padded blocks: each expert segment is cut
+// into tiles of tile_rows rows from its start.  CTA 0 writes list `a`, CTA 1
+// (when the grid has two) list `b`, from the same blocks.  Rejects (no tiles,
+// status bit) a block list that is not sorted by expert or out of range.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
                                                           const int32_t* __restrict__ num_padded,
                                                           const int32_t* __restrict__ sorted_route_ids,
-                                                          int R, int N,
-                                                          int B, long long max_rows, int tile_rows,
-                                                          GemmTile* __restrict__ tiles,
-                                                          int32_t* __restrict__ num_tiles, int max_tiles,
-                                                          int* status) {
+                                                          int R, int N, int B, long long max_rows,
+                                                          TileListOut a, TileListOut b_list, int* status) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   pdl_trigger();
+  const TileListOut L = blockIdx.x == 0 ? a : b_list;
   __shared__ int buf[256];
+  __shared__ int s_first[kMaxN], s_last[kMaxN];
   __shared__ int s_bad;
   const int P = *num_padded;
   const bool bad_count = P < 0 || (long long)P > max_rows || (P % B) != 0;
   const int nb = bad_count ? 0 : P / B;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    s_first[e] = 0;
+    s_last[e] = 0;
+  }
   if (threadIdx.x == 0) s_bad = bad_count ? 1 : 0;
   __syncthreads();
+  // one pass over the blocks checks the order and marks where each expert's
+  // blocks begin and end (an expert with no block keeps an empty range)
   for (int b = threadIdx.x; b < nb; b += blockDim.x) {
     const int e = block_expert[b];
-    if (e < 0 || e >= N || (b > 0 && block_expert[b - 1] > e)) s_bad = 1;
+    const int prev = b > 0 ? block_expert[b - 1] : -1;
+    if (e < 0 || e >= N || prev > e) {
+      s_bad = 1;
+      continue;
+    }
+    const int next = b + 1 < nb ? block_expert[b + 1] : N;
+    if (prev != e) s_first[e] = b;
+    if (next != e) s_last[e] = b + 1;
   }
   __syncthreads();
   if (s_bad) {
     if (threadIdx.x == 0) {
-      *num_tiles = 0;
+      *L.num_tiles = 0;
       atomicOr(status, kDevErrBadBlocks);
     }
     return;
   }
   const int e = threadIdx.x;
-  int first = 0, last = 0;
-  if (e < N) {
-    int lo = 0, hi = nb;  // first block with expert >= e
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (block_expert[mid] < e) lo = mid + 1; else hi = mid;
-    }
-    first = lo;
-    hi = nb;  // first block with expert >= e + 1
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (block_expert[mid] <= e) lo = mid + 1; else hi = mid;
-    }
-    last = lo;
-  }
+  const int first = e < N ? s_first[e] : 0, last = e < N ? s_last[e] : 0;
   const int rows = (last - first) * B;
-  // rows up to the segment's last route (the padding sentinels trail it)
+  // rows up to the segment's last route (the padding sentinels trail it),
+  // eight rows from the end per round trip
   int used = rows;
   while (used > 0) {
-    const int r = sorted_route_ids[first * B + used - 1];
-    if (r >= 0 && r < R) break;
-    --used;
+    const int n = min(8, used);
+    int r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = j < n ? sorted_route_ids[first * B + used - 1 - j] : -1;
+    int found = -1;
+#pragma unroll
+    for (int j = 7; j >= 0; --j)
+      if (j < n && r[j] >= 0 && r[j] < R) found = j;
+    if (found >= 0) {
+      used -= found;
+      break;
+    }
+    used -= n;
   }
+  const int tile_rows = L.tile_rows;
   const int nt = (rows + tile_rows - 1) / tile_rows;
   int total = 0;
   const int off = block_exclusive_scan(nt, buf, &total);
   for (int j = 0; j < nt; ++j) {
     const int idx = off + j;
-    if (idx < max_tiles) {
+    if (idx < L.max_tiles) {
       GemmTile tl;
       tl.expert = e;
       tl.row0 = first * B + j * tile_rows;
@@ -238,10 +261,10 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
       tl.count = nt;
       tl.valid = max(0, min(tl.rows, used - j * tile_rows));
       tl.pad[0] = tl.pad[1] = 0;
-      tiles[idx] = tl;
+      L.tiles[idx] = tl;
     }
   }
-  if (threadIdx.x == 0) *num_tiles = min(total, max_tiles);
+  if (threadIdx.x == 0) *L.num_tiles = min(total, L.max_tiles);
 }
 
 // x_perm[p] = h[r / k] for padded row p holding route r, zeros for the
@@ -626,10 +649,9 @@ void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float*
 
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
                         const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
-                        int tile_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles, int* status,
-                        cudaStream_t s) {
-  launch_pdl(build_tiles_kernel, dim3(1), dim3(256), 0, s, block_expert, num_padded, sorted_route_ids, R, N, B,
-                                       (long long)max_rows, tile_rows, tiles, num_tiles, max_tiles, status);
+                        TileListOut a, const TileListOut* b, int* status, cudaStream_t s) {
+  launch_pdl(build_tiles_kernel, dim3(b ? 2 : 1), dim3(256), 0, s, block_expert, num_padded, sorted_route_ids, R,
+             N, B, (long long)max_rows, a, b ? *b : a, status);
 }
 
 }  // namespace moe

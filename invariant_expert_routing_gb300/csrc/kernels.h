@@ -131,10 +131,16 @@ void launch_scatter_rows(const uint16_t* h, const int32_t* route_pos, const int3
 // Tile list of one GEMM: tile_rows-row tiles over each expert's padded
 // segment; a tile's valid rows end at the segment's last route (sorted ids
 // in [0, R)).
+struct TileListOut {
+  GemmTile* tiles;
+  int32_t* num_tiles;
+  int tile_rows;
+  int max_tiles;
+};
+// List a, and list b too when b is non-null (one launch, one CTA per list).
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
                         const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
-                        int tile_rows, GemmTile* tiles, int32_t* num_tiles, int max_tiles, int* status,
-                        cudaStream_t s);
+                        TileListOut a, const TileListOut* b, int* status, cudaStream_t s);
 
 // ---- diagnostics
 struct RoutingStats {  // same layout as moe_route_stats

@@ -419,10 +419,9 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
   if (!tiles_ready) {   // else the small-batch dispatch built both lists
-    moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, moe::kW13TileRows,
-                            tiles13, ntiles13, max_tiles13, status, s);
-    moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, moe::kW2TileRows,
-                            tiles2, ntiles2, max_tiles2, status, s);
+    const moe::TileListOut l13{tiles13, ntiles13, moe::kW13TileRows, max_tiles13};
+    const moe::TileListOut l2{tiles2, ntiles2, moe::kW2TileRows, max_tiles2};
+    moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, l13, &l2, status, s);
   }
   if (rows_ready) {
     // the decode front copied the routed rows
