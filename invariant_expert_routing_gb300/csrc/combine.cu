@@ -10,11 +10,12 @@
 // S is the number of route slots per token: k for token choice, N for expert
 // choice (slot e = expert e).  The kept slots are first listed in ascending j
 // in shared memory; skipping the others leaves the chain of fmas unchanged.
-// A token row is split over gridDim.y CTAs (more when there are few tokens,
-// so that a lone token's row is spread over several SMs), 4 consecutive
-// features per thread, 64-bit loads of the bf16 y_perm (with few tokens issued eight
-// slots at a time before their fmas); the order of the sum is fixed and
-// independent of T and of the grid.
+// With many tokens a CTA takes one row: 8 consecutive features per thread and
+// 16-byte accesses when the row is a multiple of 2048 features, else 4.  With few tokens a row is split over gridDim.y CTAs
+// (so that a lone token's row is spread over several SMs), 4 consecutive
+// features per thread, 64-bit loads of the bf16 y_perm issued eight slots at
+// a time before their fmas.  The order of the sum is fixed and independent of
+// T and of the grid.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -33,7 +34,26 @@ __device__ __forceinline__ float4 load_bf16x4(const uint16_t* p) {
                      __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
 }
 
-template <bool kBatch>
+// Eight consecutive bf16 values (16-byte aligned) widened to fp32.
+__device__ __forceinline__ void load_bf16x8(const uint16_t* p, float (&v)[8]) {
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
+// kForm: 0 many tokens, 4 features per thread; 1 many tokens, 8 features per
+// thread (rows of a multiple of 2048 features: every thread has whole
+// passes); 2 few tokens, a row split over gridDim.y CTAs.
+template <int kForm>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ h,
                                                       const float* __restrict__ gates,
                                                       const uint8_t* __restrict__ route_kept,
@@ -71,9 +91,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     s_gate[before] = g;
   }
   __syncthreads();
+  if (kForm == 1) {
+    // many tokens (one CTA per row): 8 consecutive features per thread,
+    // 16-byte loads and stores; occupancy hides the latency.  Each feature's
+    // chain of fmas is the one of the split-row form below.
+    for (int d = threadIdx.x * 8; d < H; d += blockDim.x * 8) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int i = 0; i < n_used; ++i) {
+        const float g = s_gate[i];
+        float y[8];
+        load_bf16x8(y_perm + (size_t)s_pos[i] * H + d, y);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, y[q], acc[q]);
+      }
+      if (y_shared) {
+        float ys[8];
+        load_bf16x8(y_shared + (size_t)t * H + d, ys);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = acc[q] + ys[q];
+      }
+      float hv[8];
+      load_bf16x8(h + (size_t)t * H + d, hv);
+      uint4 ov;
+      ov.x = pack_bf16x2(hv[0] + acc[0], hv[1] + acc[1]);
+      ov.y = pack_bf16x2(hv[2] + acc[2], hv[3] + acc[3]);
+      ov.z = pack_bf16x2(hv[4] + acc[4], hv[5] + acc[5]);
+      ov.w = pack_bf16x2(hv[6] + acc[6], hv[7] + acc[7]);
+      *reinterpret_cast<uint4*>(out + (size_t)t * H + d) = ov;
+    }
+    return;
+  }
   for (int d = (blockIdx.y * blockDim.x + threadIdx.x) * 4; d < H; d += gridDim.y * blockDim.x * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (kBatch) {   // few tokens: eight slots' loads in flight before their fmas
+    if (kForm == 2) {   // few tokens: eight slots' loads in flight before their fmas
       for (int i0 = 0; i0 < n_used; i0 += 8) {
         float4 y[8];
 #pragma unroll
@@ -91,7 +143,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
           }
         }
       }
-    } else {        // many tokens: occupancy hides the latency (fewer registers)
+    } else {            // many tokens: occupancy hides the latency (fewer registers)
       for (int i = 0; i < n_used; ++i) {
         const float g = s_gate[i];
         const float4 y = load_bf16x4(y_perm + (size_t)s_pos[i] * H + d);
@@ -133,11 +185,14 @@ void launch_combine(const uint16_t* h, const float* gates, const uint8_t* route_
   const int want = T > 0 ? (2 * (sms > 0 ? sms : 1) + T - 1) / T : 1;
   const dim3 grid((unsigned)T, (unsigned)(want < per_row ? (want > 0 ? want : 1) : per_row));
   if (grid.y > 1)
-    launch_pdl(combine_kernel<true>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
-                                              (long long)max_rows);
+    launch_pdl(combine_kernel<2>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared,
+               out, H, k, (long long)max_rows);
+  else if (H % 2048 == 0)
+    launch_pdl(combine_kernel<1>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared,
+               out, H, k, (long long)max_rows);
   else
-    launch_pdl(combine_kernel<false>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared, out, H, k,
-                                               (long long)max_rows);
+    launch_pdl(combine_kernel<0>, dim3(grid), dim3(256), 0, s, h, gates, route_kept, route_pos, y_perm, y_shared,
+               out, H, k, (long long)max_rows);
 }
 
 }  // namespace moe

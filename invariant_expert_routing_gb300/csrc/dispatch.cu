@@ -206,16 +206,28 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
   __syncthreads();
   // one pass over the blocks checks the order and marks where each expert's
   // blocks begin and end (an expert with no block keeps an empty range)
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    const int e = block_expert[b];
-    const int prev = b > 0 ? block_expert[b - 1] : -1;
-    if (e < 0 || e >= N || prev > e) {
-      s_bad = 1;
-      continue;
+  // (four blocks per thread and round: their loads are issued together)
+  constexpr int kPassUnroll = 4;
+  for (int b0 = threadIdx.x; b0 < nb; b0 += kPassUnroll * blockDim.x) {
+    int e[kPassUnroll], prev[kPassUnroll], next[kPassUnroll];
+#pragma unroll
+    for (int j = 0; j < kPassUnroll; ++j) {
+      const int b = b0 + j * blockDim.x;
+      e[j] = b < nb ? block_expert[b] : 0;
+      prev[j] = (b < nb && b > 0) ? block_expert[b - 1] : -1;
+      next[j] = b + 1 < nb ? block_expert[b + 1] : N;
     }
-    const int next = b + 1 < nb ? block_expert[b + 1] : N;
-    if (prev != e) s_first[e] = b;
-    if (next != e) s_last[e] = b + 1;
+#pragma unroll
+    for (int j = 0; j < kPassUnroll; ++j) {
+      const int b = b0 + j * blockDim.x;
+      if (b >= nb) continue;
+      if (e[j] < 0 || e[j] >= N || prev[j] > e[j]) {
+        s_bad = 1;
+        continue;
+      }
+      if (prev[j] != e[j]) s_first[e[j]] = b;
+      if (next[j] != e[j]) s_last[e[j]] = b + 1;
+    }
   }
   __syncthreads();
   if (s_bad) {
