@@ -374,6 +374,8 @@ def run_gpu(args):
 
     wl = W.WORKLOADS[args.workload]
     T = args.tokens
+    if T is None:   # the workload's largest configured batch (the Mixtral-like layer: 4096)
+        T = max(wl.tokens)
     cfg = dict(wl.cfg)
     if args.capacity_factor is not None:
         cfg["capacity_factor"] = args.capacity_factor
@@ -649,7 +651,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=["tiny", "mix", "qw", "cap", "ds"])
-    ap.add_argument("--tokens", type=int, default=TOKENS)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens per GPU (default: the workload's largest configured batch)")
     ap.add_argument("--capacity-factor", type=float, default=None,
                     help="override the workload's capacity factor")
     ap.add_argument("--policy", default="drop", choices=["drop", "reroute"],
