@@ -963,8 +963,8 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
 int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
   if (T == 0) return 0;
-  // router + dispatch, then tile lists 2 + row gather 1 + W13 + W2 +
-  // combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2
+  // router + dispatch, then tile lists 1 (both lists in one launch) + row
+  // gather 1 + W13 + W2 + combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2
   // (chunked router), or on the tensor cores transpose, norms, GEMM,
   // candidate filter, tiled recompute, finalize = 6.
   // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
@@ -983,14 +983,14 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
     front = 2 + 9;
   } else if (moe::decode_front_ok(T, cfg->hidden, cfg->num_experts, cfg->top_k)) {
     // chunk sums, then routing, dispatch, tile lists and the routed rows
-    front = 2 - 2 - 1;
+    front = 2 - 1 - 1;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {
     // dispatch and both tile lists in one launch
-    front = router + 1 - 2;
+    front = router + 1 - 1;
   } else {
     front = router + 3;
   }
-  return front + 2 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
+  return front + 1 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }
 
 moe_status moe_router_tc_logits(const moe_config* cfg, int32_t T, const uint16_t* h,
