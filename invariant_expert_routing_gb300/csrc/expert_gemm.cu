@@ -812,6 +812,7 @@ bool gemm_smem_ok() {
   return optin >= (int)GemmCfg<true, kW13TileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kW2TileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes &&
+         optin >= (int)GemmCfg<false, kRouterTileRowsNarrow>::kSmemBytes &&
          optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes &&
          optin >= (int)PairCfg<false, true>::kSmemBytes;
 }
@@ -846,8 +847,11 @@ void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CU
 }
 
 void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
-                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
-  launch<false, kRouterTileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s, int tile_rows) {
+  if (tile_rows == kRouterTileRowsNarrow)
+    launch<false, kRouterTileRowsNarrow>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  else
+    launch<false, kRouterTileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
 }
 
 }  // namespace moe

@@ -22,6 +22,10 @@ constexpr int kDevErrBadBlocks = 0x4;
 constexpr int kW13TileRows = 128;
 constexpr int kW2TileRows = 256;
 constexpr int kRouterTileRows = 128;
+// The router's logits in 64-row token tiles when 128-row tiles would leave
+// SMs idle: they only filter candidates (every output logit is recomputed in
+// the canonical order), so the tile height may follow the batch.
+constexpr int kRouterTileRowsNarrow = 64;
 constexpr int kMaxTileRows = 256;
 // Output features of one grouped-GEMM tile (the M of every MMA).
 constexpr int kTileFeat = 128;
@@ -79,6 +83,6 @@ void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const C
 void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
 void launch_router_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
-                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s);
+                        const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s, int tile_rows);
 
 }  // namespace moe

@@ -241,9 +241,13 @@ moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const ui
   const int H = c->hidden, N = c->num_experts;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
+  // 64-row token tiles while 128-row ones would not give every SM a tile
+  const long long wide_units = (long long)((T + moe::kRouterTileRows - 1) / moe::kRouterTileRows) *
+                               (N / moe::kTileFeat);
+  const int rows = wide_units < sms ? moe::kRouterTileRowsNarrow : moe::kRouterTileRows;
   CUtensorMap m_wg, m_h, m_hs;
   if (!map_2d(&m_wg, wg, (uint64_t)N, (uint64_t)H, 64, 64) ||
-      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, moe::kRouterTileRows) ||
+      !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, (uint32_t)rows) ||
       !map_2d(&m_hs, h, (uint64_t)H, (uint64_t)T, 64, 32))
     return MOE_ERR_CUDA;
   moe::GemmArgs g{};
@@ -254,8 +258,7 @@ moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const ui
   g.out = logits;
   g.out_ld = N;
   g.status = at<int>(ws, L.status);
-  moe::launch_router_gemm(m_wg, m_h, m_hs, g, (T + moe::kRouterTileRows - 1) / moe::kRouterTileRows, sms,
-                          s);
+  moe::launch_router_gemm(m_wg, m_h, m_hs, g, (T + rows - 1) / rows, sms, s, rows);
   return last_cuda();
 }
 
