@@ -9,7 +9,11 @@ tokens of the Mixtral-like layer (H 4096, 8 experts, top-2, I 14336, block
 64, T 4096), inputs resident in HBM.  Prints one JSON line: routed tokens/s
 for the whole job, the roofline of the dominant kernel, the end-to-end rate
 through the host-buffer entry point, the CPU oracle timed on the host cores,
-and the SM clocks seen during the timed region.
+the SM clocks seen during the timed region, and (key "workloads") one
+cold-L2 entry for every other configured layer and batch size: the tiny
+layer, the Mixtral-like decode sizes, the Qwen-like layer at T = 1, 32, 512
+and 8192, the capacity-limited layer and the DeepSeek-like layer at T = 1,
+64 and 16448, each with its fraction of the measured peak of its bound.
 
 Under torchrun (N > 1) every rank runs its own shard of tokens (a different
 token seed) against replicated weights: no collective on the data path
@@ -70,6 +74,44 @@ def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
         dist.barrier()
+
+
+# --------------------------------------------------------------------------- host <-> device plumbing
+def dev_bf16(a, device):
+    """uint16 bf16 bit patterns (numpy) -> torch.bfloat16 device tensor."""
+    import numpy as np
+    import torch
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def dev(a, device):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def host_bf16(t):
+    """torch.bfloat16 tensor -> uint16 bit patterns (numpy)."""
+    import numpy as np
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+OUT_ATOL, OUT_RTOL = 2e-2, 1e-2   # |gpu - ref| <= atol + rtol*|ref| (bf16 in, fp32 accumulation)
+
+
+def max_err_within_tolerance(got_bits, ref_bits):
+    """Largest |gpu - ref| over the compared elements; raises if any element
+    is outside the layer tolerance."""
+    import numpy as np
+    from synth import bf16_to_f32
+    got = bf16_to_f32(np.asarray(got_bits, np.uint16)).astype(np.float64)
+    ref = bf16_to_f32(np.asarray(ref_bits, np.uint16)).astype(np.float64)
+    err = np.abs(got - ref)
+    if not np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)):
+        raise RuntimeError("GPU rows outside the tolerance of the oracle's")
+    return float(err.max()) if err.size else 0.0
 
 
 # --------------------------------------------------------------------------- roofline inputs
@@ -318,10 +360,11 @@ def batch_counts(moe, cfg, wl, h_d, wg_d, bias_d, ws, device):
     return int(c.sum()), int((c > 0).sum()), third
 
 
-def time_graph(fwd, n):
-    """Per-forward device time of `fwd` captured once in a CUDA graph and
-    replayed n times (removes host launch overhead, which dominates small
-    batches)."""
+def time_graph_cold(fwd, n, flush):
+    """Per-forward device times of `fwd`, captured once in a CUDA graph and
+    replayed n times, each replay between its own pair of CUDA events, with
+    `flush` (a buffer larger than L2) written before each replay outside the
+    events, so that every replay reads its weights from HBM."""
     import torch
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -335,13 +378,91 @@ def time_graph(fwd, n):
     for _ in range(3):
         graph.replay()
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
         graph.replay()
-    e1.record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / n
+    del graph
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+# The configured layers and batch sizes (the layer shapes of synth.workloads;
+# batch sizes per layer as configured there, the DeepSeek-like layer at its
+# decode sizes and its largest invariance batch)
+CONFIGURED = [("tiny", (64,)), ("mix", (1, 16, 128, 4096)), ("qw", (1, 32, 512, 8192)),
+              ("cap", (8192,)), ("ds", (1, 64, 16448))]
+
+
+def run_workloads(moe, W, device, peaks, skip):
+    """One entry per configured (layer, T) except `skip` (the headline):
+    cold-L2 graph-replay time, tokens/s, the layer's algorithmic work and its
+    fraction of the bound's measured peak, and one forward's stage times."""
+    import numpy as np
+    import torch
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_gb = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ridge = peak_tf * 1e12 / (peak_gb * 1e9)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    names = ["router", "dispatch_align", "tile_list_and_row_gather", "w13_gemm", "w2_gemm",
+             "shared_expert", "combine"]
+    out = []
+    for name, Ts in CONFIGURED:
+        Ts = [t for t in Ts if (name, t) != tuple(skip)]
+        if not Ts:
+            continue
+        wl = W.WORKLOADS[name]
+        cfg = dict(wl.cfg)
+        wg, bias = W.make_router(wl)
+        wg_d = dev_bf16(wg, device)
+        bias_d = None if bias is None else dev(bias, device)
+        w13_d, w2_d, w13s_d, w2s_d = W.make_experts_device(wl, 0, device)
+        ws = moe.workspace(cfg, max(Ts), device)
+        for T in Ts:
+            h_d = dev_bf16(W.make_h(wl, T, seed=17), device)
+            o_d = torch.empty((T, wl.hidden), dtype=torch.bfloat16, device=device)
+
+            def fwd():
+                moe.moe_forward(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, o_d, ws)
+
+            moe.moe_clear_device_status(ws)
+            for _ in range(3):
+                fwd()
+            n_it = 30 if T <= 512 else 10
+            ms_eager = time_forwards(moe, fwd, 5, stream)
+            times = time_graph_cold(fwd, n_it, flush)
+            ms = float(np.mean(times))
+            # stage split of one more (cold) forward
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+            for e in ev:
+                e.record(stream)
+            flush.fill_(1)
+            moe.moe_forward_timed(cfg, h_d, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, o_d, ws, ev)
+            torch.cuda.synchronize()
+            stage = {nm: ev[i].elapsed_time(ev[i + 1]) for i, nm in enumerate(names)}
+            if moe.moe_get_device_status(ws) & moe.MOE_DEV_ERR_MASK:
+                raise RuntimeError(f"device status word set on {name} T={T}")
+            kr, tch, dropped = batch_counts(moe, cfg, wl, h_d, wg_d, bias_d, ws, device)
+            f_s, b_s = algorithmic_work(wl, T, kr, tch)
+            bound = "tensor" if f_s / b_s >= ridge else "hbm"
+            e = {"workload": name, "T": T, "ms": ms, "ms_median": float(np.median(times)),
+                 "ms_min": float(np.min(times)), "ms_eager_warm": ms_eager, "replays": n_it,
+                 "tokens_per_s": T / (ms * 1e-3), "kept_routes": kr, "dropped_routes": dropped,
+                 "touched_experts": tch, "algorithmic_gflop": f_s / 1e9, "algorithmic_gb": b_s / 1e9,
+                 "tflops": f_s / (ms * 1e-3) / 1e12, "gbs": b_s / (ms * 1e-3) / 1e9, "bound": bound,
+                 "launches": moe.moe_forward_launch_count(cfg, T),
+                 "stage_ms_one_cold_forward": stage}
+            e["frac"] = e["tflops"] / peak_tf if bound == "tensor" else e["gbs"] / peak_gb
+            e["peak"] = peak_tf if bound == "tensor" else peak_gb
+            e["peak_unit"] = "TFLOP/s (measured bf16 burst)" if bound == "tensor" else "GB/s (measured HBM copy)"
+            out.append(e)
+            del h_d, o_d
+        del w13_d, w2_d, w13s_d, w2s_d, ws, wg_d, bias_d
+        torch.cuda.empty_cache()
+    return out
 
 
 def time_forwards(moe, fwd, n, stream):
@@ -370,7 +491,6 @@ def run_gpu(args):
 
     import invariant_expert_routing_gb300 as moe
     from synth import workloads as W
-    from tests.gpu_util import dev, dev_bf16, host_bf16
 
     wl = W.WORKLOADS[args.workload]
     T = args.tokens
@@ -390,8 +510,7 @@ def run_gpu(args):
     h = W.make_h(wl, T, seed=shard_seed(rank))
     h_d = dev_bf16(h, device)
     out_d = torch.empty((T, wl.hidden), dtype=torch.bfloat16, device=device)
-    max_T = max([T] + ([] if args.no_sweep else list(wl.tokens)))
-    ws = moe.workspace(cfg, max_T, device)
+    ws = moe.workspace(cfg, T, device)
     moe.moe_clear_device_status(ws)
     stream = torch.cuda.current_stream()
 
@@ -410,7 +529,7 @@ def run_gpu(args):
     for _ in range(max(args.warmup, 3)):
         fwd()
     torch.cuda.synchronize()
-    if moe.moe_get_device_status(ws) != 0:
+    if moe.moe_get_device_status(ws) & moe.MOE_DEV_ERR_MASK:
         raise RuntimeError("device status word set during warm-up")
 
     # ---- timed region: K forwards, stage events recorded inside each one
@@ -467,7 +586,7 @@ def run_gpu(args):
     stage_ms = stage.mean(axis=0)
     names = ["router", "dispatch_align", "tile_list_and_row_gather", "w13_gemm", "w2_gemm",
              "shared_expert", "combine"]
-    if moe.moe_get_device_status(ws) != 0:
+    if moe.moe_get_device_status(ws) & moe.MOE_DEV_ERR_MASK:
         raise RuntimeError("device status word set during the timed region")
 
     # ---- algorithmic work of this batch and the roofline of the dominant kernel
@@ -550,32 +669,6 @@ def run_gpu(args):
                                                         np.quantile(m, [0.01, 0.1, 0.5]))},
                                "tokens_with_zero_margin": int((m == 0).sum())}
 
-    # ---- the workload's other batch sizes (secondary lines, same layer)
-    sweep = []
-    for Ts in ([] if args.no_sweep else [t for t in wl.tokens if t != T]):
-        hs = dev_bf16(W.make_h(wl, Ts, seed=shard_seed(rank) + 17), device)
-        outs = torch.empty((Ts, wl.hidden), dtype=torch.bfloat16, device=device)
-
-        def fwd_s():
-            moe.moe_forward(cfg, hs, wg_d, bias_d, w13_d, w2_d, w13s_d, w2s_d, outs, ws)
-
-        for _ in range(3):
-            fwd_s()
-        n_it = 50 if Ts <= 1024 else 10
-        ms_eager = time_forwards(moe, fwd_s, n_it, stream)
-        ms = time_graph(fwd_s, n_it)
-        kr, tch, _ = batch_counts(moe, cfg, wl, hs, wg_d, bias_d, ws, device)
-        f_s, b_s = algorithmic_work(wl, Ts, kr, tch)
-        entry = {"T": Ts, "ms": ms, "ms_eager": ms_eager, "timing": "CUDA graph replay",
-                 "tokens_per_s": Ts / (ms * 1e-3), "touched_experts": tch,
-                 "tflops": f_s / (ms * 1e-3) / 1e12, "gbs": b_s / (ms * 1e-3) / 1e9}
-        entry["bound"] = "tensor" if f_s / b_s >= ridge else "hbm"
-        entry["frac"] = (entry["tflops"] / peak_tf if entry["bound"] == "tensor"
-                         else entry["gbs"] / peak_gb)
-        sweep.append(entry)
-    if sweep:
-        line["sweep"] = sweep
-
     # ---- end to end through the host-buffer entry point
     h_host = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory()
     out_host = torch.empty((T, wl.hidden), dtype=torch.bfloat16).pin_memory()
@@ -602,6 +695,18 @@ def run_gpu(args):
             and default_mode and wl.weight_bytes() < (8 << 30)):
         line["cpu_baseline"] = cpu_baseline(wl, h, wg, bias, host_bf16(out_d))
 
+    # ---- every configured layer and batch size (secondary entries, one GPU)
+    if not args.no_sweep and default_mode and world == 1:
+        del w13_d, w2_d, w13s_d, w2s_d, ws
+        torch.cuda.empty_cache()
+        line["workloads"] = run_workloads(moe, W, device, peaks, skip=(wl.name, T))
+        line["workloads_timing"] = (
+            "per configured (layer, T) other than the headline: the forward captured in a CUDA graph, "
+            "each replay bracketed by its own CUDA events with a 512 MB buffer written between "
+            "replays (cold L2: the weights and tokens come from HBM every time); ms = mean over "
+            "the replays; frac against the measured bf16 burst peak (tensor-bound) or the measured "
+            "HBM copy bandwidth (HBM-bound) from the layer's algorithmic flops and bytes")
+
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -616,7 +721,6 @@ def cpu_baseline(wl, h, wg, bias, gpu_out):
     depends on its own row, so a sample of tokens is a faithful sub-batch."""
     import numpy as np
     from synth import workloads as W
-    from tests.checks import check_outputs
     cores = os.cpu_count() or 1
     w13, w2 = W.make_experts(wl)
     rng = np.random.default_rng(123)
@@ -634,7 +738,7 @@ def cpu_baseline(wl, h, wg, bias, gpu_out):
             outs = o
         done += len(sel)
     el = time.perf_counter() - t0
-    err = check_outputs(gpu_out[toks], outs)
+    err = max_err_within_tolerance(gpu_out[toks], outs)
     return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": (f"{done} tokens of the T={T} batch in groups of {len(toks)} (router, top-k, "
                        f"their {done * wl.top_k} expert FFN routes in fp64, combine), {el:.1f} s"),
@@ -649,7 +753,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the entries of the other configured layers and batch sizes")
     ap.add_argument("--workload", default=WORKLOAD, choices=["tiny", "mix", "qw", "cap", "ds"])
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per GPU (default: the workload's largest configured batch)")

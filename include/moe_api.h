@@ -80,7 +80,32 @@ typedef struct moe_config {
   int32_t shared_intermediate; /* Is of the always-on shared expert; 0: none */
   int32_t overflow_policy;     /* MOE_OVERFLOW_DROP or MOE_OVERFLOW_REROUTE (token choice) */
   int32_t routing;             /* MOE_ROUTING_TOKEN_CHOICE or MOE_ROUTING_EXPERT_CHOICE */
+  /* Testing and diagnosis only; leave zero in production.  None of these
+   * changes a result bit: each forces one of several equivalent ways of
+   * computing the same integers and floats, or shortens the bounded waits. */
+  uint32_t debug_flags;        /* MOE_DEBUG_* bits */
+  int32_t debug_grid_ctas;     /* > 0: at most this many CTAs run the reroute's grid-wide
+                                  rounds (more routes per CTA); 0: one per SM */
+  int64_t debug_wait_ns;       /* > 0: every bounded device wait gives up after this many ns
+                                  (the grouped GEMM's pipeline waits, default 2 s, and the
+                                  reroute's grid barrier, default 0.2 s); 0: the defaults */
 } moe_config;
+
+/* debug_flags bits.  Each pair of alternatives computes the same bits; a
+ * flag only selects which kernels run (the tests compare them). */
+#define MOE_DEBUG_ROUTER_TC 0x1u          /* tensor-core router with the certified filter
+                                             wherever it can serve the call (N % 128 == 0,
+                                             no logits_out), whatever T */
+#define MOE_DEBUG_ROUTER_CHUNKED 0x2u     /* chunked CUDA-core router for every batch */
+#define MOE_DEBUG_ROW_GATHER 0x4u         /* routed token rows copied in segment order */
+#define MOE_DEBUG_ROW_SCATTER 0x8u        /* routed token rows copied token by token
+                                             (moe_forward; moe_expert_ffn always gathers) */
+#define MOE_DEBUG_NO_DECODE_FRONT 0x10u   /* no fused decode front for T <= 2 */
+#define MOE_DEBUG_REROUTE_SEQUENTIAL 0x20u /* reroute: the sequential kernel alone */
+#define MOE_DEBUG_REROUTE_GRID 0x40u      /* reroute: grid-wide acceptance rounds for any batch */
+#define MOE_DEBUG_REROUTE_ONE_CTA 0x80u   /* reroute: one-CTA acceptance rounds for any batch */
+#define MOE_DEBUG_ROUTER_TILE128 0x100u   /* tensor-core router logits in 128-row token tiles */
+#define MOE_DEBUG_ROUTER_TILE64 0x200u    /* tensor-core router logits in 64-row token tiles */
 
 /* Output of moe_routing_stats (device memory, 40 bytes). */
 typedef struct moe_route_stats {
@@ -100,7 +125,7 @@ typedef enum moe_status {
   MOE_ERR_UNSUPPORTED = 2, /* shape outside the supported set above */
   MOE_ERR_WORKSPACE = 3,   /* workspace smaller than moe_workspace_bytes(cfg, T) */
   MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
-  MOE_ERR_DEVICE = 5       /* the device status word is non-zero */
+  MOE_ERR_DEVICE = 5       /* the device status word has an error bit set */
 } moe_status;
 
 /* Bits of the device status word. */
@@ -108,6 +133,12 @@ typedef enum moe_status {
 #define MOE_DEV_ERR_TIMEOUT 0x2      /* a bounded pipeline wait gave up; outputs are invalid */
 #define MOE_DEV_ERR_BAD_BLOCKS 0x4   /* moe_expert_ffn got a block list that is unsorted, out of
                                         range or longer than the bound: no expert work was done */
+/* Informational bit (not an error; moe_get_device_status still returns
+ * MOE_OK when it is the only bit set): the reroute's grid-wide acceptance
+ * rounds gave up at a device-wide barrier that waited past its limit, and the
+ * sequential kernel computed the assignment instead (valid results). */
+#define MOE_DEV_NOTE_REROUTE_FALLBACK 0x100
+#define MOE_DEV_ERR_MASK 0xFF        /* bits that mark invalid outputs */
 
 /* Text for a status code (static storage). */
 const char* moe_status_string(moe_status s);
@@ -390,7 +421,10 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T);
  *     word (MOE_DEV_ERR_EXPERT_RANGE for expert ids outside [0, N)).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  A new context on the device (after
+ *     cudaDeviceReset, for example) moves the array: the next call notices
+ *     the change of context and looks the address up again, so make the
+ *     first call after a reset before any capture too.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents (the call clears what must start at zero).  Calls that
  *     overlap on the GPU (e.g. on two streams at once) race on it: order them. */
@@ -400,7 +434,8 @@ moe_status moe_dispatch_align_noalloc(const moe_config* cfg, int32_t T, const in
                                       int32_t* num_padded, int32_t* expert_counts,
                                       int32_t* num_dropped, int32_t* status_out, void* stream);
 
-/* Reads the device status word of `ws` (synchronises `stream`). */
+/* Reads the device status word of `ws` (synchronises `stream`): the whole word
+ * in *status_out; MOE_ERR_DEVICE if any bit of MOE_DEV_ERR_MASK is set. */
 moe_status moe_get_device_status(const void* ws, int32_t* status_out, void* stream);
 
 /* Clears the device status word of `ws` (asynchronous on `stream`). */

@@ -30,6 +30,19 @@ MOE_ERR_DEVICE = 5
 MOE_DEV_ERR_EXPERT_RANGE = 0x1
 MOE_DEV_ERR_TIMEOUT = 0x2
 MOE_DEV_ERR_BAD_BLOCKS = 0x4
+MOE_DEV_NOTE_REROUTE_FALLBACK = 0x100
+MOE_DEV_ERR_MASK = 0xFF
+# debug_flags bits (testing only; each forces one of several equivalent paths)
+MOE_DEBUG_ROUTER_TC = 0x1
+MOE_DEBUG_ROUTER_CHUNKED = 0x2
+MOE_DEBUG_ROW_GATHER = 0x4
+MOE_DEBUG_ROW_SCATTER = 0x8
+MOE_DEBUG_NO_DECODE_FRONT = 0x10
+MOE_DEBUG_REROUTE_SEQUENTIAL = 0x20
+MOE_DEBUG_REROUTE_GRID = 0x40
+MOE_DEBUG_REROUTE_ONE_CTA = 0x80
+MOE_DEBUG_ROUTER_TILE128 = 0x100
+MOE_DEBUG_ROUTER_TILE64 = 0x200
 MOE_OVERFLOW_DROP = 0
 MOE_OVERFLOW_REROUTE = 1
 MOE_ROUTING_TOKEN_CHOICE = 0
@@ -41,7 +54,8 @@ class moe_config(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
                 ("shared_intermediate", ctypes.c_int32), ("overflow_policy", ctypes.c_int32),
-                ("routing", ctypes.c_int32)]
+                ("routing", ctypes.c_int32), ("debug_flags", ctypes.c_uint32),
+                ("debug_grid_ctas", ctypes.c_int32), ("debug_wait_ns", ctypes.c_int64)]
 
 
 class moe_route_stats(ctypes.Structure):
@@ -98,9 +112,11 @@ EXPORTED = tuple(_SIGS)
 
 def make_config(hidden, num_experts, top_k, intermediate, block_size, capacity_factor=0.0,
                 shared_intermediate=0, overflow_policy=MOE_OVERFLOW_DROP,
-                routing=MOE_ROUTING_TOKEN_CHOICE) -> moe_config:
+                routing=MOE_ROUTING_TOKEN_CHOICE, debug_flags=0, debug_grid_ctas=0,
+                debug_wait_ns=0) -> moe_config:
     return moe_config(hidden, num_experts, top_k, intermediate, block_size, capacity_factor,
-                      shared_intermediate, overflow_policy, routing)
+                      shared_intermediate, overflow_policy, routing, debug_flags, debug_grid_ctas,
+                      debug_wait_ns)
 
 
 def _cfg(cfg) -> moe_config:

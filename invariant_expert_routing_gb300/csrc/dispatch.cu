@@ -15,8 +15,6 @@
 // every launch shape gives the same bits.
 #include <cstdint>
 
-#include <cstdlib>
-#include <cstring>
 
 #include "kernels.h"
 #include "pdl.cuh"
@@ -611,7 +609,8 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
                              int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
                              int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
                              int32_t* num_rerouted, int32_t* rank_in_tile, int32_t* tile_count,
-                             int32_t* seg_off, const RerouteScratch& sc, int* status, cudaStream_t s) {
+                             int32_t* seg_off, const RerouteScratch& sc, int* status, const PathOpts& o,
+                             cudaStream_t s) {
   const int R = T * k;
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   // phase one: ranks and the per-expert kept counts of the drop rule
@@ -621,7 +620,7 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
              seg_off, expert_counts, num_padded, (int32_t*)nullptr, block_expert, sorted_route_ids);
   // phase two, then the stable layout of the final assignment
   launch_reroute(topk_idx, logits, T, N, k, capacity, rank_in_tile, tile_count, expert_counts, sc,
-                 route_expert, num_dropped, num_rerouted, s);
+                 route_expert, num_dropped, num_rerouted, status, o, s);
   launch_dispatch_routes(route_expert, R, N, B, route_kept, route_pos, sorted_route_ids, block_expert,
                          num_padded, expert_counts, rank_in_tile, tile_count, seg_off, status, s);
 }
@@ -638,11 +637,10 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
       expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, status);
 }
 
-// MOE_DECODE_FRONT=0 turns the two-launch front off (read at each call; the
-// bits are the same either way).
-bool decode_front_ok(int T, int H, int N, int k) {
-  const char* v = std::getenv("MOE_DECODE_FRONT");
-  if (v && std::strcmp(v, "0") == 0) return false;
+// The caller's path flags may turn the two-launch front off (the bits are
+// the same either way).
+bool decode_front_ok(int T, int H, int N, int k, uint32_t path_flags) {
+  if (path_flags & kPathNoDecodeFront) return false;
   return T >= 1 && T <= kFinishMaxT && H % 8 == 0 && N <= kMaxN && k <= 16 && T * k <= kFinishThreads;
 }
 

@@ -11,9 +11,14 @@
 //
 // Host code never uses the array's name as an address: on the host that name
 // is only a stand-in for the device symbol.  The device address is obtained
-// with cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on it, and passed to the kernels.
+// with cudaGetSymbolAddress once per device context, with that device
+// current, on the first call made in it, and passed to the kernels.  A new
+// context on the device (after cudaDeviceReset, say) reloads the module and
+// moves the array, so the address is looked up again whenever the current
+// context's unique id differs from the one it was found in.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 #include <mutex>
@@ -38,22 +43,57 @@ constexpr size_t kScratchWords = kSegOffOff + kMaxExperts;                      
 static __device__ __align__(256) int32_t g_dispatch_scratch[kScratchWords];
 
 constexpr int kMaxDevices = 64;
-int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
+struct ScratchAddr {
+  int32_t* addr = nullptr;
+  unsigned long long ctx_id = 0;   // unique id of the context the address belongs to
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current).
+// Unique id of the calling thread's current context (0 if none).  The
+// driver entry points are looked up through the runtime, as for the tensor
+// maps, so the library needs no link against the driver library.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current, again whenever the device's context has changed.
 moe_status scratch_on_current_device(int32_t** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  unsigned long long ctx_id = 0;
+  const bool have_ctx = current_context_id(&ctx_id);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (!have_ctx || !a.addr || a.ctx_id != ctx_id) {
+    // (this runtime call also makes the device's context current if no
+    // runtime call has done so on this thread yet)
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    if (!current_context_id(&ctx_id)) return MOE_ERR_CUDA;
+    a.addr = static_cast<int32_t*>(p);
+    a.ctx_id = ctx_id;
   }
-  *out = g_scratch_addr[dev];
+  *out = a.addr;
   return MOE_OK;
 }
 

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ksteps = args.K / kBK;
+  const uint64_t wlim = args.wait_ns ? args.wait_ns : kWaitLimitNs;   // pipeline waits
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < ksteps; ++ks) {
         // one lane waits, the warp follows its verdict (keeps the warp converged)
         int got = 1;
-        if (lane == 0) got = mbar_wait(empty0 + 8 * stage, phase ^ 1u, &s_abort) ? 1 : 0;
+        if (lane == 0) got = mbar_wait(empty0 + 8 * stage, phase ^ 1u, &s_abort, wlim) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           ok = false;
@@ -254,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int item = unit0; item < total && ok; item += units) {
         const bool small = work_of<BN>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
         const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d0 = tmem + acc * C::kAccCols;
         for (int ks = 0; ks < ksteps; ++ks) {
-          if (!mbar_wait(full0 + 8 * stage, phase, &s_abort)) {
+          if (!mbar_wait(full0 + 8 * stage, phase, &s_abort, wlim)) {
             ok = false;
             break;
           }
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo t = wk.t;
       const int f = wk.f;
       int got = 1;
-      if (lane == 0) got = mbar_wait(tfull0 + 8 * acc, acc_phase, &s_abort) ? 1 : 0;
+      if (lane == 0) got = mbar_wait(tfull0 + 8 * acc, acc_phase, &s_abort, wlim) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) {
         if (lane == 0) {
@@ -450,6 +451,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also returns the AND of `pred` over its threads.
+__device__ __forceinline__ int named_bar_and(int id, int threads, int pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\t"
+      "setp.ne.b32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(threads)
+      : "memory");
+  return (int)r;
+}
+
 template <bool kW13, bool kWide = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
@@ -482,6 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ksteps = args.K / kBK;
+  const uint64_t wlim = args.wait_ns ? args.wait_ns : kWaitLimitNs;   // pipeline waits
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < C::kStages; ++st) {
@@ -533,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
         int got = 1;
-        if (lane == 0) got = mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, &s_abort) ? 1 : 0;
+        if (lane == 0) got = mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, &s_abort, wlim) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           ok = false;
@@ -600,14 +616,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int item = pair0; item < total && ok; item += pairs) {
         const bool small = work_of<kPairRows>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
         const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
-        if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort)) {
+        if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d0 = tmem + acc * C::kAccCols;
         for (int ks = 0; ks < ksteps; ++ks) {
-          if (!mbar_wait_cluster(full0 + 8 * stage, phase, &s_abort)) {
+          if (!mbar_wait_cluster(full0 + 8 * stage, phase, &s_abort, wlim)) {
             ok = false;
             break;
           }
@@ -662,8 +678,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
       int got = 1;
-      if (lane == 0) got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, &s_abort) ? 1 : 0;
+      if (lane == 0) got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, &s_abort, wlim) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
+      // W13: the gate and up warps of a pair meet on a named barrier for
+      // every chunk of the tile, so they take the same verdict (one of them
+      // must not go on to the exchange while the other gives up)
+      if (kW13) got = named_bar_and(1 + xpair, 64, got);
       if (!got) {
         if (lane == 0) {
           s_abort = 1;

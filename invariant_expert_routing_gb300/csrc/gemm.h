@@ -12,6 +12,7 @@ namespace moe {
 constexpr int kDevErrExpertRange = 0x1;
 constexpr int kDevErrTimeout = 0x2;
 constexpr int kDevErrBadBlocks = 0x4;
+constexpr int kDevNoteRerouteFallback = 0x100;
 
 // Rows of one grouped-GEMM token tile (the N of every tcgen05 MMA), one
 // fixed value per GEMM for every layer and every T: one tile shape, one K
@@ -59,6 +60,7 @@ struct GemmArgs {
                        //    128-row boxes; n_feat_tiles in units of kPairFeatW13 / kPairFeatW2)
   int wide;            // W2 pairs only, 1: items of two 256-feature groups
                        //    (n_feat_tiles in units of kPairFeatW2Wide)
+  unsigned long long wait_ns;  // limit of the pipeline waits; 0: kWaitLimitNs
 };
 
 // Rows of a CTA-pair token tile, the token box each CTA of the pair loads,

@@ -8,6 +8,26 @@
 
 namespace moe {
 
+// Which of several equivalent kernel paths a call takes, and the limit of the
+// bounded device waits: moe_config's debug fields (mirrors MOE_DEBUG_* of
+// include/moe_api.h).  Zero everywhere: the defaults.  No option changes a
+// result bit.
+constexpr uint32_t kPathRouterTc = 0x1;
+constexpr uint32_t kPathRouterChunked = 0x2;
+constexpr uint32_t kPathRowGather = 0x4;
+constexpr uint32_t kPathRowScatter = 0x8;
+constexpr uint32_t kPathNoDecodeFront = 0x10;
+constexpr uint32_t kPathRerouteSequential = 0x20;
+constexpr uint32_t kPathRerouteGrid = 0x40;
+constexpr uint32_t kPathRerouteOneCta = 0x80;
+constexpr uint32_t kPathRouterTile128 = 0x100;
+constexpr uint32_t kPathRouterTile64 = 0x200;
+struct PathOpts {
+  uint32_t flags = 0;
+  int grid_ctas = 0;      // > 0: cap on the CTAs of the reroute's grid-wide rounds
+  uint64_t wait_ns = 0;   // > 0: limit of the bounded waits (else each wait's default)
+};
+
 // Router reduction chunk (elements of H summed in order before combining).
 constexpr int kRouterChunk = 256;
 // Routes handled by one CTA of the dispatch count/scatter kernels.
@@ -21,7 +41,7 @@ constexpr int kDispatchTile = 1024;
 // serves the call and T * H * N exceeds 3 * 2^28.  part:
 // chunked_router_part_floats floats.
 constexpr int kDecodeRouterMaxT = 64;
-bool chunked_router_ok(int T, int H, int N, bool tc_router);
+bool chunked_router_ok(int T, int H, int N, bool tc_router, uint32_t path_flags);
 size_t chunked_router_part_floats(int T, int H, int N);
 // the chunk sums alone (part: chunked_router_part_floats floats)
 void launch_router_partials(const uint16_t* h, const uint16_t* w_gate, float* part, int T, int H, int N,
@@ -82,7 +102,7 @@ struct RerouteScratch {
 void launch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int capacity,
                     const int32_t* rank_in_tile, const int32_t* tile_base, const int32_t* kept_count,
                     const RerouteScratch& sc, int32_t* route_expert, int32_t* num_dropped,
-                    int32_t* num_rerouted, cudaStream_t s);
+                    int32_t* num_rerouted, int* status, const PathOpts& o, cudaStream_t s);
 // phase one of launch_dispatch, overflow reroute, then the layout of the
 // final assignment (route_expert: expert per route, -1 = dropped)
 void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int B,
@@ -90,7 +110,8 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
                              int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
                              int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
                              int32_t* num_rerouted, int32_t* rank_in_tile, int32_t* tile_count,
-                             int32_t* seg_off, const RerouteScratch& sc, int* status, cudaStream_t s);
+                             int32_t* seg_off, const RerouteScratch& sc, int* status, const PathOpts& o,
+                             cudaStream_t s);
 // stable layout of routes that already carry their expert (-1 = none)
 void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, uint8_t* route_kept,
                             int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
@@ -113,7 +134,7 @@ void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int cap
 // (launch_router_partials), then in one CTA the logits in the canonical
 // order, top-k and gates, launch_dispatch_small's results and the routed
 // token rows of x_perm (padding rows untouched): two launches.
-bool decode_front_ok(int T, int H, int N, int k);
+bool decode_front_ok(int T, int H, int N, int k, uint32_t path_flags);
 void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part, int T, int H,
                          int N, int k,
                          int B, int capacity, int32_t* topk_idx, float* gates, uint8_t* route_kept,

@@ -9,8 +9,6 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -20,6 +18,17 @@ namespace {
 using moe::GemmTile;
 
 constexpr int kMaxDevices = 64;
+constexpr uint32_t kKnownDebugFlags = 0x3FFu;
+static_assert(MOE_DEBUG_ROUTER_TC == moe::kPathRouterTc && MOE_DEBUG_ROUTER_CHUNKED == moe::kPathRouterChunked &&
+                  MOE_DEBUG_ROW_GATHER == moe::kPathRowGather && MOE_DEBUG_ROW_SCATTER == moe::kPathRowScatter &&
+                  MOE_DEBUG_NO_DECODE_FRONT == moe::kPathNoDecodeFront &&
+                  MOE_DEBUG_REROUTE_SEQUENTIAL == moe::kPathRerouteSequential &&
+                  MOE_DEBUG_REROUTE_GRID == moe::kPathRerouteGrid &&
+                  MOE_DEBUG_REROUTE_ONE_CTA == moe::kPathRerouteOneCta &&
+                  MOE_DEBUG_ROUTER_TILE128 == moe::kPathRouterTile128 &&
+                  MOE_DEBUG_ROUTER_TILE64 == moe::kPathRouterTile64,
+              "debug flags mirror the internal path flags");
+static_assert(MOE_DEV_NOTE_REROUTE_FALLBACK == moe::kDevNoteRerouteFallback, "status bits");
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -40,7 +49,24 @@ moe_status check_cfg(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->routing != MOE_ROUTING_TOKEN_CHOICE && c->routing != MOE_ROUTING_EXPERT_CHOICE)
     return MOE_ERR_INVALID_ARG;
+  // debug fields: known bits only, no contradictory pair
+  const uint32_t f = c->debug_flags;
+  if (f & ~kKnownDebugFlags) return MOE_ERR_INVALID_ARG;
+  auto both = [f](uint32_t a, uint32_t b) { return (f & a) && (f & b); };
+  if (both(MOE_DEBUG_ROUTER_TC, MOE_DEBUG_ROUTER_CHUNKED) || both(MOE_DEBUG_ROW_GATHER, MOE_DEBUG_ROW_SCATTER) ||
+      both(MOE_DEBUG_REROUTE_GRID, MOE_DEBUG_REROUTE_ONE_CTA) ||
+      both(MOE_DEBUG_ROUTER_TILE128, MOE_DEBUG_ROUTER_TILE64))
+    return MOE_ERR_INVALID_ARG;
+  if (c->debug_grid_ctas < 0 || c->debug_wait_ns < 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+moe::PathOpts opts_of(const moe_config* c) {
+  moe::PathOpts o;
+  o.flags = c->debug_flags;
+  o.grid_ctas = c->debug_grid_ctas;
+  o.wait_ns = (uint64_t)c->debug_wait_ns;
+  return o;
 }
 
 bool expert_choice(const moe_config* c) { return c->routing == MOE_ROUTING_EXPERT_CHOICE; }
@@ -244,7 +270,9 @@ moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const ui
   // 64-row token tiles while 128-row ones would not give every SM a tile
   const long long wide_units = (long long)((T + moe::kRouterTileRows - 1) / moe::kRouterTileRows) *
                                (N / moe::kTileFeat);
-  const int rows = wide_units < sms ? moe::kRouterTileRowsNarrow : moe::kRouterTileRows;
+  int rows = wide_units < sms ? moe::kRouterTileRowsNarrow : moe::kRouterTileRows;
+  if (c->debug_flags & MOE_DEBUG_ROUTER_TILE128) rows = moe::kRouterTileRows;
+  if (c->debug_flags & MOE_DEBUG_ROUTER_TILE64) rows = moe::kRouterTileRowsNarrow;
   CUtensorMap m_wg, m_h, m_hs;
   if (!map_2d(&m_wg, wg, (uint64_t)N, (uint64_t)H, 64, 64) ||
       !map_2d(&m_h, h, (uint64_t)H, (uint64_t)T, 64, (uint32_t)rows) ||
@@ -258,6 +286,7 @@ moe_status tc_logits(const moe_config* c, int32_t T, const uint16_t* h, const ui
   g.out = logits;
   g.out_ld = N;
   g.status = at<int>(ws, L.status);
+  g.wait_ns = (unsigned long long)c->debug_wait_ns;
   moe::launch_router_gemm(m_wg, m_h, m_hs, g, (T + rows - 1) / rows, sms, s, rows);
   return last_cuda();
 }
@@ -266,7 +295,7 @@ moe_status route_impl(const moe_config* c, int32_t T, const uint16_t* h, const u
                       const float* bias, int32_t* idx, float* gates, float* logits, bool canonical_logits,
                       void* ws, cudaStream_t s, int32_t* n_cand = nullptr) {
   const int H = c->hidden, N = c->num_experts, k = c->top_k;
-  if (moe::chunked_router_ok(T, H, N, use_tc_router(c) && !canonical_logits) && !n_cand) {
+  if (moe::chunked_router_ok(T, H, N, use_tc_router(c) && !canonical_logits, c->debug_flags) && !n_cand) {
     // a few tokens, or a small W_g: chunk sums spread over many CTAs, the
     // same bits as either path below
     const Layout L = layout_of(c, T);
@@ -319,7 +348,7 @@ moe_status reroute_impl(const moe_config* c, int32_t T, const int32_t* idx, cons
   moe::launch_dispatch_reroute(idx, logits, T, c->num_experts, c->top_k, c->block_size, capacity_of(c, T),
                                kept, route_expert, pos, sorted, blocks, num_padded, counts, dropped,
                                rerouted, at<int32_t>(ws, L.rank), at<int32_t>(ws, L.tile_count),
-                               at<int32_t>(ws, L.seg_off), sc, at<int>(ws, L.status), s);
+                               at<int32_t>(ws, L.seg_off), sc, at<int>(ws, L.status), opts_of(c), s);
   return last_cuda();
 }
 
@@ -337,12 +366,11 @@ moe_status expert_choice_impl(const moe_config* c, int32_t T, const float* logit
 // segment-order gather fetches a row once per slot, from DRAM when h does
 // not stay in L2 (measured on the DeepSeek-like layer, whose row copy shares
 // the SMs with the shared expert: 4.488 -> 4.452 ms at T = 4096, 11.92 ->
-// 11.87 ms at T = 16448; no change at 33 MB).  MOE_ROW_COPY=gather /
-// scatter forces one (read at each call; both write the same rows).
-bool scatter_rows_ok(int T, int H) {
-  const char* force = std::getenv("MOE_ROW_COPY");
-  if (force && std::strcmp(force, "gather") == 0) return false;
-  if (force && std::strcmp(force, "scatter") == 0) return true;
+// 11.87 ms at T = 16448; no change at 33 MB).  The caller's path flags may
+// force one (both write the same rows).
+bool scatter_rows_ok(int T, int H, uint32_t path_flags) {
+  if (path_flags & MOE_DEBUG_ROW_GATHER) return false;
+  if (path_flags & MOE_DEBUG_ROW_SCATTER) return true;
   return (long long)T * H * 2 > (48ll << 20);
 }
 
@@ -387,6 +415,7 @@ moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, co
   s13.out_ld = Is;
   s13.status = status;
   s13.pair = spair13 ? 1 : 0;
+  s13.wait_ns = (unsigned long long)c->debug_wait_ns;
   moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + srows13 - 1) / srows13, sms, s);
   moe::GemmArgs s2 = s13;
   s2.K = Is;
@@ -428,7 +457,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   }
   if (rows_ready) {
     // the decode front copied the routed rows
-  } else if (route_pos && scatter_rows_ok(T, H)) {
+  } else if (route_pos && scatter_rows_ok(T, H, c->debug_flags)) {
     moe::launch_scatter_rows(h, route_pos, sorted, num_padded, k, T, H, rows, x_perm, s);
   } else {
     moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
@@ -460,6 +489,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.out_ld = I;
   g13.status = status;
   g13.pair = pair13 ? 1 : 0;
+  g13.wait_ns = (unsigned long long)c->debug_wait_ns;
   moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, pair13 ? max_tiles2 : max_tiles13, sms, s);
   mark(mk, 4);
 
@@ -591,7 +621,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
     if (st == MOE_OK)
       st = reroute_impl(c, T, idx, logits, kept, at<int32_t>(ws, L.route_expert), pos, sorted, blocks,
                         num_padded, counts, at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.rerouted), ws, s);
-  } else if (moe::decode_front_ok(T, c->hidden, c->num_experts, c->top_k)) {
+  } else if (moe::decode_front_ok(T, c->hidden, c->num_experts, c->top_k, c->debug_flags)) {
     // a few tokens: the router's chunk sums, then routing, dispatch, both
     // tile lists and the routed rows in one more launch (the same bits as
     // the separate kernels)
@@ -977,14 +1007,15 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   // after the CUDA-core router.  Expert choice: logits (2 launches), scores,
   // selection.  At most two tokens: chunk sums, then one launch for the
   // reduce, top-k, dispatch, tile lists and row gather.
-  const bool chunked = moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg));
+  const bool chunked =
+      moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg), cfg->debug_flags);
   const int router = chunked ? 2 : (use_tc_router(cfg) ? 6 : 2);
   int front = 0;
   if (expert_choice(cfg)) {   // logits (chunked router, 2), scores, selection
     front = 2 + 2;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = 2 + 9;
-  } else if (moe::decode_front_ok(T, cfg->hidden, cfg->num_experts, cfg->top_k)) {
+  } else if (moe::decode_front_ok(T, cfg->hidden, cfg->num_experts, cfg->top_k, cfg->debug_flags)) {
     // chunk sums, then routing, dispatch, tile lists and the routed rows
     front = 2 - 1 - 1;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {
@@ -1066,7 +1097,7 @@ moe_status moe_get_device_status(const void* ws, int32_t* status_out, void* stre
   if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   *status_out = v;
-  return v ? MOE_ERR_DEVICE : MOE_OK;
+  return (v & MOE_DEV_ERR_MASK) ? MOE_ERR_DEVICE : MOE_OK;
 }
 
 moe_status moe_clear_device_status(void* ws, void* stream) {

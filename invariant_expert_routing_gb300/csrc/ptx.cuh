@@ -7,8 +7,14 @@
 namespace moe {
 
 // A bounded wait gives up after this long (ns of %globaltimer) and reports
-// MOE_DEV_ERR_TIMEOUT instead of hanging the GPU.
+// MOE_DEV_ERR_TIMEOUT instead of hanging the GPU.  A caller may pass a shorter
+// limit for the pipeline waits (tests make a wait run out); the waits that
+// only let work already issued drain before exit always take this one.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Below this limit the clock is read after every failed try instead of every
+// 64th, so that a test's limit of a few ns runs out at the first wait that is
+// not already satisfied.
+constexpr uint64_t kCheckEveryTryNs = 100000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -47,15 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `parity` to complete.  Gives up (returns false) when
-// *abort is set by another role or after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// *abort is set by another role or after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 63u) == 0 || limit_ns < kCheckEveryTryNs) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }
@@ -211,14 +218,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // mbar_wait for barriers that the other CTA of the pair also arrives on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 63u) == 0 || limit_ns < kCheckEveryTryNs) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }

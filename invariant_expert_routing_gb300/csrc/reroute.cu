@@ -28,7 +28,6 @@
 // direct implementation of the sequential rule, recomputes the assignment.
 // Every decision is on integers, so the result is the same bits either way.
 #include <cstdint>
-#include <cstdlib>
 
 #include "kernels.h"
 
@@ -418,9 +417,10 @@ __global__ void __launch_bounds__(kRerouteThreads, 1) reroute_da_kernel(
 // The published arrays alternate between two buffers by round, so a buffer
 // is rewritten only after every CTA has passed the next barrier.  Data that
 // other CTAs write is read with ld.global.cg (L2), as L1 is not coherent
-// across SMs.  A barrier that waits longer than kBarrierLimitNs records an
-// error: every CTA then leaves at its next barrier, and the flag hands the
-// batch to the sequential kernel.
+// across SMs.  A barrier that waits longer than its limit (kBarrierLimitNs
+// unless the caller passes a shorter one) records an error: every CTA then
+// leaves at its next barrier, and the flag hands the batch to the sequential
+// kernel.
 constexpr unsigned long long kBarrierLimitNs = 200000000ull;   // 0.2 s
 constexpr int kGridMaxChunks = 3;   // 1024-route chunks per CTA (24 KB of shared memory each)
 
@@ -431,8 +431,10 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // gs[0] counts arrivals over the whole launch: the b-th barrier (from 0) is
-// passed once it reaches G * (b + 1).  A CTA that gives up adds kBarrierError,
-// which releases every waiter and marks the error.  Uniform result in the CTA.
+// passed once it reaches G * (b + 1) (at most 152 CTAs x 1040 rounds, far
+// below 2^30).  A CTA that gives up sets bit 30 (an OR, so that several CTAs
+// giving up at once cannot carry it away), which releases every waiter and
+// marks the error.  Uniform result in the CTA.
 constexpr uint32_t kBarrierError = 1u << 30;
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -441,7 +443,7 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
-__device__ bool grid_barrier(uint32_t* gs, uint32_t target, int* s_ok) {
+__device__ bool grid_barrier(uint32_t* gs, uint32_t target, int* s_ok, unsigned long long limit_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -450,8 +452,8 @@ __device__ bool grid_barrier(uint32_t* gs, uint32_t target, int* s_ok) {
     if (v < target) {
       const unsigned long long t0 = global_ns();
       while ((v = ld_acquire_gpu(&gs[0])) < target) {
-        if (global_ns() - t0 > kBarrierLimitNs) {
-          atomicAdd(&gs[0], kBarrierError);
+        if (global_ns() - t0 > limit_ns) {
+          atomicOr(&gs[0], kBarrierError);
           v = kBarrierError;
           break;
         }
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(kRerouteThreads, 1) reroute_da_grid_kernel(
     int capacity, const int32_t* __restrict__ rank_in_tile, const int32_t* __restrict__ tile_base,
     const int32_t* __restrict__ kept_count, RerouteScratch sc, int L, int Lc, int max_rounds, int S,
     int chunks, int32_t* __restrict__ route_expert, int32_t* __restrict__ num_dropped,
-    int32_t* __restrict__ num_rerouted) {
+    int32_t* __restrict__ num_rerouted, unsigned long long barrier_ns, int* __restrict__ status) {
   extern __shared__ __align__(16) int dyn[];
   const int cap = chunks * kRerouteThreads;
   int* e_r = dyn;
@@ -662,7 +664,7 @@ __global__ void __launch_bounds__(kRerouteThreads, 1) reroute_da_grid_kernel(
     __syncthreads();
     for (int j = tid; j < n; j += blockDim.x)
       if (e_rank[j] >= 0) srt[r0 + off[e_cand[j]] + e_rank[j]] = e_r[j];
-    if (!grid_barrier(sc.gsync, (uint32_t)G * (uint32_t)(round + 1), &s_ok)) break;
+    if (!grid_barrier(sc.gsync, (uint32_t)G * (uint32_t)(round + 1), &s_ok, barrier_ns)) break;
     // (c) every CTA's counts
     {
       const int pieces = (N + 2) * gs / 8;   // 16-byte pieces
@@ -724,7 +726,10 @@ __global__ void __launch_bounds__(kRerouteThreads, 1) reroute_da_grid_kernel(
     if (settled) break;
   }
   if (!s_ok) {
-    if (tid == 0) atomicExch(sc.flag, 1);
+    if (tid == 0) {
+      atomicExch(sc.flag, 1);
+      atomicOr(status, kDevNoteRerouteFallback);
+    }
     return;
   }
   // results: the list of overflowing routes (for the check), the targets, counts
@@ -916,24 +921,14 @@ __global__ void __launch_bounds__(kRerouteThreads) reroute_seq_kernel(
   }
 }
 
-bool force_sequential() {
-  static const bool v = [] {
-    const char* s = std::getenv("MOE_REROUTE_SEQUENTIAL");
-    return s && s[0] == '1';
-  }();
-  return v;
-}
-
-// Grid or single-CTA rounds: MOE_REROUTE_GRID=1 / 0 forces one; otherwise
+// Grid or single-CTA rounds: forced by the caller's path flags; otherwise
 // the grid from kRerouteGridMinRoutes routes on.
 constexpr long long kRerouteGridMinRoutes = 16384;
 
-bool use_grid_rounds(long long R) {
-  static const int v = [] {
-    const char* s = std::getenv("MOE_REROUTE_GRID");
-    return s ? (s[0] == '1' ? 1 : (s[0] == '0' ? 0 : -1)) : -1;
-  }();
-  return v >= 0 ? v == 1 : R >= kRerouteGridMinRoutes;
+bool use_grid_rounds(long long R, const PathOpts& o) {
+  if (o.flags & kPathRerouteGrid) return true;
+  if (o.flags & kPathRerouteOneCta) return false;
+  return R >= kRerouteGridMinRoutes;
 }
 
 // Shared copy of the preference lists of a CTA's tokens: at most this many bytes.
@@ -971,10 +966,7 @@ int grid_rounds_ctas() {
     cudaGetLastError();
     per = 0;
   }
-  int g = per > 0 ? sms : -1;
-  // MOE_REROUTE_GRID_CTAS=n caps the grid (more routes per CTA), for tests
-  const char* cap = std::getenv("MOE_REROUTE_GRID_CTAS");
-  if (g > 0 && cap && std::atoi(cap) > 0 && std::atoi(cap) < g) g = std::atoi(cap);
+  const int g = per > 0 ? sms : -1;
   if (dev >= 0 && dev < 64) cache[dev] = g;
   return g;
 }
@@ -984,9 +976,9 @@ int grid_rounds_ctas() {
 void launch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, int k, int capacity,
                     const int32_t* rank_in_tile, const int32_t* tile_base, const int32_t* kept_count,
                     const RerouteScratch& sc, int32_t* route_expert, int32_t* num_dropped,
-                    int32_t* num_rerouted, cudaStream_t s) {
+                    int32_t* num_rerouted, int* status, const PathOpts& o, cudaStream_t s) {
   const long long R = (long long)T * k;
-  if (force_sequential()) {
+  if (o.flags & kPathRerouteSequential) {
     cudaMemsetAsync(sc.flag, 0xFF, sizeof(int32_t), s);
   } else {
     const unsigned pref_blocks = (unsigned)((T + 7) / 8);
@@ -997,7 +989,8 @@ void launch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, 
                                       kRerouteListLen, sc.prefs, sc.gsync, sc.flag);
     const int max_rounds = 4 * N + 16;
     // grid-wide rounds: CTAs own whole tokens, chunks of per = k * floor(1024 / k) routes
-    const int gmax = use_grid_rounds(R) ? grid_rounds_ctas() : -1;
+    int gmax = use_grid_rounds(R, o) ? grid_rounds_ctas() : -1;
+    if (gmax > 0 && o.grid_ctas > 0 && o.grid_ctas < gmax) gmax = o.grid_ctas;   // more routes per CTA
     const long long per = (long long)(kRerouteThreads / k) * k;
     const long long nchunks = (R + per - 1) / per;
     const int chunks = gmax > 0 ? (int)((nchunks + gmax - 1) / gmax) : 0;
@@ -1017,7 +1010,8 @@ void launch_reroute(const int32_t* topk_idx, const float* logits, int T, int N, 
       cfg.numAttrs = 1;
       if (cudaLaunchKernelEx(&cfg, reroute_da_grid_kernel, topk_idx, logits, T, N, k, capacity,
                              rank_in_tile, tile_base, kept_count, sc, kRerouteListLen, Lc, max_rounds,
-                             S, chunks, route_expert, num_dropped, num_rerouted) != cudaSuccess) {
+                             S, chunks, route_expert, num_dropped, num_rerouted,
+                             o.wait_ns ? (unsigned long long)o.wait_ns : kBarrierLimitNs, status) != cudaSuccess) {
         cudaGetLastError();   // not launched: the sequential kernel decides
         cudaMemsetAsync(sc.flag, 0xFF, sizeof(int32_t), s);
       }

@@ -20,8 +20,6 @@
 // the split of work never changes a logit's order and nothing depends on T.
 #include <cuda_bf16.h>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 
 #include "kernels.h"
 #include "pdl.cuh"
@@ -192,7 +190,7 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
 // fp32 result of the chunked order both lie within their error bounds of the
 // exact dot product, so |l_tc - l_canonical| <= delta_t = beta ||h_t||
 // max_e ||w_e|| (+ the bias roundings), beta covering (K/16 + 1) MMA steps at
-// a per-step relative error of 2^-18 and the (256 + chunks + 1) fp32
+// a per-step relative error of 2^-20 and the (256 + chunks + 1) fp32
 // additions of the canonical order.  If L_k is the k-th largest l_tc, every
 // expert with l_tc < L_k - 2 delta_t has a canonical logit strictly below the
 // canonical k-th value, so only the remaining candidates get their canonical
@@ -691,15 +689,14 @@ void launch_route_certified(const float* logits_tc, const float* bias, const uin
 // router near T = 2800, 0.053 ms either way at 2048 and 0.089 chunked
 // against 0.071 at 4096; the DeepSeek-like one near T = 600, 0.132 against
 // 0.099 at 1024).  Every path gives the same bits.
-// MOE_ROUTER_PATH=tc / chunked forces one path where the tensor-core router
-// can serve the call (read at each call; tests compare the two).
+// The caller's path flags may force one path where the tensor-core router
+// can serve the call (the tests compare the two).
 constexpr long long kChunkedRouterMaxWork = 3ll << 28;
 
-bool chunked_router_ok(int T, int H, int N, bool tc_router) {
+bool chunked_router_ok(int T, int H, int N, bool tc_router, uint32_t path_flags) {
   if (!tc_router) return true;
-  const char* force = std::getenv("MOE_ROUTER_PATH");
-  if (force && std::strcmp(force, "tc") == 0) return false;
-  if (force && std::strcmp(force, "chunked") == 0) return true;
+  if (path_flags & kPathRouterTc) return false;
+  if (path_flags & kPathRouterChunked) return true;
   if (T <= kDecodeRouterMaxT) return true;
   return (long long)T * H * N <= kChunkedRouterMaxWork;
 }

@@ -140,3 +140,36 @@ class LayerCase:
                                      self.w13s[None], self.w2s[None])
         return oracle.combine_rows(tokens, h_bits, gates, route_kept, y.reshape(len(tokens), k, H),
                                    ysh)
+
+
+def edge_tokens(d: dict, T: int, k: int, B: int, tile_rows=(128, 256), small_rows: int = 32,
+                limit: int | None = None, seed: int = 0) -> np.ndarray:
+    """Tokens whose routes sit where the grouped GEMMs' schedules change: the
+    first and last routed row of every tile of each expert segment (tiles of
+    each size in tile_rows, cut from the segment's start), the last route of
+    every segment, and every route of a tile with at most small_rows routed
+    rows (those run the narrow MMA).  From the oracle's dispatch d (block size
+    B).  With limit, a seeded subset of at most that many tokens that always
+    keeps every segment's last route."""
+    counts = np.asarray(d["expert_counts"], np.int64)
+    srt = np.asarray(d["sorted_route_ids"], np.int64)
+    pads = (counts + B - 1) // B * B
+    starts = np.concatenate([[0], np.cumsum(pads)[:-1]])
+    must, rows = set(), set()
+    for e in np.flatnonzero(counts > 0):
+        s0, cnt = int(starts[e]), int(counts[e])
+        must.add(s0 + cnt - 1)
+        for tr in tile_rows:
+            for m in range(0, cnt, tr):
+                valid = min(cnt - m, tr)
+                rows.update((s0 + m, s0 + m + valid - 1))
+                if valid <= small_rows:
+                    rows.update(range(s0 + m, s0 + m + valid))
+    sentinel = T * k
+    keep = {int(srt[r]) // k for r in must if srt[r] != sentinel}
+    rest = sorted({int(srt[r]) // k for r in rows if srt[r] != sentinel} - keep)
+    if limit is not None and len(keep) + len(rest) > limit:
+        n = max(0, limit - len(keep))
+        rng = np.random.default_rng(seed)
+        rest = [int(x) for x in rng.choice(rest, min(n, len(rest)), replace=False)] if n else []
+    return np.array(sorted(keep.union(rest)), np.int64)

@@ -56,6 +56,27 @@ def test_config_validation(moe, bad, code):
     assert moe.moe_check_config(cfg) == code
 
 
+@pytest.mark.parametrize("bad", [
+    dict(debug_flags=0x400),                 # unknown bit
+    dict(debug_flags=0x1 | 0x2),             # tensor-core and chunked router at once
+    dict(debug_flags=0x4 | 0x8),             # gather and scatter row copy at once
+    dict(debug_flags=0x40 | 0x80),           # grid and one-CTA reroute rounds at once
+    dict(debug_flags=0x100 | 0x200),         # two router tile heights
+    dict(debug_grid_ctas=-1), dict(debug_wait_ns=-5)])
+def test_debug_fields_validation(moe, bad):
+    assert moe.moe_check_config(dict(TINY, **bad)) == 1
+
+
+def test_debug_fields_layout(moe):
+    # the C struct: five int32, an fp64 capacity factor, three int32, the
+    # debug flags and grid cap, an int64 wait limit (64 bytes)
+    assert ctypes.sizeof(moe.moe_config) == 64
+    assert moe.moe_config.debug_wait_ns.offset == 56
+    for f in (0x1, 0x2, 0x4, 0x8, 0x10, 0x20, 0x40, 0x80, 0x100, 0x200):
+        assert moe.moe_check_config(dict(TINY, debug_flags=f)) == 0
+    assert moe.moe_check_config(dict(TINY, debug_grid_ctas=12, debug_wait_ns=1)) == 0
+
+
 def test_good_configs(moe):
     from synth import workloads as W
     for wl in W.WORKLOADS.values():

@@ -5,13 +5,11 @@ CTA that adds them in chunk order, then the bias, selects the top-k with the
 same code, runs the same dispatch body (layout and both tile lists) and
 copies the routed rows ("Why temperature=0 Still Gives Different Answers:
 Batch Invariance": one reduction order for every batch).  Layer outputs must
-be bit-identical with the front switched off (MOE_DECODE_FRONT=0), for N = 8,
+be bit-identical with the front switched off (MOE_DEBUG_NO_DECODE_FRONT), for N = 8,
 128 and 256 experts, a 40-expert layer with a 128-element last chunk,
 capacity drops, the shared expert, and a three-token batch that takes the
 separate kernels either way.
 """
-import os
-
 import numpy as np
 import pytest
 
@@ -38,18 +36,11 @@ def _forward(c, cfg, h_bits, front):
     from tests.gpu_util import dev_bf16, host_bf16
     T = h_bits.shape[0]
     out = torch.empty((T, c.wl.hidden), dtype=torch.bfloat16, device="cuda")
+    cfg = dict(cfg, debug_flags=0 if front else moe.MOE_DEBUG_NO_DECODE_FRONT)
     ws = moe.workspace(cfg, T)
     moe.moe_clear_device_status(ws)
-    old = os.environ.get("MOE_DECODE_FRONT")
-    os.environ["MOE_DECODE_FRONT"] = "1" if front else "0"
-    try:
-        moe.moe_forward(cfg, dev_bf16(h_bits), c.wg_d, c.bias_d, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, out, ws)
-        torch.cuda.synchronize()
-    finally:
-        if old is None:
-            del os.environ["MOE_DECODE_FRONT"]
-        else:
-            os.environ["MOE_DECODE_FRONT"] = old
+    moe.moe_forward(cfg, dev_bf16(h_bits), c.wg_d, c.bias_d, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, out, ws)
+    torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
     return host_bf16(out)
 

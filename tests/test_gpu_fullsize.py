@@ -1,10 +1,14 @@
 """Full-size configurations, in the launch configuration bench.py times.
 
 Routing and dispatch are compared bit for bit over every token (the oracle
-does those cheaply); layer outputs are compared on seeded samples of tokens,
-whose oracle rows are computed one by one.  The DeepSeek-V3-like layer runs
-the batch-invariance sweep: 64 probe tokens embedded among 0..16384 filler
-tokens at shuffled positions give bitwise the probes-alone outputs.
+does those cheaply); layer outputs are compared on chosen tokens, whose
+oracle rows are computed one by one: every token with a route on the first
+or last routed row of a 128- or 256-row GEMM tile, on the last row of an
+expert segment, or in a tile of at most 32 routed rows (where the grouped
+GEMMs' schedules change), plus a seeded random sample.  The DeepSeek-V3-like
+layer runs the batch-invariance sweep: 64 probe tokens embedded among
+0..16384 filler tokens at shuffled positions give bitwise the probes-alone
+outputs, and fillers of the largest batch on tile edges match the oracle.
 """
 import numpy as np
 import pytest
@@ -27,7 +31,8 @@ def case(name):
     return _cases[name]
 
 
-def _full_check(name, T, seed, n_sample=32, must_drop=False):
+def _full_check(name, T, seed, n_sample=32, must_drop=False, edge_limit=None):
+    from tests.layer_case import edge_tokens
     c = case(name)
     h = W.make_h(c.wl, T, seed)
     out = c.forward(h)
@@ -39,7 +44,8 @@ def _full_check(name, T, seed, n_sample=32, must_drop=False):
     check_gates(got["gates"], gates)
     check_dispatch(got, d)
     rng = np.random.default_rng(T + seed)
-    toks = np.sort(rng.choice(T, n_sample, replace=False))
+    edges = edge_tokens(d, T, c.wl.top_k, c.wl.block_size, limit=edge_limit, seed=seed)
+    toks = np.union1d(np.sort(rng.choice(T, n_sample, replace=False)), edges)
     if must_drop:
         assert d["num_dropped"] > 0
         dropped = np.flatnonzero((d["route_kept"].reshape(T, -1) == 0).any(axis=1))
@@ -54,7 +60,8 @@ def test_mixtral_like_T4096_bench_batch():
 
 
 def test_qwen_like_T8192():
-    _full_check("qw", 8192, 0)
+    # ~600 tiles: a seeded 600 of their edge tokens, every segment's last route
+    _full_check("qw", 8192, 0, edge_limit=600)
 
 
 def test_capacity_T8192_drops_about_15_percent():
@@ -92,3 +99,15 @@ def test_deepseek_like_probe_sweep():
             batch[~mask] = fillers
             out = c.forward(batch)
             assert (out[pos] == alone[perm]).all(), f"F={F} shuffle={shuffle}"
+    # fillers of the largest batch (the last one run) against the oracle:
+    # routed on tile edges, segment tails and narrow tiles, plus a few at random
+    from tests.layer_case import edge_tokens
+    l, idx, gates, d = c.ref_routing(batch)
+    fill = np.flatnonzero(~mask)
+    edges = np.intersect1d(edge_tokens(d, T, wl.top_k, wl.block_size), fill)
+    rng = np.random.default_rng(77)
+    sel = np.union1d(rng.choice(edges, min(40, len(edges)), replace=False),
+                     rng.choice(fill, 8, replace=False))
+    assert len(sel) >= 32
+    ref = c.ref_outputs(batch, sel, idx, gates, d["route_kept"])
+    check_outputs(out[sel], ref)

@@ -16,10 +16,10 @@ from synth import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _route_both(moe, cfg, h_d, wg_d, bias_d, ws):
+def _route_both(moe, cfg, h_d, wg_d, bias_d, ws, tc_flags=0):
     # with logits: the chunked CUDA-core router (every logit in the canonical
     # order); without: the tensor-core path, forced for any batch size
-    import os
+    # (tc_flags may add a forced token-tile height of its logits)
     import torch
     T, N, k = h_d.shape[0], cfg["num_experts"], cfg["top_k"]
     dev = h_d.device
@@ -28,25 +28,31 @@ def _route_both(moe, cfg, h_d, wg_d, bias_d, ws):
         idx = torch.empty((T, k), dtype=torch.int32, device=dev)
         g = torch.empty((T, k), dtype=torch.float32, device=dev)
         lg = torch.empty((T, N), dtype=torch.float32, device=dev) if with_logits else None
-        old = os.environ.get("MOE_ROUTER_PATH")
-        os.environ["MOE_ROUTER_PATH"] = "chunked" if with_logits else "tc"
-        try:
-            moe.moe_route(cfg, h_d, wg_d, bias_d, idx, g, lg, ws)
-        finally:
-            if old is None:
-                del os.environ["MOE_ROUTER_PATH"]
-            else:
-                os.environ["MOE_ROUTER_PATH"] = old
+        flags = moe.MOE_DEBUG_ROUTER_CHUNKED if with_logits else moe.MOE_DEBUG_ROUTER_TC | tc_flags
+        moe.moe_route(dict(cfg, debug_flags=flags), h_d, wg_d, bias_d, idx, g, lg, ws)
         out.append((idx, g, lg))
     torch.cuda.synchronize()
     return out
 
 
-@pytest.mark.parametrize("name,T", [("qw", 1), ("qw", 65), ("qw", 700), ("qw", 8192), ("ds", 5), ("ds", 3000)])
-def test_tensor_core_router_matches_canonical_router(name, T):
+# (layer, T, forced tile height of the tensor-core logits: 0 = the default choice)
+_TC_CASES = [("qw", 1, 0), ("qw", 65, 0), ("qw", 700, 0), ("qw", 8192, 0), ("ds", 5, 0), ("ds", 3000, 0),
+             ("qw", 700, 128), ("qw", 8192, 128), ("ds", 3000, 128), ("ds", 10000, 0), ("qw", 20000, 0),
+             ("qw", 8192, 64), ("ds", 10000, 64)]
+
+
+@pytest.mark.parametrize("name,T,rows", _TC_CASES)
+def test_tensor_core_router_matches_canonical_router(name, T, rows):
+    # both router paths against each other bit for bit, and the tensor-core
+    # path's top-k directly against the oracle's (indices bit for bit, gates
+    # within the gate tolerance); T = 10000 (DeepSeek-like) and 20000
+    # (Qwen-like) give every SM a 128-row tile, so the default takes the
+    # 128-row logits there; smaller batches take 64-row tiles unless forced
     import torch
     import invariant_expert_routing_gb300 as moe
-    from tests.gpu_util import dev, dev_bf16
+    import oracle
+    from tests.checks import check_equal, check_gates
+    from tests.gpu_util import dev, dev_bf16, host
     wl = W.WORKLOADS[name]
     cfg = wl.cfg
     h = W.make_h(wl, T, seed=31)
@@ -55,12 +61,18 @@ def test_tensor_core_router_matches_canonical_router(name, T):
     bias_d = None if bias is None else dev(bias)
     ws = moe.workspace(cfg, T)
     moe.moe_clear_device_status(ws)
-    (i_c, g_c, l_c), (i_t, g_t, _) = _route_both(moe, cfg, h_d, wg_d, bias_d, ws)
+    tile = {0: 0, 128: moe.MOE_DEBUG_ROUTER_TILE128, 64: moe.MOE_DEBUG_ROUTER_TILE64}[rows]
+    (i_c, g_c, l_c), (i_t, g_t, _) = _route_both(moe, cfg, h_d, wg_d, bias_d, ws, tile)
     assert torch.equal(i_c, i_t)
     assert torch.equal(g_c.view(torch.int32), g_t.view(torch.int32))
+    # the oracle's routing of the same tokens
+    l_ref = oracle.router_logits(h, wg, bias)
+    idx_ref, g_ref = oracle.select_topk(l_ref, wl.top_k)
+    check_equal("topk_idx (tensor-core path vs oracle)", host(i_t), idx_ref)
+    check_gates(host(g_t), g_ref)
     # the tensor-core logits stay far inside the assumed bound
     ltc = torch.empty((T, wl.num_experts), dtype=torch.float32, device=h_d.device)
-    moe.moe_router_tc_logits(cfg, h_d, wg_d, ltc, ws)
+    moe.moe_router_tc_logits(dict(cfg, debug_flags=tile), h_d, wg_d, ltc, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
     lc = l_c.double().cpu().numpy() - (0 if bias is None else bias.astype(np.float64))

@@ -81,11 +81,11 @@ REROUTE_CASES = [("tiny", 64, 0.5), ("tiny", 61, 0.75), ("tiny", 1, 0.5), ("cap"
 
 
 @pytest.mark.parametrize("name,T,cf", REROUTE_CASES)
-def test_reroute_dispatch_is_bit_exact(name, T, cf):
+def test_reroute_dispatch_is_bit_exact(name, T, cf, extra=None):
     import invariant_expert_routing_gb300 as moe
     from tests.gpu_util import dev_bf16, host
     c = case(name)
-    cfg = dict(c.cfg, capacity_factor=cf, overflow_policy=1)
+    cfg = dict(c.cfg, capacity_factor=cf, overflow_policy=1, **(extra or {}))
     N, k, B = cfg["num_experts"], cfg["top_k"], cfg["block_size"]
     h = W.make_h(c.wl, T, seed=21)
     ws = moe.workspace(cfg, T)
@@ -342,40 +342,30 @@ def test_expert_choice_ties_go_to_the_lowest_token():
 
 _FORCED_PATHS = {
     # the sequential kernel (the fallback of the deferred-acceptance rounds) alone
-    "sequential": ({"MOE_REROUTE_SEQUENTIAL": "1"},
-                   "[('tiny', 61, 0.75), ('cap', 2000, 0.8), ('qw', 777, 0.6)]", ""),
+    "sequential": (dict(debug_flags=0x20),        # MOE_DEBUG_REROUTE_SEQUENTIAL
+                   [("tiny", 61, 0.75), ("cap", 2000, 0.8), ("qw", 777, 0.6)], []),
     # the grid-wide rounds on small batches (one list tile, ragged tails)
-    "grid": ({"MOE_REROUTE_GRID": "1"},
-             "[('tiny', 61, 0.75), ('tiny', 1, 0.5), ('cap', 2000, 0.8), ('qw', 777, 0.6), ('ds', 200, 1.0)]",
-             "for a in [(200, 8, 2, 0.7), (300, 32, 4, 0.8), (129, 256, 8, 1.0)]:\n"
-             "    m.test_reroute_with_nan_and_tied_logits(*a)\n"),
+    "grid": (dict(debug_flags=0x40),                    # MOE_DEBUG_REROUTE_GRID
+             [("tiny", 61, 0.75), ("tiny", 1, 0.5), ("cap", 2000, 0.8), ("qw", 777, 0.6), ("ds", 200, 1.0)],
+             [(200, 8, 2, 0.7), (300, 32, 4, 0.8), (129, 256, 8, 1.0)]),
     # the grid-wide rounds with several 1024-route chunks per CTA
-    "grid_chunks": ({"MOE_REROUTE_GRID": "1", "MOE_REROUTE_GRID_CTAS": "12"},
-                    "[('qw', 777, 0.6), ('cap', 8192, 1.0), ('qw', 8192, 1.0)]", ""),
+    "grid_chunks": (dict(debug_flags=0x40, debug_grid_ctas=12),
+                    [("qw", 777, 0.6), ("cap", 8192, 1.0), ("qw", 8192, 1.0)], []),
     # the one-CTA rounds on batches that default to the grid
-    "cta": ({"MOE_REROUTE_GRID": "0"}, "[('cap', 8192, 1.0), ('qw', 8192, 1.0)]", ""),
+    "cta": (dict(debug_flags=0x80), [                   # MOE_DEBUG_REROUTE_ONE_CTA
+        ("cap", 8192, 1.0), ("qw", 8192, 1.0)], []),
 }
 
 
 @pytest.mark.parametrize("path", sorted(_FORCED_PATHS))
 def test_reroute_forced_path_is_bit_exact(path):
-    # each way of computing the reroute on its own, in a process whose
-    # environment selects it
-    import os
-    import subprocess
-    import sys
-    env_add, cases, extra = _FORCED_PATHS[path]
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    code = ("import sys; sys.path.insert(0, %r)\n"
-            "from tests import test_gpu_routing_modes as m\n"
-            "for case in %s:\n"
-            "    m.test_reroute_dispatch_is_bit_exact(*case)\n"
-            "%s"
-            "print('path ok')\n") % (root, cases, extra)
-    env = dict(os.environ, **env_add)
-    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
-                       text=True, timeout=900)
-    assert r.returncode == 0 and "path ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+    # each way of computing the reroute on its own, selected by the
+    # configuration's path flags (MOE_DEBUG_REROUTE_*)
+    extra, cases, nan_cases = _FORCED_PATHS[path]
+    for name, T, cf in cases:
+        test_reroute_dispatch_is_bit_exact(name, T, cf, extra)
+    for args in nan_cases:
+        test_reroute_with_nan_and_tied_logits(*args, extra=extra)
 
 
 def _nan_logits(rng, T, N, ties=True):
@@ -390,7 +380,7 @@ def _nan_logits(rng, T, N, ties=True):
 
 
 @pytest.mark.parametrize("T,N,k,cf", [(200, 8, 2, 0.7), (300, 32, 4, 0.8), (129, 256, 8, 1.0)])
-def test_reroute_with_nan_and_tied_logits(T, N, k, cf):
+def test_reroute_with_nan_and_tied_logits(T, N, k, cf, extra=None):
     # crafted logits (NaN, -inf, exact ties) fed straight to the reroute
     # dispatch: NaN ranks last, ties go to the lower index, on both sides
     import torch
@@ -400,7 +390,7 @@ def test_reroute_with_nan_and_tied_logits(T, N, k, cf):
     l = _nan_logits(rng, T, N)
     idx, _ = oracle.select_topk(l, k)
     cfg = dict(hidden=128, num_experts=N, top_k=k, intermediate=128, block_size=8,
-               capacity_factor=cf, overflow_policy=1)
+               capacity_factor=cf, overflow_policy=1, **(extra or {}))
     ws = moe.workspace(cfg, T)
     moe.moe_clear_device_status(ws)
     got = _reroute_on_gpu(moe, cfg, dev(idx), dev(l), ws)

@@ -7,8 +7,6 @@ the second serves batches whose h exceeds half of L2.  The layer output must
 be bit-identical either way, with dropped routes, rerouted routes and expert
 choice, on ragged batches.
 """
-import os
-
 import numpy as np
 import pytest
 
@@ -34,18 +32,12 @@ def _forward(c, cfg, h_bits, mode):
     T = h_bits.shape[0]
     h_d = dev_bf16(h_bits)
     out = torch.empty((T, c.wl.hidden), dtype=torch.bfloat16, device="cuda")
+    flag = moe.MOE_DEBUG_ROW_GATHER if mode == "gather" else moe.MOE_DEBUG_ROW_SCATTER
+    cfg = dict(cfg, debug_flags=flag)
     ws = moe.workspace(cfg, T)
     moe.moe_clear_device_status(ws)
-    old = os.environ.get("MOE_ROW_COPY")
-    os.environ["MOE_ROW_COPY"] = mode
-    try:
-        moe.moe_forward(cfg, h_d, c.wg_d, c.bias_d, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, out, ws)
-        torch.cuda.synchronize()
-    finally:
-        if old is None:
-            del os.environ["MOE_ROW_COPY"]
-        else:
-            os.environ["MOE_ROW_COPY"] = old
+    moe.moe_forward(cfg, h_d, c.wg_d, c.bias_d, c.w13_d, c.w2_d, c.w13s_d, c.w2s_d, out, ws)
+    torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
     return host_bf16(out)
 
