@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
 }
 
 // Grouped-GEMM tile lists from the padded blocks: each expert segment is cut
-// into tiles of tile_rows rows from its start.  CTA 0 writes list `a`, CTA 1
+// into tiles of tile_rows rows from its start (segment_tiles: a short last
+// tile may join the one before it).  CTA 0 writes list `a`, CTA 1
 // (when the grid has two) list `b`, from the same blocks.  Rejects (no tiles,
 // status bit) a block list that is not sorted by expert or out of range.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
@@ -257,22 +258,12 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     used -= n;
   }
   const int tile_rows = L.tile_rows;
-  const int nt = (rows + tile_rows - 1) / tile_rows;
+  const int nt = rows > 0 ? segment_tiles(rows, used, tile_rows, L.merge_rows) : 0;
   int total = 0;
   const int off = block_exclusive_scan(nt, buf, &total);
   for (int j = 0; j < nt; ++j) {
     const int idx = off + j;
-    if (idx < L.max_tiles) {
-      GemmTile tl;
-      tl.expert = e;
-      tl.row0 = first * B + j * tile_rows;
-      tl.rows = min(tile_rows, rows - j * tile_rows);
-      tl.first = off;
-      tl.count = nt;
-      tl.valid = max(0, min(tl.rows, used - j * tile_rows));
-      tl.pad[0] = tl.pad[1] = 0;
-      L.tiles[idx] = tl;
-    }
+    if (idx < L.max_tiles) L.tiles[idx] = segment_tile(e, first * B, rows, used, tile_rows, nt, j, off);
   }
   if (threadIdx.x == 0) *L.num_tiles = min(total, L.max_tiles);
 }
@@ -381,8 +372,7 @@ __device__ __forceinline__ void dispatch_small_block(
     const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* __restrict__ route_kept,
     int32_t* route_pos, int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_dropped,
-    GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a, int rows_a, int max_a,
-    GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b, int max_b, int* status) {
+    const TileListOut& la, const TileListOut& lb, int* status) {
   __shared__ int wc[32][kMaxN + 1];
   __shared__ int kept_s[kMaxN], pad_s[kMaxN], drop_s[kMaxN], nta[kMaxN], ntb[kMaxN];
   __shared__ int seg[kMaxN], offa[kMaxN], offb[kMaxN];
@@ -410,8 +400,8 @@ __device__ __forceinline__ void dispatch_small_block(
     kept_s[x] = kept;
     pad_s[x] = padded;
     drop_s[x] = run - kept;
-    nta[x] = (padded + rows_a - 1) / rows_a;
-    ntb[x] = (padded + rows_b - 1) / rows_b;
+    nta[x] = padded > 0 ? segment_tiles(padded, kept, la.tile_rows, la.merge_rows) : 0;
+    ntb[x] = padded > 0 ? segment_tiles(padded, kept, lb.tile_rows, lb.merge_rows) : 0;
     expert_counts[x] = kept;
   }
   __syncthreads();
@@ -451,38 +441,20 @@ __device__ __forceinline__ void dispatch_small_block(
     for (int b = seg[x] / B; b < (seg[x] + pad_s[x]) / B; ++b) block_expert[b] = x;
     for (int j = 0; j < nta[x]; ++j) {
       const int idx = offa[x] + j;
-      if (idx < max_a) {
-        GemmTile tl;
-        tl.expert = x;
-        tl.row0 = seg[x] + j * rows_a;
-        tl.rows = min(rows_a, pad_s[x] - j * rows_a);
-        tl.first = offa[x];
-        tl.count = nta[x];
-        tl.valid = max(0, min(tl.rows, kept_s[x] - j * rows_a));
-        tl.pad[0] = tl.pad[1] = 0;
-        tiles_a[idx] = tl;
-      }
+      if (idx < la.max_tiles)
+        la.tiles[idx] = segment_tile(x, seg[x], pad_s[x], kept_s[x], la.tile_rows, nta[x], j, offa[x]);
     }
     for (int j = 0; j < ntb[x]; ++j) {
       const int idx = offb[x] + j;
-      if (idx < max_b) {
-        GemmTile tl;
-        tl.expert = x;
-        tl.row0 = seg[x] + j * rows_b;
-        tl.rows = min(rows_b, pad_s[x] - j * rows_b);
-        tl.first = offb[x];
-        tl.count = ntb[x];
-        tl.valid = max(0, min(tl.rows, kept_s[x] - j * rows_b));
-        tl.pad[0] = tl.pad[1] = 0;
-        tiles_b[idx] = tl;
-      }
+      if (idx < lb.max_tiles)
+        lb.tiles[idx] = segment_tile(x, seg[x], pad_s[x], kept_s[x], lb.tile_rows, ntb[x], j, offb[x]);
     }
   }
   if (tid == 0) {
     *num_padded = s_rows;
     *num_dropped = s_drop;
-    *ntiles_a = min(s_ta, max_a);
-    *ntiles_b = min(s_tb, max_b);
+    *la.num_tiles = min(s_ta, la.max_tiles);
+    *lb.num_tiles = min(s_tb, lb.max_tiles);
   }
 }
 
@@ -491,14 +463,11 @@ __global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
     uint8_t* __restrict__ route_kept, int32_t* __restrict__ route_pos,
     int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts,
-    int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
-    int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
-    int max_b, int* status) {
+    int32_t* __restrict__ num_dropped, const TileListOut la, const TileListOut lb, int* status) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   pdl_trigger();
   dispatch_small_block(topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
-                       num_padded, expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b,
-                       ntiles_b, rows_b, max_b, status);
+                       num_padded, expert_counts, num_dropped, la, lb, status);
 }
 
 // ------------------------------------------------------------------------
@@ -515,9 +484,8 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
     int N, int k, int B, int capacity, int32_t* topk_idx, float* __restrict__ gates,
     uint8_t* __restrict__ route_kept, int32_t* route_pos, int32_t* __restrict__ sorted_route_ids,
     int32_t* __restrict__ block_expert, int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts,
-    int32_t* __restrict__ num_dropped, GemmTile* __restrict__ tiles_a, int32_t* __restrict__ ntiles_a,
-    int rows_a, int max_a, GemmTile* __restrict__ tiles_b, int32_t* __restrict__ ntiles_b, int rows_b,
-    int max_b, uint16_t* __restrict__ x_perm, long long max_rows, int* status) {
+    int32_t* __restrict__ num_dropped, const TileListOut la, const TileListOut lb,
+    uint16_t* __restrict__ x_perm, long long max_rows, int* status) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   // no early trigger: the next kernel is a GEMM
   __shared__ float lrow[kFinishMaxT][kMaxN];
@@ -536,8 +504,7 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
   __syncthreads();
   const int R = T * k;
   dispatch_small_block(topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
-                       num_padded, expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b,
-                       ntiles_b, rows_b, max_b, status);
+                       num_padded, expert_counts, num_dropped, la, lb, status);
   __syncthreads();
   // the routed token rows (padding rows feed only MMA columns that are never stored)
   const int pieces = H / 8;
@@ -630,11 +597,10 @@ bool dispatch_small_ok(long long R) { return R <= kSmallDispatchMaxR; }
 void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* route_kept,
                            int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
                            int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
-                           GemmTile* tiles_a, int32_t* ntiles_a, int rows_a, int max_a, GemmTile* tiles_b,
-                           int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s) {
-  launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallDispatchMaxR), 0, s, 
-      topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert, num_padded,
-      expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, status);
+                           const TileListOut& la, const TileListOut& lb, int* status, cudaStream_t s) {
+  launch_pdl(dispatch_small_kernel, dim3(1), dim3(kSmallDispatchMaxR), 0, s, topk_idx, R, N, B, capacity,
+             route_kept, route_pos, sorted_route_ids, block_expert, num_padded, expert_counts, num_dropped, la, lb,
+             status);
 }
 
 // The caller's path flags may turn the two-launch front off (the bits are
@@ -647,14 +613,12 @@ bool decode_front_ok(int T, int H, int N, int k, uint32_t path_flags) {
 void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float* bias, float* part, int T, int H,
                          int N, int k, int B, int capacity, int32_t* topk_idx, float* gates, uint8_t* route_kept,
                          int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert, int32_t* num_padded,
-                         int32_t* expert_counts, int32_t* num_dropped, GemmTile* tiles_a, int32_t* ntiles_a,
-                         int rows_a, int max_a, GemmTile* tiles_b, int32_t* ntiles_b, int rows_b, int max_b,
-                         uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s) {
+                         int32_t* expert_counts, int32_t* num_dropped, const TileListOut& la,
+                         const TileListOut& lb, uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s) {
   launch_router_partials(h, w_gate, part, T, H, N, s);
   launch_pdl(decode_finish_kernel, dim3(1), dim3(kFinishThreads), 0, s, (const float*)part, h, bias, T, H, N, k, B,
              capacity, topk_idx, gates, route_kept, route_pos, sorted_route_ids, block_expert, num_padded,
-             expert_counts, num_dropped, tiles_a, ntiles_a, rows_a, max_a, tiles_b, ntiles_b, rows_b, max_b, x_perm,
-             (long long)max_rows, status);
+             expert_counts, num_dropped, la, lb, x_perm, (long long)max_rows, status);
 }
 
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,

@@ -125,11 +125,11 @@ void launch_expert_choice(const float* logits, int T, int N, int C, int B, unsig
 // a batch of at most 1024 routes: launch_dispatch + both launch_build_tiles
 // (tile_rows rows_a and rows_b) in one launch, the same integers
 bool dispatch_small_ok(long long R);
+struct TileListOut;
 void launch_dispatch_small(const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* route_kept,
                            int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert,
                            int32_t* num_padded, int32_t* expert_counts, int32_t* num_dropped,
-                           GemmTile* tiles_a, int32_t* ntiles_a, int rows_a, int max_a, GemmTile* tiles_b,
-                           int32_t* ntiles_b, int rows_b, int max_b, int* status, cudaStream_t s);
+                           const TileListOut& la, const TileListOut& lb, int* status, cudaStream_t s);
 // decode front (at most 2 tokens, token choice): the router's chunk sums
 // (launch_router_partials), then in one CTA the logits in the canonical
 // order, top-k and gates, launch_dispatch_small's results and the routed
@@ -139,9 +139,8 @@ void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float*
                          int N, int k,
                          int B, int capacity, int32_t* topk_idx, float* gates, uint8_t* route_kept,
                          int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert, int32_t* num_padded,
-                         int32_t* expert_counts, int32_t* num_dropped, GemmTile* tiles_a, int32_t* ntiles_a,
-                         int rows_a, int max_a, GemmTile* tiles_b, int32_t* ntiles_b, int rows_b, int max_b,
-                         uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s);
+                         int32_t* expert_counts, int32_t* num_dropped, const TileListOut& la,
+                         const TileListOut& lb, uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s);
 void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
                         int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
 // the same x_perm from the inverse map (route_pos: padded row of each route,
@@ -157,7 +156,32 @@ struct TileListOut {
   int32_t* num_tiles;
   int tile_rows;
   int max_tiles;
+  int merge_rows;   // > 0: a segment's last tile with at most this many routed rows joins the one
+                    // before it (lists for merged CTA-pair items); 0: never
 };
+// Tiles of one expert segment of `padded` rows (the first `valid` hold
+// routes), cut into tile_rows-row tiles from the segment's start, the last
+// merged into the one before it when the list allows and it holds at most
+// merge_rows routed rows.  Tile j of nt: rows from row0 + j * tile_rows; the
+// last runs to the segment's end.
+__host__ __device__ inline int segment_tiles(int padded, int valid, int tile_rows, int merge_rows) {
+  const int nt = (padded + tile_rows - 1) / tile_rows;
+  if (merge_rows > 0 && nt >= 2 && valid - (nt - 1) * tile_rows <= merge_rows) return nt - 1;
+  return nt;
+}
+__host__ __device__ inline GemmTile segment_tile(int expert, int seg_row0, int padded, int valid, int tile_rows,
+                                                 int nt, int j, int first) {
+  GemmTile tl;
+  tl.expert = expert;
+  tl.row0 = seg_row0 + j * tile_rows;
+  tl.rows = j == nt - 1 ? padded - j * tile_rows : tile_rows;
+  tl.first = first;
+  tl.count = nt;
+  const int v = valid - j * tile_rows;
+  tl.valid = v < 0 ? 0 : (v < tl.rows ? v : tl.rows);
+  tl.pad[0] = tl.pad[1] = 0;
+  return tl;
+}
 // List a, and list b too when b is non-null (one launch, one CTA per list).
 void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
                         const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,

@@ -18,7 +18,7 @@ namespace {
 using moe::GemmTile;
 
 constexpr int kMaxDevices = 64;
-constexpr uint32_t kKnownDebugFlags = 0x3FFu;
+constexpr uint32_t kKnownDebugFlags = 0x3FFFu;
 static_assert(MOE_DEBUG_ROUTER_TC == moe::kPathRouterTc && MOE_DEBUG_ROUTER_CHUNKED == moe::kPathRouterChunked &&
                   MOE_DEBUG_ROW_GATHER == moe::kPathRowGather && MOE_DEBUG_ROW_SCATTER == moe::kPathRowScatter &&
                   MOE_DEBUG_NO_DECODE_FRONT == moe::kPathNoDecodeFront &&
@@ -196,6 +196,33 @@ P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
 }
 
+// The routed GEMMs of a forward: which kernel runs each, and the tile list
+// each consumes (list a: W13, list b: W2).  A property of the layer's shape,
+// except the wide W2 items, which also need enough touched experts.  Lists
+// consumed by CTA-pair kernels that can run merged items hand a segment's
+// short last tile to the tile before it (kMergeRows).
+struct GemmPlan {
+  bool pair13, pair2, wide2;
+  int rows13, rows2;     // token rows per tile of lists a and b
+  int merge13, merge2;   // merge_rows of lists a and b
+};
+
+moe_status check_ws(const moe_config* c, int32_t T, const void* ws, size_t ws_bytes);
+GemmPlan plan_of(const moe_config* c, int32_t T, int sms);
+int num_sms();
+
+// The W13 (a) and W2 (b) tile lists of a forward, in the workspace.
+moe::TileListOut list_a(const moe_config* c, int32_t T, const Layout& L, void* ws) {
+  const GemmPlan gp = plan_of(c, T, num_sms());
+  return moe::TileListOut{at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles), gp.rows13,
+                          (int)max_gemm_tiles_of(c, T, gp.rows13), gp.merge13};
+}
+moe::TileListOut list_b(const moe_config* c, int32_t T, const Layout& L, void* ws) {
+  const GemmPlan gp = plan_of(c, T, num_sms());
+  return moe::TileListOut{at<GemmTile>(ws, L.gemm_tiles2), at<int32_t>(ws, L.num_gemm_tiles2), gp.rows2,
+                          (int)max_gemm_tiles_of(c, T, gp.rows2), gp.merge2};
+}
+
 moe_status check_ws(const moe_config* c, int32_t T, const void* ws, size_t ws_bytes) {
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < layout_of(c, T).total) return MOE_ERR_WORKSPACE;
@@ -214,6 +241,28 @@ int num_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+GemmPlan plan_of(const moe_config* c, int32_t T, int sms) {
+  const int N = c->num_experts, H = c->hidden, I = c->intermediate;
+  const int k = expert_choice(c) ? N : c->top_k;
+  GemmPlan p{};
+  p.pair13 = moe::gemm_pair_ok(true, I, H) || ((c->debug_flags & MOE_DEBUG_W13_PAIR) && I % 128 == 0);
+  p.pair2 = moe::gemm_pair_ok(false, H, I);
+  const bool wide_shape = moe::gemm_wide_ok(H, I) ||
+                          ((c->debug_flags & MOE_DEBUG_W2_WIDE) && H % moe::kPairFeatW2Wide == 0);
+  // wide W2 items (two 256-feature groups per token tile, the same MMAs)
+  // where the layer has a long reduction and the batch touches enough
+  // experts to keep a quarter of the SMs busy with them (at T = 1 the
+  // Mixtral-like W2 took 0.196 ms with them against 0.167 without)
+  const long long touched = std::min<long long>(N, (long long)T * k);
+  p.wide2 = p.pair2 && wide_shape && touched * (H / moe::kPairFeatW2Wide) * 4 >= sms;
+  const bool no_merge = (c->debug_flags & MOE_DEBUG_NO_MERGE) != 0;
+  p.rows13 = p.pair13 ? moe::kPairTileRows : moe::kW13TileRows;
+  p.rows2 = moe::kW2TileRows;
+  p.merge13 = (p.pair13 && !no_merge) ? moe::kMergeRows : 0;
+  p.merge2 = (p.pair2 && !p.wide2 && !no_merge) ? moe::kMergeRows : 0;
+  return p;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -438,10 +487,11 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   const Layout L = layout_of(c, T);
   const int N = c->num_experts, H = c->hidden, I = c->intermediate, k = slots_of(c);
   const int64_t rows = max_rows_of(c, T);
-  const int max_tiles13 = (int)max_gemm_tiles_of(c, T, moe::kW13TileRows);
-  const int max_tiles2 = (int)max_gemm_tiles_of(c, T, moe::kW2TileRows);
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
+  const GemmPlan gp = plan_of(c, T, sms);
+  const int max_tiles13 = (int)max_gemm_tiles_of(c, T, gp.rows13);
+  const int max_tiles2 = (int)max_gemm_tiles_of(c, T, gp.rows2);
   int* status = at<int>(ws, L.status);
   GemmTile* tiles13 = at<GemmTile>(ws, L.gemm_tiles);
   int32_t* ntiles13 = at<int32_t>(ws, L.num_gemm_tiles);
@@ -451,8 +501,8 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
   if (!tiles_ready) {   // else the small-batch dispatch built both lists
-    const moe::TileListOut l13{tiles13, ntiles13, moe::kW13TileRows, max_tiles13};
-    const moe::TileListOut l2{tiles2, ntiles2, moe::kW2TileRows, max_tiles2};
+    const moe::TileListOut l13{tiles13, ntiles13, gp.rows13, max_tiles13, gp.merge13};
+    const moe::TileListOut l2{tiles2, ntiles2, gp.rows2, max_tiles2, gp.merge2};
     moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, l13, &l2, status, s);
   }
   if (rows_ready) {
@@ -467,7 +517,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   // CTA-pair kernels where the output features are a multiple of 256 (a
   // property of the layer, the same for every T); they take the 256-row tile
   // list and load 128-row token boxes per CTA
-  const bool pair13 = moe::gemm_pair_ok(true, I, H), pair2 = moe::gemm_pair_ok(false, H, I);
+  const bool pair13 = gp.pair13, pair2 = gp.pair2;
   const int box13 = pair13 ? moe::kPairBoxRows : moe::kW13TileRows;
   const int box2 = pair2 ? moe::kPairBoxRows : moe::kW2TileRows;
   CUtensorMap m_w13, m_x, m_xs, m_w2, m_a, m_as;
@@ -482,23 +532,19 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.n_feat_tiles = pair13 ? I / moe::kPairFeatW13 : I / moe::kTileFeat;
   g13.w_rows_per_e = H;
   g13.up_col = I;
-  g13.tiles = pair13 ? tiles2 : tiles13;
-  g13.num_tiles = pair13 ? ntiles2 : ntiles13;
+  g13.tiles = tiles13;
+  g13.num_tiles = ntiles13;
   g13.identity_T = 0;
   g13.out = a;
   g13.out_ld = I;
   g13.status = status;
   g13.pair = pair13 ? 1 : 0;
+  g13.merge = gp.merge13 > 0 ? 1 : 0;
   g13.wait_ns = (unsigned long long)c->debug_wait_ns;
-  moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, pair13 ? max_tiles2 : max_tiles13, sms, s);
+  moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, max_tiles13, sms, s);
   mark(mk, 4);
 
-  // wide W2 items (two 256-feature groups per token tile, the same MMAs)
-  // where the layer has a long reduction and the batch touches enough
-  // experts to keep a quarter of the SMs busy with them (at T = 1 the
-  // Mixtral-like W2 took 0.196 ms with them against 0.167 without)
-  const long long touched = std::min<long long>(N, (long long)T * k);
-  const bool wide2 = pair2 && moe::gemm_wide_ok(H, I) && touched * (H / moe::kPairFeatW2Wide) * 4 >= sms;
+  const bool wide2 = gp.wide2;
   moe::GemmArgs g2 = g13;
   g2.K = I;
   g2.n_feat_tiles = wide2 ? H / moe::kPairFeatW2Wide : (pair2 ? H / moe::kPairFeatW2 : H / moe::kTileFeat);
@@ -511,6 +557,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.out_bf16 = 1;
   g2.pair = pair2 ? 1 : 0;
   g2.wide = wide2 ? 1 : 0;
+  g2.merge = gp.merge2 > 0 ? 1 : 0;
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
@@ -591,7 +638,8 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
   // routed GEMMs
   std::unique_lock<std::mutex> side_lock;
   SideStream side;
-  const bool shared = c->shared_intermediate > 0;
+  // (the debug flag MOE_DEBUG_SHARED_SERIAL runs it on `s` after the routed GEMMs instead)
+  const bool shared = c->shared_intermediate > 0 && !(c->debug_flags & MOE_DEBUG_SHARED_SERIAL);
   bool forked = false;
   auto fork_shared = [&]() -> moe_status {
     if (!shared) return MOE_OK;
@@ -628,10 +676,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
     moe::launch_decode_front(h, wg, bias, at<float>(ws, L.rpart), T, c->hidden, c->num_experts, c->top_k,
                              c->block_size, capacity_of(c, T),
                              idx, gates, kept, pos, sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
-                             at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles), moe::kW13TileRows,
-                             (int)max_gemm_tiles_of(c, T, moe::kW13TileRows), at<GemmTile>(ws, L.gemm_tiles2),
-                             at<int32_t>(ws, L.num_gemm_tiles2), moe::kW2TileRows,
-                             (int)max_gemm_tiles_of(c, T, moe::kW2TileRows), at<uint16_t>(ws, L.x_perm),
+                             list_a(c, T, L, ws), list_b(c, T, L, ws), at<uint16_t>(ws, L.x_perm),
                              max_rows_of(c, T), at<int>(ws, L.status), s);
     st = last_cuda();
     mk.at(1);
@@ -647,10 +692,7 @@ moe_status forward_impl(const moe_config* c, int32_t T, const uint16_t* h, const
       // a few routes: dispatch, alignment and both tile lists in one launch
       moe::launch_dispatch_small(idx, T * c->top_k, c->num_experts, c->block_size, capacity_of(c, T), kept, pos,
                                  sorted, blocks, num_padded, counts, at<int32_t>(ws, L.dropped),
-                                 at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles),
-                                 moe::kW13TileRows, (int)max_gemm_tiles_of(c, T, moe::kW13TileRows),
-                                 at<GemmTile>(ws, L.gemm_tiles2), at<int32_t>(ws, L.num_gemm_tiles2),
-                                 moe::kW2TileRows, (int)max_gemm_tiles_of(c, T, moe::kW2TileRows),
+                                 list_a(c, T, L, ws), list_b(c, T, L, ws),
                                  at<int>(ws, L.status), s);
       tiles_ready = true;
       st = last_cuda();
