@@ -111,8 +111,6 @@ typedef struct moe_config {
 #define MOE_DEBUG_W13_PAIR 0x800u         /* routed W13 on CTA pairs whatever the reduction length */
 #define MOE_DEBUG_W2_WIDE 0x1000u         /* routed W2 pairs in wide items (two 256-feature groups per
                                              token tile) whatever the reduction length */
-#define MOE_DEBUG_NO_MERGE 0x2000u        /* no merged items: an expert's short last tile is a CTA-pair
-                                             work item of its own */
 
 /* Output of moe_routing_stats (device memory, 40 bytes). */
 typedef struct moe_route_stats {

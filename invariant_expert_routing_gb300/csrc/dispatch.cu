@@ -179,8 +179,7 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
 }
 
 // Grouped-GEMM tile lists from the padded blocks: each expert segment is cut
-// into tiles of tile_rows rows from its start (segment_tiles: a short last
-// tile may join the one before it).  CTA 0 writes list `a`, CTA 1
+// into tiles of tile_rows rows from its start.  CTA 0 writes list `a`, CTA 1
 // (when the grid has two) list `b`, from the same blocks.  Rejects (no tiles,
 // status bit) a block list that is not sorted by expert or out of range.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
@@ -258,7 +257,7 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     used -= n;
   }
   const int tile_rows = L.tile_rows;
-  const int nt = rows > 0 ? segment_tiles(rows, used, tile_rows, L.merge_rows) : 0;
+  const int nt = segment_tiles(rows, tile_rows);
   int total = 0;
   const int off = block_exclusive_scan(nt, buf, &total);
   for (int j = 0; j < nt; ++j) {
@@ -400,8 +399,8 @@ __device__ __forceinline__ void dispatch_small_block(
     kept_s[x] = kept;
     pad_s[x] = padded;
     drop_s[x] = run - kept;
-    nta[x] = padded > 0 ? segment_tiles(padded, kept, la.tile_rows, la.merge_rows) : 0;
-    ntb[x] = padded > 0 ? segment_tiles(padded, kept, lb.tile_rows, lb.merge_rows) : 0;
+    nta[x] = segment_tiles(padded, la.tile_rows);
+    ntb[x] = segment_tiles(padded, lb.tile_rows);
     expert_counts[x] = kept;
   }
   __syncthreads();

@@ -435,30 +435,26 @@ constexpr int kPairM = 256;         // weight rows per pair (the MMA's M)
 // item is bound by the operand bytes an SM takes in; its single
 // 512-column accumulator costs the overlap of the epilogue, a few per cent
 // of a 14336-deep reduction.
-template <bool kW13, bool kWide = false, bool kMerge = false>
+template <bool kW13, bool kWide = false>
 struct PairCfg {
   static_assert(!(kW13 && kWide), "wide items are W2 only");
-  static_assert(!(kWide && kMerge), "a wide item's accumulator fills the tensor memory");
   static constexpr int kGroups = kWide ? 2 : 1;              // 256-feature groups per item
   static constexpr int kRowsCta = kPairRows / 2;
   static constexpr int kFeatCta = kW13 ? 64 : 128;           // output features per CTA and group
   static constexpr int kFeatTile = 2 * kFeatCta * kGroups;   // output features per pair tile
   static constexpr uint32_t kABytes = 2 * kBoxBytes * kGroups;   // 128 weight rows x 64 K per group
   static constexpr uint32_t kBTileBytes = kRowsCta * kBK * 2;
-  // merged items: the tail's token rows (kSmallRows per CTA) ride in the
-  // same stage as the main tile's
-  static constexpr uint32_t kTailBytes = kMerge ? kSmallRows * kBK * 2 : 0;
-  static constexpr uint32_t kStageBytes = kABytes + kBTileBytes + kTailBytes;
-  // W2 fits a seventh 32 KB stage in the 227 KB of shared memory; W13 keeps
-  // room for the u exchange (two buffers, or one beside the larger stages
-  // of a merged instance)
-  static constexpr uint32_t kXchgBuffers = kMerge ? 1 : 2;
-  static constexpr uint32_t kXchgBytes = kW13 ? 4 * kXchgBuffers * 32 * 16 * 4 : 0;
-  static constexpr uint32_t kPairBudget = kW13 ? (kMerge ? 216 * 1024 : kStageBudget) : 224 * 1024;
+  static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
+  // W2 fits a seventh 32 KB stage in the 227 KB of shared memory; W13 needs
+  // 16 KB for the u exchange
+  static constexpr uint32_t kPairBudget = kW13 ? kStageBudget : 224 * 1024;
   static constexpr int kStages = (int)(kPairBudget / kStageBytes) < 7 ? (int)(kPairBudget / kStageBytes) : 7;
   static constexpr uint32_t kAccCols = kPairRows * kGroups;
   static constexpr int kNumAcc = kWide ? 1 : 2;
   static constexpr uint32_t kTmemCols = 512;
+  // W13: u handed from the up warps to the gate warps, 4 warp pairs x 2
+  // buffers x 32 lanes x 16 fp32
+  static constexpr uint32_t kXchgBytes = kW13 ? 4 * 2 * 32 * 16 * 4 : 0;
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kXchgBytes + kBarBytes + 1024;
 };
@@ -481,23 +477,14 @@ __device__ __forceinline__ int named_bar_and(int id, int threads, int pred) {
   return (int)r;
 }
 
-// Merged items (kMerge): a tile list may hand an expert's last tile, when
-// it holds at most 2 kSmallRows routed rows, to the tile before it (GemmTile
-// valid > kPairRows).  Such an item loads the tail's rows beside the main
-// tile's in every stage and runs, per K step, the main MMAs (N = 256) and the
-// tail MMAs (N = 2 kSmallRows) on the same weight stage, into the two
-// accumulator buffers: the weights are streamed once for both, instead of a
-// second time for a handful of rows.  Each MMA is the one a separate item
-// would issue, so the bits do not change.  The accumulators form a ring of
-// two; a merged item takes two consecutive slots (main, then tail).
-template <bool kW13, bool kWide = false, bool kMerge = false>
+template <bool kW13, bool kWide = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
                             const __grid_constant__ CUtensorMap x_map,
                             const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   // no early trigger: CTAs of the next kernel would hold SMs idle while they wait
-  using C = PairCfg<kW13, kWide, kMerge>;
+  using C = PairCfg<kW13, kWide>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
@@ -552,14 +539,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
 
-  // ring of accumulator slots: slot -> (buffer, phase)
-  auto next_slot = [](int& acc, uint32_t& phase) {
-    if (++acc == C::kNumAcc) {
-      acc = 0;
-      phase ^= 1u;
-    }
-  };
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     const uint64_t pol_w = policy_evict_normal();
@@ -577,10 +556,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // rounded up to 32-row boxes) and the MMAs run N = 2 b_rows; rows past
       // the routed ones are padding or beyond the tile, in columns that are
       // never stored
-      const bool merged = kMerge && t.valid > kPairRows;
-      const int b_rows = covered_rows((min(t.valid, kPairRows) + 1) / 2, C::kRowsCta);
+      const int b_rows = covered_rows((t.valid + 1) / 2, C::kRowsCta);
       const int brow0 = t.row0 + (int)rank * b_rows;                     // this CTA's half of the rows
-      const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2 + (merged ? kSmallRows * kBK * 2 : 0);
+      const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
         int got = 1;
         if (lane == 0) got = mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, &s_abort, wlim) ? 1 : 0;
@@ -610,9 +588,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_2d_pair(smem_u32(sB) + j * kSmallRows * kBK * 2, &x_map_small, k0, brow0 + j * kSmallRows,
                                fb, pol_x);
           }
-          if (merged)   // the tail's rows: kSmallRows per CTA after the main tile
-            tma_load_2d_pair(smem_u32(sB + C::kBTileBytes), &x_map_small, k0,
-                             t.row0 + kPairRows + (int)rank * kSmallRows, fb, pol_x);
         }
         __syncwarp();
         armed = min(armed + 1, C::kStages);
@@ -657,28 +632,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int item = pair0; item < total && ok; item += pairs) {
-        const TileInfo t = work_of<kPairRows>(args, item, num_tiles, nfe).t;
-        const bool merged = kMerge && t.valid > kPairRows;
-        const int b_rows = covered_rows((min(t.valid, kPairRows) + 1) / 2, C::kRowsCta);
+        const int b_rows = covered_rows((work_of<kPairRows>(args, item, num_tiles, nfe).t.valid + 1) / 2,
+                                        C::kRowsCta);
         const uint32_t idesc = idesc_bf16(kPairM, 2 * b_rows, true, false);
-        const uint32_t idesc_tail = idesc_bf16(kPairM, 2 * kSmallRows, true, false);
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
           break;
         }
-        const int acc_main = acc;
-        int acc_tail = acc;
-        if (merged) {   // the next slot of the ring holds the tail
-          next_slot(acc, acc_phase);
-          acc_tail = acc;
-          if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
-            ok = false;
-            break;
-          }
-        }
         tc_fence_after();
-        const uint32_t d0 = tmem + acc_main * C::kAccCols;
-        const uint32_t d1 = tmem + acc_tail * C::kAccCols;
+        const uint32_t d0 = tmem + acc * C::kAccCols;
         for (int ks = 0; ks < ksteps; ++ks) {
           if (!mbar_wait_cluster(full0 + 8 * stage, phase, &s_abort, wlim)) {
             ok = false;
@@ -696,10 +658,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t adesc1 = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
               mma_bf16_pair(d0 + kPairRows, adesc1, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
             }
-            if (merged) {
-              const uint64_t bdesc_t = sdesc_sw128(b_base + C::kBTileBytes + kk * 32, 16, 1024);
-              mma_bf16_pair(d1, adesc, bdesc_t, idesc_tail, (ks > 0 || kk > 0) ? 1u : 0u);
-            }
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == C::kStages) {
@@ -708,9 +666,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit_pair(tfull0 + 8 * acc_main, 0x3);
-        if (merged) mma_commit_pair(tfull0 + 8 * acc_tail, 0x3);
-        next_slot(acc, acc_phase);
+        mma_commit_pair(tfull0 + 8 * acc, 0x3);
+        if (++acc == C::kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       if (!ok) {
         s_abort = 1;
@@ -724,83 +684,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;                       // TMEM lanes this warp may access
-    const int half = (warp - 2) / 4;                    // its half of the columns
+    const int half = (warp - 2) / 4;                    // its half of the 256 columns
+    const int col0 = half * (kPairRows / 2), col1 = col0 + kPairRows / 2;
     // W13: quarters 0,1 hold g (features 0..63 of the CTA), quarters 2,3 hold u
     const bool up_warp = kW13 && quarter >= 2;
     const int xpair = (quarter & 1) + 2 * half;         // W13: the (gate, up) warp pair
-    float* xbuf = xchg + (size_t)xpair * C::kXchgBuffers * 32 * 16;   // per pair: buffers of 32 lanes x 16
+    float* xbuf = xchg + (size_t)xpair * 2 * 32 * 16;   // two buffers of 32 lanes x 16
     int acc = 0;
     uint32_t acc_phase = 0;
     int chunk = 0;                                      // W13: exchange buffer parity
-    // stores the accumulator columns [c_lo, c_hi) of buffer `buf` (rows
-    // row_base + column) for this warp's lane quarter
-    auto drain_cols = [&](uint32_t buf_col0, int grp, int c_lo, int c_hi, int row_base, int feat) {
-      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + buf_col0 + grp * kPairRows;
-      for (int c = c_lo; c < c_hi; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
-        tmem_wait_ld();
-        if (kW13) {
-          // [column][lane] order: the 32 lanes touch 32 consecutive words
-          // two buffers: one barrier per chunk (the partner's next write goes
-          // to the other buffer); one buffer: a second barrier after the
-          // gate warp's read, which both warps pass (the same count of
-          // barriers in both warps, chunk by chunk)
-          float* buf = xbuf + (C::kXchgBuffers == 2 ? (chunk & 1) * (32 * 16) : 0) + lane;
-          if (up_warp) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) buf[jj * 32] = v[jj];
-            named_bar_sync(1 + xpair, 64);
-            if (C::kXchgBuffers == 1) named_bar_sync(1 + xpair, 64);   // the gate warp has read it
-          } else {
-            named_bar_sync(1 + xpair, 64);
-            float u[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) u[jj] = buf[jj * 32];
-            if (C::kXchgBuffers == 1) named_bar_sync(1 + xpair, 64);   // buffer free again
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int j = c + jj;
-              const float x = v[jj];
-              const float a = (x / (1.0f + expf(-x))) * u[jj];
-              if (j < c_hi) out[(size_t)(row_base + j) * args.out_ld + feat] = __float2bfloat16_rn(a);
-            }
-          }
-          ++chunk;
-        } else if (args.out_bf16) {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = c + jj;
-            if (j < c_hi) out[(size_t)(row_base + j) * args.out_ld + feat] = __float2bfloat16_rn(v[jj]);
-          }
-        } else {
-          float* out = reinterpret_cast<float*>(args.out);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = c + jj;
-            if (j < c_hi) out[(size_t)(row_base + j) * args.out_ld + feat] = v[jj];
-          }
-        }
-      }
-    };
     for (int item = pair0; item < total; item += pairs) {
       const Work wk = work_of<kPairRows>(args, item, num_tiles, nfe);
       const TileInfo t = wk.t;
-      const bool merged = kMerge && t.valid > kPairRows;
       int got = 1;
       if (lane == 0) got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, &s_abort, wlim) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
-      const int acc_main = acc;
-      int acc_tail = acc;
-      if (merged) {
-        next_slot(acc, acc_phase);
-        acc_tail = acc;
-        int got2 = 1;
-        if (lane == 0 && got) got2 = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, &s_abort, wlim) ? 1 : 0;
-        got = got && __shfl_sync(0xffffffffu, got2, 0);
-      }
       // W13: the gate and up warps of a pair meet on a named barrier for
       // every chunk of the tile, so they take the same verdict (one of them
       // must not go on to the exchange while the other gives up)
@@ -813,29 +711,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int main_valid = min(t.valid, kPairRows);
       for (int grp = 0; grp < C::kGroups; ++grp) {
-        const int feat = wk.f * C::kFeatTile + grp * 256 + (int)rank * C::kFeatCta +
-                         (kW13 ? (quarter & 1) * 32 : quarter * 32) + lane;
-        // this warp's half of the main tile's columns
-        const int c0 = half * (kPairRows / 2);
-        drain_cols((uint32_t)(acc_main * C::kAccCols), grp, c0, min(c0 + kPairRows / 2, main_valid), t.row0, feat);
-        if (merged) {   // and of the tail's (2 kSmallRows columns)
-          const int tv = t.valid - kPairRows;
-          const int tc0 = half * kSmallRows;
-          drain_cols((uint32_t)(acc_tail * C::kAccCols), grp, tc0, min(tc0 + kSmallRows, tv), t.row0 + kPairRows,
-                     feat);
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols + grp * kPairRows;
+      const int feat = wk.f * C::kFeatTile + grp * 256 + (int)rank * C::kFeatCta +
+                       (kW13 ? (quarter & 1) * 32 : quarter * 32) + lane;
+      for (int c = col0; c < col1 && c < t.valid; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_wait_ld();
+        if (kW13) {
+          // [column][lane] order: the 32 lanes touch 32 consecutive words
+          float* buf = xbuf + (chunk & 1) * (32 * 16) + lane;
+          if (up_warp) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) buf[jj * 32] = v[jj];
+            named_bar_sync(1 + xpair, 64);
+          } else {
+            named_bar_sync(1 + xpair, 64);
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = c + jj;
+              if (j < t.valid) {   // padding rows are not stored: nothing reads them
+                const float x = v[jj];
+                const float a = (x / (1.0f + expf(-x))) * buf[jj * 32];
+                out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(a);
+              }
+            }
+          }
+          ++chunk;
+        } else if (args.out_bf16) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.valid) out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v[jj]);
+          }
+        } else {
+          float* out = reinterpret_cast<float*>(args.out);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c + jj;
+            if (j < t.valid) out[(size_t)(t.row0 + j) * args.out_ld + feat] = v[jj];
+          }
         }
+      }
       }   // groups
       tc_fence_before();
       __syncwarp();
       // (every tcgen05.ld of this warp completed at its wait::ld; the y / a
       // stores need no ordering against the MMA thread)
-      if (lane == 0) {
-        mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8 * acc_main, 0));
-        if (merged) mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8 * acc_tail, 0));
+      if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8 * acc, 0));
+      if (++acc == C::kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
       }
-      next_slot(acc, acc_phase);
     }
   }
 
@@ -867,7 +797,7 @@ void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMa
 
 // Pairs of CTAs that can be resident at once (one CTA per SM; a pair needs
 // two SMs of one GPC), looked up once per device and kernel.
-template <bool kW13, bool kWide = false, bool kMerge = false>
+template <bool kW13, bool kWide = false>
 int resident_pairs(int num_sms) {
   static int cache[64] = {0};
   int dev = 0;
@@ -877,7 +807,7 @@ int resident_pairs(int num_sms) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<kW13, kWide, kMerge>::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<kW13, kWide>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -885,8 +815,7 @@ int resident_pairs(int num_sms) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13, kWide, kMerge>, &cfg) != cudaSuccess ||
-      n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13, kWide>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
   }
@@ -895,11 +824,11 @@ int resident_pairs(int num_sms) {
   return n;
 }
 
-template <bool kW13, bool kWide = false, bool kMerge = false>
+template <bool kW13, bool kWide = false>
 void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small, GemmArgs a,
                  int max_tiles, int num_sms, cudaStream_t s) {
-  auto kernel = expert_gemm_pair_kernel<kW13, kWide, kMerge>;
-  const int smem = (int)PairCfg<kW13, kWide, kMerge>::kSmemBytes;
+  auto kernel = expert_gemm_pair_kernel<kW13, kWide>;
+  const int smem = (int)PairCfg<kW13, kWide>::kSmemBytes;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -909,7 +838,7 @@ void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUten
   }
   const long long items = (long long)max_tiles * a.n_feat_tiles;
   if (items <= 0) return;
-  const int cap = resident_pairs<kW13, kWide, kMerge>(num_sms);
+  const int cap = resident_pairs<kW13, kWide>(num_sms);
   const int pairs = (int)(items < cap ? items : cap);
   a.concurrent = pairs;
   launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, w_map, x_map, x_small, a);
@@ -926,8 +855,7 @@ bool gemm_smem_ok() {
          optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kRouterTileRowsNarrow>::kSmemBytes &&
          optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes &&
-         optin >= (int)PairCfg<false, true>::kSmemBytes && optin >= (int)PairCfg<true, false, true>::kSmemBytes &&
-         optin >= (int)PairCfg<false, false, true>::kSmemBytes;
+         optin >= (int)PairCfg<false, true>::kSmemBytes;
 }
 
 bool gemm_pair_ok(bool w13, int features, int K) {
@@ -943,9 +871,7 @@ bool gemm_wide_ok(int features, int K) {
 
 void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                      const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
-  if (a.pair && a.merge)
-    launch_pair<true, false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
-  else if (a.pair)
+  if (a.pair)
     launch_pair<true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else
     launch<true, kW13TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
@@ -955,8 +881,6 @@ void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CU
                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
   if (a.pair && a.wide)
     launch_pair<false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
-  else if (a.pair && a.merge)
-    launch_pair<false, false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else if (a.pair)
     launch_pair<false>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else

@@ -61,14 +61,7 @@ struct GemmArgs {
   int wide;            // W2 pairs only, 1: items of two 256-feature groups
                        //    (n_feat_tiles in units of kPairFeatW2Wide)
   unsigned long long wait_ns;  // limit of the pipeline waits; 0: kWaitLimitNs
-  int merge;           // pairs (not wide), 1: the tile list may hold merged tiles (valid up to
-                       //    kPairRows + kMergeRows: a main tile and its segment's short tail)
 };
-
-// A segment's last tile with at most this many routed rows joins the tile
-// before it in tile lists built for merged CTA-pair items (two 32-row boxes,
-// one per CTA of the pair).
-constexpr int kMergeRows = 64;
 
 // Rows of a CTA-pair token tile, the token box each CTA of the pair loads,
 // and the output features of one pair tile.

@@ -156,18 +156,12 @@ struct TileListOut {
   int32_t* num_tiles;
   int tile_rows;
   int max_tiles;
-  int merge_rows;   // > 0: a segment's last tile with at most this many routed rows joins the one
-                    // before it (lists for merged CTA-pair items); 0: never
 };
 // Tiles of one expert segment of `padded` rows (the first `valid` hold
-// routes), cut into tile_rows-row tiles from the segment's start, the last
-// merged into the one before it when the list allows and it holds at most
-// merge_rows routed rows.  Tile j of nt: rows from row0 + j * tile_rows; the
-// last runs to the segment's end.
-__host__ __device__ inline int segment_tiles(int padded, int valid, int tile_rows, int merge_rows) {
-  const int nt = (padded + tile_rows - 1) / tile_rows;
-  if (merge_rows > 0 && nt >= 2 && valid - (nt - 1) * tile_rows <= merge_rows) return nt - 1;
-  return nt;
+// routes), cut into tile_rows-row tiles from the segment's start.  Tile j of
+// nt: rows from row0 + j * tile_rows; the last runs to the segment's end.
+__host__ __device__ inline int segment_tiles(int padded, int tile_rows) {
+  return (padded + tile_rows - 1) / tile_rows;
 }
 __host__ __device__ inline GemmTile segment_tile(int expert, int seg_row0, int padded, int valid, int tile_rows,
                                                  int nt, int j, int first) {

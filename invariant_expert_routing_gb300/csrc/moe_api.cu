@@ -18,7 +18,7 @@ namespace {
 using moe::GemmTile;
 
 constexpr int kMaxDevices = 64;
-constexpr uint32_t kKnownDebugFlags = 0x3FFFu;
+constexpr uint32_t kKnownDebugFlags = 0x1FFFu;
 static_assert(MOE_DEBUG_ROUTER_TC == moe::kPathRouterTc && MOE_DEBUG_ROUTER_CHUNKED == moe::kPathRouterChunked &&
                   MOE_DEBUG_ROW_GATHER == moe::kPathRowGather && MOE_DEBUG_ROW_SCATTER == moe::kPathRowScatter &&
                   MOE_DEBUG_NO_DECODE_FRONT == moe::kPathNoDecodeFront &&
@@ -198,13 +198,10 @@ P* at(void* ws, size_t off) {
 
 // The routed GEMMs of a forward: which kernel runs each, and the tile list
 // each consumes (list a: W13, list b: W2).  A property of the layer's shape,
-// except the wide W2 items, which also need enough touched experts.  Lists
-// consumed by CTA-pair kernels that can run merged items hand a segment's
-// short last tile to the tile before it (kMergeRows).
+// except the wide W2 items, which also need enough touched experts.
 struct GemmPlan {
   bool pair13, pair2, wide2;
   int rows13, rows2;     // token rows per tile of lists a and b
-  int merge13, merge2;   // merge_rows of lists a and b
 };
 
 moe_status check_ws(const moe_config* c, int32_t T, const void* ws, size_t ws_bytes);
@@ -215,12 +212,12 @@ int num_sms();
 moe::TileListOut list_a(const moe_config* c, int32_t T, const Layout& L, void* ws) {
   const GemmPlan gp = plan_of(c, T, num_sms());
   return moe::TileListOut{at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles), gp.rows13,
-                          (int)max_gemm_tiles_of(c, T, gp.rows13), gp.merge13};
+                          (int)max_gemm_tiles_of(c, T, gp.rows13)};
 }
 moe::TileListOut list_b(const moe_config* c, int32_t T, const Layout& L, void* ws) {
   const GemmPlan gp = plan_of(c, T, num_sms());
   return moe::TileListOut{at<GemmTile>(ws, L.gemm_tiles2), at<int32_t>(ws, L.num_gemm_tiles2), gp.rows2,
-                          (int)max_gemm_tiles_of(c, T, gp.rows2), gp.merge2};
+                          (int)max_gemm_tiles_of(c, T, gp.rows2)};
 }
 
 moe_status check_ws(const moe_config* c, int32_t T, const void* ws, size_t ws_bytes) {
@@ -257,11 +254,8 @@ GemmPlan plan_of(const moe_config* c, int32_t T, int sms) {
   // Mixtral-like W2 took 0.196 ms with them against 0.167 without)
   const long long touched = std::min<long long>(N, (long long)T * k);
   p.wide2 = p.pair2 && wide_shape && touched * (H / moe::kPairFeatW2Wide) * 4 >= sms;
-  const bool no_merge = (c->debug_flags & MOE_DEBUG_NO_MERGE) != 0;
   p.rows13 = p.pair13 ? moe::kPairTileRows : moe::kW13TileRows;
   p.rows2 = moe::kW2TileRows;
-  p.merge13 = (p.pair13 && !no_merge) ? moe::kMergeRows : 0;
-  p.merge2 = (p.pair2 && !p.wide2 && !no_merge) ? moe::kMergeRows : 0;
   return p;
 }
 
@@ -501,8 +495,8 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
   if (!tiles_ready) {   // else the small-batch dispatch built both lists
-    const moe::TileListOut l13{tiles13, ntiles13, gp.rows13, max_tiles13, gp.merge13};
-    const moe::TileListOut l2{tiles2, ntiles2, gp.rows2, max_tiles2, gp.merge2};
+    const moe::TileListOut l13{tiles13, ntiles13, gp.rows13, max_tiles13};
+    const moe::TileListOut l2{tiles2, ntiles2, gp.rows2, max_tiles2};
     moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, l13, &l2, status, s);
   }
   if (rows_ready) {
@@ -539,7 +533,6 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.out_ld = I;
   g13.status = status;
   g13.pair = pair13 ? 1 : 0;
-  g13.merge = gp.merge13 > 0 ? 1 : 0;
   g13.wait_ns = (unsigned long long)c->debug_wait_ns;
   moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, max_tiles13, sms, s);
   mark(mk, 4);
@@ -557,7 +550,6 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.out_bf16 = 1;
   g2.pair = pair2 ? 1 : 0;
   g2.wide = wide2 ? 1 : 0;
-  g2.merge = gp.merge2 > 0 ? 1 : 0;
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
