@@ -38,7 +38,7 @@ constexpr int kBK = 64;                             // K per stage: one 128-byte
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // 64 K rows x 64 features of bf16
 constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter, one column half each
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr int kSmallRows = 32;                      // token rows of the small box (partial tiles)
+constexpr int kSmallRows = 32;                      // token box when a tile has <= 32 routed rows
 constexpr uint32_t kStageBudget = 192 * 1024;       // shared memory for the operand stages
 
 constexpr uint32_t pow2_at_least(uint32_t x) {
@@ -61,19 +61,9 @@ struct GemmCfg {
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
   // M = 128 features, N = BN token rows; A (weights) MN-major, B (tokens) K-major.
+  static constexpr uint32_t kIdesc = idesc_bf16(kTileFeat, BN, true, false);
+  static constexpr uint32_t kIdescSmall = idesc_bf16(kTileFeat, kSmallRows, true, false);
 };
-
-// Token rows a tile's MMAs cover: the rows that hold routes rounded up to a
-// multiple of kSmallRows, at most `cap` (the tile height, or one CTA's half
-// of a pair tile).  The MMA's N follows it.  Each column of an MMA is one
-// token's dot products over the same K steps, so N changes which columns are
-// computed, never how: a partial tile (the last of an expert's segment, or a
-// decode tile) loads and multiplies only its routed rows' boxes.
-__device__ __forceinline__ int covered_rows(int rows_needed, int cap) {
-  int r = (rows_needed + kSmallRows - 1) / kSmallRows * kSmallRows;
-  r = r < kSmallRows ? kSmallRows : r;
-  return r < cap ? r : cap;
-}
 
 struct TileInfo {
   int expert, row0, rows, valid;
@@ -199,9 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int f = wk.f;
       const int wrow0 = t.expert * args.w_rows_per_e;
       const int fcol = f * kTileFeat;
-      // a partial tile loads its routed rows in 32-row boxes and runs
-      // MMAs of N = those rows (see covered_rows)
-      const int b_rows = covered_rows(t.valid, BN);
+      // A tile with at most 32 rows holding routes (decode) loads a 32-row
+      // token box and runs N = 32 MMAs (columns of an MMA are independent:
+      // each token column's sum over K runs in the same order for any N).
+      const bool small = t.valid <= kSmallRows;
+      const int b_rows = small ? kSmallRows : BN;
       const uint32_t stage_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
         // one lane waits, the warp follows its verdict (keeps the warp converged)
@@ -224,13 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
             tma_load_2d(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb, pol_w);
           }
-          if (b_rows == BN) {
-            tma_load_2d(smem_u32(sB), &x_map, k0, t.row0, fb, pol_x);
-          } else {
-            for (int j = 0; j < b_rows / kSmallRows; ++j)
-              tma_load_2d(smem_u32(sB) + j * kSmallRows * kBK * 2, &x_map_small, k0, t.row0 + j * kSmallRows,
-                          fb, pol_x);
-          }
+          tma_load_2d(smem_u32(sB), small ? &x_map_small : &x_map, k0, t.row0, fb, pol_x);
         }
         __syncwarp();
         armed = min(armed + 1, C::kStages);
@@ -267,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int item = unit0; item < total && ok; item += units) {
-        const int b_rows = covered_rows(work_of<BN>(args, item, num_tiles, nfe).t.valid, BN);
-        const uint32_t idesc = idesc_bf16(kTileFeat, b_rows, true, false);
+        const bool small = work_of<BN>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
+        const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
           break;
@@ -411,13 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 //        a = silu(g) * u.
 // One weight tile shape and one K order (from 0 to the end, 64 per stage, 16
 // per MMA) for every tile and every batch.  The MMA's N (token columns) is
-// 256 for a full tile, else twice the 32-row boxes each CTA loads (64, 128,
-// 192: a partial tile, the last of a segment or a decode tile): the columns
-// of an MMA are independent dot products over the same K steps, so a token
-// row's arithmetic does not depend on the batch, on N, or on which half of
-// the tile holds it (the GPU batch-invariance tests compare rows computed
-// with N = 64 against the same rows computed with every other N, bit for
-// bit).
+// 256, or 64 for a tile with at most 32 routed rows (decode): the columns of
+// an MMA are independent dot products over the same K steps, so a token row's
+// arithmetic does not depend on the batch, on N, or on which half of the
+// tile holds it (the GPU batch-invariance tests compare rows computed with
+// N = 64 against the same rows computed with N = 256, bit for bit).
 //
 // Synchronisation: the even CTA's producer expects the bytes of both CTAs on
 // its full barrier, and both CTAs' TMA loads complete there; the even CTA's
@@ -457,6 +441,10 @@ struct PairCfg {
   static constexpr uint32_t kXchgBytes = kW13 ? 4 * 2 * 32 * 16 * 4 : 0;
   static constexpr uint32_t kBarBytes = 256;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kXchgBytes + kBarBytes + 1024;
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairM, kPairRows, true, false);
+  // tiles with at most kSmallRows routed rows: N = 2 x kSmallRows (each CTA
+  // supplies kSmallRows token rows)
+  static constexpr uint32_t kIdescSmall = idesc_bf16(kPairM, 2 * kSmallRows, true, false);
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
@@ -552,11 +540,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const TileInfo t = wk.t;
       const int wrow0 = t.expert * args.w_rows_per_e;
       const int fcol = wk.f * C::kFeatTile + (int)rank * C::kFeatCta;   // this CTA's features (group 0)
-      // a partial tile: each CTA loads b_rows rows (half of the routed rows,
-      // rounded up to 32-row boxes) and the MMAs run N = 2 b_rows; rows past
-      // the routed ones are padding or beyond the tile, in columns that are
-      // never stored
-      const int b_rows = covered_rows((t.valid + 1) / 2, C::kRowsCta);
+      // tiles with at most kSmallRows routed rows (decode): a kSmallRows-row
+      // token box per CTA and N = 2 kSmallRows MMAs; the odd CTA's rows are
+      // padding or beyond the tile, in columns that are never stored
+      const bool small = t.valid <= kSmallRows;
+      const int b_rows = small ? kSmallRows : C::kRowsCta;
       const int brow0 = t.row0 + (int)rank * b_rows;                     // this CTA's half of the rows
       const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
@@ -581,13 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(smem_u32(sA + 2 * kBoxBytes), &w_map, fcol + 256, wrow0 + k0, fb, pol_w);
             tma_load_2d_pair(smem_u32(sA + 3 * kBoxBytes), &w_map, fcol + 256 + 64, wrow0 + k0, fb, pol_w);
           }
-          if (b_rows == C::kRowsCta) {
-            tma_load_2d_pair(smem_u32(sB), &x_map, k0, brow0, fb, pol_x);
-          } else {
-            for (int j = 0; j < b_rows / kSmallRows; ++j)
-              tma_load_2d_pair(smem_u32(sB) + j * kSmallRows * kBK * 2, &x_map_small, k0, brow0 + j * kSmallRows,
-                               fb, pol_x);
-          }
+          tma_load_2d_pair(smem_u32(sB), small ? &x_map_small : &x_map, k0, brow0, fb, pol_x);
         }
         __syncwarp();
         armed = min(armed + 1, C::kStages);
@@ -632,9 +614,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int item = pair0; item < total && ok; item += pairs) {
-        const int b_rows = covered_rows((work_of<kPairRows>(args, item, num_tiles, nfe).t.valid + 1) / 2,
-                                        C::kRowsCta);
-        const uint32_t idesc = idesc_bf16(kPairM, 2 * b_rows, true, false);
+        const bool small = work_of<kPairRows>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
+        const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
           break;
@@ -759,9 +740,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }   // groups
       tc_fence_before();
       __syncwarp();
-      // (every tcgen05.ld of this warp completed at its wait::ld; the y / a
-      // stores need no ordering against the MMA thread)
-      if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8 * acc, 0));
+      if (lane == 0) mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
       if (++acc == C::kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;

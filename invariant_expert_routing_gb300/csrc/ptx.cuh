@@ -205,15 +205,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// The same arrive without release semantics: it orders none of the thread's
-// earlier memory accesses (a cluster-scope release would wait for every
-// global store the thread issued before it to be performed).  For the
-// epilogue's "accumulator drained" signal, whose only hazard is tensor-memory
-// reads that tcgen05.wait::ld has already completed.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
