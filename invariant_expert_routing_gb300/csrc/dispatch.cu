@@ -371,7 +371,7 @@ __device__ __forceinline__ void dispatch_small_block(
     const int32_t* topk_idx, int R, int N, int B, int capacity, uint8_t* __restrict__ route_kept,
     int32_t* route_pos, int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ num_padded, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_dropped,
-    const TileListOut& la, const TileListOut& lb, int* status) {
+    const TileListOut& la, const TileListOut& lb, int* status, int32_t* pos_smem = nullptr) {
   __shared__ int wc[32][kMaxN + 1];
   __shared__ int kept_s[kMaxN], pad_s[kMaxN], drop_s[kMaxN], nta[kMaxN], ntb[kMaxN];
   __shared__ int seg[kMaxN], offa[kMaxN], offb[kMaxN];
@@ -420,20 +420,20 @@ __device__ __forceinline__ void dispatch_small_block(
   }
   __syncthreads();
   if (r < R) {
+    int p = -1;
     if (valid) {
       const int rk = wc[w][e] + rank;
       const bool kept = capacity < 0 || rk < capacity;
       route_kept[r] = kept ? 1 : 0;
       if (kept) {
-        route_pos[r] = seg[e] + rk;
-        sorted_route_ids[seg[e] + rk] = r;
-      } else {
-        route_pos[r] = -1;
+        p = seg[e] + rk;
+        sorted_route_ids[p] = r;
       }
     } else {
       route_kept[r] = 0;
-      route_pos[r] = -1;
     }
+    route_pos[r] = p;
+    if (pos_smem) pos_smem[r] = p;   // the caller's copy of the rows reads it here
   }
   for (int x = tid; x < N; x += blockDim.x) {
     for (int j = kept_s[x]; j < pad_s[x]; ++j) sorted_route_ids[seg[x] + j] = R;
@@ -488,6 +488,11 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
   pdl_wait();      // earlier kernels' outputs are visible from here on
   // no early trigger: the next kernel is a GEMM
   __shared__ float lrow[kFinishMaxT][kMaxN];
+  // the routes' experts and padded rows stay in shared memory for the steps
+  // of this CTA that read them (their global copies are for later kernels)
+  __shared__ int32_t s_idx[kFinishMaxT * 16];
+  __shared__ float s_gate[kFinishMaxT * 16];
+  __shared__ int32_t s_pos[kFinishMaxT * 16];
   const int C = (H + kRouterChunk - 1) / kRouterChunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int x = tid; x < T * N; x += blockDim.x) {
@@ -499,19 +504,39 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
     lrow[t][e] = total;
   }
   __syncthreads();
-  if (warp < T) sel::topk_select_warp(lrow[warp], N, k, lane, topk_idx + (size_t)warp * k, gates + (size_t)warp * k);
+  if (warp < T) sel::topk_select_warp(lrow[warp], N, k, lane, s_idx + warp * k, s_gate + warp * k);
   __syncthreads();
   const int R = T * k;
-  dispatch_small_block(topk_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
-                       num_padded, expert_counts, num_dropped, la, lb, status);
+  if (tid < R) {
+    topk_idx[tid] = s_idx[tid];
+    gates[tid] = s_gate[tid];
+  }
+  dispatch_small_block(s_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
+                       num_padded, expert_counts, num_dropped, la, lb, status, s_pos);
   __syncthreads();
-  // the routed token rows (padding rows feed only MMA columns that are never stored)
+  // the routed token rows (padding rows feed only MMA columns that are never
+  // stored), four 16-byte pieces per thread and round, loads before stores
   const int pieces = H / 8;
-  for (int x = tid; x < R * pieces; x += blockDim.x) {
-    const int r = x / pieces, q = x % pieces;
-    const long long p = route_pos[r];
-    if (p >= 0 && p < max_rows)
-      reinterpret_cast<uint4*>(x_perm + p * H)[q] = __ldg(reinterpret_cast<const uint4*>(h + (size_t)(r / k) * H) + q);
+  const int total = R * pieces;
+  for (int x0 = tid; x0 < total; x0 += 4 * blockDim.x) {
+    uint4 v[4];
+    long long dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + u * blockDim.x;
+      dst[u] = -1;
+      if (x < total) {
+        const int r = x / pieces, q = x % pieces;
+        const long long p = s_pos[r];
+        if (p >= 0 && p < max_rows) {
+          v[u] = __ldg(reinterpret_cast<const uint4*>(h + (size_t)(r / k) * H) + q);
+          dst[u] = p * H + (long long)q * 8;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dst[u] >= 0) *reinterpret_cast<uint4*>(x_perm + dst[u]) = v[u];
   }
 }
 
