@@ -493,6 +493,12 @@ def run_gpu(args):
     from synth import workloads as W
 
     wl = W.WORKLOADS[args.workload]
+    if args.num_experts is not None:
+        # a smaller case of the same layer (fewer routed experts, the same
+        # kernels), for profilers: the full-set counters want a few GB on the
+        # device at most
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}{args.num_experts}", num_experts=args.num_experts)
     T = args.tokens
     if T is None:   # the workload's largest configured batch (the Mixtral-like layer: 4096)
         T = max(wl.tokens)
@@ -764,9 +770,13 @@ def main():
                     help="overflow policy for routes past an expert's capacity")
     ap.add_argument("--routing", default="token", choices=["token", "expert"],
                     help="token choice (top-k) or expert choice (top-C tokens per expert)")
+    ap.add_argument("--num-experts", type=int, default=None,
+                    help="with --profile-run: the layer with this many routed experts (a small case)")
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up + steps forwards of the main workload (for ncu)")
     args = ap.parse_args()
+    if args.num_experts is not None and not args.profile_run:
+        ap.error("--num-experts is for --profile-run captures only")
     if args.warmup < 3 and not args.profile_run:
         args.warmup = 3
     if args.impl == "reference":
