@@ -315,12 +315,34 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
   for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < T + P;
        item += warps) {
     if (item < T) {
+      // each 16-byte piece of the row is loaded once and stored to every
+      // kept slot; lane l holds the padded row of slot g * 32 + l, for the
+      // slot groups g of 32 (one group for token choice, k <= 16)
       const uint4* src = reinterpret_cast<const uint4*>(h + (size_t)item * H);
-      for (int j = 0; j < k; ++j) {
-        const long long p = route_pos[item * k + j];
-        if (p < 0 || p >= P) continue;   // dropped
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + p * H);
-        for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+      auto slot_row = [&](int j) -> long long {
+        const long long p = j < k ? route_pos[item * k + j] : -1;
+        return (p < 0 || p >= P) ? -1 : p;   // dropped
+      };
+      const long long p0 = slot_row(lane);
+      const unsigned kept0 = __ballot_sync(0xffffffffu, p0 >= 0);
+      // (the loop bounds are the same in every lane: the shuffles below need the whole warp)
+      for (int base = 0; base < chunks; base += 4 * 32) {
+        const int c0 = base + lane;
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c0 + u * 32 < chunks) v[u] = __ldg(src + c0 + u * 32);
+        for (int g = 0; g * 32 < k; ++g) {
+          const long long my_p = g == 0 ? p0 : slot_row(g * 32 + lane);
+          const unsigned kept = g == 0 ? kept0 : __ballot_sync(0xffffffffu, my_p >= 0);
+          for (unsigned m = kept; m; m &= m - 1) {
+            const long long p = __shfl_sync(0xffffffffu, my_p, __ffs(m) - 1);
+            uint4* dst = reinterpret_cast<uint4*>(x_perm + p * H);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (c0 + u * 32 < chunks) dst[c0 + u * 32] = v[u];
+          }
+        }
       }
     } else {
       const long long row = item - T;
