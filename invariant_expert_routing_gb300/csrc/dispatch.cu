@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
   if (s_bad) {
     if (threadIdx.x == 0) {
       *L.num_tiles = 0;
+      if (L.next_item) *L.next_item = 0;
       atomicOr(status, kDevErrBadBlocks);
     }
     return;
@@ -264,7 +265,10 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     const int idx = off + j;
     if (idx < L.max_tiles) L.tiles[idx] = segment_tile(e, first * B, rows, used, tile_rows, nt, j, off);
   }
-  if (threadIdx.x == 0) *L.num_tiles = min(total, L.max_tiles);
+  if (threadIdx.x == 0) {
+    *L.num_tiles = min(total, L.max_tiles);
+    if (L.next_item) *L.next_item = 0;
+  }
 }
 
 // x_perm[p] = h[r / k] for padded row p holding route r, zeros for the
@@ -476,6 +480,8 @@ __device__ __forceinline__ void dispatch_small_block(
     *num_dropped = s_drop;
     *la.num_tiles = min(s_ta, la.max_tiles);
     *lb.num_tiles = min(s_tb, lb.max_tiles);
+    if (la.next_item) *la.next_item = 0;
+    if (lb.next_item) *lb.next_item = 0;
   }
 }
 

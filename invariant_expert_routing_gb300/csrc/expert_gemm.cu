@@ -40,6 +40,9 @@ constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmallRows = 32;                      // token box when a tile has <= 32 routed rows
 constexpr uint32_t kStageBudget = 192 * 1024;       // shared memory for the operand stages
+// Work items reach the MMA issuer and the epilogue warps through a ring of
+// this many slots, filled by the producer (which fetches them).
+constexpr int kItemRing = 8;
 
 constexpr uint32_t pow2_at_least(uint32_t x) {
   uint32_t p = 32;
@@ -117,6 +120,38 @@ __device__ __forceinline__ Work work_of(const GemmArgs& a, int item, int num_til
   return w;
 }
 
+// A slot of the item ring: the item and the tile it names (item -1: no
+// more items).  The producer that fetches an item fills its slot, so the
+// MMA issuer and the epilogue warps read the tile from shared memory.
+struct ItemSlot {
+  int item, f, expert, row0, valid, pad[3];
+};
+
+template <int BN>
+__device__ __forceinline__ ItemSlot slot_of(const GemmArgs& a, int item, int total, int num_tiles, int nf) {
+  ItemSlot v{};
+  v.item = -1;
+  if (item >= 0 && item < total) {
+    const Work w = work_of<BN>(a, item, num_tiles, nf);
+    v.item = item;
+    v.f = w.f;
+    v.expert = w.t.expert;
+    v.row0 = w.t.row0;
+    v.valid = w.t.valid;
+  }
+  return v;
+}
+
+__device__ __forceinline__ ItemSlot shfl_slot(const ItemSlot& v) {
+  ItemSlot r{};
+  r.item = __shfl_sync(0xffffffffu, v.item, 0);
+  r.f = __shfl_sync(0xffffffffu, v.f, 0);
+  r.expert = __shfl_sync(0xffffffffu, v.expert, 0);
+  r.row0 = __shfl_sync(0xffffffffu, v.row0, 0);
+  r.valid = __shfl_sync(0xffffffffu, v.valid, 0);
+  return r;
+}
+
 template <bool kW13, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
@@ -128,6 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
+  __shared__ __align__(8) uint64_t s_ibar[2 * kItemRing];   // item ring: full, then empty barriers
+  __shared__ ItemSlot s_ring[kItemRing];
 
   const int num_tiles = args.identity_T ? (args.identity_T + BN - 1) / BN : *args.num_tiles;
   const int nfe = args.n_feat_tiles;
@@ -143,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tfull0 = empty0 + 8 * C::kStages;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
+  const uint32_t ifull0 = smem_u32(s_ibar), iempty0 = ifull0 + 8 * kItemRing;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ksteps = args.K / kBK;
@@ -158,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty0 + 8 * b, kEpiWarps * 32);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(ifull0 + 8 * i, 1);
+      mbar_init(iempty0 + 8 * i, 1 + kEpiWarps);   // the MMA issuer and each epilogue warp
+    }
     s_abort = 0;
     fence_mbar_init();
   }
@@ -183,16 +225,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int armed = 0;  // stages armed and not yet known consumed (for the abort path)
     bool ok = true;
-    for (int item = unit0; item < total && ok; item += units) {
-      const Work wk = work_of<BN>(args, item, num_tiles, nfe);
-      const TileInfo t = wk.t;
-      const int f = wk.f;
-      const int wrow0 = t.expert * args.w_rows_per_e;
-      const int fcol = f * kTileFeat;
+    // Items: the CTA's own index first, then from the tile counter
+    // (whichever CTA is free takes the next tile) or, without one, every
+    // units-th.  Lane 0 fetches one item ahead (the counter's round trip
+    // overlaps the current item's loads) and publishes item n + 1 to the
+    // ring after the first stage of item n.
+    int fetched = 0;
+    auto fetch = [&]() -> int {   // the CTA's first item is its own index; the counter hands out the rest
+      const int k = fetched++;
+      if (k == 0) return unit0;
+      return args.next_item ? units + atomicAdd(args.next_item, 1) : unit0 + k * units;
+    };
+    auto publish = [&](int n, const ItemSlot& v) -> bool {
+      const int slot = n & (kItemRing - 1);
+      if (!mbar_wait(iempty0 + 8 * slot, ((n / kItemRing) & 1) ^ 1u, &s_abort, wlim)) return false;
+      s_ring[slot] = v;
+      mbar_arrive(ifull0 + 8 * slot);
+      return true;
+    };
+    ItemSlot cur{}, next{};
+    int nxt = -1, got = 1;
+    if (lane == 0) {
+      cur = slot_of<BN>(args, fetch(), total, num_tiles, nfe);
+      got = publish(0, cur) ? 1 : 0;
+      if (cur.item >= 0) nxt = fetch();
+    }
+    if (!__shfl_sync(0xffffffffu, got, 0)) ok = false;
+    cur = shfl_slot(cur);
+    for (int n = 0; ok && cur.item >= 0; ++n) {
+      const int wrow0 = cur.expert * args.w_rows_per_e;
+      const int fcol = cur.f * kTileFeat;
       // A tile with at most 32 rows holding routes (decode) loads a 32-row
       // token box and runs N = 32 MMAs (columns of an MMA are independent:
       // each token column's sum over K runs in the same order for any N).
-      const bool small = t.valid <= kSmallRows;
+      const bool small = cur.valid <= kSmallRows;
       const int b_rows = small ? kSmallRows : BN;
       const uint32_t stage_tx = C::kABytes + b_rows * kBK * 2;
       for (int ks = 0; ks < ksteps; ++ks) {
@@ -216,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem_u32(sA + 2 * kBoxBytes), &w_map, args.up_col + fcol, wrow0 + k0, fb, pol_w);
             tma_load_2d(smem_u32(sA + 3 * kBoxBytes), &w_map, args.up_col + fcol + 64, wrow0 + k0, fb, pol_w);
           }
-          tma_load_2d(smem_u32(sB), small ? &x_map_small : &x_map, k0, t.row0, fb, pol_x);
+          tma_load_2d(smem_u32(sB), small ? &x_map_small : &x_map, k0, cur.row0, fb, pol_x);
         }
         __syncwarp();
         armed = min(armed + 1, C::kStages);
@@ -224,7 +290,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
+        if (ks == 0) {
+          int pub = 1;
+          if (lane == 0) {
+            next = slot_of<BN>(args, nxt, total, num_tiles, nfe);
+            pub = publish(n + 1, next) ? 1 : 0;
+            if (pub && next.item >= 0) nxt = fetch();
+          }
+          if (!__shfl_sync(0xffffffffu, pub, 0)) {
+            ok = false;
+            break;
+          }
+        }
       }
+      cur = shfl_slot(next);
     }
     if (!ok) {
       s_abort = 1;
@@ -252,8 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int item = unit0; item < total && ok; item += units) {
-        const bool small = work_of<BN>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
+      for (int n = 0; ok; ++n) {
+        const int slot = n & (kItemRing - 1);
+        if (!mbar_wait(ifull0 + 8 * slot, (n / kItemRing) & 1, &s_abort, wlim)) {
+          ok = false;
+          break;
+        }
+        const ItemSlot it = s_ring[slot];
+        mbar_arrive(iempty0 + 8 * slot);
+        if (it.item < 0) break;
+        const bool small = it.valid <= kSmallRows;
         const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
@@ -313,12 +400,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = ((warp - 2) / 4) * (BN / 2), col1 = col0 + BN / 2;  // this warp's column half
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int item = unit0; item < total; item += units) {
-      const Work wk = work_of<BN>(args, item, num_tiles, nfe);
-      const TileInfo t = wk.t;
-      const int f = wk.f;
+    for (int n = 0;; ++n) {
+      ItemSlot it{};
+      it.item = -1;
       int got = 1;
-      if (lane == 0) got = mbar_wait(tfull0 + 8 * acc, acc_phase, &s_abort, wlim) ? 1 : 0;
+      if (lane == 0) {
+        const int slot = n & (kItemRing - 1);
+        got = mbar_wait(ifull0 + 8 * slot, (n / kItemRing) & 1, &s_abort, wlim) ? 1 : 0;
+        if (got) {
+          it = s_ring[slot];
+          mbar_arrive(iempty0 + 8 * slot);
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      it = shfl_slot(it);
+      if (got && it.item < 0) break;
+      TileInfo t{};
+      t.row0 = it.row0;
+      t.valid = it.valid;
+      const int f = it.f;
+      if (got && lane == 0) got = mbar_wait(tfull0 + 8 * acc, acc_phase, &s_abort, wlim) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) {
         if (lane == 0) {

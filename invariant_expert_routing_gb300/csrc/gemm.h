@@ -61,6 +61,10 @@ struct GemmArgs {
   int wide;            // W2 pairs only, 1: items of two 256-feature groups
                        //    (n_feat_tiles in units of kPairFeatW2Wide)
   unsigned long long wait_ns;  // limit of the pipeline waits; 0: kWaitLimitNs
+  int32_t* next_item;  // one-CTA kernel, routed mode: the launch's tile counter (zero before the
+                       // launch); each CTA takes the next item from it when it is free.  nullptr
+                       // (and the pair kernels): CTA (pair) u takes items u, u + grid, ...  Only
+                       // which CTA runs a tile changes, never the tile's arithmetic.
 };
 
 // Rows of a CTA-pair token tile, the token box each CTA of the pair loads,

@@ -156,6 +156,7 @@ struct TileListOut {
   int32_t* num_tiles;
   int tile_rows;
   int max_tiles;
+  int32_t* next_item;   // the GEMM's tile counter: zeroed where num_tiles is written
 };
 // Tiles of one expert segment of `padded` rows (the first `valid` hold
 // routes), cut into tile_rows-row tiles from the segment's start.  Tile j of

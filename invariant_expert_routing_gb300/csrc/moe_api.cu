@@ -175,9 +175,9 @@ Layout layout_of(const moe_config* c, int32_t T) {
   L.ec_keys = take(expert_choice(c) ? sizeof(unsigned long long) * N * T : 0);
   // tile lists of the W13 (128-row) and W2 (256-row) GEMMs
   L.gemm_tiles = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW13TileRows));
-  L.num_gemm_tiles = take(sizeof(int32_t));
+  L.num_gemm_tiles = take(2 * sizeof(int32_t));   // the tile count, then the GEMM's tile counter
   L.gemm_tiles2 = take(sizeof(GemmTile) * (size_t)max_gemm_tiles_of(c, T, moe::kW2TileRows));
-  L.num_gemm_tiles2 = take(sizeof(int32_t));
+  L.num_gemm_tiles2 = take(2 * sizeof(int32_t));
   // x_perm and a keep one tile of rows of slack so every tile load stays inside them
   L.x_perm = take(sizeof(uint16_t) * (rows + moe::kMaxTileRows) * H);
   L.a = take(sizeof(uint16_t) * (rows + moe::kMaxTileRows) * c->intermediate);
@@ -212,12 +212,12 @@ int num_sms();
 moe::TileListOut list_a(const moe_config* c, int32_t T, const Layout& L, void* ws) {
   const GemmPlan gp = plan_of(c, T, num_sms());
   return moe::TileListOut{at<GemmTile>(ws, L.gemm_tiles), at<int32_t>(ws, L.num_gemm_tiles), gp.rows13,
-                          (int)max_gemm_tiles_of(c, T, gp.rows13)};
+                          (int)max_gemm_tiles_of(c, T, gp.rows13), at<int32_t>(ws, L.num_gemm_tiles) + 1};
 }
 moe::TileListOut list_b(const moe_config* c, int32_t T, const Layout& L, void* ws) {
   const GemmPlan gp = plan_of(c, T, num_sms());
   return moe::TileListOut{at<GemmTile>(ws, L.gemm_tiles2), at<int32_t>(ws, L.num_gemm_tiles2), gp.rows2,
-                          (int)max_gemm_tiles_of(c, T, gp.rows2)};
+                          (int)max_gemm_tiles_of(c, T, gp.rows2), at<int32_t>(ws, L.num_gemm_tiles2) + 1};
 }
 
 moe_status check_ws(const moe_config* c, int32_t T, const void* ws, size_t ws_bytes) {
@@ -495,8 +495,8 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
   if (!tiles_ready) {   // else the small-batch dispatch built both lists
-    const moe::TileListOut l13{tiles13, ntiles13, gp.rows13, max_tiles13};
-    const moe::TileListOut l2{tiles2, ntiles2, gp.rows2, max_tiles2};
+    const moe::TileListOut l13{tiles13, ntiles13, gp.rows13, max_tiles13, ntiles13 + 1};
+    const moe::TileListOut l2{tiles2, ntiles2, gp.rows2, max_tiles2, ntiles2 + 1};
     moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, l13, &l2, status, s);
   }
   if (rows_ready) {
@@ -528,6 +528,10 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.up_col = I;
   g13.tiles = tiles13;
   g13.num_tiles = ntiles13;
+  // the one-CTA kernel takes its tiles from a counter (zeroed with the tile
+  // count): whichever CTA is free takes the next tile.  The pair kernels
+  // keep the fixed assignment (item u + n * pairs), which measured faster.
+  g13.next_item = pair13 ? nullptr : ntiles13 + 1;
   g13.identity_T = 0;
   g13.out = a;
   g13.out_ld = I;
@@ -545,6 +549,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.up_col = 0;
   g2.tiles = tiles2;
   g2.num_tiles = ntiles2;
+  g2.next_item = pair2 ? nullptr : ntiles2 + 1;
   g2.out = y_perm;
   g2.out_ld = H;
   g2.out_bf16 = 1;
