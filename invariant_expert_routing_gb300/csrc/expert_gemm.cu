@@ -331,6 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // The MMA issue must keep up with the tensor pipe (an M = 128 x N = 128
+      // MMA takes ~64 cycles), so the descriptors are built once: those of
+      // stage 0 and K step 0, to which a stage adds kStageBytes and a K = 16
+      // step 2 KB (A) or 32 B (B) in the 16-byte units of the start-address
+      // field.  A: MN-major, 64-feature atoms 8 KB apart (LBO), 8-row K
+      // groups 1 KB apart (SBO); B: K-major rows of 128 B.
+      const uint64_t adesc0 = sdesc_sw128(smem_u32(smem), kBoxBytes, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(smem_u32(smem) + C::kABytes, 16, 1024);
+      constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
+      uint32_t soff = 0;   // stage * kStageUnits
       for (int n = 0; ok; ++n) {
         const int slot = n & (kItemRing - 1);
         if (!mbar_wait(ifull0 + 8 * slot, (n / kItemRing) & 1, &s_abort, wlim)) {
@@ -354,26 +364,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t b_base = a_base + C::kABytes;
+          const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // B: K-major rows of 128 B; a K=16 step is 32 B inside the swizzle row.
-            const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
-            // A: MN-major; 64-feature atoms 8 KB apart (LBO), 8-row K groups
-            // 1 KB apart (SBO); a K=16 step is 16 rows = 2 KB.
-            const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
-            const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16(d0, adesc, bdesc, idesc, accum);
-            if (kW13) {
-              const uint64_t adesc_up = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
-              mma_bf16(d0 + BN, adesc_up, bdesc, idesc, accum);
-            }
+            const uint32_t accum = (ks | kk) != 0 ? 1u : 0u;
+            mma_bf16(d0, ad + kk * 128, bd + kk * 2, idesc, accum);
+            if (kW13) mma_bf16(d0 + BN, ad + ((2 * kBoxBytes) >> 4) + kk * 128, bd + kk * 2, idesc, accum);
           }
           mma_commit(empty0 + 8 * stage);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
+            soff = 0;
+          } else {
+            soff += kStageUnits;
           }
         }
         if (!ok) break;
@@ -714,9 +718,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // descriptors built once (see the one-CTA kernel); a stage adds
+      // kStageBytes, a K = 16 step 2 KB (A) or 32 B (B), wide items' second
+      // group 16 KB (A)
+      const uint64_t adesc0 = sdesc_sw128(smem_u32(smem), kBoxBytes, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(smem_u32(smem) + C::kABytes, 16, 1024);
+      constexpr uint32_t kStageUnits = C::kStageBytes >> 4;
+      uint32_t soff = 0;   // stage * kStageUnits
+      // the routed rows of the next item's tile are loaded one item ahead
+      int valid = pair0 < total ? work_of<kPairRows>(args, pair0, num_tiles, nfe).t.valid : 0;
       for (int item = pair0; item < total && ok; item += pairs) {
-        const bool small = work_of<kPairRows>(args, item, num_tiles, nfe).t.valid <= kSmallRows;
+        const bool small = valid <= kSmallRows;
         const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
+        valid = item + pairs < total ? work_of<kPairRows>(args, item + pairs, num_tiles, nfe).t.valid : 0;
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
           ok = false;
           break;
@@ -729,22 +743,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t b_base = a_base + C::kABytes;
+          const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
-            const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
-            mma_bf16_pair(d0, adesc, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-            if (kWide) {
-              const uint64_t adesc1 = sdesc_sw128(a_base + 2 * kBoxBytes + kk * 2048, kBoxBytes, 1024);
-              mma_bf16_pair(d0 + kPairRows, adesc1, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-            }
+            const uint32_t accum = (ks | kk) != 0 ? 1u : 0u;
+            mma_bf16_pair(d0, ad + kk * 128, bd + kk * 2, idesc, accum);
+            if (kWide) mma_bf16_pair(d0 + kPairRows, ad + ((2 * kBoxBytes) >> 4) + kk * 128, bd + kk * 2, idesc, accum);
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
+            soff = 0;
+          } else {
+            soff += kStageUnits;
           }
         }
         if (!ok) break;
