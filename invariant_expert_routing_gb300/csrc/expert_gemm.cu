@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = c + jj;
             if (j < t.valid) {   // padding rows are not stored: nothing reads them
               const float x = g[jj];
-              const float v = (x / (1.0f + expf(-x))) * u[jj];
+              const float v = __fdividef(x, 1.0f + __expf(-x)) * u[jj];
               out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(v);
             }
           }
@@ -828,7 +828,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int j = c + jj;
               if (j < t.valid) {   // padding rows are not stored: nothing reads them
                 const float x = v[jj];
-                const float a = (x / (1.0f + expf(-x))) * buf[jj * 32];
+                const float a = __fdividef(x, 1.0f + __expf(-x)) * buf[jj * 32];
                 out[(size_t)(t.row0 + j) * args.out_ld + feat] = __float2bfloat16_rn(a);
               }
             }
