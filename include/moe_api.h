@@ -108,9 +108,12 @@ typedef struct moe_config {
 #define MOE_DEBUG_ROUTER_TILE64 0x200u    /* tensor-core router logits in 64-row token tiles */
 #define MOE_DEBUG_SHARED_SERIAL 0x400u    /* moe_forward: the shared expert on the caller's stream after
                                              the routed GEMMs instead of on a second stream */
-#define MOE_DEBUG_W13_PAIR 0x800u         /* routed W13 on CTA pairs whatever the reduction length */
+#define MOE_DEBUG_W13_PAIR 0x800u         /* routed W13 on CTA pairs (the default wherever the
+                                             intermediate size is a multiple of 128) */
 #define MOE_DEBUG_W2_WIDE 0x1000u         /* routed W2 pairs in wide items (two 256-feature groups per
                                              token tile) whatever the reduction length */
+#define MOE_DEBUG_W13_SINGLE 0x2000u      /* routed W13 on single CTAs (M = 128 features x N = 128
+                                             token rows, gate and up MMAs per K step) */
 
 /* Output of moe_routing_stats (device memory, 40 bytes). */
 typedef struct moe_route_stats {

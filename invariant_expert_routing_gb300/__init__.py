@@ -46,6 +46,7 @@ MOE_DEBUG_ROUTER_TILE64 = 0x200
 MOE_DEBUG_SHARED_SERIAL = 0x400
 MOE_DEBUG_W13_PAIR = 0x800
 MOE_DEBUG_W2_WIDE = 0x1000
+MOE_DEBUG_W13_SINGLE = 0x2000
 MOE_OVERFLOW_DROP = 0
 MOE_OVERFLOW_REROUTE = 1
 MOE_ROUTING_TOKEN_CHOICE = 0

@@ -951,10 +951,11 @@ bool gemm_smem_ok() {
 }
 
 bool gemm_pair_ok(bool w13, int features, int K) {
-  if (features % (w13 ? PairCfg<true>::kFeatTile : PairCfg<false>::kFeatTile) != 0) return false;
-  // W13 pairs carry half the features per CTA of the one-CTA kernel: with a
-  // short reduction (K < 4096) the one-CTA kernel measured faster
-  return !w13 || K >= 4096;
+  // (the one-CTA W13, two M = 128 x N = 128 MMAs per K step, measured slower
+  // for every reduction length once the MMA issue loop was tight: Qwen-like
+  // W13 0.307 against 0.279 ms at K = 2048)
+  (void)K;
+  return features % (w13 ? PairCfg<true>::kFeatTile : PairCfg<false>::kFeatTile) == 0;
 }
 
 bool gemm_wide_ok(int features, int K) {

@@ -18,7 +18,7 @@ namespace {
 using moe::GemmTile;
 
 constexpr int kMaxDevices = 64;
-constexpr uint32_t kKnownDebugFlags = 0x1FFFu;
+constexpr uint32_t kKnownDebugFlags = 0x3FFFu;
 static_assert(MOE_DEBUG_ROUTER_TC == moe::kPathRouterTc && MOE_DEBUG_ROUTER_CHUNKED == moe::kPathRouterChunked &&
                   MOE_DEBUG_ROW_GATHER == moe::kPathRowGather && MOE_DEBUG_ROW_SCATTER == moe::kPathRowScatter &&
                   MOE_DEBUG_NO_DECODE_FRONT == moe::kPathNoDecodeFront &&
@@ -244,7 +244,7 @@ GemmPlan plan_of(const moe_config* c, int32_t T, int sms) {
   const int N = c->num_experts, H = c->hidden, I = c->intermediate;
   const int k = expert_choice(c) ? N : c->top_k;
   GemmPlan p{};
-  p.pair13 = moe::gemm_pair_ok(true, I, H) || ((c->debug_flags & MOE_DEBUG_W13_PAIR) && I % 128 == 0);
+  p.pair13 = moe::gemm_pair_ok(true, I, H) && !(c->debug_flags & MOE_DEBUG_W13_SINGLE);
   p.pair2 = moe::gemm_pair_ok(false, H, I);
   const bool wide_shape = moe::gemm_wide_ok(H, I) ||
                           ((c->debug_flags & MOE_DEBUG_W2_WIDE) && H % moe::kPairFeatW2Wide == 0);

@@ -57,7 +57,7 @@ def test_config_validation(moe, bad, code):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(debug_flags=0x2000),                # unknown bit
+    dict(debug_flags=0x4000),                # unknown bit
     dict(debug_flags=0x1 | 0x2),             # tensor-core and chunked router at once
     dict(debug_flags=0x4 | 0x8),             # gather and scatter row copy at once
     dict(debug_flags=0x40 | 0x80),           # grid and one-CTA reroute rounds at once
@@ -72,7 +72,7 @@ def test_debug_fields_layout(moe):
     # debug flags and grid cap, an int64 wait limit (64 bytes)
     assert ctypes.sizeof(moe.moe_config) == 64
     assert moe.moe_config.debug_wait_ns.offset == 56
-    for f in (0x1, 0x2, 0x4, 0x8, 0x10, 0x20, 0x40, 0x80, 0x100, 0x200, 0x400, 0x800, 0x1000):
+    for f in (0x1, 0x2, 0x4, 0x8, 0x10, 0x20, 0x40, 0x80, 0x100, 0x200, 0x400, 0x800, 0x1000, 0x2000):
         assert moe.moe_check_config(dict(TINY, debug_flags=f)) == 0
     assert moe.moe_check_config(dict(TINY, debug_grid_ctas=12, debug_wait_ns=1)) == 0
 

@@ -1,11 +1,11 @@
 """Kernel paths that a configuration's debug flags can force give the bits of
 the default path.
 
-The W13 GEMM runs on single CTAs for short reductions and on CTA pairs for
-long ones (a property of the layer's shape); forced onto pairs, the
-Qwen-like and tiny layers must give the same output bits, because a pair's
-M = 256 MMA computes each output element with the same K steps in the same
-order as a single CTA's M = 128 MMAs ("Why temperature=0 Still Gives
+The W13 GEMM runs on CTA pairs wherever the intermediate size is a multiple
+of 128 (a property of the layer's shape); forced onto single CTAs, the tiny,
+Qwen-like and Mixtral-like layers must give the same output bits, because a
+pair's M = 256 MMA computes each output element with the same K steps in the
+same order as a single CTA's M = 128 MMAs ("Why temperature=0 Still Gives
 Different Answers: Batch Invariance": the arithmetic of a row must not depend
 on how the work is tiled).  The shared expert of the DeepSeek-like layer runs
 on a second stream; run on the caller's stream after the routed GEMMs it
@@ -44,8 +44,8 @@ def _forward(c, cfg, h_bits):
 
 
 @pytest.mark.parametrize("name,T,flag", [
-    ("tiny", 64, 0x800), ("tiny", 1, 0x800), ("qw", 1, 0x800), ("qw", 300, 0x800), ("qw", 4096, 0x800),
-    ("ds", 3, 0x400), ("ds", 700, 0x400), ("qw", 4096, 0x1000), ("ds", 700, 0x1000)])
+    ("tiny", 64, 0x2000), ("tiny", 1, 0x2000), ("qw", 1, 0x2000), ("qw", 300, 0x2000), ("qw", 4096, 0x2000),
+    ("mix", 200, 0x2000), ("ds", 3, 0x400), ("ds", 700, 0x400), ("qw", 4096, 0x1000), ("ds", 700, 0x1000)])
 def test_forced_path_gives_default_bits(name, T, flag):
     c = layer(name)
     h = W.make_h(c.wl, T, seed=60 + T)
