@@ -49,10 +49,13 @@ def _ffn(moe, c, cfg, h_d, srt, blk, npad, T):
     return y, ysh, moe.moe_get_device_status(ws)
 
 
-# tiny: one-CTA W13 and W2; qw: one-CTA W13, CTA-pair W2; mix: CTA-pair W13
-# (gate/up exchange between epilogue warps) and wide CTA-pair W2
-@pytest.mark.parametrize("name,T", [("tiny", 64), ("qw", 512), ("mix", 256)])
-def test_gemm_pipeline_wait_runs_out_and_reports(name, T):
+# tiny: CTA-pair W13, one-CTA W2; qw: CTA-pair W13 and W2; mix: CTA-pair W13
+# (gate/up exchange between epilogue warps) and wide CTA-pair W2; with
+# MOE_DEBUG_W13_SINGLE (0x2000) W13 runs on the one-CTA kernel, whose work
+# items come from a tile counter through a shared-memory ring
+@pytest.mark.parametrize("name,T,flags", [("tiny", 64, 0), ("qw", 512, 0), ("mix", 256, 0),
+                                          ("tiny", 64, 0x2000), ("qw", 512, 0x2000)])
+def test_gemm_pipeline_wait_runs_out_and_reports(name, T, flags):
     import torch
     import invariant_expert_routing_gb300 as moe
     from tests.gpu_util import dev_bf16
@@ -69,16 +72,17 @@ def test_gemm_pipeline_wait_runs_out_and_reports(name, T):
     srt[:P] = torch.from_numpy(st["sorted_route_ids"]).cuda()
     blk[:P // B] = torch.from_numpy(st["block_expert"]).cuda()
     npad = torch.tensor([P], dtype=torch.int32, device="cuda")
-    y_ref, ysh_ref, s0 = _ffn(moe, c, c.cfg, h_d, srt, blk, npad, T)
+    cfg = dict(c.cfg, debug_flags=flags)
+    y_ref, ysh_ref, s0 = _ffn(moe, c, cfg, h_d, srt, blk, npad, T)
     assert s0 == 0
     # a 1 ns limit: the first pipeline wait that is not already satisfied gives up
-    short = dict(c.cfg, debug_wait_ns=1)
+    short = dict(cfg, debug_wait_ns=1)
     for _ in range(2):
         _, _, s1 = _ffn(moe, c, short, h_d, srt, blk, npad, T)
         assert s1 & moe.MOE_DEV_ERR_TIMEOUT, f"status {s1:#x}"
     # the default limits again: same bits as before (the GPU and its tensor
     # memory are free again)
-    y2, ysh2, s2 = _ffn(moe, c, c.cfg, h_d, srt, blk, npad, T)
+    y2, ysh2, s2 = _ffn(moe, c, cfg, h_d, srt, blk, npad, T)
     assert s2 == 0
     assert torch.equal(y2[:P].view(torch.int16), y_ref[:P].view(torch.int16))
     if ysh_ref is not None:
