@@ -199,45 +199,57 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
 // therefore bit-identical to the CUDA-core router's; only the work differs.
 // Every decision depends on the token's own values alone.
 
-__global__ void __launch_bounds__(256) gate_transpose_kernel(const uint16_t* __restrict__ wg,
-                                                             uint16_t* __restrict__ wgT, int H, int N) {
+// W_g prepared for the certified router in one launch: blocks below
+// `tblocks` transpose 32 x 32 tiles of W_g [H, N] into wgT [N, H] (the
+// candidates' rows for the recompute); the others each compute
+// norm_w[e] >= ||W_g[:, e]||_2 for eight experts from W_g itself (fp32 sums
+// of squares in a fixed order, scaled up to cover their rounding).
+__global__ void __launch_bounds__(256) gate_prep_kernel(const uint16_t* __restrict__ wg,
+                                                        uint16_t* __restrict__ wgT,
+                                                        float* __restrict__ norm_w, int H, int N,
+                                                        int tblocks) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   pdl_trigger();
   __shared__ uint16_t tile[32][33];
-  const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
-  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-    const int i = i0 + r, e = e0 + threadIdx.x;
-    tile[r][threadIdx.x] = (i < H && e < N) ? wg[(size_t)i * N + e] : 0;
+  __shared__ float part[256][9];
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  if ((int)blockIdx.x < tblocks) {
+    const int ex = (N + 31) / 32;
+    const int e0 = (blockIdx.x % ex) * 32, i0 = (blockIdx.x / ex) * 32;
+    for (int r = ty; r < 32; r += 8) {
+      const int i = i0 + r, e = e0 + tx;
+      tile[r][tx] = (i < H && e < N) ? wg[(size_t)i * N + e] : 0;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+      const int e = e0 + r, i = i0 + tx;
+      if (e < N && i < H) wgT[(size_t)e * H + i] = tile[tx][r];
+    }
+    return;
   }
-  __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-    const int e = e0 + r, i = i0 + threadIdx.x;
-    if (e < N && i < H) wgT[(size_t)e * H + i] = tile[threadIdx.x][r];
-  }
-}
-
-// norm_w[e] >= ||W_g[:, e]||_2 (fp32 sum of squares scaled up to cover its rounding).
-__global__ void __launch_bounds__(256) gate_norm_kernel(const uint16_t* __restrict__ wgT,
-                                                        float* __restrict__ norm_w, int H, int N) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (e >= N) return;
-  float ss = 0.0f;
-  for (int i = lane * 8; i < H; i += 256) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(wgT + (size_t)e * H + i));
+  // eight experts e0 .. e0+7 (N % 8 == 0): thread t sums rows t, t+256, ...
+  // (one 16-byte load per row), then expert q adds the 256 partial sums in
+  // thread order
+  const int e0 = ((int)blockIdx.x - tblocks) * 8;
+  float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int i = tid; i < H; i += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)i * N + e0));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
+      ss[2 * j] = fmaf(a, a, ss[2 * j]);
+      ss[2 * j + 1] = fmaf(b, b, ss[2 * j + 1]);
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if (lane == 0) norm_w[e] = sqrtf(ss * (1.0f + 0x1p-7f)) * (1.0f + 0x1p-7f);
+  for (int q = 0; q < 8; ++q) part[tid][q] = ss[q];
+  __syncthreads();
+  if (tid < 8) {
+    float t = 0.0f;
+    for (int r = 0; r < 256; ++r) t += part[r][tid];
+    norm_w[e0 + tid] = sqrtf(t * (1.0f + 0x1p-7f)) * (1.0f + 0x1p-7f);
+  }
 }
 
 constexpr int kCertWarps = 8;
@@ -323,25 +335,12 @@ __global__ void __launch_bounds__(kCertWarps * 32) route_certified_kernel(
   // V = k-th best of the 32 lane bests: at least k experts have l_tc >= V,
   // so the canonical k-th logit is >= V - delta and every expert with
   // l_tc < V - 2 delta is out.  (N >= 128 here: every lane holds experts.)
-  float V = 0.0f;
+  float V = lane_best;
   {
-    // k rounds of a warp tournament over the lane bests; the k-th winner is V
-    bool out = false;
-    for (int j = 0; j < k; ++j) {
-      float bv = out ? 0.0f : lane_best;
-      int bi = out ? -1 : lane_best_e;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(full, bv, off);
-        const int oi = __shfl_xor_sync(full, bi, off);
-        if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      V = bv;
-      if (bi == lane_best_e) out = true;
-    }
+    // the lane bests sorted best first; V is the k-th
+    int vk = lane_best_e;
+    sel::warp_sort_best_first(V, vk, lane);
+    V = __shfl_sync(full, V, k - 1);
   }
   const float cut = V - 2.0f * delta;
   int nc = 0;
@@ -614,35 +613,22 @@ __global__ void __launch_bounds__(256) cert_finalize_kernel(
     }
     cv = bias ? total + bias[e] : total;
   }
-  int sel[16];
-  float selv[16];
-  bool taken = false;
-  for (int j = 0; j < k; ++j) {
-    float bv = cv;
-    int bi = (mine && !taken) ? e : -1;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(full, bv, off);
-      const int oi = __shfl_xor_sync(full, bi, off);
-      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    sel[j] = bi;
-    selv[j] = bv;
-    if (mine && bi == e) taken = true;
-  }
-  write_slots_and_gates(sel, selv, k, topk_idx + (size_t)t * k, gates + (size_t)t * k, lane);
+  // sort the candidates best first, keyed by their position q (the list is in
+  // ascending expert order, so q breaks ties like the expert index); the
+  // first k positions are the selection, written in expert order
+  float sv = cv;
+  int sq = mine ? lane : -1;
+  sel::warp_sort_best_first(sv, sq, lane);
+  const unsigned chosen = __reduce_or_sync(full, (lane < k && sq >= 0) ? 1u << sq : 0u);
+  sel::write_gates_lanes(chosen, e, cv, lane, topk_idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
 }  // namespace
 
 void launch_gate_prep(const uint16_t* w_gate, uint16_t* wgT, float* norm_w, int H, int N,
                       cudaStream_t s) {
-  dim3 grid((N + 31) / 32, (H + 31) / 32), block(32, 8);
-  launch_pdl(gate_transpose_kernel, dim3(grid), dim3(block), 0, s, w_gate, wgT, H, N);
-  launch_pdl(gate_norm_kernel, dim3((N + 7) / 8), dim3(256), 0, s, wgT, norm_w, H, N);
+  const int tblocks = ((N + 31) / 32) * ((H + 31) / 32);
+  launch_pdl(gate_prep_kernel, dim3(tblocks + N / 8), dim3(256), 0, s, w_gate, wgT, norm_w, H, N, tblocks);
 }
 
 float router_cert_beta(int H) {

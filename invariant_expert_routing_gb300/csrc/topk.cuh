@@ -18,6 +18,57 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return ia < ib;
 }
 
+// a beats b: a holds an entry (key >= 0) and b none, or both do and a ranks
+// first.  Keys are expert indices or positions in an ascending expert list.
+__device__ __forceinline__ bool beats(float va, int ka, float vb, int kb) {
+  return ka >= 0 && (kb < 0 || ranks_before(va, ka, vb, kb));
+}
+
+// Bitonic sort of one (value, key) entry per lane across the warp, best
+// first under ranks_before: afterwards lane p holds the p-th best entry and
+// lanes without an entry (key -1) come last.  15 compare-exchange steps,
+// each one shuffle pair and one comparison.
+__device__ __forceinline__ void warp_sort_best_first(float& v, int& key, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+      const int ok = __shfl_xor_sync(0xffffffffu, key, stride);
+      // the lower lane of a pair keeps the better entry in blocks sorted
+      // best first ((lane & size) == 0), the worse one in the others
+      const bool keep_better = ((lane & stride) == 0) == ((lane & size) == 0);
+      const bool take = keep_better ? beats(ov, ok, v, key) : beats(v, key, ov, ok);
+      if (take) {
+        v = ov;
+        key = ok;
+      }
+    }
+  }
+}
+
+// Lane-parallel form of write_slots_and_gates: the lanes set in `selected`
+// (at most 32) hold the selected experts in ascending expert order; the one
+// with the s-th lowest lane writes slot s.  Same arithmetic as
+// write_slots_and_gates: m = max selected logit, exp(l - m) per slot, the sum
+// taken in slot order, each gate one division.
+__device__ __forceinline__ void write_gates_lanes(unsigned selected, int e, float v, int lane,
+                                                  int32_t* __restrict__ idx_out,
+                                                  float* __restrict__ gate_out) {
+  const bool mine = (selected >> lane) & 1u;
+  float m = mine ? v : -INFINITY;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float ex = mine ? expf(v - m) : 0.0f;
+  float S = 0.0f;
+  for (unsigned mm = selected; mm != 0u; mm &= mm - 1u) S = S + __shfl_sync(0xffffffffu, ex, __ffs(mm) - 1);
+  if (mine) {
+    const int slot = __popc(selected & ((1u << lane) - 1u));
+    idx_out[slot] = e;
+    gate_out[slot] = ex / S;
+  }
+}
+
 // Sorts the k selected (expert, logit) pairs by expert index and writes the
 // renormalised gates exp(l_j - m) / sum_s exp(l_s - m), m = max selected,
 // summed in slot order.  Every router path calls it, so all agree bitwise.
