@@ -178,18 +178,15 @@ __global__ void __launch_bounds__(1024) dispatch_scatter_kernel(
   }
 }
 
-// Grouped-GEMM tile lists from the padded blocks: each expert segment is cut
-// into tiles of tile_rows rows from its start.  CTA 0 writes list `a`, CTA 1
-// (when the grid has two) list `b`, from the same blocks.  Rejects (no tiles,
-// status bit) a block list that is not sorted by expert or out of range.
-__global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ block_expert,
-                                                          const int32_t* __restrict__ num_padded,
-                                                          const int32_t* __restrict__ sorted_route_ids,
-                                                          int R, int N, int B, long long max_rows,
-                                                          TileListOut a, TileListOut b_list, int* status) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  pdl_trigger();
-  const TileListOut L = blockIdx.x == 0 ? a : b_list;
+// Grouped-GEMM tile list from the padded blocks, by one CTA: each expert
+// segment is cut into tiles of tile_rows rows from its start.  Rejects (no
+// tiles, status bit) a block list that is not sorted by expert or out of
+// range.
+__device__ __forceinline__ void build_tiles_block(const int32_t* __restrict__ block_expert,
+                                                  const int32_t* __restrict__ num_padded,
+                                                  const int32_t* __restrict__ sorted_route_ids, int R, int N,
+                                                  int B, long long max_rows, const TileListOut& L,
+                                                  int* status) {
   __shared__ int buf[256];
   __shared__ int s_first[kMaxN], s_last[kMaxN];
   __shared__ int s_bad;
@@ -273,51 +270,54 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
 
 // x_perm[p] = h[r / k] for padded row p holding route r, zeros for the
 // sentinel: the routed token rows in expert-segment order, so that the W13
-// GEMM loads whole 128-row tiles.  One warp per row, 16-byte accesses.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ h,
-                                                          const int32_t* __restrict__ sorted_route_ids,
-                                                          const int32_t* __restrict__ num_padded, int k,
-                                                          int R, int H, long long max_rows,
-                                                          uint16_t* __restrict__ x_perm) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  // no early trigger: the next kernel is a GEMM or the combine, whose CTAs
-  // would hold SMs idle while they wait
-  const long long P = min((long long)*num_padded, max_rows);
+// GEMM loads whole 128-row tiles.  One warp per row (warps w0, w0 + warps,
+// ...), 16-byte accesses, up to eight pieces per lane loaded before they are
+// stored, the next row's route id in flight meanwhile.
+__device__ __forceinline__ void gather_rows_warps(const uint16_t* __restrict__ h,
+                                                  const int32_t* __restrict__ sorted_route_ids,
+                                                  long long P, int k, int R, int H,
+                                                  uint16_t* __restrict__ x_perm, long long w0,
+                                                  long long warps) {
   const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int chunks = H / 8;
-  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < P;
-       row += warps) {
-    const int r = sorted_route_ids[row];
+  int r = w0 < P ? sorted_route_ids[w0] : -1;
+  for (long long row = w0; row < P; row += warps) {
+    const long long nrow = row + warps;
+    const int rn = nrow < P ? sorted_route_ids[nrow] : -1;
     uint4* dst = reinterpret_cast<uint4*>(x_perm + row * H);
     if (r >= 0 && r < R) {
       const uint4* src = reinterpret_cast<const uint4*>(h + (size_t)(r / k) * H);
-      for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+      for (int c0 = lane; c0 < chunks; c0 += 8 * 32) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u < chunks) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u < chunks) dst[c0 + 32 * u] = v[u];
+      }
     } else {
       for (int c = lane; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
     }
+    r = rn;
   }
 }
 
-// The same x_perm token by token: warp per token, h[t] read once from DRAM
+// The same x_perm token by token (warps w0, w0 + warps, ... over the T tokens,
+// then the padded rows): warp per token, h[t] read once from DRAM
 // and copied (from L1) to the padded row route_pos[t k + j] of each kept
 // slot; then zeros in the padding rows.  When h is larger than L2 the
 // segment-order gather fetches a token's row once per slot.
-__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __restrict__ h,
-                                                           const int32_t* __restrict__ route_pos,
-                                                           const int32_t* __restrict__ sorted_route_ids,
-                                                           const int32_t* __restrict__ num_padded, int k,
-                                                           int T, int H, long long max_rows,
-                                                           uint16_t* __restrict__ x_perm) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  // no early trigger: the next kernel is a GEMM
-  const long long P = min((long long)*num_padded, max_rows);
+__device__ __forceinline__ void scatter_rows_warps(const uint16_t* __restrict__ h,
+                                                   const int32_t* __restrict__ route_pos,
+                                                   const int32_t* __restrict__ sorted_route_ids,
+                                                   long long P, int k, int T, int H,
+                                                   uint16_t* __restrict__ x_perm, long long w0,
+                                                   long long warps) {
   const long long R = (long long)T * k;
   const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int chunks = H / 8;
-  for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < T + P;
-       item += warps) {
+  for (long long item = w0; item < T + P; item += warps) {
     if (item < T) {
       // each 16-byte piece of the row is loaded once and stored to every
       // kept slot; lane l holds the padded row of slot g * 32 + l, for the
@@ -357,6 +357,37 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __res
       }
     }
   }
+}
+
+// The GEMM tile lists and the routed token rows in one launch: CTAs below
+// `lists` each build one tile list (CTA 0 list a, CTA 1 list b); the others
+// copy the rows (kRows 1: in padded-row order, 2: token by token, 0: none).
+// No early trigger: the next kernel is a GEMM, whose CTAs would hold SMs
+// idle while they wait.
+template <int kRows>
+__global__ void __launch_bounds__(256) tiles_rows_kernel(const int32_t* __restrict__ block_expert,
+                                                         const int32_t* __restrict__ num_padded,
+                                                         const int32_t* __restrict__ sorted_route_ids,
+                                                         int k, int T, int N, int B, long long max_rows,
+                                                         int lists, TileListOut a, TileListOut b,
+                                                         int* status, const uint16_t* __restrict__ h,
+                                                         const int32_t* __restrict__ route_pos, int H,
+                                                         uint16_t* __restrict__ x_perm) {
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  const int R = T * k;
+  if ((int)blockIdx.x < lists) {
+    build_tiles_block(block_expert, num_padded, sorted_route_ids, R, N, B, max_rows, blockIdx.x == 0 ? a : b,
+                      status);
+    return;
+  }
+  if (kRows == 0) return;
+  const long long P = min((long long)*num_padded, max_rows);
+  const long long w0 = (long long)(blockIdx.x - lists) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long warps = (long long)(gridDim.x - lists) * (blockDim.x >> 5);
+  if (kRows == 1)
+    gather_rows_warps(h, sorted_route_ids, P, k, R, H, x_perm, w0, warps);
+  else
+    scatter_rows_warps(h, route_pos, sorted_route_ids, P, k, T, H, x_perm, w0, warps);
 }
 
 // Dispatch, alignment and both GEMM tile lists of a batch of at most 1024
@@ -570,31 +601,6 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
 
 }  // namespace
 
-void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
-                        int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s) {
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long want = (max_rows + 7) / 8;
-  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
-  const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-  launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, h, sorted_route_ids, num_padded, k, R, H, (long long)max_rows,
-                                          x_perm);
-}
-
-void launch_scatter_rows(const uint16_t* h, const int32_t* route_pos, const int32_t* sorted_route_ids,
-                         const int32_t* num_padded, int k, int T, int H, int64_t max_rows, uint16_t* x_perm,
-                         cudaStream_t s) {
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long want = ((long long)T + max_rows + 7) / 8;
-  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
-  const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-  launch_pdl(scatter_rows_kernel, dim3(grid), dim3(256), 0, s, h, route_pos, sorted_route_ids, num_padded, k, T,
-             H, (long long)max_rows, x_perm);
-}
-
 void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int capacity,
                      uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                      int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
@@ -673,11 +679,38 @@ void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float*
              expert_counts, num_dropped, la, lb, x_perm, (long long)max_rows, status);
 }
 
-void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
-                        const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
-                        TileListOut a, const TileListOut* b, int* status, cudaStream_t s) {
-  launch_pdl(build_tiles_kernel, dim3(b ? 2 : 1), dim3(256), 0, s, block_expert, num_padded, sorted_route_ids, R,
-             N, B, (long long)max_rows, a, b ? *b : a, status);
+void launch_tiles_and_rows(const int32_t* block_expert, const int32_t* num_padded,
+                           const int32_t* sorted_route_ids, int k, int T, int N, int B, int64_t max_rows,
+                           const TileListOut* a, const TileListOut* b, int* status, int row_mode,
+                           const uint16_t* h, const int32_t* route_pos, int H, uint16_t* x_perm,
+                           cudaStream_t s) {
+  const int lists = a ? (b ? 2 : 1) : 0;
+  auto kernel = row_mode == 1 ? tiles_rows_kernel<1> : (row_mode == 2 ? tiles_rows_kernel<2> : tiles_rows_kernel<0>);
+  int row_blocks = 0;
+  if (row_mode != 0) {
+    // every CTA resident at once (SMs x resident CTAs per SM, less the list
+    // CTAs), each row warp then striding over the rows
+    static int cache[64][3] = {};   // per device and row mode: SMs x resident CTAs
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int cap = (dev >= 0 && dev < 64) ? cache[dev][row_mode] : 0;
+    if (cap <= 0) {
+      int sms = 0, per = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, 256, 0);
+      cap = (sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+      if (dev >= 0 && dev < 64) cache[dev][row_mode] = cap;
+    }
+    cap = cap > lists ? cap - lists : 1;   // the list CTAs take resident slots too
+    const long long items = row_mode == 2 ? (long long)T + max_rows : (long long)max_rows;
+    const long long want = (items + 7) / 8;
+    row_blocks = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+  }
+  if (lists + row_blocks == 0) return;
+  const TileListOut la = a ? *a : TileListOut{};
+  const TileListOut lb = b ? *b : la;
+  launch_pdl(kernel, dim3(lists + row_blocks), dim3(256), 0, s, block_expert, num_padded, sorted_route_ids, k, T,
+             N, B, (long long)max_rows, lists, la, lb, status, h, route_pos, H, x_perm);
 }
 
 }  // namespace moe

@@ -122,7 +122,7 @@ void launch_expert_choice(const float* logits, int T, int N, int C, int B, unsig
                           float* gates, uint8_t* route_kept, int32_t* route_pos, int32_t* sorted_route_ids,
                           int32_t* block_expert, int32_t* num_padded, int32_t* expert_counts,
                           cudaStream_t s);
-// a batch of at most 1024 routes: launch_dispatch + both launch_build_tiles
+// a batch of at most 1024 routes: launch_dispatch + both tile lists of launch_tiles_and_rows
 // (tile_rows rows_a and rows_b) in one launch, the same integers
 bool dispatch_small_ok(long long R);
 struct TileListOut;
@@ -141,13 +141,6 @@ void launch_decode_front(const uint16_t* h, const uint16_t* w_gate, const float*
                          int32_t* route_pos, int32_t* sorted_route_ids, int32_t* block_expert, int32_t* num_padded,
                          int32_t* expert_counts, int32_t* num_dropped, const TileListOut& la,
                          const TileListOut& lb, uint16_t* x_perm, int64_t max_rows, int* status, cudaStream_t s);
-void launch_gather_rows(const uint16_t* h, const int32_t* sorted_route_ids, const int32_t* num_padded,
-                        int k, int R, int H, int64_t max_rows, uint16_t* x_perm, cudaStream_t s);
-// the same x_perm from the inverse map (route_pos: padded row of each route,
-// -1 dropped): each token row read once
-void launch_scatter_rows(const uint16_t* h, const int32_t* route_pos, const int32_t* sorted_route_ids,
-                         const int32_t* num_padded, int k, int T, int H, int64_t max_rows, uint16_t* x_perm,
-                         cudaStream_t s);
 // Tile list of one GEMM: tile_rows-row tiles over each expert's padded
 // segment; a tile's valid rows end at the segment's last route (sorted ids
 // in [0, R)).
@@ -177,10 +170,16 @@ __host__ __device__ inline GemmTile segment_tile(int expert, int seg_row0, int p
   tl.pad[0] = tl.pad[1] = 0;
   return tl;
 }
-// List a, and list b too when b is non-null (one launch, one CTA per list).
-void launch_build_tiles(const int32_t* block_expert, const int32_t* num_padded,
-                        const int32_t* sorted_route_ids, int R, int N, int B, int64_t max_rows,
-                        TileListOut a, const TileListOut* b, int* status, cudaStream_t s);
+// One launch: tile list a (when non-null) and b (when both are), one CTA
+// each, beside the routed token rows of x_perm (row_mode 1: gathered in
+// padded-row order by sorted_route_ids; 2: token by token from the inverse
+// map route_pos (padded row of each route, -1 dropped), each token row read
+// once; 0: none).  Padding rows are written as zeros.
+void launch_tiles_and_rows(const int32_t* block_expert, const int32_t* num_padded,
+                           const int32_t* sorted_route_ids, int k, int T, int N, int B, int64_t max_rows,
+                           const TileListOut* a, const TileListOut* b, int* status, int row_mode,
+                           const uint16_t* h, const int32_t* route_pos, int H, uint16_t* x_perm,
+                           cudaStream_t s);
 
 // ---- diagnostics
 struct RoutingStats {  // same layout as moe_route_stats

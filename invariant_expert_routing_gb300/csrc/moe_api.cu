@@ -494,17 +494,15 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   uint16_t* a = at<uint16_t>(ws, L.a);
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
 
-  if (!tiles_ready) {   // else the small-batch dispatch built both lists
+  {
+    // the tile lists (unless the small-batch dispatch built both) and the
+    // routed rows (unless the decode front copied them), in one launch
     const moe::TileListOut l13{tiles13, ntiles13, gp.rows13, max_tiles13, ntiles13 + 1};
     const moe::TileListOut l2{tiles2, ntiles2, gp.rows2, max_tiles2, ntiles2 + 1};
-    moe::launch_build_tiles(blocks, num_padded, sorted, T * k, N, c->block_size, rows, l13, &l2, status, s);
-  }
-  if (rows_ready) {
-    // the decode front copied the routed rows
-  } else if (route_pos && scatter_rows_ok(T, H, c->debug_flags)) {
-    moe::launch_scatter_rows(h, route_pos, sorted, num_padded, k, T, H, rows, x_perm, s);
-  } else {
-    moe::launch_gather_rows(h, sorted, num_padded, k, T * k, H, rows, x_perm, s);
+    const int row_mode = rows_ready ? 0 : (route_pos && scatter_rows_ok(T, H, c->debug_flags) ? 2 : 1);
+    moe::launch_tiles_and_rows(blocks, num_padded, sorted, k, T, N, c->block_size, rows,
+                               tiles_ready ? nullptr : &l13, tiles_ready ? nullptr : &l2, status, row_mode, h,
+                               route_pos, H, x_perm, s);
   }
   mark(mk, 3);
 
