@@ -85,9 +85,41 @@ __device__ __forceinline__ int capacity_left(int capacity, const int32_t* __rest
   return expert_offset ? max(0, capacity - expert_offset[e]) : capacity;
 }
 
-// One CTA of 256 threads; thread e owns expert e.  Turns per-tile counts into
-// per-tile bases (in place), applies the capacity, lays out the segments.
-__global__ void __launch_bounds__(256) dispatch_scan_kernel(
+// Exclusive scan of v over experts 0..N-1 by warp 0 (N <= 256, 8 per lane);
+// out[e] = sum of v[0..e-1], returns the total (to lane 0..31).
+__device__ int warp_scan_experts(const int* v, int* out, int N, int lane) {
+  int loc[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * 8 + i;
+    loc[i] = e < N ? v[e] : 0;
+    sum += loc[i];
+  }
+  int incl = sum;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane * 8 + i;
+    if (e < N) out[e] = run;
+    run += loc[i];
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// One CTA of kScanThreads threads.  Turns per-tile counts into per-tile
+// bases (in place), applies the capacity, lays out the segments.  Thread
+// (part p, expert e) owns a contiguous run of route tiles of expert e: it
+// sums their counts, and once the parts before it are summed writes each
+// tile's base (earlier tiles' counts first, tiles in order); warp 0 then
+// scans the experts' padded sizes and drops in expert order.
+constexpr int kScanThreads = 1024;
+constexpr int kScanParts = 16;
+
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     int32_t* __restrict__ tile_count, int ntiles, int N, int B, int capacity,
     const int32_t* __restrict__ expert_offset, int R,
     int32_t* __restrict__ seg_off, int32_t* __restrict__ expert_counts, int32_t* __restrict__ num_padded,
@@ -95,50 +127,78 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(
     int32_t* __restrict__ sorted_route_ids) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
   pdl_trigger();
-  __shared__ int buf[256];
+  __shared__ int part_sum[kScanParts][kMaxN];
+  __shared__ int s_pad[kMaxN], s_drop[kMaxN], s_seg[kMaxN], s_tmp[kMaxN];
   __shared__ int blk_off[kMaxN + 1];
-  const int e = threadIdx.x;
-  int load = 0;
-  if (e < N) {
-    // the counts of kScanBatch route tiles are loaded before any is
-    // overwritten by its exclusive prefix: one L2 round trip per batch
-    // instead of one per tile
-    constexpr int kScanBatch = 16;
-    for (int tl0 = 0; tl0 < ntiles; tl0 += kScanBatch) {
-      int c[kScanBatch];
+  __shared__ int s_rows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = min(min(kScanThreads / N, kScanParts), max(ntiles, 1));
+  const int per = (ntiles + P - 1) / P;
+  const int e = tid % N, p = tid / N;
+  const bool active = p < P;
+  const int t0 = p * per, t1 = min(ntiles, t0 + per);
+  constexpr int kBatch = 8;
+  if (active) {
+    int sum = 0;
+    for (int b0 = t0; b0 < t1; b0 += kBatch) {
+      int c[kBatch];
 #pragma unroll
-      for (int j = 0; j < kScanBatch; ++j)
-        c[j] = (tl0 + j < ntiles) ? tile_count[(size_t)(tl0 + j) * N + e] : 0;
+      for (int j = 0; j < kBatch; ++j) c[j] = (b0 + j < t1) ? tile_count[(size_t)(b0 + j) * N + e] : 0;
 #pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) {
-        if (tl0 + j < ntiles) {
-          tile_count[(size_t)(tl0 + j) * N + e] = load;
-          load += c[j];
+      for (int j = 0; j < kBatch; ++j) sum += c[j];
+    }
+    part_sum[p][e] = sum;
+  }
+  __syncthreads();
+  if (active) {
+    int run = 0;
+    for (int q = 0; q < p; ++q) run += part_sum[q][e];
+    for (int b0 = t0; b0 < t1; b0 += kBatch) {
+      int c[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) c[j] = (b0 + j < t1) ? tile_count[(size_t)(b0 + j) * N + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (b0 + j < t1) {
+          tile_count[(size_t)(b0 + j) * N + e] = run;
+          run += c[j];
         }
       }
     }
   }
-  const int cap_e = (e < N) ? capacity_left(capacity, expert_offset, e) : 0;
-  const int kept = (e < N) ? (cap_e < 0 ? load : min(load, cap_e)) : 0;
-  const int padded = (kept + B - 1) / B * B;
-  int total_rows = 0, total_drop = 0;
-  const int seg = block_exclusive_scan(padded, buf, &total_rows);
-  block_exclusive_scan(load - kept, buf, &total_drop);
-  if (e < N) {
-    seg_off[e] = seg;
-    expert_counts[e] = kept;
-    for (int j = kept; j < padded; ++j) sorted_route_ids[seg + j] = R;
-    blk_off[e] = seg / B;
+  if (tid < N) {
+    int load = 0;
+    for (int q = 0; q < P; ++q) load += part_sum[q][tid];
+    const int cap_e = capacity_left(capacity, expert_offset, tid);
+    const int kept = cap_e < 0 ? load : min(load, cap_e);
+    s_pad[tid] = (kept + B - 1) / B * B;
+    s_drop[tid] = load - kept;
+    expert_counts[tid] = kept;
+    s_tmp[tid] = kept;
   }
-  if (e == 0) {
-    blk_off[N] = total_rows / B;
-    *num_padded = total_rows;
-    if (num_dropped) *num_dropped = total_drop;
+  __syncthreads();
+  if (warp == 0) {
+    const int rows = warp_scan_experts(s_pad, s_seg, N, lane);
+    const int drops = warp_scan_experts(s_drop, s_drop, N, lane);
+    if (lane == 0) {
+      s_rows = rows;
+      *num_padded = rows;
+      if (num_dropped) *num_dropped = drops;
+    }
   }
+  __syncthreads();
+  const int total_rows = s_rows;
+  if (tid < N) {
+    const int seg = s_seg[tid];
+    seg_off[tid] = seg;
+    for (int j = s_tmp[tid]; j < s_pad[tid]; ++j) sorted_route_ids[seg + j] = R;
+    blk_off[tid] = seg / B;
+  }
+  if (tid == 0) blk_off[N] = total_rows / B;
   __syncthreads();
   // block b belongs to the last expert whose first block is <= b
   const int nb = total_rows / B;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+  for (int b = tid; b < nb; b += blockDim.x) {
     // largest e in [0, N) with blk_off[e] <= b; it has blk_off[e+1] > b, so
     // empty segments (equal offsets) are skipped
     int lo = 0, hi = N;
@@ -396,30 +456,6 @@ __global__ void __launch_bounds__(256) tiles_rows_kernel(const int32_t* __restri
 // warp order, segment and tile offsets by ordered scans), in one launch.
 constexpr int kSmallDispatchMaxR = 1024;
 
-// Exclusive scan of v over experts 0..N-1 by warp 0 (N <= 256, 8 per lane);
-// out[e] = sum of v[0..e-1], returns the total (to lane 0..31).
-__device__ int warp_scan_experts(const int* v, int* out, int N, int lane) {
-  int loc[8], sum = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane * 8 + i;
-    loc[i] = e < N ? v[e] : 0;
-    sum += loc[i];
-  }
-  int incl = sum;
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
-  }
-  int run = incl - sum;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane * 8 + i;
-    if (e < N) out[e] = run;
-    run += loc[i];
-  }
-  return __shfl_sync(0xffffffffu, incl, 31);
-}
 
 // The body: one CTA of at least R threads (full warps), thread r handles
 // route r.  topk_idx is read with plain loads (the decode front writes it in
@@ -610,7 +646,7 @@ void launch_dispatch(const int32_t* topk_idx, int T, int N, int k, int B, int ca
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, 0, rank_in_tile, tile_count,
                                                          status);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, expert_offset, R,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, tile_count, ntiles, N, B, capacity, expert_offset, R,
              seg_off, expert_counts, num_padded, num_dropped, block_expert, sorted_route_ids);
   launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, capacity,
              expert_offset, rank_in_tile, tile_count, seg_off, route_kept, route_pos, sorted_route_ids);
@@ -623,7 +659,7 @@ void launch_dispatch_routes(const int32_t* route_expert, int R, int N, int B, ui
   const int ntiles = (R + kDispatchTile - 1) / kDispatchTile;
   launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, 1, rank_in_tile, tile_count,
                                                          status);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, -1, (const int32_t*)nullptr, R,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, tile_count, ntiles, N, B, -1, (const int32_t*)nullptr, R,
              seg_off, expert_counts, num_padded, (int32_t*)nullptr, block_expert, sorted_route_ids);
   launch_pdl(dispatch_scatter_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, route_expert, R, N, -1,
              (const int32_t*)nullptr, rank_in_tile, tile_count, seg_off, route_kept, route_pos, sorted_route_ids);
@@ -641,7 +677,7 @@ void launch_dispatch_reroute(const int32_t* topk_idx, const float* logits, int T
   // phase one: ranks and the per-expert kept counts of the drop rule
   launch_pdl(dispatch_count_kernel, dim3(ntiles), dim3(kDispatchTile), 0, s, topk_idx, R, N, 0, rank_in_tile, tile_count,
                                                          status);
-  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, s, tile_count, ntiles, N, B, capacity, (const int32_t*)nullptr, R,
+  launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, tile_count, ntiles, N, B, capacity, (const int32_t*)nullptr, R,
              seg_off, expert_counts, num_padded, (int32_t*)nullptr, block_expert, sorted_route_ids);
   // phase two, then the stable layout of the final assignment
   launch_reroute(topk_idx, logits, T, N, k, capacity, rank_in_tile, tile_count, expert_counts, sc,
