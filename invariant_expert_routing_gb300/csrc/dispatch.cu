@@ -591,11 +591,21 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
   const int C = (H + kRouterChunk - 1) / kRouterChunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int x = tid; x < T * N; x += blockDim.x) {
+    // the chunk sums (and the bias) requested sixteen at a time, then added
+    // in ascending chunk order
     const int t = x / N, e = x % N;
     const float* pe = part + (size_t)t * C * N + e;
+    const float be = bias ? bias[e] : 0.0f;
     float total = 0.0f;
-    for (int c = 0; c < C; ++c) total = total + pe[(size_t)c * N];
-    if (bias) total = total + bias[e];
+    for (int c0 = 0; c0 < C; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = c0 + j < C ? pe[(size_t)(c0 + j) * N] : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < C) total = total + v[j];
+    }
+    if (bias) total = total + be;
     lrow[t][e] = total;
   }
   __syncthreads();

@@ -102,31 +102,33 @@ __device__ __forceinline__ void write_slots_and_gates(int (&sel)[16], float (&se
 }
 
 // One warp: k rounds of a warp-shuffle tournament over the N logits of one
-// token (lrow, global or shared memory), slots sorted by expert index, gates
-// = softmax over the selected.
+// token (lrow, global or shared memory, N <= 256) pick the k best; the slots
+// then go in ascending expert order (ballots per group of 32 experts) and
+// the gates are the softmax over the selected, with the arithmetic of
+// write_slots_and_gates (m = max selected logit, exp(l - m) per slot, the sum
+// in slot order, one division each).  No per-lane arrays are indexed at run
+// time.
 __device__ __forceinline__ void topk_select_warp(const float* lrow, int N, int k, int lane,
                                                  int32_t* __restrict__ idx_out,
                                                  float* __restrict__ gate_out) {
   float v[8];
-  uint32_t used = 0;
+  uint32_t avail = 0;   // bit s: expert lane + 32 s exists and is not taken yet
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const int e = lane + 32 * s;
+    v[s] = 0.0f;
     if (e < N) {
       v[s] = lrow[e];
-    } else {
-      v[s] = 0.0f;
-      used |= 1u << s;
+      avail |= 1u << s;
     }
   }
-  int sel[16];
-  float selv[16];
+  const uint32_t present = avail;
   for (int j = 0; j < k; ++j) {
     float bv = 0.0f;
     int bi = -1;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      if (!((used >> s) & 1u) && (bi < 0 || ranks_before(v[s], lane + 32 * s, bv, bi))) {
+      if (((avail >> s) & 1u) && (bi < 0 || ranks_before(v[s], lane + 32 * s, bv, bi))) {
         bv = v[s];
         bi = lane + 32 * s;
       }
@@ -140,11 +142,35 @@ __device__ __forceinline__ void topk_select_warp(const float* lrow, int N, int k
         bi = oi;
       }
     }
-    sel[j] = bi;
-    selv[j] = bv;
-    if ((bi & 31) == lane) used |= 1u << (bi >> 5);
+    if (bi >= 0 && (bi & 31) == lane) avail &= ~(1u << (bi >> 5));
   }
-  write_slots_and_gates(sel, selv, k, idx_out, gate_out, lane);
+  const uint32_t chosen = present & ~avail;
+  unsigned M[8];
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    M[s] = __ballot_sync(0xffffffffu, (chosen >> s) & 1u);
+    if ((chosen >> s) & 1u) m = fmaxf(m, v[s]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float ex[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) ex[s] = ((chosen >> s) & 1u) ? expf(v[s] - m) : 0.0f;
+  float S = 0.0f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+    for (unsigned mm = M[s]; mm != 0u; mm &= mm - 1u) S = S + __shfl_sync(0xffffffffu, ex[s], __ffs(mm) - 1);
+  int base = 0;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if ((chosen >> s) & 1u) {
+      const int slot = base + __popc(M[s] & ((1u << lane) - 1u));
+      idx_out[slot] = lane + 32 * s;
+      gate_out[slot] = ex[s] / S;
+    }
+    base += __popc(M[s]);
+  }
 }
 
 }  // namespace sel
