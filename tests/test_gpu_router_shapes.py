@@ -25,6 +25,9 @@ CASES = [
     (5, 128, 2, 1), (5, 384, 2, 300), (12, 256, 3, 65), (12, 384, 3, 7),
     (40, 640, 4, 64), (40, 640, 4, 129), (200, 384, 8, 3), (200, 384, 8, 257),
     (8, 128, 1, 1000), (96, 1152, 6, 33),
+    # every lane holding eight experts, and up to 16 selected (the top-k's
+    # slot ballots over all eight groups of 32 experts)
+    (256, 256, 16, 40), (256, 512, 12, 3), (17, 128, 16, 9),
 ]
 
 
