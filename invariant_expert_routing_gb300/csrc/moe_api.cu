@@ -1033,10 +1033,11 @@ moe_status moe_forward_timed(const moe_config* cfg, int32_t T, const uint16_t* h
 int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
   if (T == 0) return 0;
-  // router + dispatch, then tile lists 1 (both lists in one launch) + row
-  // gather 1 + W13 + W2 + combine 1 (+ shared W13, W2).  Router: chunk sums + reduce/top-k = 2
-  // (chunked router), or on the tensor cores transpose, norms, GEMM,
-  // candidate filter, tiled recompute, finalize = 6.
+  // router + dispatch, then the tile lists with the routed-row copy 1 (one
+  // launch; the row copy alone after the small-batch dispatch, nothing after
+  // the decode front) + W13 + W2 + combine 1 (+ shared W13, W2).  Router:
+  // chunk sums + reduce/top-k = 2 (chunked router), or on the tensor cores
+  // W_g preparation, GEMM, candidate filter, tiled recompute, finalize = 5.
   // Dispatch: count, scan, scatter = 3, or for at most 1024 routes one
   // launch that also builds both tile lists; with reroute count, scan,
   // preference lists, deferred acceptance, check, sequential fallback
@@ -1046,22 +1047,23 @@ int32_t moe_forward_launch_count(const moe_config* cfg, int32_t T) {
   // reduce, top-k, dispatch, tile lists and row gather.
   const bool chunked =
       moe::chunked_router_ok(T, cfg->hidden, cfg->num_experts, use_tc_router(cfg), cfg->debug_flags);
-  const int router = chunked ? 2 : (use_tc_router(cfg) ? 6 : 2);
-  int front = 0;
+  const int router = chunked ? 2 : (use_tc_router(cfg) ? 5 : 2);
+  int front = 0, rows = 1;
   if (expert_choice(cfg)) {   // logits (chunked router, 2), scores, selection
     front = 2 + 2;
   } else if (cfg->overflow_policy == MOE_OVERFLOW_REROUTE && cfg->capacity_factor > 0.0) {
     front = 2 + 9;
   } else if (moe::decode_front_ok(T, cfg->hidden, cfg->num_experts, cfg->top_k, cfg->debug_flags)) {
     // chunk sums, then routing, dispatch, tile lists and the routed rows
-    front = 2 - 1 - 1;
+    front = 2;
+    rows = 0;
   } else if (moe::dispatch_small_ok((long long)T * cfg->top_k)) {
     // dispatch and both tile lists in one launch
-    front = router + 1 - 1;
+    front = router + 1;
   } else {
     front = router + 3;
   }
-  return front + 1 + 1 + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
+  return front + rows + 2 + 1 + (cfg->shared_intermediate > 0 ? 2 : 0);
 }
 
 moe_status moe_router_tc_logits(const moe_config* cfg, int32_t T, const uint16_t* h,

@@ -168,18 +168,18 @@ def test_launch_counts(moe):
     qw = dict(hidden=2048, num_experts=128, top_k=8, intermediate=768, block_size=16)
     ds = dict(hidden=7168, num_experts=256, top_k=8, intermediate=2048, block_size=16)
     T = 4096
-    # after routing and dispatch: both tile lists (one launch), the row copy, W13, W2, combine = 5
-    assert moe.moe_forward_launch_count(mix, T) == 2 + 3 + 5
-    assert moe.moe_forward_launch_count(qw, T) == 6 + 3 + 5   # T * H * N above 3 * 2^28: tensor cores
-    assert moe.moe_forward_launch_count(qw, 3072) == 2 + 3 + 5   # chunked router up to 3 * 2^28
-    assert moe.moe_forward_launch_count(qw, 3073) == 6 + 3 + 5
-    assert moe.moe_forward_launch_count(ds, 438) == 2 + 3 + 5
-    assert moe.moe_forward_launch_count(ds, 439) == 6 + 3 + 5
-    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 5
-    assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 4 + 5
-    assert moe.moe_forward_launch_count(dict(ds, routing=1), T) == 4 + 5
-    assert moe.moe_forward_launch_count(ds, T) == 6 + 3 + 5
-    assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 5 + 2
+    # after routing and dispatch: both tile lists with the row copy (one launch), W13, W2, combine = 4
+    assert moe.moe_forward_launch_count(mix, T) == 2 + 3 + 4
+    assert moe.moe_forward_launch_count(qw, T) == 5 + 3 + 4   # T * H * N above 3 * 2^28: tensor cores
+    assert moe.moe_forward_launch_count(qw, 3072) == 2 + 3 + 4   # chunked router up to 3 * 2^28
+    assert moe.moe_forward_launch_count(qw, 3073) == 5 + 3 + 4
+    assert moe.moe_forward_launch_count(ds, 438) == 2 + 3 + 4
+    assert moe.moe_forward_launch_count(ds, 439) == 5 + 3 + 4
+    assert moe.moe_forward_launch_count(dict(mix, capacity_factor=1.0, overflow_policy=1), T) == 11 + 4
+    assert moe.moe_forward_launch_count(dict(qw, routing=1), T) == 4 + 4
+    assert moe.moe_forward_launch_count(dict(ds, routing=1), T) == 4 + 4
+    assert moe.moe_forward_launch_count(ds, T) == 5 + 3 + 4
+    assert moe.moe_forward_launch_count(dict(mix, shared_intermediate=128), T) == 2 + 3 + 4 + 2
     # up to 64 tokens (or any batch of small router work) are routed in two
     # launches (chunk sums, reduce + top-k), and up to 1024 routes are
     # dispatched with both tile lists in one launch
@@ -190,12 +190,12 @@ def test_launch_counts(moe):
     assert moe.moe_forward_launch_count(mix, 64) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 65) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 512) == 2 + 1 + 4
-    assert moe.moe_forward_launch_count(mix, 513) == 2 + 3 + 5
+    assert moe.moe_forward_launch_count(mix, 513) == 2 + 3 + 4
     assert moe.moe_forward_launch_count(qw, 1) == 2 + 3
     assert moe.moe_forward_launch_count(qw, 64) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(qw, 65) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(qw, 128) == 2 + 1 + 4
-    assert moe.moe_forward_launch_count(dict(qw, routing=1), 64) == 4 + 5
+    assert moe.moe_forward_launch_count(dict(qw, routing=1), 64) == 4 + 4
     assert moe.moe_forward_launch_count(ds, 64) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(ds, 65) == 2 + 1 + 4
     assert moe.moe_forward_launch_count(mix, 0) == 0
