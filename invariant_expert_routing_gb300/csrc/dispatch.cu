@@ -422,8 +422,8 @@ __device__ __forceinline__ void scatter_rows_warps(const uint16_t* __restrict__ 
 // The GEMM tile lists and the routed token rows in one launch: CTAs below
 // `lists` each build one tile list (CTA 0 list a, CTA 1 list b); the others
 // copy the rows (kRows 1: in padded-row order, 2: token by token, 0: none).
-// No early trigger: the next kernel is a GEMM, whose CTAs would hold SMs
-// idle while they wait.
+// The grid is sized to be resident at once, so the GEMM may launch early:
+// its CTAs set up on the SMs this grid releases and wait for it to finish.
 template <int kRows>
 __global__ void __launch_bounds__(256) tiles_rows_kernel(const int32_t* __restrict__ block_expert,
                                                          const int32_t* __restrict__ num_padded,
@@ -434,6 +434,7 @@ __global__ void __launch_bounds__(256) tiles_rows_kernel(const int32_t* __restri
                                                          const int32_t* __restrict__ route_pos, int H,
                                                          uint16_t* __restrict__ x_perm) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
   const int R = T * k;
   if ((int)blockIdx.x < lists) {
     build_tiles_block(block_expert, num_padded, sorted_route_ids, R, N, B, max_rows, blockIdx.x == 0 ? a : b,
@@ -581,7 +582,9 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
     int32_t* __restrict__ num_dropped, const TileListOut la, const TileListOut lb,
     uint16_t* __restrict__ x_perm, long long max_rows, int* status) {
   pdl_wait();      // earlier kernels' outputs are visible from here on
-  // no early trigger: the next kernel is a GEMM
+  // one CTA: the GEMM's CTAs may set up on the other SMs meanwhile (they
+  // wait for this kernel to finish)
+  pdl_trigger();
   __shared__ float lrow[kFinishMaxT][kMaxN];
   // the routes' experts and padded rows stay in shared memory for the steps
   // of this CTA that read them (their global copies are for later kernels)

@@ -157,8 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap w_map,
                        const __grid_constant__ CUtensorMap x_map,
                        const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  // no early trigger: CTAs of the next kernel would hold SMs idle while they wait
   using C = GemmCfg<kW13, BN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
@@ -166,12 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t s_ibar[2 * kItemRing];   // item ring: full, then empty barriers
   __shared__ ItemSlot s_ring[kItemRing];
 
-  const int num_tiles = args.identity_T ? (args.identity_T + BN - 1) / BN : *args.num_tiles;
   const int nfe = args.n_feat_tiles;
   const int unit0 = (int)blockIdx.x;
   const int units = (int)gridDim.x;
-  const int total = num_tiles * nfe;
-  if (unit0 >= total) return;  // uniform for the whole CTA
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -216,6 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+  // The set-up above reads nothing an earlier kernel writes: it overlaps the
+  // end of that kernel.  Every CTA of this persistent grid is resident, so
+  // the next kernel may launch now (its CTAs wait for this grid to finish).
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
+  const int num_tiles = args.identity_T ? (args.identity_T + BN - 1) / BN : *args.num_tiles;
+  const int total = num_tiles * nfe;   // a CTA past it publishes no item and only tears down
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -575,8 +577,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
                             const __grid_constant__ CUtensorMap x_map,
                             const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
-  pdl_wait();      // earlier kernels' outputs are visible from here on
-  // no early trigger: CTAs of the next kernel would hold SMs idle while they wait
   using C = PairCfg<kW13, kWide>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
@@ -584,12 +584,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const uint32_t rank = cluster_ctarank();            // 0: issues the MMAs
   const bool lead = rank == 0;
-  const int num_tiles = args.identity_T ? (args.identity_T + kPairRows - 1) / kPairRows : *args.num_tiles;
   const int nfe = args.n_feat_tiles;                  // pair feature tiles (C::kFeatTile features)
   const int pair0 = (int)(blockIdx.x >> 1);
   const int pairs = (int)(gridDim.x >> 1);
-  const int total = num_tiles * nfe;
-  if (pair0 >= total) return;  // the same verdict in both CTAs of the pair
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
@@ -631,6 +628,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();   // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+  // The set-up above reads nothing an earlier kernel writes: it overlaps the
+  // end of that kernel.  Every CTA of this persistent grid is resident, so
+  // the next kernel may launch now (its CTAs wait for this grid to finish).
+  pdl_wait();      // earlier kernels' outputs are visible from here on
+  pdl_trigger();
+  const int num_tiles = args.identity_T ? (args.identity_T + kPairRows - 1) / kPairRows : *args.num_tiles;
+  const int total = num_tiles * nfe;   // a pair past it runs no item and only tears down
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
