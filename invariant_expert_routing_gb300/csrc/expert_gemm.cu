@@ -39,6 +39,7 @@ constexpr uint32_t kBoxBytes = 64 * 64 * 2;         // 64 K rows x 64 features o
 constexpr int kEpiWarps = 8;                        // two per TMEM lane quarter, one column half each
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmallRows = 32;                      // token box when a tile has <= 32 routed rows
+static_assert(kSmallRows == kDecodeMaxT, "the decode instances take small tiles only");
 constexpr uint32_t kStageBudget = 192 * 1024;       // shared memory for the operand stages
 // Work items reach the MMA issuer and the epilogue warps through a ring of
 // this many slots, filled by the producer (which fetches them).
@@ -526,20 +527,27 @@ constexpr int kPairM = 256;         // weight rows per pair (the MMA's M)
 // item is bound by the operand bytes an SM takes in; its single
 // 512-column accumulator costs the overlap of the epilogue, a few per cent
 // of a 14336-deep reduction.
-template <bool kW13, bool kWide = false>
+// kDecode (batches of at most 32 tokens, whose tiles all have at most
+// kSmallRows routed rows): a stage holds the weight boxes and a kSmallRows-row
+// token box, so 9 (W13) or 11 (W2) stages fit instead of 6 or 7.  The MMAs
+// are those of a small tile in the other instances (same bits).
+template <bool kW13, bool kWide = false, bool kDecode = false>
 struct PairCfg {
   static_assert(!(kW13 && kWide), "wide items are W2 only");
+  static_assert(!(kWide && kDecode), "decode instances have plain items");
   static constexpr int kGroups = kWide ? 2 : 1;              // 256-feature groups per item
   static constexpr int kRowsCta = kPairRows / 2;
   static constexpr int kFeatCta = kW13 ? 64 : 128;           // output features per CTA and group
   static constexpr int kFeatTile = 2 * kFeatCta * kGroups;   // output features per pair tile
   static constexpr uint32_t kABytes = 2 * kBoxBytes * kGroups;   // 128 weight rows x 64 K per group
-  static constexpr uint32_t kBTileBytes = kRowsCta * kBK * 2;
+  static constexpr uint32_t kBTileBytes = (kDecode ? kSmallRows : kRowsCta) * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBTileBytes;
   // W2 fits a seventh 32 KB stage in the 227 KB of shared memory; W13 needs
   // 16 KB for the u exchange
   static constexpr uint32_t kPairBudget = kW13 ? kStageBudget : 224 * 1024;
-  static constexpr int kStages = (int)(kPairBudget / kStageBytes) < 7 ? (int)(kPairBudget / kStageBytes) : 7;
+  static constexpr int kMaxStages = kDecode ? 12 : 7;
+  static constexpr int kStages =
+      (int)(kPairBudget / kStageBytes) < kMaxStages ? (int)(kPairBudget / kStageBytes) : kMaxStages;
   static constexpr uint32_t kAccCols = kPairRows * kGroups;
   static constexpr int kNumAcc = kWide ? 1 : 2;
   static constexpr uint32_t kTmemCols = 512;
@@ -572,12 +580,12 @@ __device__ __forceinline__ int named_bar_and(int id, int threads, int pred) {
   return (int)r;
 }
 
-template <bool kW13, bool kWide = false>
+template <bool kW13, bool kWide = false, bool kDecode = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap w_map,
                             const __grid_constant__ CUtensorMap x_map,
                             const __grid_constant__ CUtensorMap x_map_small, const GemmArgs args) {
-  using C = PairCfg<kW13, kWide>;
+  using C = PairCfg<kW13, kWide, kDecode>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
@@ -652,7 +660,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // tiles with at most kSmallRows routed rows (decode): a kSmallRows-row
       // token box per CTA and N = 2 kSmallRows MMAs; the odd CTA's rows are
       // padding or beyond the tile, in columns that are never stored
-      const bool small = t.valid <= kSmallRows;
+      const bool small = kDecode || t.valid <= kSmallRows;
+      // (a decode instance given a tile of more rows computes only its first
+      // kSmallRows: reported, never silent)
+      if (kDecode && t.valid > kSmallRows && lane == 0) atomicOr(args.status, kDevErrBadBlocks);
       const int b_rows = small ? kSmallRows : C::kRowsCta;
       const int brow0 = t.row0 + (int)rank * b_rows;                     // this CTA's half of the rows
       const uint32_t cta_tx = C::kABytes + b_rows * kBK * 2;
@@ -732,7 +743,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // the routed rows of the next item's tile are loaded one item ahead
       int valid = pair0 < total ? work_of<kPairRows>(args, pair0, num_tiles, nfe).t.valid : 0;
       for (int item = pair0; item < total && ok; item += pairs) {
-        const bool small = valid <= kSmallRows;
+        const bool small = kDecode || valid <= kSmallRows;
         const uint32_t idesc = small ? C::kIdescSmall : C::kIdesc;
         valid = item + pairs < total ? work_of<kPairRows>(args, item + pairs, num_tiles, nfe).t.valid : 0;
         if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, &s_abort, wlim)) {
@@ -893,7 +904,7 @@ void launch(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMa
 
 // Pairs of CTAs that can be resident at once (one CTA per SM; a pair needs
 // two SMs of one GPC), looked up once per device and kernel.
-template <bool kW13, bool kWide = false>
+template <bool kW13, bool kWide = false, bool kDecode = false>
 int resident_pairs(int num_sms) {
   static int cache[64] = {0};
   int dev = 0;
@@ -903,7 +914,7 @@ int resident_pairs(int num_sms) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<kW13, kWide>::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<kW13, kWide, kDecode>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -911,7 +922,8 @@ int resident_pairs(int num_sms) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13, kWide>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, expert_gemm_pair_kernel<kW13, kWide, kDecode>, &cfg) != cudaSuccess ||
+      n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
   }
@@ -920,11 +932,11 @@ int resident_pairs(int num_sms) {
   return n;
 }
 
-template <bool kW13, bool kWide = false>
+template <bool kW13, bool kWide = false, bool kDecode = false>
 void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small, GemmArgs a,
                  int max_tiles, int num_sms, cudaStream_t s) {
-  auto kernel = expert_gemm_pair_kernel<kW13, kWide>;
-  const int smem = (int)PairCfg<kW13, kWide>::kSmemBytes;
+  auto kernel = expert_gemm_pair_kernel<kW13, kWide, kDecode>;
+  const int smem = (int)PairCfg<kW13, kWide, kDecode>::kSmemBytes;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -934,7 +946,7 @@ void launch_pair(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUten
   }
   const long long items = (long long)max_tiles * a.n_feat_tiles;
   if (items <= 0) return;
-  const int cap = resident_pairs<kW13, kWide>(num_sms);
+  const int cap = resident_pairs<kW13, kWide, kDecode>(num_sms);
   const int pairs = (int)(items < cap ? items : cap);
   a.concurrent = pairs;
   launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, w_map, x_map, x_small, a);
@@ -951,7 +963,9 @@ bool gemm_smem_ok() {
          optin >= (int)GemmCfg<false, kRouterTileRows>::kSmemBytes &&
          optin >= (int)GemmCfg<false, kRouterTileRowsNarrow>::kSmemBytes &&
          optin >= (int)PairCfg<true>::kSmemBytes && optin >= (int)PairCfg<false>::kSmemBytes &&
-         optin >= (int)PairCfg<false, true>::kSmemBytes;
+         optin >= (int)PairCfg<false, true>::kSmemBytes &&
+         optin >= (int)PairCfg<true, false, true>::kSmemBytes &&
+         optin >= (int)PairCfg<false, false, true>::kSmemBytes;
 }
 
 bool gemm_pair_ok(bool w13, int features, int K) {
@@ -968,7 +982,9 @@ bool gemm_wide_ok(int features, int K) {
 
 void launch_w13_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CUtensorMap& x_small,
                      const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
-  if (a.pair)
+  if (a.pair && a.decode)
+    launch_pair<true, false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  else if (a.pair)
     launch_pair<true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else
     launch<true, kW13TileRows>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
@@ -978,6 +994,8 @@ void launch_w2_gemm(const CUtensorMap& w_map, const CUtensorMap& x_map, const CU
                     const GemmArgs& a, int max_tiles, int num_sms, cudaStream_t s) {
   if (a.pair && a.wide)
     launch_pair<false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
+  else if (a.pair && a.decode)
+    launch_pair<false, false, true>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else if (a.pair)
     launch_pair<false>(w_map, x_map, x_small, a, max_tiles, num_sms, s);
   else

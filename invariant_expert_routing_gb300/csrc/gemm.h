@@ -12,6 +12,9 @@ namespace moe {
 constexpr int kDevErrExpertRange = 0x1;
 constexpr int kDevErrTimeout = 0x2;
 constexpr int kDevErrBadBlocks = 0x4;
+// Calls whose tiles hold at most this many routed rows run the CTA-pair
+// GEMMs' decode instances (the small-tile token box of the other instances).
+constexpr int kDecodeMaxT = 32;
 constexpr int kDevNoteRerouteFallback = 0x100;
 
 // Rows of one grouped-GEMM token tile (the N of every tcgen05 MMA), one
@@ -60,6 +63,10 @@ struct GemmArgs {
                        //    128-row boxes; n_feat_tiles in units of kPairFeatW13 / kPairFeatW2)
   int wide;            // W2 pairs only, 1: items of two 256-feature groups
                        //    (n_feat_tiles in units of kPairFeatW2Wide)
+  int decode;          // pairs only, 1: every tile holds at most 32 routed rows (the
+                       //    caller's batch has at most 32 tokens); stages then hold a
+                       //    32-row token box, so more of them fit
+
   unsigned long long wait_ns;  // limit of the pipeline waits; 0: kWaitLimitNs
   int32_t* next_item;  // one-CTA kernel, routed mode: the launch's tile counter (zero before the
                        // launch); each CTA takes the next item from it when it is free.  nullptr

@@ -458,6 +458,7 @@ moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, co
   s13.out_ld = Is;
   s13.status = status;
   s13.pair = spair13 ? 1 : 0;
+  s13.decode = T <= moe::kDecodeMaxT ? 1 : 0;   // identity tiles of at most T rows
   s13.wait_ns = (unsigned long long)c->debug_wait_ns;
   moe::launch_w13_gemm(m_w13s, m_h, m_hs, s13, (T + srows13 - 1) / srows13, sms, s);
   moe::GemmArgs s2 = s13;
@@ -469,6 +470,7 @@ moe_status shared_ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, co
   s2.out_ld = H;
   s2.out_bf16 = 1;
   s2.pair = pair2 ? 1 : 0;
+  s2.decode = T <= moe::kDecodeMaxT ? 1 : 0;
   moe::launch_w2_gemm(m_w2s, m_ash, m_ashs, s2, (T + moe::kW2TileRows - 1) / moe::kW2TileRows, sms, s);
   return last_cuda();
 }
@@ -535,6 +537,13 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g13.out_ld = I;
   g13.status = status;
   g13.pair = pair13 ? 1 : 0;
+  // decode instances: no tile of this call holds more than kDecodeMaxT
+  // routed rows — at most that many tokens in the forward (a token routes to
+  // an expert at most once), or that many routes in all for a caller's own
+  // block list
+  const bool decode =
+      T <= moe::kDecodeMaxT && (route_pos != nullptr || (long long)T * k <= moe::kDecodeMaxT);
+  g13.decode = decode ? 1 : 0;
   g13.wait_ns = (unsigned long long)c->debug_wait_ns;
   moe::launch_w13_gemm(m_w13, m_x, m_xs, g13, max_tiles13, sms, s);
   mark(mk, 4);
@@ -553,6 +562,7 @@ moe_status ffn_impl(const moe_config* c, int32_t T, const uint16_t* h, const uin
   g2.out_bf16 = 1;
   g2.pair = pair2 ? 1 : 0;
   g2.wide = wide2 ? 1 : 0;
+  g2.decode = (decode && !wide2) ? 1 : 0;
   moe::launch_w2_gemm(m_w2, m_a, m_as, g2, max_tiles2, sms, s);
   mark(mk, 5);
 
