@@ -67,6 +67,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   __shared__ int s_pos[kMaxSlots];
   __shared__ float s_gate[kMaxSlots];
   __shared__ int s_wcnt[8];
+  // few tokens: this thread's first h (and y_shared) piece is requested
+  // before the slot list is built (it depends on neither)
+  const int d_first = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  uint2 h_first = make_uint2(0u, 0u), ys_first = make_uint2(0u, 0u);
+  if (kForm == 2 && d_first < H) {
+    h_first = __ldg(reinterpret_cast<const uint2*>(h + (size_t)t * H + d_first));
+    if (y_shared) ys_first = __ldg(reinterpret_cast<const uint2*>(y_shared + (size_t)t * H + d_first));
+  }
   // list the kept slots in ascending j (k <= 256 = blockDim.x: one slot per thread)
   const int j = threadIdx.x, lane = j & 31, w = j >> 5;
   bool use = false;
@@ -153,14 +161,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
         acc.w = fmaf(g, y.w, acc.w);
       }
     }
+    const bool first = kForm == 2 && d == d_first;
     if (y_shared) {
-      const float4 ys = load_bf16x4(y_shared + (size_t)t * H + d);
+      const float4 ys = first ? make_float4(__uint_as_float(ys_first.x << 16), __uint_as_float(ys_first.x & 0xFFFF0000u),
+                                            __uint_as_float(ys_first.y << 16), __uint_as_float(ys_first.y & 0xFFFF0000u))
+                              : load_bf16x4(y_shared + (size_t)t * H + d);
       acc.x = acc.x + ys.x;
       acc.y = acc.y + ys.y;
       acc.z = acc.z + ys.z;
       acc.w = acc.w + ys.w;
     }
-    const uint2 hv = __ldg(reinterpret_cast<const uint2*>(h + (size_t)t * H + d));
+    const uint2 hv = first ? h_first : __ldg(reinterpret_cast<const uint2*>(h + (size_t)t * H + d));
     const float h0 = __uint_as_float(hv.x << 16), h1 = __uint_as_float(hv.x & 0xFFFF0000u);
     const float h2 = __uint_as_float(hv.y << 16), h3 = __uint_as_float(hv.y & 0xFFFF0000u);
     const __nv_bfloat16 o0 = __float2bfloat16_rn(h0 + acc.x), o1 = __float2bfloat16_rn(h1 + acc.y);
