@@ -471,7 +471,9 @@ __device__ __forceinline__ void dispatch_small_block(
   __shared__ int seg[kMaxN], offa[kMaxN], offb[kMaxN];
   __shared__ int s_rows, s_drop, s_ta, s_tb;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < 32 * (kMaxN + 1); i += blockDim.x) (&wc[0][0])[i] = 0;
+  // warps holding routes (R <= 1024 = 32 warps): only their counts are used
+  const int rw = (R + 31) >> 5;
+  for (int i = tid; i < rw * (kMaxN + 1); i += blockDim.x) (&wc[0][0])[i] = 0;
   __syncthreads();
   const int r = tid;
   const int e = (r < R) ? topk_idx[r] : -1;
@@ -483,7 +485,7 @@ __device__ __forceinline__ void dispatch_small_block(
   __syncthreads();
   for (int x = tid; x < N; x += blockDim.x) {
     int run = 0;
-    for (int ww = 0; ww < 32; ++ww) {
+    for (int ww = 0; ww < rw; ++ww) {
       const int c = wc[ww][x];
       wc[ww][x] = run;
       run += c;
@@ -573,6 +575,7 @@ __global__ void __launch_bounds__(kSmallDispatchMaxR) dispatch_small_kernel(
 // routed token rows of x_perm.
 constexpr int kFinishThreads = 512;
 constexpr int kFinishMaxT = 2;
+constexpr int kRowPieces = 4;   // token-row pieces per thread requested at the start
 
 __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
     const float* __restrict__ part, const uint16_t* __restrict__ h, const float* __restrict__ bias, int T, int H,
@@ -593,6 +596,18 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
   __shared__ int32_t s_pos[kFinishMaxT * 16];
   const int C = (H + kRouterChunk - 1) / kRouterChunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the token rows do not depend on the routing: with at most four 16-byte
+  // pieces per thread they are requested now, and stored to their routes'
+  // padded rows once the dispatch has placed them
+  const int pieces = H / 8;
+  const bool early_rows = T * pieces <= kRowPieces * kFinishThreads;
+  uint4 rowv[kRowPieces];
+#pragma unroll
+  for (int u = 0; u < kRowPieces; ++u) {
+    const int x = tid + u * kFinishThreads;
+    if (early_rows && x < T * pieces)
+      rowv[u] = __ldg(reinterpret_cast<const uint4*>(h + (size_t)(x / pieces) * H) + x % pieces);
+  }
   for (int x = tid; x < T * N; x += blockDim.x) {
     // the chunk sums (and the bias) requested sixteen at a time, then added
     // in ascending chunk order
@@ -622,9 +637,23 @@ __global__ void __launch_bounds__(kFinishThreads, 1) decode_finish_kernel(
   dispatch_small_block(s_idx, R, N, B, capacity, route_kept, route_pos, sorted_route_ids, block_expert,
                        num_padded, expert_counts, num_dropped, la, lb, status, s_pos);
   __syncthreads();
+  if (early_rows) {
+    // each requested piece to the padded row of each kept route of its token
+#pragma unroll
+    for (int u = 0; u < kRowPieces; ++u) {
+      const int x = tid + u * kFinishThreads;
+      if (x < T * pieces) {
+        const int t = x / pieces, q = x % pieces;
+        for (int j = 0; j < k; ++j) {
+          const long long p = s_pos[t * k + j];
+          if (p >= 0 && p < max_rows) *(reinterpret_cast<uint4*>(x_perm + p * H) + q) = rowv[u];
+        }
+      }
+    }
+    return;
+  }
   // the routed token rows (padding rows feed only MMA columns that are never
   // stored), four 16-byte pieces per thread and round, loads before stores
-  const int pieces = H / 8;
   const int total = R * pieces;
   for (int x0 = tid; x0 < total; x0 += 4 * blockDim.x) {
     uint4 v[4];
